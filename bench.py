@@ -1,0 +1,324 @@
+#!/usr/bin/env python
+"""Throughput of the LatentMoE layer forward (top-16 of 896 experts, SwiGLU
+experts on MXFP4 weights) on GB300, one process per GPU.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload decode|tiny|prefill|skewed] [--no-cpu-baseline]
+
+A step is one lmoe_forward call (route -> permute -> MXFP8 activations ->
+gate/up GEMM + SwiGLU -> down GEMM -> combine) over one batch of seeded
+synthetic tokens with the whole expert bank resident in HBM.  With N > 1
+(torchrun) every rank runs its own replica of the layer on its own batch:
+the layer has no exchange step on one node's replicas, so there is no
+collective on the data path ("scaling": "weak").  Rank 0 prints one JSON line.
+
+`--impl reference` times the CPU oracle (plain single-threaded C, fp64) on a
+bounded sample of the same workload on the host cores; it is the only other
+place besides the CPU-baseline leg where this script runs the oracle.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "LatentMoE layer tokens/s; % HBM BW (decode) / % block-scaled TC peak (prefill)"
+UNIT = "tokens/s"
+# MXFP4 bytes per weight element (4-bit code + one E8M0 byte per 32 elements)
+MXFP4_B = 0.5 + 1.0 / 32
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sample-tokens", type=int, default=2)
+    return ap.parse_args()
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled while it runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.uuid, self.proc, self.t0, self.t1 = uuid, None, None, None
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu=timestamp,{self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"]
+        if self.uuid:
+            cmd.insert(1, f"--id={self.uuid}")
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.25)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = [[c.strip() for c in l.split(",")] for l in out.strip().splitlines() if l.count(",") >= 8]
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------------
+
+def setup_layer(wl, dev):
+    import numpy as np
+    import torch
+
+    import lmoe_inputs as gen
+    from top_routing_mxfp4_gb300 import lmoe
+    bank = lmoe.ExpertBank(wl.E, wl.d, wl.I, dev)
+    for e0 in range(0, wl.E, 32):
+        e1 = min(wl.E, e0 + 32)
+        for which in ("gate", "up", "down"):
+            bank.load(which, e0, torch.from_numpy(gen.expert_f32(wl, which, e0, e1)).to(dev))
+    bias = gen.router_bias(wl)
+    layer = lmoe.Layer(torch.from_numpy(gen.router_f32(wl)).to(dev), bank, k=wl.k,
+                       bias=None if bias is None else torch.from_numpy(bias).to(dev))
+    x = gen.x_bf16(wl)
+    xd = torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).to(dev).view(torch.bfloat16)
+    torch.cuda.synchronize()
+    return layer, x, xd
+
+
+def cpu_baseline(wl, ntok: int):
+    """The oracle as it stands, on `ntok` tokens of the workload, one core."""
+    import numpy as np
+
+    import lmoe_inputs as gen
+    import oracle
+    x = gen.x_bf16(wl, 0, ntok)
+    Wr = gen.router_f32(wl)
+    bias = gen.router_bias(wl)
+    # weights of the experts these tokens route to, quantised by the oracle (not timed: load-time work)
+    lg = oracle.router_logits(x, Wr, bias)
+    idx, _ = oracle.topk_softmax(lg, wl.k)
+    bank = oracle.quantize_experts(wl, experts=np.unique(idx))
+    t0 = time.perf_counter()
+    lg = oracle.router_logits(x, Wr, bias)
+    idx, w = oracle.topk_softmax(lg, wl.k)
+    oracle.permute(idx, wl.E)
+    oracle.moe_tokens(x, idx, w, bank, wl.d, wl.E, wl.I)
+    dt = time.perf_counter() - t0
+    return {"value": ntok / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{ntok} of the {wl.T} tokens of the {wl.name} workload through the whole layer "
+                      f"(routing over all {wl.E} experts, top-{wl.k}, permute, SwiGLU experts, combine); "
+                      f"{dt:.1f} s of CPU time"}
+
+
+def run_ours(args, ws, rank, local):
+    import numpy as np
+    import torch
+    import torch.distributed as tdist
+
+    import lmoe_inputs as gen
+    from top_routing_mxfp4_gb300 import build as lbuild
+    lbuild.build()
+    from top_routing_mxfp4_gb300 import lmoe
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl = gen.WORKLOADS[args.workload]
+    layer, x, xd = setup_layer(wl, dev)
+    T = wl.T
+    st = torch.cuda.current_stream()
+    idx = torch.empty((T, wl.k), dtype=torch.int32, device=dev)
+    y = torch.empty((T, wl.d), dtype=torch.bfloat16, device=dev)
+    for _ in range(max(3, args.warmup)):
+        layer.forward(xd, y=y, topk_idx=idx)
+    torch.cuda.synchronize()
+    assert layer.device_status() == 0
+    counts = torch.bincount(idx.view(-1).long(), minlength=wl.E)
+    touched = int((counts > 0).sum())
+
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        uuid = None
+    sampler = ClockSampler(uuid)
+    sampler.start()
+    time.sleep(0.3)
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(lmoe.NUM_STAGE_EVENTS)] for _ in range(K)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if ws > 1:
+        tdist.barrier()
+    torch.cuda.synchronize()
+    t_start.record(st)
+    for i in range(K):
+        lmoe.set_stage_events(evs[i])
+        layer.forward(xd, y=y, topk_idx=idx)
+    t_end.record(st)
+    torch.cuda.synchronize()
+    if ws > 1:
+        tdist.barrier()
+    lmoe.set_stage_events(None)
+    clocks = sampler.stop()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    stage_ms = {name: sum(e[j].elapsed_time(e[j + 1]) for e in evs) / K for j, name in enumerate(lmoe.STAGES)}
+    if ws > 1:
+        t = torch.tensor([elapsed_ms], device=dev)
+        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    ms_per_step = elapsed_ms / K
+    value = ws * T / (ms_per_step / 1e3)
+
+    # end to end through host buffers: H2D of x from pinned memory, forward, D2H of y
+    xh = torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16).pin_memory()
+    yh = torch.empty((T, wl.d), dtype=torch.bfloat16).pin_memory()
+    xdev = torch.empty_like(xd)
+    for _ in range(3):
+        xdev.copy_(xh, non_blocking=True)
+        layer.forward(xdev, y=y)
+        yh.copy_(y, non_blocking=True)
+    torch.cuda.synchronize()
+    if ws > 1:
+        tdist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for _ in range(K):
+        xdev.copy_(xh, non_blocking=True)
+        layer.forward(xdev, y=y)
+        yh.copy_(y, non_blocking=True)
+    e1.record(st)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if ws > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+        tdist.barrier()
+
+    peaks = load_peaks()
+    per_expert_w = 3 * wl.I * wl.d * MXFP4_B           # gate + up + down bytes of one expert
+    gateup_bytes = touched * 2 * wl.I * wl.d * MXFP4_B  # weights the gate/up GEMM must stream once
+    t_gu = stage_ms["gate_up"] / 1e3
+    achieved = gateup_bytes / t_gu / 1e9
+    layer_weight_gbs = touched * per_expert_w / (ms_per_step / 1e3) / 1e9
+    launches_per_step = 10  # router, top-k, 3 permute passes, scatter, 3 expert-FFN kernels, combine
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "mxfp4 x mxfp8 -> f32 acc", "data": "synthetic (seeded counter-based generator)",
+        "config": {"workload": wl.name, "T": T, "d": wl.d, "E": wl.E, "k": wl.k, "I": wl.I,
+                   "per_gpu_batch_tokens": T, "parallelism": f"replicas x{ws}",
+                   "l2": f"inputs larger than L2: {touched} touched experts = {touched * per_expert_w / 1e9:.2f} GB "
+                         f"of weights read per step (L2 129 MB)"},
+        "roofline": {"bound": "hbm", "kernel": "gate/up expert GEMM", "achieved": achieved,
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                     "traffic": None, "peak_source": peaks["source"],
+                     "layer_weight_gbs": layer_weight_gbs, "layer_frac": layer_weight_gbs / peaks["hbm_gbs"]},
+        "stage_ms": stage_ms, "touched_experts": touched,
+        "e2e": {"value": ws * T / (e2e_ms / K / 1e3), "unit": UNIT, "h2d_bytes_per_step": xh.numel() * 2,
+                "d2h_bytes_per_step": yh.numel() * 2},
+        "gpu_launches": K * launches_per_step, "clocks": clocks,
+    }
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_sample_tokens)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------------
+# reference arm: the CPU oracle as it stands
+# ---------------------------------------------------------------------------------
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return
+    import lmoe_inputs as gen
+    import oracle
+    lmoe_inputs_built = gen.build()
+    oracle.build()
+    del lmoe_inputs_built
+    wl = gen.WORKLOADS[args.workload]
+    ntok = 1
+    for _ in range(args.warmup):
+        pass  # the oracle has no warm-up state; sample preparation happens in cpu_baseline
+    times = []
+    info = None
+    for _ in range(max(1, args.steps if args.steps <= 3 else 3)):
+        info = cpu_baseline(wl, ntok)
+        times.append(ntok / info["value"])
+    dt = statistics.median(times)
+    value = ntok / dt
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": len(times),
+            "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic (seeded counter-based generator)",
+            "config": {"workload": wl.name, "T": wl.T, "d": wl.d, "E": wl.E, "k": wl.k, "I": wl.I},
+            "impl": "reference",
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": info["sample"]},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    ws, rank, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+        return
+    if ws > 1:
+        import torch
+        import torch.distributed as tdist
+        torch.cuda.set_device(local)
+        tdist.init_process_group("nccl")
+    try:
+        run_ours(args, ws, rank, local)
+    finally:
+        if ws > 1:
+            import torch.distributed as tdist
+            tdist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,205 @@
+/*
+ * lmoe -- forward pass of a LatentMoE layer (route to the top 16 of 896
+ * experts, SwiGLU experts on MXFP4 weights, weighted combine) as a C ABI over
+ * hand-written CUDA kernels for sm_103a (GB300).
+ *
+ * Sources (page title, section) that define the operations:
+ *  [MoE]  "SGLang 0.5.17: Kimi K3 原生 MXFP4 推理架构解析", section "MoE 稀疏激活：
+ *         896 专家中选 16 的 104B 激活逻辑": the router scores every token
+ *         against all 896 experts (token embeddings x router weights), keeps
+ *         the 16 best, and only those experts compute; their outputs are
+ *         summed with weights.
+ *  [MX]   same page, section "MXFP4 原生支持": 4-bit values sharing one scale
+ *         per block of 32 (or 64) elements; dequantisation fused into the GEMM.
+ *  [L1]   "从Kimi K3到MiniMax-H3：国产大模型竞争进入“推理系统战”", section 二,
+ *         first layer: 4-bit weights meet higher-precision activations and
+ *         accumulation; section 一: 896 experts, 16 active, routing and
+ *         expert compute in a 3584-wide latent space (LatentMoE), gated FFN.
+ *  [EP]   "Kimi K3 Day-0 适配剖析", section 四: dispatch tokens to experts
+ *         (index computation, buffer planning, bucketing), expert compute,
+ *         combine the results back by weight; section 三: weights converted
+ *         to the hardware's form at load time, layer by layer.
+ *
+ * Readings where the pages are silent (the same in the CPU oracle):
+ *  - block size 32, E8M0 scales, shared exponent floor(log2 amax) - emax
+ *    (emax 2 for e2m1, 8 for e4m3), elements rounded to nearest even and
+ *    saturated (6 for e2m1, 448 for e4m3);
+ *  - gate weights: softmax over the 16 selected logits;
+ *  - top-16 order: larger logit first, equal logits by smaller expert id;
+ *  - the gated activation is SiLU (SwiGLU);
+ *  - activations entering each expert GEMM (the latent x and the gated
+ *    product h) are MXFP8 (e4m3 + E8M0 per 32), accumulation is fp32.
+ *
+ * Conventions for every call:
+ *  - Array pointers are DEVICE pointers owned by the caller, 16-byte aligned
+ *    (MXFP4 weight codes: 32-byte aligned).  Structs (lmoe_dims,
+ *    lmoe_expert_weights) are host pointers read during the call.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls only
+ *    enqueue work; LMOE_OK means "enqueued".
+ *  - Argument errors are reported synchronously before anything is enqueued
+ *    and leave every output untouched.  Launch failures return LMOE_ERR_CUDA.
+ *  - Errors found by kernels (an expert id out of range, a bounded wait that
+ *    ran out) are recorded in a status word at the start of the workspace;
+ *    read it with lmoe_last_device_status.
+ *  - No call allocates device memory; scratch comes from the caller's
+ *    workspace (size from the matching *_workspace_size query).
+ *  - Bit layouts:
+ *      bf16 tensors are passed as uint16_t bit patterns;
+ *      MXFP4 canonical: codes[r][K/2] (element 2i in the low nibble of byte
+ *        i), scales[r][K/32] (E8M0);
+ *      MXFP4 tensor-core layout (LMOE_LAYOUT_TC, the form lmoe_expert_ffn
+ *        reads): each matrix of `rows` x K is stored with K padded to
+ *        Kp = roundup(K, 128) (padding codes 0); scales are grouped in
+ *        512-byte atoms, one per 128 rows x 128 columns: atom (rt, kc) of
+ *        matrix m starts at ((m * RT + rt) * KC + kc) * 512 with
+ *        RT = ceil(rows/128), KC = Kp/128, and holds the scale of row
+ *        rt*128 + 32*j + i, column block kc*4 + b at byte 16*i + 4*j + b
+ *        (rows and blocks beyond the matrix hold 0);
+ *      MXFP8: codes[r][K] (e4m3), scales[r][K/32] (E8M0).
+ */
+#ifndef LMOE_H
+#define LMOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    LMOE_OK = 0,
+    LMOE_ERR_INVALID_ARG = -1,  /* bad size, null or misaligned pointer       */
+    LMOE_ERR_UNSUPPORTED = -2,  /* valid request this build does not handle   */
+    LMOE_ERR_WORKSPACE = -3,    /* workspace missing or too small             */
+    LMOE_ERR_CUDA = -4,         /* a CUDA runtime/driver call or launch failed */
+    LMOE_ERR_DEVICE_CHECK = -5, /* a kernel found bad input (status word)     */
+    LMOE_ERR_TIMEOUT = -6       /* a kernel's bounded wait ran out            */
+} lmoe_status;
+
+typedef enum { LMOE_ACT_MXFP8 = 1 } lmoe_act_fmt;
+typedef enum { LMOE_LAYOUT_CANONICAL = 0, LMOE_LAYOUT_TC = 1 } lmoe_layout;
+
+/* Layer shape: T tokens, latent width d, E experts, top-k, expert
+ * intermediate width I, activation format.
+ * Limits: T >= 0, d % 128 == 0, I % 32 == 0, 1 <= k <= min(E, 32),
+ * 1 <= E <= 2048, act == LMOE_ACT_MXFP8. */
+typedef struct {
+    int32_t T, d, E, k, I;
+    int32_t act;
+} lmoe_dims;
+
+/* The expert bank: for every expert e, gate and up [I][d] and down [d][I]
+ * MXFP4 matrices, stacked over e (matrix index m = e).  `layout` says which
+ * byte layout the six arrays use (see above). */
+typedef struct {
+    const uint8_t *gate_q, *gate_s;
+    const uint8_t *up_q, *up_s;
+    const uint8_t *down_q, *down_s;
+    int32_t layout;
+} lmoe_expert_weights;
+
+/* ---- load-time conversion ([MX], [EP] section 三) ------------------------ */
+
+/* Bytes of the codes (return value) and scales (*scale_bytes) of `nmat`
+ * stacked MXFP4 matrices of rows x K in the given layout; 0 on bad sizes. */
+size_t lmoe_mxfp4_bytes(int64_t nmat, int32_t rows, int32_t K, int32_t layout, size_t *scale_bytes);
+
+/* Quantise nmat stacked fp32 matrices w[nmat][rows][K] to MXFP4 codes q and
+ * scales s in `layout`.  K % 32 == 0.  Each block of 32 along K: scale byte
+ * clamp(floor(log2 amax) - 2 + 127, 0, 254) (0 for an all-zero block),
+ * element code = e2m1 round-to-nearest-even of w / 2^(byte-127), saturated
+ * at 6, sign kept. */
+lmoe_status lmoe_quant_mxfp4(const float *w, int64_t nmat, int32_t rows, int32_t K, uint8_t *q, uint8_t *s,
+                             int32_t layout, void *stream);
+
+/* ---- stages -------------------------------------------------------------- */
+
+/* MXFP8 quantisation of bf16 rows x[rows][K] (K % 32 == 0): per block of
+ * 32, scale byte clamp(floor(log2 amax) - 8 + 127, 0, 254), codes = e4m3
+ * round-to-nearest-even of x / 2^(byte-127), saturated at 448. */
+lmoe_status lmoe_quant_mxfp8(const uint16_t *x_bf16, int64_t rows, int32_t K, uint8_t *q, uint8_t *s, void *stream);
+
+/* Router [MoE]: logits[t][e] = fp32(sum_c x[t][c] * Wr[e][c]) (+ bias[e]),
+ * x bf16 [T][d], Wr fp32 [E][d], bias fp32 [E] or NULL (the skewed
+ * workload's popularity bias); then the top-k of each row (larger logit
+ * first, ties by smaller id) into topk_idx[T][k] and the softmax over those
+ * k logits into topk_w[T][k].  logits [T][E] is a required output. */
+lmoe_status lmoe_route(const uint16_t *x_bf16, const float *Wr, const float *bias, const lmoe_dims *dims,
+                       float *logits, int32_t *topk_idx, float *topk_w, void *stream);
+
+/* The top-k + softmax half of lmoe_route on given fp32 logits [T][E]. */
+lmoe_status lmoe_topk_from_logits(const float *logits, const lmoe_dims *dims, int32_t *topk_idx, float *topk_w,
+                                  void *stream);
+
+/* Scratch bytes lmoe_permute needs for these dims. */
+size_t lmoe_permute_workspace_size(const lmoe_dims *dims);
+
+/* Dispatch metadata [EP]: stable counting sort of the pairs p = t*k + j by
+ * expert topk_idx[p]: counts[E], offsets[E+1] (exclusive prefix sum),
+ * perm[T*k] (pairs of expert 0, then expert 1, ..., each in ascending p),
+ * inv[p] = position of p in perm.  An id outside [0, E) is skipped and
+ * recorded as LMOE_ERR_DEVICE_CHECK in the workspace status word. */
+lmoe_status lmoe_permute(const int32_t *topk_idx, const lmoe_dims *dims, int32_t *counts, int32_t *offsets,
+                         int32_t *perm, int32_t *inv, void *workspace, size_t ws_bytes, void *stream);
+
+/* Scratch bytes lmoe_expert_ffn needs for these dims. */
+size_t lmoe_expert_ffn_workspace_size(const lmoe_dims *dims);
+
+/* Expert compute [MoE], [MX], [L1]: for every position q of perm (pair
+ * p = perm[q], token t = p / k, expert e, gate weight w = topk_w[p]):
+ *   g = Wg[e] x^_t, u = Wu[e] x^_t (fp32 accumulation),
+ *   h^ = MXFP8(silu(g) * u) along I,
+ *   yp[q][:] = w * (Wd[e] h^),
+ * x^_t the MXFP8 activation (xq[T][d] codes, xs[T][d/32] scales, as made by
+ * lmoe_quant_mxfp8), weights in LMOE_LAYOUT_TC, offsets/perm from
+ * lmoe_permute, yp fp32 [T*k][d] in permuted order. */
+lmoe_status lmoe_expert_ffn(const uint8_t *xq, const uint8_t *xs, const lmoe_expert_weights *W,
+                            const int32_t *offsets, const int32_t *perm, const float *topk_w, const lmoe_dims *dims,
+                            float *yp, void *workspace, size_t ws_bytes, void *stream);
+
+/* Combine [EP]: y[t][c] = bf16( sum_{j=0..k-1} yp[inv[t*k+j]][c] ), summed
+ * in fp32 in slot order, rounded to nearest even. */
+lmoe_status lmoe_combine(const float *yp, const int32_t *inv, const lmoe_dims *dims, uint16_t *y_bf16, void *stream);
+
+/* ---- whole layer ----------------------------------------------------------- */
+
+/* Scratch bytes lmoe_forward needs for these dims. */
+size_t lmoe_workspace_size(const lmoe_dims *dims);
+
+/* route -> permute -> MXFP8 activations -> expert FFN -> combine, all on
+ * `stream`.  y bf16 [T][d].  Optional outputs (NULL to skip): topk_idx
+ * [T][k], topk_w [T][k], logits [T][E]. */
+lmoe_status lmoe_forward(const uint16_t *x_bf16, const float *Wr, const float *bias, const lmoe_expert_weights *W,
+                         const lmoe_dims *dims, uint16_t *y_bf16, int32_t *topk_idx, float *topk_w, float *logits,
+                         void *workspace, size_t ws_bytes, void *stream);
+
+/* ---- helpers --------------------------------------------------------------- */
+
+/* Reads (synchronously, after all prior work on the device) the status word
+ * kernels left in `workspace`: LMOE_OK, LMOE_ERR_DEVICE_CHECK or
+ * LMOE_ERR_TIMEOUT into *device_status; returns LMOE_ERR_CUDA if the read
+ * itself fails. */
+lmoe_status lmoe_last_device_status(const void *workspace, int32_t *device_status);
+
+/* Clears the status word (enqueued on `stream`). */
+lmoe_status lmoe_clear_device_status(void *workspace, void *stream);
+
+/* Profiling hook: when set, lmoe_forward records the n = LMOE_NUM_STAGE_EVENTS
+ * CUDA events (cudaEvent_t handles, created by the caller) on its stream at
+ * the stage boundaries: [0] start, [1] after routing, [2] after permute,
+ * [3] after the MXFP8 activation scatter, [4] after the gate/up GEMM,
+ * [5] after the down GEMM, [6] after combine.  n = 0 clears the hook.  The
+ * setting is process-wide and not thread-safe; it only adds event records. */
+#define LMOE_NUM_STAGE_EVENTS 7
+lmoe_status lmoe_set_stage_events(void *const *events, int32_t n);
+
+const char *lmoe_status_string(lmoe_status s);
+
+/* Library build tag (arch and version), e.g. "lmoe 0.1 sm_103a". */
+const char *lmoe_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LMOE_H */

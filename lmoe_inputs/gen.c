@@ -38,8 +38,29 @@ static inline uint64_t stream_key(uint64_t seed, uint64_t stream)
 
 static inline uint64_t draw(uint64_t key, uint64_t ctr) { return mix64(key + (ctr + 1) * GOLDEN_GAMMA); }
 
+/* Series coefficients, computed once by exact-as-possible double division
+ * (the same IEEE operations on every host, so the same bits). */
+static double g_inv_odd[16];     /* 1/(2j+1)          */
+static double g_sin_c[13];       /* (-1)^k/(2k+1)!    */
+static double g_cos_c[13];       /* (-1)^k/(2k)!      */
+static pthread_once_t g_once = PTHREAD_ONCE_INIT;
+
+static void init_tables(void)
+{
+    for (int j = 0; j < 16; ++j) g_inv_odd[j] = 1.0 / (double)(2 * j + 1);
+    double f = 1.0; /* running factorial */
+    for (int k = 0; k < 13; ++k) {
+        double f_even = f;                      /* (2k)!   */
+        double f_odd = f * (double)(2 * k + 1); /* (2k+1)! */
+        g_cos_c[k] = ((k & 1) ? -1.0 : 1.0) / f_even;
+        g_sin_c[k] = ((k & 1) ? -1.0 : 1.0) / f_odd;
+        f = f_odd * (double)(2 * k + 2);
+    }
+}
+
 /* Natural logarithm of a positive finite x: x = m * 2^e with m in [sqrt(1/2), sqrt(2)),
- * ln x = e ln 2 + 2 atanh((m-1)/(m+1)), atanh by its odd power series. */
+ * ln x = e ln 2 + 2 atanh((m-1)/(m+1)), atanh by its odd power series
+ * (|s| <= 0.1716, 16 terms leave < 1e-24). */
 static double det_log(double x)
 {
     int e;
@@ -47,22 +68,22 @@ static double det_log(double x)
     if (m < 0.70710678118654752440) { m *= 2.0; e -= 1; }
     double s = (m - 1.0) / (m + 1.0);
     double s2 = s * s;
-    double term = s, sum = 0.0;
-    for (int k = 1; k <= 41; k += 2) { sum += term / (double)k; term *= s2; }
-    return (double)e * 0.69314718055994530942 + 2.0 * sum;
+    double p = g_inv_odd[15];
+    for (int j = 14; j >= 0; --j) p = p * s2 + g_inv_odd[j];
+    return (double)e * 0.69314718055994530942 + 2.0 * s * p;
 }
 
-/* sin and cos of phi in [0, pi/2] by Taylor series (terms to phi^25). */
+/* sin and cos of phi in [0, pi/2] by their Taylor polynomials (to phi^25 / phi^24). */
 static void det_sincos_quarter(double phi, double *s, double *c)
 {
     double p2 = phi * phi;
-    double ts = phi, tc = 1.0, ss = 0.0, cc = 0.0;
-    for (int k = 0; k < 13; ++k) {
-        ss += ts; cc += tc;
-        ts *= -p2 / (double)((2 * k + 2) * (2 * k + 3));
-        tc *= -p2 / (double)((2 * k + 1) * (2 * k + 2));
+    double ps = g_sin_c[12], pc = g_cos_c[12];
+    for (int k = 11; k >= 0; --k) {
+        ps = ps * p2 + g_sin_c[k];
+        pc = pc * p2 + g_cos_c[k];
     }
-    *s = ss; *c = cc;
+    *s = phi * ps;
+    *c = pc;
 }
 
 /* sin and cos of 2*pi*u for u in [0, 1), reduced to a quarter turn exactly. */
@@ -81,18 +102,18 @@ static void det_sincos_turn(double u, double *s, double *c)
     }
 }
 
-/* Standard normal number `idx` of stream (seed, stream).  Elements 2j and
- * 2j+1 are the two outputs of one Box-Muller pair. */
-static double normal_at(uint64_t key, uint64_t idx)
+/* The Box-Muller pair number `pair` of a stream: standard normals 2*pair
+ * (cosine branch) and 2*pair+1 (sine branch). */
+static void normal_pair(uint64_t key, uint64_t pair, double *z0, double *z1)
 {
-    uint64_t pair = idx >> 1;
     uint64_t r1 = draw(key, 2 * pair), r2 = draw(key, 2 * pair + 1);
     double u1 = ((double)(r1 >> 11) + 0.5) * (1.0 / 9007199254740992.0); /* (0,1) */
     double u2 = (double)(r2 >> 11) * (1.0 / 9007199254740992.0);         /* [0,1) */
     double rad = sqrt(-2.0 * det_log(u1));
     double s, c;
     det_sincos_turn(u2, &s, &c);
-    return (idx & 1) ? rad * s : rad * c;
+    *z0 = rad * c;
+    *z1 = rad * s;
 }
 
 static uint16_t f32_to_bf16_rne(float f)
@@ -111,22 +132,37 @@ typedef struct {
     void *out;
 } job_t;
 
+static void put(job_t *j, uint64_t i, double z)
+{
+    if (j->kind == 0) ((float *)j->out)[i] = (float)(j->sigma * z);
+    else ((uint16_t *)j->out)[i] = f32_to_bf16_rne((float)(j->sigma * z));
+}
+
 static void *run_job(void *arg)
 {
     job_t *j = (job_t *)arg;
-    if (j->kind == 0) {
-        float *o = (float *)j->out;
-        for (uint64_t i = 0; i < j->n; ++i) o[i] = (float)(j->sigma * normal_at(j->key, j->start + i));
-    } else {
-        uint16_t *o = (uint16_t *)j->out;
-        for (uint64_t i = 0; i < j->n; ++i)
-            o[i] = f32_to_bf16_rne((float)(j->sigma * normal_at(j->key, j->start + i)));
+    uint64_t i = 0;
+    double z0, z1;
+    if (j->n && (j->start & 1)) { /* leading odd element: sine branch of its pair */
+        normal_pair(j->key, j->start >> 1, &z0, &z1);
+        put(j, 0, z1);
+        i = 1;
+    }
+    for (; i + 1 < j->n; i += 2) {
+        normal_pair(j->key, (j->start + i) >> 1, &z0, &z1);
+        put(j, i, z0);
+        put(j, i + 1, z1);
+    }
+    if (i < j->n) {
+        normal_pair(j->key, (j->start + i) >> 1, &z0, &z1);
+        put(j, i, z0);
     }
     return NULL;
 }
 
 static void run_parallel(uint64_t key, uint64_t start, uint64_t n, double sigma, int kind, void *out, int threads)
 {
+    pthread_once(&g_once, init_tables);
     if (threads < 1) threads = 1;
     if (threads > 64) threads = 64;
     if (n < (1u << 16)) threads = 1;
@@ -172,8 +208,17 @@ void lmoe_gen_raw_u64(uint64_t seed, uint64_t stream, uint64_t start, uint64_t n
 }
 
 /* The deterministic log / sincos used by Box-Muller, exposed for tests. */
-double lmoe_gen_det_log(double x) { return det_log(x); }
-void lmoe_gen_det_sincos_turn(double u, double *s, double *c) { det_sincos_turn(u, s, c); }
+double lmoe_gen_det_log(double x)
+{
+    pthread_once(&g_once, init_tables);
+    return det_log(x);
+}
+
+void lmoe_gen_det_sincos_turn(double u, double *s, double *c)
+{
+    pthread_once(&g_once, init_tables);
+    det_sincos_turn(u, s, c);
+}
 
 /* exp(y) for finite y: y = n ln2 + f with |f| <= ln2/2, exp(f) by Taylor series,
  * then an exact power-of-two scaling. */
@@ -193,6 +238,7 @@ static double det_exp(double y)
  * (Zipf law with exponent s; expert e has popularity rank e+1). */
 void lmoe_gen_zipf_bias(int E, double s, double beta, float *bias)
 {
+    pthread_once(&g_once, init_tables);
     double z = 0.0;
     for (int r = 1; r <= E; ++r) z += det_exp(-s * det_log((double)r));
     double lnz = det_log(z);

@@ -1,0 +1,76 @@
+"""The C-ABI library: it builds, loads, exports every entry point the public
+header declares, and rejects bad arguments on the host before touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "lmoe.h")
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(lmoe_[a-z0-9_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from top_routing_mxfp4_gb300 import build
+    return ctypes.CDLL(build.build())
+
+
+def test_header_declares_the_layer_calls():
+    names = _declared()
+    for n in ("lmoe_quant_mxfp4", "lmoe_route", "lmoe_permute", "lmoe_expert_ffn", "lmoe_combine", "lmoe_forward"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    missing = [n for n in _declared() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_host_side_argument_checks(lib):
+    from top_routing_mxfp4_gb300 import lmoe
+    D = lmoe.Dims
+    ws_size = lib.lmoe_workspace_size
+    ws_size.restype = ctypes.c_size_t
+    ws_size.argtypes = [ctypes.POINTER(D)]
+    assert ws_size(ctypes.byref(D(64, 3584, 896, 16, 512, 1))) > 0
+    for bad in (D(8, 500, 896, 16, 64, 1), D(8, 512, 896, 33, 64, 1), D(8, 512, 8, 16, 64, 1),
+                D(-1, 512, 896, 16, 64, 1), D(8, 512, 896, 16, 48, 1), D(8, 512, 4096, 16, 64, 1)):
+        assert ws_size(ctypes.byref(bad)) == 0
+    fwd = lib.lmoe_forward
+    fwd.restype = ctypes.c_int
+    good = D(8, 512, 896, 16, 64, 1)
+    # null weights / null pointers / bad dims are refused before any launch
+    assert fwd(None, None, None, None, ctypes.byref(good), None, None, None, None, None, 0, None) == lmoe.ERR_INVALID_ARG
+    assert fwd(None, None, None, None, ctypes.byref(D(8, 500, 896, 16, 64, 1)), None, None, None, None, None, 0,
+               None) == lmoe.ERR_INVALID_ARG
+    # unsupported activation format
+    assert fwd(None, None, None, None, ctypes.byref(D(8, 512, 896, 16, 64, 0)), None, None, None, None, None, 0,
+               None) == lmoe.ERR_UNSUPPORTED
+    # weights in the canonical layout are refused by the expert GEMMs
+    W = lmoe.ExpertWeights(256, 256, 256, 256, 256, 256, lmoe.LAYOUT_CANONICAL)
+    assert fwd(ctypes.c_void_p(256), ctypes.c_void_p(256), None, ctypes.byref(W), ctypes.byref(good),
+               ctypes.c_void_p(256), None, None, None, ctypes.c_void_p(256), 1 << 30, None) == lmoe.ERR_INVALID_ARG
+    # too small a workspace
+    W = lmoe.ExpertWeights(256, 256, 256, 256, 256, 256, lmoe.LAYOUT_TC)
+    assert fwd(ctypes.c_void_p(256), ctypes.c_void_p(256), None, ctypes.byref(W), ctypes.byref(good),
+               ctypes.c_void_p(256), None, None, None, ctypes.c_void_p(256), 16, None) == lmoe.ERR_WORKSPACE
+    # empty batch is a no-op
+    assert fwd(None, None, None, None, ctypes.byref(D(0, 512, 896, 16, 64, 1)), None, None, None, None, None, 0,
+               None) == lmoe.OK
+
+
+def test_mxfp4_byte_counts(lib):
+    from top_routing_mxfp4_gb300 import lmoe
+    assert lmoe.mxfp4_bytes(896, 512, 3584, lmoe.LAYOUT_CANONICAL) == (896 * 512 * 1792, 896 * 512 * 112)
+    assert lmoe.mxfp4_bytes(896, 512, 3584, lmoe.LAYOUT_TC) == (896 * 512 * 1792, 896 * 512 * 112)
+    # K padded to 128, rows to whole 128-row atoms
+    assert lmoe.mxfp4_bytes(2, 64, 64, lmoe.LAYOUT_TC) == (2 * 64 * 64, 2 * 1 * 1 * 512)
+    with pytest.raises(ValueError):
+        lmoe.mxfp4_bytes(1, 8, 48, lmoe.LAYOUT_TC)

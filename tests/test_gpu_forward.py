@@ -1,0 +1,95 @@
+"""End-to-end parity of lmoe_forward (through the C ABI) with the CPU oracle.
+
+Routing is compared bit-exactly given the GPU's own fp32 logits (the oracle's
+top-k runs on them); the layer output must be within 1e-2 of each row's RMS
+(max abs error / rms(y_ref[t])) against the oracle evaluated on the same
+routing.  Large workloads compare a sample of tokens.
+"""
+import numpy as np
+import pytest
+import torch
+
+import lmoe_inputs as gen
+import oracle
+from _util import device_bank, from_dev_bf16, row_rel_err, to_dev_bf16
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+TOL = 1e-2
+
+_banks = {}
+
+
+def _bank(wl):
+    key = (wl.E, wl.d, wl.I, wl.seed)
+    if key not in _banks:
+        _banks.clear()
+        _banks[key] = device_bank(wl, DEV)
+    return _banks[key]
+
+
+def _run_forward(lmoe, wl, x=None):
+    x = gen.x_bf16(wl) if x is None else x
+    bias = gen.router_bias(wl)
+    layer = lmoe.Layer(torch.from_numpy(gen.router_f32(wl)).to(DEV), _bank(wl), k=wl.k,
+                       bias=None if bias is None else torch.from_numpy(bias).to(DEV))
+    T = x.shape[0]
+    idx = torch.empty((T, wl.k), dtype=torch.int32, device=DEV)
+    w = torch.empty((T, wl.k), dtype=torch.float32, device=DEV)
+    logits = torch.empty((T, wl.E), dtype=torch.float32, device=DEV)
+    y = layer.forward(to_dev_bf16(x, DEV), topk_idx=idx, topk_w=w, logits=logits)
+    torch.cuda.synchronize()
+    assert layer.device_status() == 0
+    return x, from_dev_bf16(y), idx.cpu().numpy(), w.cpu().numpy(), logits.cpu().numpy()
+
+
+def _check(wl, x, y, idx, w, logits, tokens):
+    ridx, rw = oracle.topk_softmax(logits, wl.k)
+    np.testing.assert_array_equal(idx, ridx)
+    np.testing.assert_allclose(w, rw, rtol=1e-6, atol=1e-9)
+    ob = oracle.quantize_experts(wl, experts=np.unique(ridx[tokens]))
+    yref = oracle.moe_tokens(x, ridx, rw, ob, wl.d, wl.E, wl.I, tokens=np.asarray(tokens, np.int32))
+    err = row_rel_err(y[tokens], yref)
+    assert err.max() <= TOL, f"max row error {err.max():.3e}"
+    return err
+
+
+def test_forward_tiny_all_tokens(cuda_lib):
+    wl = gen.WORKLOADS["tiny"]
+    x, y, idx, w, lg = _run_forward(cuda_lib, wl)
+    _check(wl, x, y, idx, w, lg, list(range(wl.T)))
+
+
+def test_forward_decode_sampled(cuda_lib):
+    wl = gen.WORKLOADS["decode"]
+    x, y, idx, w, lg = _run_forward(cuda_lib, wl)
+    _check(wl, x, y, idx, w, lg, [0, 1, 17, 33, 62, 63])
+
+
+@pytest.mark.parametrize("T", [1, 3, 131])
+def test_forward_ragged_token_counts(cuda_lib, T):
+    wl = gen.custom(f"ragged{T}", T=T, d=512, I=64)
+    x, y, idx, w, lg = _run_forward(cuda_lib, wl)
+    _check(wl, x, y, idx, w, lg, sorted(set([0, T // 2, T - 1])))
+
+
+def test_forward_ragged_shapes(cuda_lib):
+    wl = gen.custom("oddshape", T=45, d=384, I=160, E=70, k=7)
+    x, y, idx, w, lg = _run_forward(cuda_lib, wl)
+    _check(wl, x, y, idx, w, lg, list(range(0, 45, 4)))
+
+
+def test_forward_zero_input_gives_zero(cuda_lib):
+    wl = gen.WORKLOADS["tiny"]
+    x = np.zeros((4, wl.d), np.uint16)
+    _, y, _, _, _ = _run_forward(cuda_lib, wl, x)
+    assert np.all((y & 0x7FFF) == 0)
+
+
+def test_forward_empty_batch_is_noop(cuda_lib):
+    lmoe = cuda_lib
+    wl = gen.WORKLOADS["tiny"]
+    layer = lmoe.Layer(torch.from_numpy(gen.router_f32(wl)).to(DEV), _bank(wl), k=wl.k)
+    y = layer.forward(torch.empty((0, wl.d), dtype=torch.bfloat16, device=DEV))
+    torch.cuda.synchronize()
+    assert y.shape == (0, wl.d)

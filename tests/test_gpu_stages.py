@@ -1,0 +1,195 @@
+"""Stage-by-stage parity of the CUDA library (through the C ABI) with the CPU oracle.
+
+Integer and byte outputs (quantised codes and scales, top-k indices, the
+permutation) must be bit-exact; floating-point outputs stay within the
+tolerances stated per test.
+"""
+import numpy as np
+import pytest
+import torch
+
+import lmoe_inputs as gen
+import oracle
+from _util import bf16_to_f64, canonical_to_tc, from_dev_bf16, to_dev_bf16
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+def _special_weight_rows(K):
+    """Blocks that hit rounding ties, saturation, zeros, tiny and negative values."""
+    rows = []
+    ties = np.array([4.0, 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, -0.25, -0.75, -5.0, 0.1, -0.1, 0.0, -0.0, 6.0,
+                     7.0, 5.5, 0.2500001, 4.9999, 3.0, 2.0, 1.0, 0.5, -1.5, -3.5, -2.5, 1.4999, 0.7499, 0.2499, 3.25,
+                     -6.5], np.float32)
+    for scale in (1.0, 2.0 ** -60, 2.0 ** 40, 2.0 ** -120):
+        r = np.zeros(K, np.float32)
+        r[:32] = ties * np.float32(scale)
+        rows.append(r)
+    z = np.zeros(K, np.float32)
+    z[32:64] = 1e-42  # subnormal block
+    rows.append(z)
+    return np.stack(rows)
+
+
+@pytest.mark.parametrize("nmat,rows,K", [(1, 5, 256), (3, 200, 96), (2, 128, 3584), (4, 64, 512), (1, 512, 64)])
+def test_quant_mxfp4_bit_exact(cuda_lib, nmat, rows, K):
+    lmoe = cuda_lib
+    rng = np.random.default_rng(nmat * 1000 + rows + K)
+    w = (rng.standard_normal((nmat, rows, K)) * np.exp2(rng.integers(-30, 30, (nmat, rows, 1)))).astype(np.float32)
+    sp = _special_weight_rows(K)
+    n = min(rows, sp.shape[0])
+    w[0, :n] = sp[:n]
+    wd = torch.from_numpy(w).to(DEV)
+    q, s = lmoe.quant_mxfp4(wd, lmoe.LAYOUT_CANONICAL)
+    qt, st = lmoe.quant_mxfp4(wd, lmoe.LAYOUT_TC)
+    torch.cuda.synchronize()
+    oq, os_ = oracle.quant_mxfp4(w.reshape(nmat * rows, K))
+    np.testing.assert_array_equal(s.cpu().numpy(), os_.reshape(-1))
+    np.testing.assert_array_equal(q.cpu().numpy(), oq.reshape(-1))
+    rq, rs = canonical_to_tc(oq, os_, nmat, rows, K)
+    np.testing.assert_array_equal(qt.cpu().numpy(), rq)
+    np.testing.assert_array_equal(st.cpu().numpy(), rs)
+
+
+@pytest.mark.parametrize("rows,K", [(1, 32), (7, 512), (64, 3584), (33, 96)])
+def test_quant_mxfp8_bit_exact(cuda_lib, rows, K):
+    lmoe = cuda_lib
+    x = gen.normal_bf16(1, 40 + rows, 0, rows * K, 1.0).reshape(rows, K)
+    if rows >= 4:
+        x[0, :32] = 0
+        mids = np.array([1.0625, 1.1875, 448.0, 460.0, 2 ** -9, 2 ** -10, 1.5 * 2 ** -9, -1.0625, 0.1, -0.1, 256.0,
+                         300.0, 1e-3, -7.0, 3.0, 5.0], np.float32) / 256.0
+        mids = np.concatenate([mids, np.float32([1.0 / 256.0 * 2.0])])  # amax 2/256 -> X = -15
+        row = np.zeros(32, np.float32)
+        row[:mids.size] = mids
+        row[-1] = 1.0 / 256 * 1.75
+        x[1, :32] = (row.view(np.uint32) >> 16).astype(np.uint16)
+        x[2, :] = gen.normal_bf16(2, 9, 0, K, 1e-36)  # clamped scale byte, e4m3 subnormals
+        x[3, :] = gen.normal_bf16(2, 10, 0, K, 1e30)
+    q, s = lmoe.quant_mxfp8(to_dev_bf16(x, DEV))
+    torch.cuda.synchronize()
+    oq, os_ = oracle.quant_mxfp8(x)
+    np.testing.assert_array_equal(s.cpu().numpy(), os_)
+    np.testing.assert_array_equal(q.cpu().numpy(), oq)
+
+
+def _route_case(lmoe, wl):
+    x = gen.x_bf16(wl)
+    Wr = gen.router_f32(wl)
+    bias = gen.router_bias(wl)
+    bd = None if bias is None else torch.from_numpy(bias).to(DEV)
+    logits, idx, w = lmoe.route(to_dev_bf16(x, DEV), torch.from_numpy(Wr).to(DEV), wl.k, bias=bd)
+    torch.cuda.synchronize()
+    return x, Wr, bias, logits.cpu().numpy(), idx.cpu().numpy(), w.cpu().numpy()
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode", "skewed_small"])
+def test_route_topk_exact_given_logits(cuda_lib, name):
+    lmoe = cuda_lib
+    wl = gen.WORKLOADS.get(name) or gen.custom(name, T=512, d=3584, I=512, zipf_s=1.2, zipf_beta=0.18)
+    x, Wr, bias, lg, idx, w = _route_case(lmoe, wl)
+    # the GPU's fp32 logits are close to the oracle's (fp32 accumulation order only)
+    ref = oracle.router_logits(x, Wr, bias)
+    assert np.max(np.abs(lg - ref)) <= 1e-4 * np.sqrt((ref.astype(np.float64) ** 2).mean())
+    # given identical logits, indices are bit-exact and weights within 1e-6
+    ridx, rw = oracle.topk_softmax(lg, wl.k)
+    np.testing.assert_array_equal(idx, ridx)
+    np.testing.assert_allclose(w, rw, rtol=1e-6, atol=1e-9)
+    # fully independent routing differs only on near-ties of the 16th/17th logit
+    oidx, _ = oracle.topk_softmax(ref, wl.k)
+    bad = np.flatnonzero((np.sort(oidx, 1) != np.sort(idx, 1)).any(1))
+    for t in bad:
+        s = np.sort(ref[t].astype(np.float64))[::-1]
+        assert s[wl.k - 1] - s[wl.k] <= 1e-5 * np.sqrt((ref[t].astype(np.float64) ** 2).mean())
+
+
+def test_topk_ties_and_signed_zero(cuda_lib):
+    lmoe = cuda_lib
+    rng = np.random.default_rng(11)
+    T, E, k = 40, 896, 16
+    l = rng.standard_normal((T, E)).astype(np.float32)
+    l[0] = 0.0
+    l[1, ::2] = -0.0
+    l[2] = np.round(l[2] * 2) / 2
+    l[3, 100:140] = 7.0
+    l[4] = -1e30
+    l[5, 895] = 50.0
+    for E2, k2 in ((896, 16), (32, 32), (1, 1), (2048, 16), (300, 5)):
+        ll = l[:, :E2] if E2 <= E else np.tile(l, (1, 3))[:, :E2].copy()
+        idx, w = lmoe.topk_from_logits(torch.from_numpy(np.ascontiguousarray(ll)).to(DEV), k2)
+        torch.cuda.synchronize()
+        ridx, rw = oracle.topk_softmax(ll, k2)
+        np.testing.assert_array_equal(idx.cpu().numpy(), ridx)
+        np.testing.assert_allclose(w.cpu().numpy(), rw, rtol=1e-6, atol=1e-9)
+
+
+@pytest.mark.parametrize("T,E,k,skew", [(8, 896, 16, 0), (64, 896, 16, 0), (300, 896, 16, 1), (8192, 896, 16, 1),
+                                        (1000, 2048, 8, 0), (1, 4, 4, 0), (0, 896, 16, 0), (5000, 7, 3, 0)])
+def test_permute_bit_exact(cuda_lib, T, E, k, skew):
+    lmoe = cuda_lib
+    rng = np.random.default_rng(T + E + k)
+    if T:
+        score = rng.standard_normal((T, E)) + (skew * 3.0 * -np.log1p(np.arange(E)))[None, :]
+        idx = np.argsort(-score, 1, kind="stable")[:, :k].astype(np.int32)
+    else:
+        idx = np.zeros((0, k), np.int32)
+    counts, offsets, perm, inv, ws = lmoe.permute(torch.from_numpy(idx).to(DEV), E)
+    torch.cuda.synchronize()
+    assert lmoe.last_device_status(ws) == 0
+    rc, ro, rp, ri = oracle.permute(idx, E)
+    np.testing.assert_array_equal(counts.cpu().numpy(), rc)
+    np.testing.assert_array_equal(offsets.cpu().numpy(), ro)
+    np.testing.assert_array_equal(perm.cpu().numpy(), rp)
+    np.testing.assert_array_equal(inv.cpu().numpy(), ri)
+
+
+def test_permute_flags_out_of_range_ids(cuda_lib):
+    lmoe = cuda_lib
+    idx = np.tile(np.arange(16, dtype=np.int32), (10, 1))
+    idx[3, 5] = 896  # out of range
+    counts, offsets, perm, inv, ws = lmoe.permute(torch.from_numpy(idx).to(DEV), 896)
+    torch.cuda.synchronize()
+    assert lmoe.last_device_status(ws) == lmoe.ERR_DEVICE_CHECK
+    assert int(inv[3 * 16 + 5]) == -1 and int(offsets[-1]) == 159
+
+
+def test_combine_slot_order_fp32(cuda_lib):
+    lmoe = cuda_lib
+    rng = np.random.default_rng(12)
+    for T, d, k in ((5, 512, 16), (64, 3584, 16), (3, 128, 1), (1, 256, 32)):
+        P = T * k
+        yp = (rng.standard_normal((P, d)) * 10).astype(np.float32)
+        inv = rng.permutation(P).astype(np.int32)
+        y = lmoe.combine(torch.from_numpy(yp).to(DEV), torch.from_numpy(inv).to(DEV), T, k)
+        torch.cuda.synchronize()
+        acc = np.zeros((T, d), np.float32)
+        for j in range(k):
+            acc = acc + yp[inv.reshape(T, k)[:, j]]
+        ref = torch.from_numpy(acc).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        np.testing.assert_array_equal(from_dev_bf16(y), ref)
+
+
+@pytest.mark.parametrize("name", ["tiny", "ragged"])
+def test_expert_ffn_against_oracle_per_pair(cuda_lib, name):
+    from _util import device_bank
+    lmoe = cuda_lib
+    wl = gen.WORKLOADS["tiny"] if name == "tiny" else gen.custom("ragged", T=37, d=256, I=96, E=40, k=6)
+    x = gen.x_bf16(wl)
+    xd = to_dev_bf16(x, DEV)
+    logits, idx, w = lmoe.route(xd, torch.from_numpy(gen.router_f32(wl)).to(DEV), wl.k)
+    counts, offsets, perm, inv, _ = lmoe.permute(idx, wl.E)
+    xq, xs = lmoe.quant_mxfp8(xd)
+    bank = device_bank(wl, DEV)
+    yp, _ = lmoe.expert_ffn(xq, xs, bank, offsets, perm, w, wl.k)
+    torch.cuda.synchronize()
+    yp, perm_h, idx_h, w_h = yp.cpu().numpy(), perm.cpu().numpy(), idx.cpu().numpy(), w.cpu().numpy()
+    ob = oracle.quantize_experts(wl, experts=np.unique(idx_h))
+    worst = 0.0
+    for q in range(0, wl.P, max(1, wl.P // 64)):
+        p = perm_h[q]
+        t, j = divmod(int(p), wl.k)
+        ref = float(w_h[t, j]) * oracle.expert_ffn_token(x[t], ob, int(idx_h[t, j]), wl.d, wl.I)
+        err = np.max(np.abs(yp[q] - ref)) / np.sqrt((ref ** 2).mean())
+        worst = max(worst, err)
+    assert worst <= 1e-2, worst

@@ -1,0 +1,44 @@
+// Combine ("Kimi K3 Day-0 适配剖析" section 四: collect the expert results back
+// by weight): y[t] = bf16( sum_j yp[inv[t*k + j]] ), slot order, fp32 sums.
+// The gate weight was already applied by the down-projection epilogue.
+#include <cuda_bf16.h>
+
+#include "lmoe_internal.cuh"
+
+namespace lmoe {
+namespace {
+
+__global__ void __launch_bounds__(128) k_combine(const float *__restrict__ yp, const int32_t *__restrict__ inv, int T,
+                                                 int d, int k, uint16_t *__restrict__ y)
+{
+    __shared__ int32_t rows[32];
+    const int t = blockIdx.x;
+    if (threadIdx.x < k) rows[threadIdx.x] = __ldg(inv + int64_t(t) * k + threadIdx.x);
+    __syncthreads();
+    const int nv = d / 4;
+    for (int c = threadIdx.x + blockIdx.y * blockDim.x; c < nv; c += blockDim.x * gridDim.y) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j = 0; j < k; ++j) {
+            const float4 v = __ldg(reinterpret_cast<const float4 *>(yp + int64_t(rows[j]) * d) + c);
+            acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+        }
+        __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+        __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+        uint2 out;
+        out.x = *reinterpret_cast<uint32_t *>(&lo);
+        out.y = *reinterpret_cast<uint32_t *>(&hi);
+        reinterpret_cast<uint2 *>(y + int64_t(t) * d)[c] = out;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const float *yp, const int32_t *inv, int T, int d, int k, uint16_t *y, cudaStream_t st)
+{
+    if (T == 0) return cudaSuccess;
+    const int ysplit = T >= 1024 ? 1 : (T >= 128 ? 2 : 7);  // enough CTAs for small T
+    k_combine<<<dim3(T, ysplit), 128, 0, st>>>(yp, inv, T, d, k, y);
+    return cudaGetLastError();
+}
+
+}  // namespace lmoe

@@ -1,0 +1,170 @@
+// Dispatch metadata ("Kimi K3 Day-0 适配剖析" section 四: index computation and
+// bucketing of token->expert pairs): a stable counting sort of the pair ids
+// p = t*k + j by expert, in three passes with no atomics deciding any order.
+//
+//   1. k_perm_hist    per chunk of CHUNK pairs: histogram over experts
+//                     (shared-memory atomics only count, so order-free).
+//   2. k_perm_scan    per expert: exclusive scan over chunks, counts; then an
+//                     exclusive scan over experts -> offsets; every chunk's
+//                     start position per expert.
+//   3. k_perm_scatter per chunk, 8 warps on 8 consecutive sub-chunks: per-warp
+//                     histograms -> each warp's start per expert; each warp then
+//                     walks its pairs in order, ranking equal experts within a
+//                     32-pair step with __match_any_sync.
+#include "lmoe_internal.cuh"
+
+namespace lmoe {
+namespace {
+
+constexpr int CHUNK = 4096;
+constexpr int WARPS = 8;
+constexpr int SUB = CHUNK / WARPS;  // 512 pairs per warp
+constexpr int MAXE = 2048;
+
+__global__ void __launch_bounds__(256) k_perm_hist(const int32_t *__restrict__ idx, int64_t P, int E,
+                                                   int32_t *__restrict__ blockhist, int32_t *status)
+{
+    __shared__ int32_t h[MAXE];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) h[e] = 0;
+    __syncthreads();
+    const int64_t p0 = int64_t(blockIdx.x) * CHUNK;
+    const int64_t p1 = min(P, p0 + CHUNK);
+    for (int64_t p = p0 + threadIdx.x; p < p1; p += blockDim.x) {
+        const int e = __ldg(idx + p);
+        if (e < 0 || e >= E) set_status(status, LMOE_ERR_DEVICE_CHECK);
+        else atomicAdd(&h[e], 1);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) blockhist[int64_t(blockIdx.x) * E + e] = h[e];
+}
+
+// Single CTA of 1024 threads.
+__global__ void __launch_bounds__(1024) k_perm_scan(int32_t *__restrict__ blockhist, int nblk, int E,
+                                                    int32_t *__restrict__ counts, int32_t *__restrict__ offsets)
+{
+    __shared__ int32_t cnt[MAXE];
+    __shared__ int32_t warp_tot[32];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int32_t run = 0;
+        for (int b = 0; b < nblk; ++b) {
+            const int32_t c = blockhist[int64_t(b) * E + e];
+            blockhist[int64_t(b) * E + e] = run;
+            run += c;
+        }
+        cnt[e] = run;
+        counts[e] = run;
+    }
+    __syncthreads();
+    // exclusive scan of cnt[0..E) -- each thread owns two consecutive entries
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const int i0 = 2 * threadIdx.x;
+    const int32_t a = i0 < E ? cnt[i0] : 0, b = i0 + 1 < E ? cnt[i0 + 1] : 0;
+    int32_t s = a + b, incl = s;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int32_t n = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += n;
+    }
+    if (lane == 31) warp_tot[wid] = incl;
+    __syncthreads();
+    if (wid == 0) {
+        int32_t wt = warp_tot[lane], wi = wt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t n = __shfl_up_sync(0xFFFFFFFFu, wi, o);
+            if (lane >= o) wi += n;
+        }
+        warp_tot[lane] = wi - wt;  // exclusive prefix of warp totals
+    }
+    __syncthreads();
+    const int32_t excl = warp_tot[wid] + incl - s;
+    if (i0 < E) offsets[i0] = excl;
+    if (i0 + 1 < E) offsets[i0 + 1] = excl + a;
+    if (i0 + 1 == E || i0 + 2 == E) offsets[E] = excl + a + (i0 + 1 < E ? b : 0);
+    __syncthreads();
+    // chunk starts: offsets[e] + exclusive count over earlier chunks
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        const int32_t base = offsets[e];
+        for (int bb = 0; bb < nblk; ++bb) blockhist[int64_t(bb) * E + e] += base;
+    }
+}
+
+__global__ void __launch_bounds__(256) k_perm_scatter(const int32_t *__restrict__ idx, int64_t P, int E,
+                                                      const int32_t *__restrict__ blockstart,
+                                                      int32_t *__restrict__ perm, int32_t *__restrict__ inv)
+{
+    extern __shared__ int32_t wh[];  // [WARPS][E] per-warp counts, then cursors
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    for (int i = threadIdx.x; i < WARPS * E; i += blockDim.x) wh[i] = 0;
+    __syncthreads();
+    const int64_t c0 = int64_t(blockIdx.x) * CHUNK;
+    const int64_t s0 = c0 + int64_t(wid) * SUB;
+    const int64_t s1 = min(P, s0 + SUB);
+    int32_t my[SUB / 32];
+#pragma unroll
+    for (int i = 0; i < SUB / 32; ++i) {
+        const int64_t p = s0 + 32 * i + lane;
+        my[i] = p < s1 ? __ldg(idx + p) : -1;
+        if (my[i] >= E) my[i] = -1;  // recorded by k_perm_hist
+        if (my[i] >= 0) atomicAdd(&wh[wid * E + my[i]], 1);
+    }
+    __syncthreads();
+    // per expert: exclusive scan over the warps, plus the chunk start
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int32_t run = blockstart[int64_t(blockIdx.x) * E + e];
+#pragma unroll
+        for (int w = 0; w < WARPS; ++w) {
+            const int32_t c = wh[w * E + e];
+            wh[w * E + e] = run;
+            run += c;
+        }
+    }
+    __syncthreads();
+    int32_t *cur = wh + wid * E;
+    const unsigned lt = (1u << lane) - 1u;
+#pragma unroll
+    for (int i = 0; i < SUB / 32; ++i) {
+        const int e = my[i];
+        const int64_t p = s0 + 32 * i + lane;
+        const unsigned m = __match_any_sync(0xFFFFFFFFu, e);
+        int32_t pos = -1;
+        if (e >= 0) pos = cur[e] + __popc(m & lt);
+        __syncwarp();
+        if (e >= 0 && (m & lt) == 0) cur[e] += __popc(m);
+        __syncwarp();
+        if (p < s1) {
+            inv[p] = pos;
+            if (pos >= 0) perm[pos] = int32_t(p);
+        }
+    }
+}
+
+}  // namespace
+
+size_t permute_scratch_bytes(int64_t P, int E)
+{
+    const int64_t nblk = ceil_div(P, CHUNK);
+    return size_t(round_up(nblk * E * 4, 256));
+}
+
+cudaError_t launch_permute(const int32_t *idx, int64_t P, int E, int32_t *counts, int32_t *offsets, int32_t *perm,
+                           int32_t *inv, void *scratch, int32_t *status, cudaStream_t st)
+{
+    const int nblk = int(ceil_div(P, CHUNK));
+    int32_t *blockhist = static_cast<int32_t *>(scratch);
+    if (nblk > 0) {
+        k_perm_hist<<<nblk, 256, 0, st>>>(idx, P, E, blockhist, status);
+    }
+    k_perm_scan<<<1, 1024, 0, st>>>(blockhist, nblk, E, counts, offsets);
+    if (nblk > 0) {
+        const size_t smem = size_t(WARPS) * E * sizeof(int32_t);
+        if (smem > 48 * 1024) {  // above the default dynamic shared-memory limit (E > 1536)
+            cudaError_t e = cudaFuncSetAttribute(k_perm_scatter, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+            if (e != cudaSuccess) return e;
+        }
+        k_perm_scatter<<<nblk, 256, smem, st>>>(idx, P, E, blockhist, perm, inv);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace lmoe

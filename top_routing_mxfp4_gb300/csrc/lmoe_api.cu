@@ -1,0 +1,308 @@
+// C ABI of the lmoe library: argument checks, workspace carving, launches.
+// Every entry point validates before it enqueues anything, so an argument
+// error leaves all outputs untouched.
+#include <stdio.h>
+
+#include "lmoe_internal.cuh"
+
+using namespace lmoe;
+
+namespace {
+
+constexpr int32_t kStatusBytes = 256;
+
+cudaEvent_t g_stage_events[LMOE_NUM_STAGE_EVENTS] = {};
+bool g_stage_events_on = false;
+
+cudaError_t mark(int i, cudaStream_t st)
+{
+    return g_stage_events_on ? cudaEventRecord(g_stage_events[i], st) : cudaSuccess;
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool dims_ok(const lmoe_dims *d)
+{
+    if (!d) return false;
+    if (d->T < 0 || d->d <= 0 || d->E <= 0 || d->k <= 0 || d->I <= 0) return false;
+    if (d->d % 128 != 0 || d->I % 32 != 0) return false;
+    if (d->k > 32 || d->k > d->E || d->E > 2048) return false;
+    if (int64_t(d->T) * d->k > INT32_MAX / 2) return false;
+    return true;
+}
+
+lmoe_status act_ok(const lmoe_dims *d) { return d->act == LMOE_ACT_MXFP8 ? LMOE_OK : LMOE_ERR_UNSUPPORTED; }
+
+lmoe_status cuda_status(cudaError_t e)
+{
+    if (e == cudaSuccess) return LMOE_OK;
+    fprintf(stderr, "lmoe: CUDA error %s\n", cudaGetErrorString(e));
+    return LMOE_ERR_CUDA;
+}
+
+bool weights_ok(const lmoe_expert_weights *W)
+{
+    if (!W || W->layout != LMOE_LAYOUT_TC) return false;
+    const uint8_t *codes[3] = {W->gate_q, W->up_q, W->down_q};
+    const uint8_t *scales[3] = {W->gate_s, W->up_s, W->down_s};
+    for (int i = 0; i < 3; ++i)
+        if (!codes[i] || !scales[i] || !aligned(codes[i], 32) || !aligned(scales[i], 16)) return false;
+    return true;
+}
+
+// Workspace layout of lmoe_forward (each region 256-byte aligned):
+//   status | logits | idx | w | counts | offsets | perm | inv | permute scratch
+//   | xq sorted | xs sorted | ffn scratch | yp
+struct FwdLayout {
+    size_t status, logits, idx, w, counts, offsets, perm, inv, pscratch, xq, xs, fscratch, yp, total;
+};
+
+FwdLayout fwd_layout(const lmoe_dims *d)
+{
+    const int64_t T = d->T, P = T * d->k, E = d->E;
+    FwdLayout L{};
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        size_t o = off;
+        off += size_t(round_up(int64_t(bytes), 256));
+        return o;
+    };
+    L.status = take(kStatusBytes);
+    L.logits = take(size_t(T * E * 4));
+    L.idx = take(size_t(P * 4));
+    L.w = take(size_t(P * 4));
+    L.counts = take(size_t(E * 4));
+    L.offsets = take(size_t((E + 1) * 4));
+    L.perm = take(size_t(P * 4));
+    L.inv = take(size_t(P * 4));
+    L.pscratch = take(permute_scratch_bytes(P, int(E)));
+    L.xq = take(size_t(P * d->d));
+    L.xs = take(size_t(P * (d->d / 32)));
+    L.fscratch = take(ffn_scratch_bytes(P, d->d, int(E), d->I));
+    L.yp = take(size_t(P * d->d * 4));
+    L.total = off;
+    return L;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *lmoe_version(void) { return "lmoe 0.1 sm_103a"; }
+
+const char *lmoe_status_string(lmoe_status s)
+{
+    switch (s) {
+    case LMOE_OK: return "ok";
+    case LMOE_ERR_INVALID_ARG: return "invalid argument";
+    case LMOE_ERR_UNSUPPORTED: return "unsupported";
+    case LMOE_ERR_WORKSPACE: return "workspace missing or too small";
+    case LMOE_ERR_CUDA: return "CUDA error";
+    case LMOE_ERR_DEVICE_CHECK: return "device-side input check failed";
+    case LMOE_ERR_TIMEOUT: return "device-side bounded wait timed out";
+    }
+    return "unknown status";
+}
+
+size_t lmoe_mxfp4_bytes(int64_t nmat, int32_t rows, int32_t K, int32_t layout, size_t *scale_bytes)
+{
+    if (nmat < 0 || rows <= 0 || K <= 0 || K % 32 != 0) return 0;
+    if (layout == LMOE_LAYOUT_CANONICAL) {
+        if (scale_bytes) *scale_bytes = size_t(nmat) * rows * (K / 32);
+        return size_t(nmat) * rows * (K / 2);
+    }
+    if (layout == LMOE_LAYOUT_TC) {
+        const int64_t Kp = round_up(K, 128);
+        if (scale_bytes) *scale_bytes = size_t(nmat) * ceil_div(rows, 128) * (Kp / 128) * 512;
+        return size_t(nmat) * rows * (Kp / 2);
+    }
+    return 0;
+}
+
+lmoe_status lmoe_quant_mxfp4(const float *w, int64_t nmat, int32_t rows, int32_t K, uint8_t *q, uint8_t *s,
+                             int32_t layout, void *stream)
+{
+    if (nmat < 0 || rows <= 0 || K <= 0 || K % 32 != 0) return LMOE_ERR_INVALID_ARG;
+    if (layout != LMOE_LAYOUT_CANONICAL && layout != LMOE_LAYOUT_TC) return LMOE_ERR_INVALID_ARG;
+    if (nmat == 0) return LMOE_OK;
+    if (!w || !q || !s || !aligned(w, 16) || !aligned(q, 32) || !aligned(s, 16)) return LMOE_ERR_INVALID_ARG;
+    return cuda_status(launch_quant_mxfp4(w, nmat, rows, K, q, s, layout, cudaStream_t(stream)));
+}
+
+lmoe_status lmoe_quant_mxfp8(const uint16_t *x_bf16, int64_t rows, int32_t K, uint8_t *q, uint8_t *s, void *stream)
+{
+    if (rows < 0 || K <= 0 || K % 32 != 0) return LMOE_ERR_INVALID_ARG;
+    if (rows == 0) return LMOE_OK;
+    if (!x_bf16 || !q || !s || !aligned(x_bf16, 16) || !aligned(q, 16)) return LMOE_ERR_INVALID_ARG;
+    return cuda_status(launch_quant_mxfp8(x_bf16, rows, K, q, s, cudaStream_t(stream)));
+}
+
+lmoe_status lmoe_route(const uint16_t *x_bf16, const float *Wr, const float *bias, const lmoe_dims *dims,
+                       float *logits, int32_t *topk_idx, float *topk_w, void *stream)
+{
+    if (!dims_ok(dims)) return LMOE_ERR_INVALID_ARG;
+    if (dims->T == 0) return LMOE_OK;
+    if (!x_bf16 || !Wr || !logits || !topk_idx || !topk_w) return LMOE_ERR_INVALID_ARG;
+    cudaStream_t st = cudaStream_t(stream);
+    cudaError_t e = launch_router_logits(x_bf16, Wr, bias, dims->T, dims->d, dims->E, logits, st);
+    if (e == cudaSuccess) e = launch_topk_softmax(logits, dims->T, dims->E, dims->k, topk_idx, topk_w, st);
+    return cuda_status(e);
+}
+
+lmoe_status lmoe_topk_from_logits(const float *logits, const lmoe_dims *dims, int32_t *topk_idx, float *topk_w,
+                                  void *stream)
+{
+    if (!dims_ok(dims)) return LMOE_ERR_INVALID_ARG;
+    if (dims->T == 0) return LMOE_OK;
+    if (!logits || !topk_idx || !topk_w) return LMOE_ERR_INVALID_ARG;
+    return cuda_status(launch_topk_softmax(logits, dims->T, dims->E, dims->k, topk_idx, topk_w, cudaStream_t(stream)));
+}
+
+size_t lmoe_permute_workspace_size(const lmoe_dims *dims)
+{
+    if (!dims_ok(dims)) return 0;
+    return kStatusBytes + permute_scratch_bytes(int64_t(dims->T) * dims->k, dims->E);
+}
+
+lmoe_status lmoe_permute(const int32_t *topk_idx, const lmoe_dims *dims, int32_t *counts, int32_t *offsets,
+                         int32_t *perm, int32_t *inv, void *workspace, size_t ws_bytes, void *stream)
+{
+    if (!dims_ok(dims)) return LMOE_ERR_INVALID_ARG;
+    if (!counts || !offsets || (dims->T > 0 && (!topk_idx || !perm || !inv))) return LMOE_ERR_INVALID_ARG;
+    if (!workspace || ws_bytes < lmoe_permute_workspace_size(dims) || !aligned(workspace, 256))
+        return LMOE_ERR_WORKSPACE;
+    char *ws = static_cast<char *>(workspace);
+    cudaError_t e0 = cudaMemsetAsync(ws, 0, sizeof(int32_t), cudaStream_t(stream));
+    if (e0 != cudaSuccess) return cuda_status(e0);
+    return cuda_status(launch_permute(topk_idx, int64_t(dims->T) * dims->k, dims->E, counts, offsets, perm, inv,
+                                      ws + kStatusBytes, reinterpret_cast<int32_t *>(ws), cudaStream_t(stream)));
+}
+
+size_t lmoe_expert_ffn_workspace_size(const lmoe_dims *dims)
+{
+    if (!dims_ok(dims)) return 0;
+    const int64_t P = int64_t(dims->T) * dims->k;
+    return kStatusBytes + size_t(round_up(P * dims->d, 256) + round_up(P * (dims->d / 32), 256)) +
+           ffn_scratch_bytes(P, dims->d, dims->E, dims->I);
+}
+
+lmoe_status lmoe_expert_ffn(const uint8_t *xq, const uint8_t *xs, const lmoe_expert_weights *W,
+                            const int32_t *offsets, const int32_t *perm, const float *topk_w, const lmoe_dims *dims,
+                            float *yp, void *workspace, size_t ws_bytes, void *stream)
+{
+    if (!dims_ok(dims)) return LMOE_ERR_INVALID_ARG;
+    lmoe_status a = act_ok(dims);
+    if (a != LMOE_OK) return a;
+    if (dims->T == 0) return LMOE_OK;
+    if (!xq || !xs || !offsets || !perm || !topk_w || !yp || !aligned(xq, 16) || !aligned(yp, 16))
+        return LMOE_ERR_INVALID_ARG;
+    if (!weights_ok(W)) return LMOE_ERR_INVALID_ARG;
+    if (!workspace || ws_bytes < lmoe_expert_ffn_workspace_size(dims) || !aligned(workspace, 256))
+        return LMOE_ERR_WORKSPACE;
+    const int64_t P = int64_t(dims->T) * dims->k;
+    char *ws = static_cast<char *>(workspace);
+    uint8_t *xq_sorted = reinterpret_cast<uint8_t *>(ws + kStatusBytes);
+    uint8_t *xs_sorted = xq_sorted + round_up(P * dims->d, 256);
+    void *fscratch = xs_sorted + round_up(P * (dims->d / 32), 256);
+    cudaStream_t st = cudaStream_t(stream);
+    cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(int32_t), st);
+    if (e == cudaSuccess) e = launch_gather_rows(xq, xs, dims->T, dims->d, dims->k, perm, xq_sorted, xs_sorted, st);
+    if (e != cudaSuccess) return cuda_status(e);
+    FfnArgs f{xq_sorted, xs_sorted, W, offsets, perm, topk_w, int(P), dims->d, dims->E, dims->k, dims->I,
+              yp, fscratch, reinterpret_cast<int32_t *>(ws)};
+    return cuda_status(launch_expert_ffn(f, st));
+}
+
+lmoe_status lmoe_combine(const float *yp, const int32_t *inv, const lmoe_dims *dims, uint16_t *y_bf16, void *stream)
+{
+    if (!dims_ok(dims)) return LMOE_ERR_INVALID_ARG;
+    if (dims->T == 0) return LMOE_OK;
+    if (!yp || !inv || !y_bf16 || !aligned(yp, 16) || !aligned(y_bf16, 16)) return LMOE_ERR_INVALID_ARG;
+    return cuda_status(launch_combine(yp, inv, dims->T, dims->d, dims->k, y_bf16, cudaStream_t(stream)));
+}
+
+size_t lmoe_workspace_size(const lmoe_dims *dims)
+{
+    if (!dims_ok(dims)) return 0;
+    return fwd_layout(dims).total;
+}
+
+lmoe_status lmoe_forward(const uint16_t *x_bf16, const float *Wr, const float *bias, const lmoe_expert_weights *W,
+                         const lmoe_dims *dims, uint16_t *y_bf16, int32_t *topk_idx, float *topk_w, float *logits,
+                         void *workspace, size_t ws_bytes, void *stream)
+{
+    if (!dims_ok(dims)) return LMOE_ERR_INVALID_ARG;
+    lmoe_status a = act_ok(dims);
+    if (a != LMOE_OK) return a;
+    if (dims->T == 0) return LMOE_OK;
+    if (!x_bf16 || !Wr || !y_bf16 || !aligned(x_bf16, 16) || !aligned(y_bf16, 16)) return LMOE_ERR_INVALID_ARG;
+    if (!weights_ok(W)) return LMOE_ERR_INVALID_ARG;
+    const FwdLayout L = fwd_layout(dims);
+    if (!workspace || ws_bytes < L.total || !aligned(workspace, 256)) return LMOE_ERR_WORKSPACE;
+    char *ws = static_cast<char *>(workspace);
+    cudaStream_t st = cudaStream_t(stream);
+    const int T = dims->T, E = dims->E, k = dims->k, d = dims->d;
+    const int64_t P = int64_t(T) * k;
+    float *lg = logits ? logits : reinterpret_cast<float *>(ws + L.logits);
+    int32_t *idx = topk_idx ? topk_idx : reinterpret_cast<int32_t *>(ws + L.idx);
+    float *w = topk_w ? topk_w : reinterpret_cast<float *>(ws + L.w);
+    int32_t *counts = reinterpret_cast<int32_t *>(ws + L.counts);
+    int32_t *offsets = reinterpret_cast<int32_t *>(ws + L.offsets);
+    int32_t *perm = reinterpret_cast<int32_t *>(ws + L.perm);
+    int32_t *inv = reinterpret_cast<int32_t *>(ws + L.inv);
+    uint8_t *xq = reinterpret_cast<uint8_t *>(ws + L.xq);
+    uint8_t *xs = reinterpret_cast<uint8_t *>(ws + L.xs);
+    float *yp = reinterpret_cast<float *>(ws + L.yp);
+    int32_t *status = reinterpret_cast<int32_t *>(ws + L.status);
+
+    cudaError_t e = mark(0, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(status, 0, sizeof(int32_t), st);
+    if (e == cudaSuccess) e = launch_router_logits(x_bf16, Wr, bias, T, d, E, lg, st);
+    if (e == cudaSuccess) e = launch_topk_softmax(lg, T, E, k, idx, w, st);
+    if (e == cudaSuccess) e = mark(1, st);
+    if (e == cudaSuccess) e = launch_permute(idx, P, E, counts, offsets, perm, inv, ws + L.pscratch, status, st);
+    if (e == cudaSuccess) e = mark(2, st);
+    if (e == cudaSuccess) e = launch_quant_mxfp8_scatter(x_bf16, T, d, k, inv, xq, xs, st);
+    if (e == cudaSuccess) e = mark(3, st);
+    if (e == cudaSuccess) {
+        FfnArgs f{xq, xs, W, offsets, perm, w, int(P), d, E, k, dims->I, yp, ws + L.fscratch, status};
+        e = launch_expert_ffn(f, st, g_stage_events_on ? g_stage_events[4] : nullptr);
+    }
+    if (e == cudaSuccess) e = mark(5, st);
+    if (e == cudaSuccess) e = launch_combine(yp, inv, T, d, k, y_bf16, st);
+    if (e == cudaSuccess) e = mark(6, st);
+    return cuda_status(e);
+}
+
+lmoe_status lmoe_set_stage_events(void *const *events, int32_t n)
+{
+    if (n == 0) {
+        g_stage_events_on = false;
+        return LMOE_OK;
+    }
+    if (n != LMOE_NUM_STAGE_EVENTS || !events) return LMOE_ERR_INVALID_ARG;
+    for (int i = 0; i < n; ++i)
+        if (!events[i]) return LMOE_ERR_INVALID_ARG;
+    for (int i = 0; i < n; ++i) g_stage_events[i] = cudaEvent_t(events[i]);
+    g_stage_events_on = true;
+    return LMOE_OK;
+}
+
+lmoe_status lmoe_last_device_status(const void *workspace, int32_t *device_status)
+{
+    if (!workspace || !device_status) return LMOE_ERR_INVALID_ARG;
+    int32_t v = 0;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = cudaMemcpy(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_status(e);
+    *device_status = v;
+    return LMOE_OK;
+}
+
+lmoe_status lmoe_clear_device_status(void *workspace, void *stream)
+{
+    if (!workspace) return LMOE_ERR_INVALID_ARG;
+    return cuda_status(cudaMemsetAsync(workspace, 0, sizeof(int32_t), cudaStream_t(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,129 @@
+// Internal declarations shared by the lmoe CUDA translation units.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/lmoe.h"
+
+namespace lmoe {
+
+// ---- status word (first 4 bytes of a workspace) ---------------------------------
+// Kernels record the first error they see; the host reads it back with
+// lmoe_last_device_status.
+__device__ __forceinline__ void set_status(int32_t *status, int32_t code)
+{
+    if (status) atomicCAS(status, 0, code);
+}
+
+// ---- small numeric helpers ----------------------------------------------------------
+__device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) { return __uint_as_float(uint32_t(b) << 16); }
+
+// Shared block exponent as an E8M0 byte: clamp(floor(log2 amax) - emax + 127, 0, 254),
+// 0 for amax == 0.  floor(log2) is read from the fp32 bit pattern (normals:
+// exponent field - 127; subnormals: position of the leading mantissa bit).
+__device__ __forceinline__ uint32_t mx_scale_byte(float amax, int emax)
+{
+    uint32_t u = __float_as_uint(amax) & 0x7FFFFFFFu;
+    if (u == 0) return 0;
+    int ex = int(u >> 23);
+    int fl = ex ? ex - 127 : (31 - __clz(u)) - 149;
+    int b = fl - emax + 127;
+    return uint32_t(b < 0 ? 0 : (b > 254 ? 254 : b));
+}
+
+// 2^(127 - byte) as fp32 (byte in [0, 254] -> exponent in [-127, 127]); the
+// multiplier that divides a block by its scale.  2^-127 is a subnormal.
+__device__ __forceinline__ float mx_inv_scale(uint32_t byte)
+{
+    int e = 127 - int(byte);  // in [-127, 127]
+    return e >= -126 ? __uint_as_float(uint32_t(e + 127) << 23) : __uint_as_float(0x00400000u);
+}
+
+// 2^(byte - 127) as fp32 (decode of an E8M0 byte in [0, 254]).
+__device__ __forceinline__ float e8m0_to_f32(uint32_t byte)
+{
+    return byte ? __uint_as_float(byte << 23) : __uint_as_float(0x00400000u);
+}
+
+// Eight fp32 values (already divided by the block scale) -> eight e2m1 codes
+// packed in a 32-bit word, element i in nibble i.  Hardware conversion:
+// round to nearest even, saturate to the largest finite value.
+__device__ __forceinline__ uint32_t e2m1x8(const float *v)
+{
+    uint32_t out;
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+        "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+        : "=r"(out)
+        : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
+    return out;
+}
+
+// Two fp32 values -> two e4m3 codes (lo in the low byte), round to nearest
+// even, saturate to +-448.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi)
+{
+    uint16_t out;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %2, %1;" : "=h"(out) : "f"(lo), "f"(hi));
+    return out;
+}
+
+// Four fp32 -> four e4m3 codes in one word (element i in byte i).
+__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d)
+{
+    return e4m3x2(a, b) | (e4m3x2(c, d) << 16);
+}
+
+// e4m3 byte -> fp32 via the hardware f16x2 conversion (exact).
+__device__ __forceinline__ float e4m3_to_f32(uint32_t code)
+{
+    uint32_t h2;
+    uint16_t in = uint16_t(code & 0xFF);
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(in));
+    return __half2float(__ushort_as_half(uint16_t(h2 & 0xFFFF)));
+}
+
+__host__ __device__ constexpr int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+__host__ __device__ constexpr int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
+
+// ---- host-side launch wrappers (each returns cudaError_t of the launch) --------------
+cudaError_t launch_quant_mxfp4(const float *w, int64_t nmat, int rows, int K, uint8_t *q, uint8_t *s, int layout,
+                               cudaStream_t st);
+cudaError_t launch_quant_mxfp8(const uint16_t *x, int64_t rows, int K, uint8_t *q, uint8_t *s, cudaStream_t st);
+// x[T][d] -> MXFP8 rows written at the k permuted positions inv[t*k + j].
+cudaError_t launch_quant_mxfp8_scatter(const uint16_t *x, int T, int d, int k, const int32_t *inv, uint8_t *q_sorted,
+                                       uint8_t *s_sorted, cudaStream_t st);
+// rows of xq/xs [T][...] gathered into permuted order (row q <- token perm[q]/k).
+cudaError_t launch_gather_rows(const uint8_t *xq, const uint8_t *xs, int T, int d, int k, const int32_t *perm,
+                               uint8_t *q_sorted, uint8_t *s_sorted, cudaStream_t st);
+
+cudaError_t launch_router_logits(const uint16_t *x, const float *Wr, const float *bias, int T, int d, int E,
+                                 float *logits, cudaStream_t st);
+cudaError_t launch_topk_softmax(const float *logits, int T, int E, int k, int32_t *idx, float *w, cudaStream_t st);
+
+size_t permute_scratch_bytes(int64_t P, int E);
+cudaError_t launch_permute(const int32_t *idx, int64_t P, int E, int32_t *counts, int32_t *offsets, int32_t *perm,
+                           int32_t *inv, void *scratch, int32_t *status, cudaStream_t st);
+
+struct FfnArgs {
+    const uint8_t *xq_sorted, *xs_sorted;  // [P][d], [P][d/32]
+    const lmoe_expert_weights *W;
+    const int32_t *offsets, *perm;
+    const float *topk_w;
+    int P, d, E, k, I;
+    float *yp;        // [P][d]
+    void *scratch;    // ffn_scratch_bytes
+    int32_t *status;
+};
+size_t ffn_scratch_bytes(int64_t P, int d, int E, int I);
+// gate/up GEMM + SwiGLU + MXFP8 of h, then (after `mid`, if not null) the down GEMM.
+cudaError_t launch_expert_ffn(const FfnArgs &a, cudaStream_t st, cudaEvent_t mid = nullptr);
+
+cudaError_t launch_combine(const float *yp, const int32_t *inv, int T, int d, int k, uint16_t *y, cudaStream_t st);
+
+}  // namespace lmoe

@@ -1,0 +1,325 @@
+"""ctypes binding of liblmoe.so, the LatentMoE layer's C ABI (include/lmoe.h).
+
+Argument marshalling only: every function takes torch CUDA tensors, checks
+shapes and dtypes, and passes `data_ptr()` plus the current CUDA stream to
+the C entry point of the same name.  All arithmetic runs in the library's
+CUDA kernels.  Importing this module fails loudly when the library has not
+been built (there is no fallback path).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "liblmoe.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"{LIB_PATH} is missing: build it with `python -c \"import __graft_entry__ as g; g.build()\"` "
+                      "or `python top_routing_mxfp4_gb300/build.py`")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+OK = 0
+ERR_INVALID_ARG = -1
+ERR_UNSUPPORTED = -2
+ERR_WORKSPACE = -3
+ERR_CUDA = -4
+ERR_DEVICE_CHECK = -5
+ERR_TIMEOUT = -6
+ACT_MXFP8 = 1
+LAYOUT_CANONICAL = 0
+LAYOUT_TC = 1
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int32), ("d", ctypes.c_int32), ("E", ctypes.c_int32), ("k", ctypes.c_int32),
+                ("I", ctypes.c_int32), ("act", ctypes.c_int32)]
+
+
+class ExpertWeights(ctypes.Structure):
+    _fields_ = [("gate_q", ctypes.c_void_p), ("gate_s", ctypes.c_void_p), ("up_q", ctypes.c_void_p),
+                ("up_s", ctypes.c_void_p), ("down_q", ctypes.c_void_p), ("down_s", ctypes.c_void_p),
+                ("layout", ctypes.c_int32)]
+
+
+_vp, _i32, _i64, _sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+_DP, _WP = ctypes.POINTER(Dims), ctypes.POINTER(ExpertWeights)
+
+
+def _sig(name, restype, *argtypes):
+    f = getattr(_lib, name)
+    f.restype = restype
+    f.argtypes = list(argtypes)
+    return f
+
+
+_lib_version = _sig("lmoe_version", ctypes.c_char_p)
+_status_string = _sig("lmoe_status_string", ctypes.c_char_p, ctypes.c_int)
+_mxfp4_bytes = _sig("lmoe_mxfp4_bytes", _sz, _i64, _i32, _i32, _i32, ctypes.POINTER(_sz))
+_quant_mxfp4 = _sig("lmoe_quant_mxfp4", ctypes.c_int, _vp, _i64, _i32, _i32, _vp, _vp, _i32, _vp)
+_quant_mxfp8 = _sig("lmoe_quant_mxfp8", ctypes.c_int, _vp, _i64, _i32, _vp, _vp, _vp)
+_route = _sig("lmoe_route", ctypes.c_int, _vp, _vp, _vp, _DP, _vp, _vp, _vp, _vp)
+_topk = _sig("lmoe_topk_from_logits", ctypes.c_int, _vp, _DP, _vp, _vp, _vp)
+_perm_ws = _sig("lmoe_permute_workspace_size", _sz, _DP)
+_permute = _sig("lmoe_permute", ctypes.c_int, _vp, _DP, _vp, _vp, _vp, _vp, _vp, _sz, _vp)
+_ffn_ws = _sig("lmoe_expert_ffn_workspace_size", _sz, _DP)
+_ffn = _sig("lmoe_expert_ffn", ctypes.c_int, _vp, _vp, _WP, _vp, _vp, _vp, _DP, _vp, _vp, _sz, _vp)
+_combine = _sig("lmoe_combine", ctypes.c_int, _vp, _vp, _DP, _vp, _vp)
+_ws_size = _sig("lmoe_workspace_size", _sz, _DP)
+_forward = _sig("lmoe_forward", ctypes.c_int, _vp, _vp, _vp, _WP, _DP, _vp, _vp, _vp, _vp, _vp, _sz, _vp)
+_last_status = _sig("lmoe_last_device_status", ctypes.c_int, _vp, ctypes.POINTER(_i32))
+_clear_status = _sig("lmoe_clear_device_status", ctypes.c_int, _vp, _vp)
+_set_events = _sig("lmoe_set_stage_events", ctypes.c_int, ctypes.POINTER(_vp), _i32)
+NUM_STAGE_EVENTS = 7
+STAGES = ("route", "permute", "act_quant", "gate_up", "down", "combine")
+
+
+def set_stage_events(events):
+    """Record these torch.cuda.Event objects at lmoe_forward's stage boundaries
+    (start, after route, permute, activation scatter, gate/up GEMM, down GEMM,
+    combine); None clears the hook."""
+    if events is None:
+        _check(_set_events(None, 0), "lmoe_set_stage_events")
+        return
+    assert len(events) == NUM_STAGE_EVENTS
+    arr = (_vp * NUM_STAGE_EVENTS)(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    _check(_set_events(arr, NUM_STAGE_EVENTS), "lmoe_set_stage_events")
+
+
+class LmoeError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {status_string(code)} ({code})")
+        self.code = code
+
+
+def status_string(code: int) -> str:
+    return _status_string(code).decode()
+
+
+def version() -> str:
+    return _lib_version().decode()
+
+
+def _check(code: int, what: str):
+    if code != OK:
+        raise LmoeError(code, what)
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _need(t, dtype, shape, name):
+    if t.dtype != dtype or tuple(t.shape) != tuple(shape) or not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name}: expected contiguous CUDA {dtype} {tuple(shape)}, got {t.dtype} "
+                         f"{tuple(t.shape)} on {t.device}")
+
+
+def dims(T: int, d: int, E: int, k: int, I: int, act: int = ACT_MXFP8) -> Dims:
+    return Dims(T, d, E, k, I, act)
+
+
+def _empty(shape, dtype, device):
+    return torch.empty(shape, dtype=dtype, device=device)
+
+
+def workspace(nbytes: int, device) -> torch.Tensor:
+    # torch's caching allocator returns 512-byte aligned blocks
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+# ---- load-time conversion ----------------------------------------------------------
+
+def mxfp4_bytes(nmat: int, rows: int, K: int, layout: int):
+    sb = _sz()
+    qb = _mxfp4_bytes(nmat, rows, K, layout, ctypes.byref(sb))
+    if qb == 0 and nmat > 0:
+        raise ValueError("bad MXFP4 matrix sizes")
+    return int(qb), int(sb.value)
+
+
+def quant_mxfp4(w: torch.Tensor, layout: int = LAYOUT_TC, q=None, s=None, stream=None):
+    """fp32 [nmat, rows, K] (or [rows, K]) -> (codes, scales) as flat uint8 tensors."""
+    w3 = w if w.dim() == 3 else w.unsqueeze(0)
+    nmat, rows, K = w3.shape
+    _need(w3, torch.float32, (nmat, rows, K), "w")
+    qb, sb = mxfp4_bytes(nmat, rows, K, layout)
+    q = _empty(qb, torch.uint8, w.device) if q is None else q
+    s = _empty(sb, torch.uint8, w.device) if s is None else s
+    assert q.numel() >= qb and s.numel() >= sb
+    _check(_quant_mxfp4(_ptr(w3), nmat, rows, K, _ptr(q), _ptr(s), layout, _stream(stream)), "lmoe_quant_mxfp4")
+    return q, s
+
+
+def quant_mxfp8(x: torch.Tensor, stream=None):
+    """bf16 [rows, K] -> (e4m3 codes uint8 [rows, K], scales uint8 [rows, K/32])."""
+    rows, K = x.shape
+    _need(x, torch.bfloat16, (rows, K), "x")
+    q = _empty((rows, K), torch.uint8, x.device)
+    s = _empty((rows, K // 32), torch.uint8, x.device)
+    _check(_quant_mxfp8(_ptr(x), rows, K, _ptr(q), _ptr(s), _stream(stream)), "lmoe_quant_mxfp8")
+    return q, s
+
+
+class ExpertBank:
+    """An expert bank in the tensor-core MXFP4 layout, resident on the device.
+
+    Built matrix by matrix from fp32 weights (load-time conversion), so the
+    fp32 copy of the whole bank never has to exist on the device."""
+
+    def __init__(self, E: int, d: int, I: int, device):
+        self.E, self.d, self.I = E, d, I
+        self.device = torch.device(device)
+        gqb, gsb = mxfp4_bytes(E, I, d, LAYOUT_TC)
+        dqb, dsb = mxfp4_bytes(E, d, I, LAYOUT_TC)
+        self.gate_q, self.gate_s = _empty(gqb, torch.uint8, device), _empty(gsb, torch.uint8, device)
+        self.up_q, self.up_s = _empty(gqb, torch.uint8, device), _empty(gsb, torch.uint8, device)
+        self.down_q, self.down_s = _empty(dqb, torch.uint8, device), _empty(dsb, torch.uint8, device)
+        self._struct = None
+
+    @property
+    def nbytes(self) -> int:
+        return sum(t.numel() for t in (self.gate_q, self.gate_s, self.up_q, self.up_s, self.down_q, self.down_s))
+
+    def load(self, which: str, e0: int, w: torch.Tensor, stream=None):
+        """Quantise fp32 weights of experts [e0, e0 + w.shape[0]) into the bank."""
+        n = w.shape[0]
+        if which in ("gate", "up"):
+            rows, K = self.I, self.d
+        else:
+            rows, K = self.d, self.I
+        qb1, sb1 = mxfp4_bytes(1, rows, K, LAYOUT_TC)
+        q = getattr(self, which + "_q")[e0 * qb1:(e0 + n) * qb1]
+        s = getattr(self, which + "_s")[e0 * sb1:(e0 + n) * sb1]
+        quant_mxfp4(w.reshape(n, rows, K), LAYOUT_TC, q, s, stream)
+
+    def struct(self) -> ExpertWeights:
+        if self._struct is None:
+            self._struct = ExpertWeights(self.gate_q.data_ptr(), self.gate_s.data_ptr(), self.up_q.data_ptr(),
+                                         self.up_s.data_ptr(), self.down_q.data_ptr(), self.down_s.data_ptr(),
+                                         LAYOUT_TC)
+        return self._struct
+
+
+# ---- stages ------------------------------------------------------------------------
+
+def route(x, Wr, k: int, bias=None, stream=None):
+    T, d = x.shape
+    E = Wr.shape[0]
+    _need(x, torch.bfloat16, (T, d), "x")
+    _need(Wr, torch.float32, (E, d), "Wr")
+    if bias is not None:
+        _need(bias, torch.float32, (E,), "bias")
+    D = dims(T, d, E, k, 32)
+    logits = _empty((T, E), torch.float32, x.device)
+    idx = _empty((T, k), torch.int32, x.device)
+    w = _empty((T, k), torch.float32, x.device)
+    _check(_route(_ptr(x), _ptr(Wr), _ptr(bias), ctypes.byref(D), _ptr(logits), _ptr(idx), _ptr(w),
+                  _stream(stream)), "lmoe_route")
+    return logits, idx, w
+
+
+def topk_from_logits(logits, k: int, stream=None):
+    T, E = logits.shape
+    _need(logits, torch.float32, (T, E), "logits")
+    D = dims(T, 128, E, k, 32)
+    idx = _empty((T, k), torch.int32, logits.device)
+    w = _empty((T, k), torch.float32, logits.device)
+    _check(_topk(_ptr(logits), ctypes.byref(D), _ptr(idx), _ptr(w), _stream(stream)), "lmoe_topk_from_logits")
+    return idx, w
+
+
+def permute_workspace_size(T: int, E: int, k: int) -> int:
+    D = dims(T, 128, E, k, 32)
+    return int(_perm_ws(ctypes.byref(D)))
+
+
+def permute(idx, E: int, ws=None, stream=None):
+    T, k = idx.shape
+    _need(idx, torch.int32, (T, k), "topk_idx")
+    D = dims(T, 128, E, k, 32)
+    dev = idx.device
+    counts = _empty(E, torch.int32, dev)
+    offsets = _empty(E + 1, torch.int32, dev)
+    perm = _empty(T * k, torch.int32, dev)
+    inv = _empty(T * k, torch.int32, dev)
+    ws = workspace(_perm_ws(ctypes.byref(D)), dev) if ws is None else ws
+    _check(_permute(_ptr(idx), ctypes.byref(D), _ptr(counts), _ptr(offsets), _ptr(perm), _ptr(inv), _ptr(ws),
+                    ws.numel(), _stream(stream)), "lmoe_permute")
+    return counts, offsets, perm, inv, ws
+
+
+def expert_ffn(xq, xs, bank: ExpertBank, offsets, perm, topk_w, k: int, ws=None, stream=None):
+    T, d = xq.shape
+    D = dims(T, d, bank.E, k, bank.I)
+    _need(xq, torch.uint8, (T, d), "xq")
+    _need(xs, torch.uint8, (T, d // 32), "xs")
+    _need(offsets, torch.int32, (bank.E + 1,), "offsets")
+    _need(perm, torch.int32, (T * k,), "perm")
+    _need(topk_w, torch.float32, (T, k), "topk_w")
+    yp = _empty((T * k, d), torch.float32, xq.device)
+    ws = workspace(_ffn_ws(ctypes.byref(D)), xq.device) if ws is None else ws
+    W = bank.struct()
+    _check(_ffn(_ptr(xq), _ptr(xs), ctypes.byref(W), _ptr(offsets), _ptr(perm), _ptr(topk_w), ctypes.byref(D),
+                _ptr(yp), _ptr(ws), ws.numel(), _stream(stream)), "lmoe_expert_ffn")
+    return yp, ws
+
+
+def combine(yp, inv, T: int, k: int, stream=None):
+    P, d = yp.shape
+    _need(yp, torch.float32, (T * k, d), "yp")
+    _need(inv, torch.int32, (T * k,), "inv")
+    D = dims(T, d, 32, k, 32)
+    y = _empty((T, d), torch.bfloat16, yp.device)
+    _check(_combine(_ptr(yp), _ptr(inv), ctypes.byref(D), _ptr(y), _stream(stream)), "lmoe_combine")
+    return y
+
+
+# ---- whole layer -------------------------------------------------------------------
+
+def workspace_size(T: int, d: int, E: int, k: int, I: int) -> int:
+    D = dims(T, d, E, k, I)
+    return int(_ws_size(ctypes.byref(D)))
+
+
+class Layer:
+    """A LatentMoE layer: router weights, optional logit bias, expert bank."""
+
+    def __init__(self, Wr: torch.Tensor, bank: ExpertBank, k: int = 16, bias=None):
+        self.Wr, self.bank, self.k, self.bias = Wr, bank, k, bias
+        self._ws = None
+
+    def workspace(self, T: int) -> torch.Tensor:
+        need = workspace_size(T, self.bank.d, self.bank.E, self.k, self.bank.I)
+        if self._ws is None or self._ws.numel() < need:
+            self._ws = workspace(need, self.Wr.device)
+        return self._ws
+
+    def forward(self, x, y=None, topk_idx=None, topk_w=None, logits=None, stream=None):
+        T, d = x.shape
+        _need(x, torch.bfloat16, (T, d), "x")
+        D = dims(T, d, self.bank.E, self.k, self.bank.I)
+        y = _empty((T, d), torch.bfloat16, x.device) if y is None else y
+        ws = self.workspace(T)
+        W = self.bank.struct()
+        _check(_forward(_ptr(x), _ptr(self.Wr), _ptr(self.bias), ctypes.byref(W), ctypes.byref(D), _ptr(y),
+                        _ptr(topk_idx), _ptr(topk_w), _ptr(logits), _ptr(ws), ws.numel(), _stream(stream)),
+               "lmoe_forward")
+        return y
+
+    def device_status(self) -> int:
+        return last_device_status(self._ws)
+
+
+def last_device_status(ws) -> int:
+    v = _i32()
+    _check(_last_status(_ptr(ws), ctypes.byref(v)), "lmoe_last_device_status")
+    return int(v.value)
