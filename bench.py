@@ -189,6 +189,9 @@ def run_ours(args, ws, rank, local):
     time.sleep(0.3)
     K = args.steps
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(lmoe.NUM_STAGE_EVENTS)] for _ in range(K)]
+    for row in evs:  # torch creates the CUDA event objects on first record
+        for e in row:
+            e.record(st)
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if ws > 1:
         tdist.barrier()

@@ -193,3 +193,56 @@ def test_expert_ffn_against_oracle_per_pair(cuda_lib, name):
         err = np.max(np.abs(yp[q] - ref)) / np.sqrt((ref ** 2).mean())
         worst = max(worst, err)
     assert worst <= 1e-2, worst
+
+
+def _ffn_case(lmoe, wl, idx, seed=0):
+    """Expert FFN stage on a given routing; checks sampled pairs against the oracle."""
+    from _util import device_bank
+    rng = np.random.default_rng(seed)
+    x = gen.x_bf16(wl)
+    xd = to_dev_bf16(x, DEV)
+    w = rng.uniform(0.01, 1.0, idx.shape).astype(np.float32)
+    counts, offsets, perm, inv, _ = lmoe.permute(torch.from_numpy(idx).to(DEV), wl.E)
+    xq, xs = lmoe.quant_mxfp8(xd)
+    bank = device_bank(wl, DEV)
+    yp, ws = lmoe.expert_ffn(xq, xs, bank, offsets, perm, torch.from_numpy(w).to(DEV), wl.k)
+    torch.cuda.synchronize()
+    assert lmoe.last_device_status(ws) == 0
+    yp, perm_h = yp.cpu().numpy(), perm.cpu().numpy()
+    ob = oracle.quantize_experts(wl, experts=np.unique(idx))
+    worst = 0.0
+    qs = sorted(set(list(range(0, wl.P, max(1, wl.P // 48))) + [wl.P - 1]))
+    for q in qs:
+        t, j = divmod(int(perm_h[q]), wl.k)
+        ref = float(w[t, j]) * oracle.expert_ffn_token(x[t], ob, int(idx[t, j]), wl.d, wl.I)
+        worst = max(worst, np.max(np.abs(yp[q] - ref)) / np.sqrt((ref ** 2).mean()))
+    return worst
+
+
+def test_expert_ffn_multi_tile_and_last_expert_small_tiles(cuda_lib):
+    """Token tiles of 32 (few tokens per expert): an expert with 75 tokens spans
+    three tiles; the last expert's weight rows run past the bank (I = 64)."""
+    wl = gen.custom("multi32", T=80, d=256, I=64, E=60, k=4)
+    idx = np.zeros((wl.T, wl.k), np.int32)
+    for t in range(wl.T):
+        idx[t] = [59, (t % 50) + 1, (t % 7) + 51, 0 if t < 75 else 58]
+    assert lmoe_nt(cuda_lib, wl) == 32
+    assert _ffn_case(cuda_lib, wl, idx) <= 1e-2
+
+
+def test_expert_ffn_large_tiles_ragged_I(cuda_lib):
+    """Token tiles of 128 (many tokens per expert), experts with 1..300 tokens,
+    I = 160 (a partial 128-row tile and a partial K chunk in the down GEMM)."""
+    wl = gen.custom("multi128", T=600, d=384, I=160, E=8, k=2)
+    rng = np.random.default_rng(3)
+    idx = np.zeros((wl.T, wl.k), np.int32)
+    for t in range(wl.T):
+        idx[t] = rng.choice(7, 2, replace=False, p=np.array([50, 20, 10, 10, 5, 4, 1.0]) / 100) + (t == 0)
+    idx[0] = [7, 0]  # expert 7: a single token
+    assert lmoe_nt(cuda_lib, wl) == 128
+    assert _ffn_case(cuda_lib, wl, idx) <= 1e-2
+
+
+def lmoe_nt(lmoe, wl):
+    # the token tile the library picks: 32 when tokens per expert are few, else 128
+    return 32 if wl.P <= 16 * wl.E else 128

@@ -1,0 +1,643 @@
+// Expert FFN on the 5th-generation tensor cores: two grouped GEMMs over the
+// experts, MXFP4 weights x MXFP8 activations with hardware block scaling
+// (tcgen05.mma kind::mxf8f6f4, E8M0 scales), fp32 accumulation in TMEM.
+//   [MX]  "SGLang 0.5.17: Kimi K3 原生 MXFP4 推理架构解析", section "MXFP4 原生支持":
+//         one scale per 32-element block, dequantisation fused into the GEMM.
+//   [L1]  "从Kimi K3到MiniMax-H3", section 二 first layer: 4-bit weights with
+//         higher-precision activations and accumulation; section 一: gated
+//         expert FFN in the latent space (SiLU gating assumed, K3's SiTU is
+//         not defined on the pages).
+//
+// Orientation ("swap AB"): the weight rows are the M = 128 operand (A, e2m1,
+// K-major) and the expert's tokens are the N operand (B, e4m3, K-major), so N
+// follows the token count of the expert (16..NT in steps of 16) and small
+// batches waste no tensor work on padding rows.
+//
+//   gate/up GEMM, item (expert e, 128 rows of I, token tile):
+//     G = Wg[e] x^T, U = Wu[e] x^T (two TMEM accumulators), epilogue
+//     h = silu(G) * U, MXFP8-quantised along I (a warp's 32 lanes are one
+//     32-row block of I) -> hq / hs in the padded token layout;
+//   down GEMM, item (expert e, 128 rows of d, token tile):
+//     Y = Wd[e] h^T, epilogue yp[q][row] = topk_w[perm[q]] * Y.
+//
+// Token layout: the activations of expert e occupy `ntiles(e)` slots of SLOT
+// = roundup(NT, 128) rows starting at pad_off[e] (a multiple of 128); token r
+// of the expert sits at row pad_off[e] + (r / NT) * SLOT + r % NT.  So every
+// token tile starts on a 128-row boundary, and its scale factors are whole
+// 512-byte atoms (128 rows x 4 K-blocks) that one bulk copy moves and one
+// tcgen05.cp puts in TMEM.
+//
+// Persistent, warp-specialised CTA (192 threads, one per SM):
+//   warp 0     TMA producer (A tiles via the packed-FP4 tensor map that
+//              expands 16 x 4-bit into 16-byte smem units, B tile, scale atoms)
+//   warp 1     TMEM allocator + single-thread MMA issuer
+//   warps 2-5  epilogue (TMEM lane quarter = warp % 4)
+// Every mbarrier wait is bounded; a wait that runs out records
+// LMOE_ERR_TIMEOUT in the status word and the CTA winds down.
+#include <cuda.h>
+
+#include "lmoe_internal.cuh"
+#include "tc_ptx.cuh"
+
+namespace lmoe {
+namespace {
+
+using namespace tc;
+
+enum { GATEUP = 0, DOWN = 1 };
+
+struct GemmArgs {
+    const uint8_t *sfa0, *sfa1;  // weight scale atoms [E][RTa][KC][512]
+    const uint8_t *sfb;          // activation scale atoms [rows/128][KC][512]
+    const int32_t *offsets;      // [E+1] segment starts in permuted order
+    const int32_t *pad_off;      // [E+1] slot starts in the padded token layout
+    const int32_t *tiles;        // [E+1] first work item of each expert
+    const int32_t *perm;
+    const float *topk_w;
+    uint8_t *hq;    // gate/up out: [rows][Ih] e4m3
+    uint8_t *hs;    // gate/up out: scale atoms [rows/128][KCh][512]
+    float *yp;      // down out: [P][Mtot]
+    int E, Mtot, MT, KC, KCh, Ih;
+    int32_t *status;
+};
+
+template <int MODE, int NT>
+struct Cfg {
+    static constexpr int MATS = MODE == GATEUP ? 2 : 1;
+    static constexpr int SLOT = (NT + 127) / 128 * 128;
+    static constexpr int NAT = (NT + 127) / 128;  // B scale atoms per stage
+    static constexpr uint32_t A_TILE = 128 * 128;  // smem bytes of one expanded FP4 A tile
+    static constexpr uint32_t B_TILE = NT * 128;
+    static constexpr uint32_t SFA_OFF = MATS * A_TILE + B_TILE;
+    static constexpr uint32_t SFB_OFF = SFA_OFF + MATS * 512;
+    static constexpr uint32_t STAGE_BYTES = (SFB_OFF + NAT * 512 + 1023) / 1024 * 1024;
+    // global bytes per stage: packed FP4 tiles count 64 bytes per 128-element row
+    static constexpr uint32_t TX_BYTES = MATS * 128 * 64 + B_TILE + MATS * 512 + NAT * 512;
+    static constexpr int ACC_STAGES = (2 * MATS * NT <= 256) ? 2 : 1;
+    static constexpr int SF_COLS = 4 * (MATS + NAT);
+    static constexpr int SMEM_BUDGET = 200 * 1024;
+    static constexpr int STAGES_RAW = SMEM_BUDGET / int(STAGE_BYTES);
+    static constexpr int STAGES = STAGES_RAW > 10 ? 10 : STAGES_RAW;
+    static constexpr int ACC_COLS = ACC_STAGES * MATS * NT;
+    static constexpr int SF_BASE = (ACC_COLS + 31) / 32 * 32;
+    static_assert(SF_BASE + STAGES * SF_COLS <= 512, "TMEM columns");
+    static_assert(STAGES >= 2, "pipeline depth");
+};
+
+struct Item {
+    int e, n_tile, m_tile, n_valid;
+};
+
+__device__ __forceinline__ Item decode_item(int it, const int32_t *s_tiles, const int32_t *s_off, int E, int MT, int nt)
+{
+    int lo = 0, hi = E;  // s_tiles[lo] <= it < s_tiles[hi]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (s_tiles[mid] <= it) lo = mid;
+        else hi = mid;
+    }
+    // skip experts with no items (equal starts)
+    Item r;
+    r.e = lo;
+    const int local = it - s_tiles[lo];
+    r.n_tile = local / MT;
+    r.m_tile = local - r.n_tile * MT;
+    const int n_e = s_off[lo + 1] - s_off[lo];
+    r.n_valid = min(nt, n_e - r.n_tile * nt);
+    return r;
+}
+
+template <int MODE, int NT>
+__global__ void __launch_bounds__(192, 1)
+    k_moe_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
+               const __grid_constant__ CUtensorMap tmB, const GemmArgs p)
+{
+    using C = Cfg<MODE, NT>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *stages = smem;
+    uint64_t *full = reinterpret_cast<uint64_t *>(stages + C::STAGES * C::STAGE_BYTES);
+    uint64_t *empty = full + C::STAGES;
+    uint64_t *acc_full = empty + C::STAGES;
+    uint64_t *acc_empty = acc_full + C::ACC_STAGES;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_empty + C::ACC_STAGES);
+    int32_t *s_tiles = reinterpret_cast<int32_t *>(tmem_slot + 4);
+    int32_t *s_off = s_tiles + (p.E + 1);
+    int32_t *s_pad = s_off + (p.E + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int i = threadIdx.x; i <= p.E; i += blockDim.x) {
+        s_tiles[i] = p.tiles[i];
+        s_off[i] = p.offsets[i];
+        s_pad[i] = p.pad_off[i];
+    }
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < C::ACC_STAGES; ++a) {
+            mbar_init(&acc_full[a], 1);
+            mbar_init(&acc_empty[a], 128);
+        }
+        mbar_init_fence();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tensormap(&tmA0);
+        if (C::MATS == 2) prefetch_tensormap(&tmA1);
+        prefetch_tensormap(&tmB);
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const int total = s_tiles[p.E];
+
+    if (warp == 0) {
+        // ---------------- TMA producer ----------------
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int it = blockIdx.x; it < total && ok; it += gridDim.x) {
+                const Item w = decode_item(it, s_tiles, s_off, p.E, p.MT, NT);
+                const int R = s_pad[w.e] + w.n_tile * C::SLOT;
+                const int arow = w.e * p.Mtot + w.m_tile * 128;
+                const int64_t sfa_base = (int64_t(w.e) * p.MT + w.m_tile) * p.KC;
+                for (int kc = 0; kc < p.KC; ++kc) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1)) {
+                        set_status(p.status, LMOE_ERR_TIMEOUT);
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *sb = stages + stage * C::STAGE_BYTES;
+                    mbar_arrive_expect_tx(&full[stage], C::TX_BYTES);
+                    tma_load_2d(sb, &tmA0, kc * 128, arow, &full[stage]);
+                    if (C::MATS == 2) tma_load_2d(sb + C::A_TILE, &tmA1, kc * 128, arow, &full[stage]);
+                    tma_load_2d(sb + C::MATS * C::A_TILE, &tmB, kc * 128, R, &full[stage]);
+                    bulk_load(sb + C::SFA_OFF, p.sfa0 + (sfa_base + kc) * 512, 512, &full[stage]);
+                    if (C::MATS == 2) bulk_load(sb + C::SFA_OFF + 512, p.sfa1 + (sfa_base + kc) * 512, 512, &full[stage]);
+#pragma unroll
+                    for (int a = 0; a < C::NAT; ++a)
+                        bulk_load(sb + C::SFB_OFF + a * 512, p.sfb + (int64_t(R / 128 + a) * p.KC + kc) * 512, 512,
+                                  &full[stage]);
+                    if (++stage == C::STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            int stage = 0, acc = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            bool ok = true;
+            for (int it = blockIdx.x; it < total && ok; it += gridDim.x) {
+                const Item w = decode_item(it, s_tiles, s_off, p.E, p.MT, NT);
+                const uint32_t N = uint32_t((w.n_valid + 15) & ~15);
+                if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1)) {
+                    set_status(p.status, LMOE_ERR_TIMEOUT);
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d0 = tmem + uint32_t(acc * C::MATS * NT);
+                for (int kc = 0; kc < p.KC; ++kc) {
+                    if (!mbar_wait(&full[stage], phase)) {
+                        set_status(p.status, LMOE_ERR_TIMEOUT);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint8_t *sb = stages + stage * C::STAGE_BYTES;
+                    const uint32_t sf = tmem + uint32_t(C::SF_BASE + stage * C::SF_COLS);
+                    const uint32_t sfb = sf + 4 * C::MATS;
+                    tc_cp_sf(sf, sdesc_sf(smem_u32(sb + C::SFA_OFF)));
+                    if (C::MATS == 2) tc_cp_sf(sf + 4, sdesc_sf(smem_u32(sb + C::SFA_OFF + 512)));
+#pragma unroll
+                    for (int a = 0; a < C::NAT; ++a) tc_cp_sf(sfb + 4 * a, sdesc_sf(smem_u32(sb + C::SFB_OFF + a * 512)));
+                    const uint64_t ad0 = sdesc_k128(smem_u32(sb));
+                    const uint64_t ad1 = sdesc_k128(smem_u32(sb + C::A_TILE));
+                    const uint64_t bd = sdesc_k128(smem_u32(sb + C::MATS * C::A_TILE));
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint32_t id = idesc_mxf4_e4m3(N, uint32_t(kk));
+                        const uint32_t accum = (kc | kk) ? 1u : 0u;
+                        mma_mxf8f6f4(d0, ad0 + 2 * kk, bd + 2 * kk, id, sf, sfb, accum);
+                        if (C::MATS == 2) mma_mxf8f6f4(d0 + NT, ad1 + 2 * kk, bd + 2 * kk, id, sf + 4, sfb, accum);
+                    }
+                    tc_commit(&empty[stage]);
+                    if (++stage == C::STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (!ok) break;
+                tc_commit(&acc_full[acc]);
+                if (++acc == C::ACC_STAGES) {
+                    acc = 0;
+                    acc_phase ^= 1;
+                }
+            }
+        }
+    } else {
+        // ---------------- epilogue ----------------
+        const int q = warp & 3;  // TMEM lane quarter of this warp
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int it = blockIdx.x; it < total; it += gridDim.x) {
+            const Item w = decode_item(it, s_tiles, s_off, p.E, p.MT, NT);
+            if (!mbar_wait(&acc_full[acc], acc_phase)) {
+                set_status(p.status, LMOE_ERR_TIMEOUT);
+                break;
+            }
+            tc_fence_after();
+            const int row0 = w.m_tile * 128 + 32 * q;  // first A row (feature) of this warp
+            const uint32_t tbase = tmem + (uint32_t(32 * q) << 16) + uint32_t(acc * C::MATS * NT);
+            if (row0 < p.Mtot) {
+                const int row = row0 + lane;
+                const int64_t Rbase = int64_t(s_pad[w.e]) + int64_t(w.n_tile) * C::SLOT;
+                if (MODE == GATEUP) {
+                    const int blk = row0 / 32;  // MX block of I held by this warp
+                    for (int c0 = 0; c0 < w.n_valid; c0 += 16) {
+                        uint32_t g[16], u[16];
+                        tmem_ld16(tbase + c0, g);
+                        tmem_ld16(tbase + NT + c0, u);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const int c = c0 + j;
+                            if (c >= w.n_valid) break;
+                            const float gv = __uint_as_float(g[j]), uv = __uint_as_float(u[j]);
+                            const float h = gv / (1.f + expf(-gv)) * uv;
+                            uint32_t amax;
+                            asm("redux.sync.max.u32 %0, %1, 0xffffffff;" : "=r"(amax) : "r"(__float_as_uint(h) & 0x7FFFFFFFu));
+                            const uint32_t sb = mx_scale_byte(__uint_as_float(amax), 8);
+                            const uint32_t code = e4m3x2(h * mx_inv_scale(sb), 0.f) & 0xFF;
+                            const int64_t R = Rbase + c;
+                            p.hq[R * p.Ih + row] = uint8_t(code);
+                            if (lane == 0) {
+                                const int64_t off = ((R >> 7) * p.KCh + (blk >> 2)) * 512 + (R & 31) * 16 +
+                                                    ((R & 127) >> 5) * 4 + (blk & 3);
+                                p.hs[off] = uint8_t(sb);
+                            }
+                        }
+                    }
+                } else {
+                    const int qbase = s_off[w.e] + w.n_tile * NT;
+                    for (int c0 = 0; c0 < w.n_valid; c0 += 16) {
+                        float wl = 0.f;
+                        if (lane < 16 && c0 + lane < w.n_valid) wl = __ldg(p.topk_w + __ldg(p.perm + qbase + c0 + lane));
+                        uint32_t y[16];
+                        tmem_ld16(tbase + c0, y);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const int c = c0 + j;
+                            const float wc = __shfl_sync(0xFFFFFFFFu, wl, j);
+                            if (c >= w.n_valid) break;
+                            p.yp[int64_t(qbase + c) * p.Mtot + row] = wc * __uint_as_float(y[j]);
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&acc_empty[acc]);
+            if (++acc == C::ACC_STAGES) {
+                acc = 0;
+                acc_phase ^= 1;
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+// ---- schedule: slot starts and work-item prefixes (one CTA) ---------------------------
+// Exclusive scan of v over [0, n), n <= 2048, by a 1024-thread block.
+__device__ void block_exclusive_scan(const int32_t *v, int n, int32_t *out, int32_t *total, int32_t *warp_tot)
+{
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const int i0 = 2 * threadIdx.x;
+    const int32_t a = i0 < n ? v[i0] : 0, b = i0 + 1 < n ? v[i0 + 1] : 0;
+    const int32_t s = a + b;
+    int32_t incl = s;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += t;
+    }
+    if (lane == 31) warp_tot[wid] = incl;
+    __syncthreads();
+    if (wid == 0) {
+        const int32_t wt = warp_tot[lane];
+        int32_t wi = wt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t t = __shfl_up_sync(0xFFFFFFFFu, wi, o);
+            if (lane >= o) wi += t;
+        }
+        warp_tot[lane] = wi - wt;
+        if (lane == 31) *total = wi;
+    }
+    __syncthreads();
+    const int32_t excl = warp_tot[wid] + incl - s;
+    if (i0 < n) out[i0] = excl;
+    if (i0 + 1 < n) out[i0 + 1] = excl + a;
+    __syncthreads();
+}
+
+__global__ void __launch_bounds__(1024) k_ffn_schedule(const int32_t *__restrict__ offsets, int E, int NT, int SLOT,
+                                                      int MT_gu, int MT_dn, int32_t *pad_off, int32_t *tiles_gu,
+                                                      int32_t *tiles_dn)
+{
+    __shared__ int32_t v[2048], o[2048], warp_tot[32], tot;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        const int n = offsets[e + 1] - offsets[e];
+        v[e] = (n + NT - 1) / NT;  // token tiles of expert e
+    }
+    __syncthreads();
+    block_exclusive_scan(v, E, o, &tot, warp_tot);
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        pad_off[e] = o[e] * SLOT;
+        tiles_gu[e] = o[e] * MT_gu;
+        tiles_dn[e] = o[e] * MT_dn;
+    }
+    if (threadIdx.x == 0) {
+        pad_off[E] = tot * SLOT;
+        tiles_gu[E] = tot * MT_gu;
+        tiles_dn[E] = tot * MT_dn;
+    }
+}
+
+// ---- activations into the padded token layout ------------------------------------------
+__device__ __forceinline__ int64_t pad_row(int r, int32_t pad, int NT, int SLOT)
+{
+    return int64_t(pad) + int64_t(r / NT) * SLOT + (r % NT);
+}
+__device__ __forceinline__ int64_t atom_off(int64_t R, int b, int KC)
+{
+    return ((R >> 7) * KC + (b >> 2)) * 512 + (R & 31) * 16 + ((R & 127) >> 5) * 4 + (b & 3);
+}
+
+// bf16 x[T][d] -> MXFP8 rows at every (expert, slot) position the token is routed to.
+__global__ void k_quant_scatter_pad(const uint16_t *__restrict__ x, int64_t nblocks, int d, int k,
+                                    const int32_t *__restrict__ idx, const int32_t *__restrict__ inv,
+                                    const int32_t *__restrict__ offsets, const int32_t *__restrict__ pad_off, int NT,
+                                    int SLOT, uint8_t *__restrict__ xq, uint8_t *__restrict__ xs)
+{
+    const int nb = d / 32, KC = d / 128;
+    for (int64_t g = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; g < nblocks; g += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t t = g / nb;
+        const int b = int(g - t * nb);
+        const uint4 *src = reinterpret_cast<const uint4 *>(x + t * d + b * 32);
+        uint4 raw[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) raw[i] = __ldg(src + i);
+        const uint32_t *rw = reinterpret_cast<const uint32_t *>(raw);
+        float v[32];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            v[2 * i] = __uint_as_float(rw[i] << 16);
+            v[2 * i + 1] = __uint_as_float(rw[i] & 0xFFFF0000u);
+        }
+        uint32_t amax = 0;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) amax = max(amax, __float_as_uint(v[i]) & 0x7FFFFFFFu);
+        const uint32_t sb = mx_scale_byte(__uint_as_float(amax), 8);
+        const float iv = mx_inv_scale(sb);
+        uint32_t c[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) c[i] = e4m3x4(v[4 * i] * iv, v[4 * i + 1] * iv, v[4 * i + 2] * iv, v[4 * i + 3] * iv);
+        for (int j = 0; j < k; ++j) {
+            const int e = __ldg(idx + t * k + j);
+            const int r = __ldg(inv + t * k + j) - __ldg(offsets + e);
+            const int64_t R = pad_row(r, __ldg(pad_off + e), NT, SLOT);
+            uint4 *dst = reinterpret_cast<uint4 *>(xq + R * d + b * 32);
+            dst[0] = make_uint4(c[0], c[1], c[2], c[3]);
+            dst[1] = make_uint4(c[4], c[5], c[6], c[7]);
+            xs[atom_off(R, b, KC)] = uint8_t(sb);
+        }
+    }
+}
+
+// MXFP8 rows xq/xs [T][d] (canonical) -> padded layout, row q of perm taking token perm[q]/k.
+__global__ void k_gather_pad(const uint8_t *__restrict__ xq, const uint8_t *__restrict__ xs, int64_t P, int d, int k,
+                             int E, const int32_t *__restrict__ offsets, const int32_t *__restrict__ perm,
+                             const int32_t *__restrict__ pad_off, int NT, int SLOT, uint8_t *__restrict__ q_pad,
+                             uint8_t *__restrict__ s_pad)
+{
+    const int cq = d / 16, nb = d / 32, KC = d / 128;
+    const int per_row = cq + nb;
+    for (int64_t g = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; g < P * per_row; g += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t qrow = g / per_row;
+        const int c = int(g - qrow * per_row);
+        int lo = 0, hi = E;  // offsets[lo] <= qrow < offsets[hi]
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (__ldg(offsets + mid) <= qrow) lo = mid;
+            else hi = mid;
+        }
+        const int64_t R = pad_row(int(qrow - __ldg(offsets + lo)), __ldg(pad_off + lo), NT, SLOT);
+        const int64_t t = __ldg(perm + qrow) / k;
+        if (c < cq) {
+            reinterpret_cast<uint4 *>(q_pad + R * d)[c] = __ldg(reinterpret_cast<const uint4 *>(xq + t * d) + c);
+        } else {
+            const int b = c - cq;
+            s_pad[atom_off(R, b, KC)] = __ldg(xs + t * nb + b);
+        }
+    }
+}
+
+// ---- host side --------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encoder()
+{
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        cudaDriverEntryPointQueryResult q;
+        void *f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    }
+    return fn;
+}
+
+// rows x K 2-D tensor map with 128-element x box_rows boxes, 128-byte swizzle.
+bool make_map(CUtensorMap *m, const void *base, bool fp4, uint64_t K, uint64_t rows, uint64_t row_bytes,
+              uint32_t box_rows)
+{
+    EncodeTiledFn enc = encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {K, rows};
+    const cuuint64_t strides[1] = {row_bytes};
+    const cuuint32_t box[2] = {128, box_rows};
+    const cuuint32_t es[2] = {1, 1};
+    return enc(m, fp4 ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+               const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int num_sms()
+{
+    int dev = 0, n = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    return n > 0 ? n : 148;
+}
+
+template <int MODE, int NT>
+size_t gemm_smem(int E)
+{
+    using C = Cfg<MODE, NT>;
+    return 1024 + size_t(C::STAGES) * C::STAGE_BYTES + (2 * C::STAGES + 2 * C::ACC_STAGES) * 8 + 16 +
+           size_t(3) * (E + 1) * 4;
+}
+
+template <int MODE, int NT>
+cudaError_t launch_gemm(const CUtensorMap &a0, const CUtensorMap &a1, const CUtensorMap &b, const GemmArgs &args,
+                        cudaStream_t st)
+{
+    const size_t smem = gemm_smem<MODE, NT>(args.E);
+    cudaError_t e = cudaFuncSetAttribute(k_moe_gemm<MODE, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return e;
+    k_moe_gemm<MODE, NT><<<num_sms(), 192, smem, st>>>(a0, a1, b, args);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+FfnLayout ffn_layout(int64_t P, int d, int E, int I)
+{
+    FfnLayout L{};
+    L.NT = (P <= 16 * int64_t(E)) ? 32 : 128;
+    L.SLOT = int(round_up(L.NT, 128));
+    const int64_t touched = P < E ? P : E;
+    L.rows = (ceil_div(P, L.NT) + touched) * L.SLOT;
+    const int64_t atoms = L.rows / 128 + 2;
+    const int Ip = int(round_up(I, 128));
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off += size_t(round_up(int64_t(bytes), 256));
+        return o;
+    };
+    L.pad_off = take(size_t(E + 1) * 4);
+    L.tiles_gu = take(size_t(E + 1) * 4);
+    L.tiles_dn = take(size_t(E + 1) * 4);
+    L.xq = take(size_t(L.rows) * d);
+    L.xs = take(size_t(atoms) * (d / 128) * 512);
+    L.hq = take(size_t(L.rows) * I);
+    L.hs = take(size_t(atoms) * (Ip / 128) * 512);
+    L.hs_bytes = size_t(atoms) * (Ip / 128) * 512;
+    L.total = off;
+    return L;
+}
+
+cudaError_t launch_ffn_schedule(const int32_t *offsets, int E, int d, int I, const FfnLayout &L, char *scratch,
+                                cudaStream_t st)
+{
+    k_ffn_schedule<<<1, 1024, 0, st>>>(offsets, E, L.NT, L.SLOT, int(ceil_div(I, 128)), d / 128,
+                                       reinterpret_cast<int32_t *>(scratch + L.pad_off),
+                                       reinterpret_cast<int32_t *>(scratch + L.tiles_gu),
+                                       reinterpret_cast<int32_t *>(scratch + L.tiles_dn));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quant_scatter_pad(const uint16_t *x, int T, int d, int k, const int32_t *idx, const int32_t *inv,
+                                     const int32_t *offsets, const FfnLayout &L, char *scratch, cudaStream_t st)
+{
+    const int64_t nblocks = int64_t(T) * (d / 32);
+    if (nblocks == 0) return cudaSuccess;
+    const int grid = int(ceil_div(nblocks, 128) < 152 * 32 ? ceil_div(nblocks, 128) : 152 * 32);
+    k_quant_scatter_pad<<<grid, 128, 0, st>>>(x, nblocks, d, k, idx, inv, offsets,
+                                              reinterpret_cast<const int32_t *>(scratch + L.pad_off), L.NT, L.SLOT,
+                                              reinterpret_cast<uint8_t *>(scratch + L.xq),
+                                              reinterpret_cast<uint8_t *>(scratch + L.xs));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gather_pad(const uint8_t *xq, const uint8_t *xs, int T, int d, int k, int E, const int32_t *offsets,
+                              const int32_t *perm, const FfnLayout &L, char *scratch, cudaStream_t st)
+{
+    const int64_t P = int64_t(T) * k;
+    const int64_t n = P * (d / 16 + d / 32);
+    if (n == 0) return cudaSuccess;
+    const int grid = int(ceil_div(n, 256) < 152 * 64 ? ceil_div(n, 256) : 152 * 64);
+    k_gather_pad<<<grid, 256, 0, st>>>(xq, xs, P, d, k, E, offsets, perm,
+                                       reinterpret_cast<const int32_t *>(scratch + L.pad_off), L.NT, L.SLOT,
+                                       reinterpret_cast<uint8_t *>(scratch + L.xq),
+                                       reinterpret_cast<uint8_t *>(scratch + L.xs));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_expert_gemms(const FfnArgs &a, const FfnLayout &L, char *scratch, cudaStream_t st, cudaEvent_t mid)
+{
+    if (a.P == 0) return cudaSuccess;
+    const int Ip = int(round_up(a.I, 128));
+    uint8_t *xq = reinterpret_cast<uint8_t *>(scratch + L.xq);
+    uint8_t *xs = reinterpret_cast<uint8_t *>(scratch + L.xs);
+    uint8_t *hq = reinterpret_cast<uint8_t *>(scratch + L.hq);
+    uint8_t *hs = reinterpret_cast<uint8_t *>(scratch + L.hs);
+    if (a.I % 128 != 0) {
+        // scale blocks past I in the last K chunk of h must be finite (the
+        // matching A codes and B values are zero)
+        cudaError_t e = cudaMemsetAsync(hs, 0, L.hs_bytes, st);
+        if (e != cudaSuccess) return e;
+    }
+    CUtensorMap mg, mu, mx, md, mh;
+    const bool ok = make_map(&mg, a.W->gate_q, true, uint64_t(a.d), uint64_t(a.E) * a.I, uint64_t(a.d) / 2, 128) &&
+                    make_map(&mu, a.W->up_q, true, uint64_t(a.d), uint64_t(a.E) * a.I, uint64_t(a.d) / 2, 128) &&
+                    make_map(&md, a.W->down_q, true, uint64_t(Ip), uint64_t(a.E) * a.d, uint64_t(Ip) / 2, 128) &&
+                    make_map(&mx, xq, false, uint64_t(a.d), uint64_t(L.rows), uint64_t(a.d), uint32_t(L.NT)) &&
+                    make_map(&mh, hq, false, uint64_t(a.I), uint64_t(L.rows), uint64_t(a.I), uint32_t(L.NT));
+    if (!ok) return cudaErrorInvalidValue;
+    const int32_t *pad_off = reinterpret_cast<const int32_t *>(scratch + L.pad_off);
+    GemmArgs g{};
+    g.offsets = a.offsets;
+    g.pad_off = pad_off;
+    g.perm = a.perm;
+    g.topk_w = a.topk_w;
+    g.E = a.E;
+    g.status = a.status;
+    // gate/up
+    g.sfa0 = a.W->gate_s;
+    g.sfa1 = a.W->up_s;
+    g.sfb = xs;
+    g.tiles = reinterpret_cast<const int32_t *>(scratch + L.tiles_gu);
+    g.hq = hq;
+    g.hs = hs;
+    g.Mtot = a.I;
+    g.MT = int(ceil_div(a.I, 128));
+    g.KC = a.d / 128;
+    g.KCh = Ip / 128;
+    g.Ih = a.I;
+    cudaError_t e = L.NT == 32 ? launch_gemm<GATEUP, 32>(mg, mu, mx, g, st) : launch_gemm<GATEUP, 128>(mg, mu, mx, g, st);
+    if (e != cudaSuccess) return e;
+    if (mid) {
+        e = cudaEventRecord(mid, st);
+        if (e != cudaSuccess) return e;
+    }
+    // down
+    g.sfa0 = a.W->down_s;
+    g.sfa1 = nullptr;
+    g.sfb = hs;
+    g.tiles = reinterpret_cast<const int32_t *>(scratch + L.tiles_dn);
+    g.yp = a.yp;
+    g.Mtot = a.d;
+    g.MT = a.d / 128;
+    g.KC = Ip / 128;
+    return L.NT == 32 ? launch_gemm<DOWN, 32>(md, md, mh, g, st) : launch_gemm<DOWN, 128>(md, md, mh, g, st);
+}
+
+}  // namespace lmoe

@@ -99,46 +99,6 @@ __global__ void k_quant_mxfp8(const uint16_t *__restrict__ x, int64_t nblocks, i
     }
 }
 
-__global__ void k_quant_mxfp8_scatter(const uint16_t *__restrict__ x, int64_t nblocks, int d, int k,
-                                      const int32_t *__restrict__ inv, uint8_t *__restrict__ q, uint8_t *__restrict__ s)
-{
-    const int nb = d / 32;
-    for (int64_t g = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; g < nblocks; g += int64_t(gridDim.x) * blockDim.x) {
-        const int64_t t = g / nb;
-        const int b = int(g - t * nb);
-        uint4 lo, hi;
-        const uint32_t sb = quant_block_e4m3(x + t * d + b * 32, lo, hi);
-        for (int j = 0; j < k; ++j) {
-            const int64_t r = __ldg(inv + t * k + j);
-            uint4 *dst = reinterpret_cast<uint4 *>(q + r * d + b * 32);
-            dst[0] = lo;
-            dst[1] = hi;
-            s[r * nb + b] = uint8_t(sb);
-        }
-    }
-}
-
-// Row gather in 16-byte pieces: destination row q takes token perm[q] / k.
-__global__ void k_gather_rows(const uint8_t *__restrict__ xq, const uint8_t *__restrict__ xs, int64_t P, int d, int k,
-                              const int32_t *__restrict__ perm, uint8_t *__restrict__ q_sorted,
-                              uint8_t *__restrict__ s_sorted)
-{
-    const int cq = d / 16, cs = d / 32 / 4;  // 16-byte code pieces, 4-byte scale pieces per row
-    const int per_row = cq + cs;
-    for (int64_t g = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; g < P * per_row; g += int64_t(gridDim.x) * blockDim.x) {
-        const int64_t r = g / per_row;
-        const int c = int(g - r * per_row);
-        const int64_t t = __ldg(perm + r) / k;
-        if (c < cq) {
-            reinterpret_cast<uint4 *>(q_sorted + r * d)[c] = __ldg(reinterpret_cast<const uint4 *>(xq + t * d) + c);
-        } else {
-            const int cc = c - cq;
-            reinterpret_cast<uint32_t *>(s_sorted + r * (d / 32))[cc] =
-                __ldg(reinterpret_cast<const uint32_t *>(xs + t * (d / 32)) + cc);
-        }
-    }
-}
-
 int grid_for(int64_t n, int threads)
 {
     int64_t g = ceil_div(n, threads);
@@ -170,25 +130,6 @@ cudaError_t launch_quant_mxfp8(const uint16_t *x, int64_t rows, int K, uint8_t *
     const int64_t nblocks = rows * (K / 32);
     if (nblocks == 0) return cudaSuccess;
     k_quant_mxfp8<<<grid_for(nblocks, 256), 256, 0, st>>>(x, nblocks, K, q, s);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_quant_mxfp8_scatter(const uint16_t *x, int T, int d, int k, const int32_t *inv, uint8_t *q_sorted,
-                                       uint8_t *s_sorted, cudaStream_t st)
-{
-    const int64_t nblocks = int64_t(T) * (d / 32);
-    if (nblocks == 0) return cudaSuccess;
-    k_quant_mxfp8_scatter<<<grid_for(nblocks, 128), 128, 0, st>>>(x, nblocks, d, k, inv, q_sorted, s_sorted);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_gather_rows(const uint8_t *xq, const uint8_t *xs, int T, int d, int k, const int32_t *perm,
-                               uint8_t *q_sorted, uint8_t *s_sorted, cudaStream_t st)
-{
-    const int64_t P = int64_t(T) * k;
-    const int64_t n = P * (d / 16 + d / 128);
-    if (n == 0) return cudaSuccess;
-    k_gather_rows<<<grid_for(n, 256), 256, 0, st>>>(xq, xs, P, d, k, perm, q_sorted, s_sorted);
     return cudaGetLastError();
 }
 

@@ -52,9 +52,9 @@ bool weights_ok(const lmoe_expert_weights *W)
 
 // Workspace layout of lmoe_forward (each region 256-byte aligned):
 //   status | logits | idx | w | counts | offsets | perm | inv | permute scratch
-//   | xq sorted | xs sorted | ffn scratch | yp
+//   | ffn scratch (padded MXFP8 activations, h, schedule) | yp
 struct FwdLayout {
-    size_t status, logits, idx, w, counts, offsets, perm, inv, pscratch, xq, xs, fscratch, yp, total;
+    size_t status, logits, idx, w, counts, offsets, perm, inv, pscratch, fscratch, yp, total;
 };
 
 FwdLayout fwd_layout(const lmoe_dims *d)
@@ -76,9 +76,7 @@ FwdLayout fwd_layout(const lmoe_dims *d)
     L.perm = take(size_t(P * 4));
     L.inv = take(size_t(P * 4));
     L.pscratch = take(permute_scratch_bytes(P, int(E)));
-    L.xq = take(size_t(P * d->d));
-    L.xs = take(size_t(P * (d->d / 32)));
-    L.fscratch = take(ffn_scratch_bytes(P, d->d, int(E), d->I));
+    L.fscratch = take(ffn_layout(P, d->d, int(E), d->I).total);
     L.yp = take(size_t(P * d->d * 4));
     L.total = off;
     return L;
@@ -182,8 +180,7 @@ size_t lmoe_expert_ffn_workspace_size(const lmoe_dims *dims)
 {
     if (!dims_ok(dims)) return 0;
     const int64_t P = int64_t(dims->T) * dims->k;
-    return kStatusBytes + size_t(round_up(P * dims->d, 256) + round_up(P * (dims->d / 32), 256)) +
-           ffn_scratch_bytes(P, dims->d, dims->E, dims->I);
+    return kStatusBytes + ffn_layout(P, dims->d, dims->E, dims->I).total;
 }
 
 lmoe_status lmoe_expert_ffn(const uint8_t *xq, const uint8_t *xs, const lmoe_expert_weights *W,
@@ -201,16 +198,15 @@ lmoe_status lmoe_expert_ffn(const uint8_t *xq, const uint8_t *xs, const lmoe_exp
         return LMOE_ERR_WORKSPACE;
     const int64_t P = int64_t(dims->T) * dims->k;
     char *ws = static_cast<char *>(workspace);
-    uint8_t *xq_sorted = reinterpret_cast<uint8_t *>(ws + kStatusBytes);
-    uint8_t *xs_sorted = xq_sorted + round_up(P * dims->d, 256);
-    void *fscratch = xs_sorted + round_up(P * (dims->d / 32), 256);
+    char *fs = ws + kStatusBytes;
+    const FfnLayout L = ffn_layout(P, dims->d, dims->E, dims->I);
     cudaStream_t st = cudaStream_t(stream);
     cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(int32_t), st);
-    if (e == cudaSuccess) e = launch_gather_rows(xq, xs, dims->T, dims->d, dims->k, perm, xq_sorted, xs_sorted, st);
+    if (e == cudaSuccess) e = launch_ffn_schedule(offsets, dims->E, dims->d, dims->I, L, fs, st);
+    if (e == cudaSuccess) e = launch_gather_pad(xq, xs, dims->T, dims->d, dims->k, dims->E, offsets, perm, L, fs, st);
     if (e != cudaSuccess) return cuda_status(e);
-    FfnArgs f{xq_sorted, xs_sorted, W, offsets, perm, topk_w, int(P), dims->d, dims->E, dims->k, dims->I,
-              yp, fscratch, reinterpret_cast<int32_t *>(ws)};
-    return cuda_status(launch_expert_ffn(f, st));
+    FfnArgs f{W, offsets, perm, topk_w, int(P), dims->d, dims->E, dims->k, dims->I, yp, reinterpret_cast<int32_t *>(ws)};
+    return cuda_status(launch_expert_gemms(f, L, fs, st));
 }
 
 lmoe_status lmoe_combine(const float *yp, const int32_t *inv, const lmoe_dims *dims, uint16_t *y_bf16, void *stream)
@@ -250,8 +246,8 @@ lmoe_status lmoe_forward(const uint16_t *x_bf16, const float *Wr, const float *b
     int32_t *offsets = reinterpret_cast<int32_t *>(ws + L.offsets);
     int32_t *perm = reinterpret_cast<int32_t *>(ws + L.perm);
     int32_t *inv = reinterpret_cast<int32_t *>(ws + L.inv);
-    uint8_t *xq = reinterpret_cast<uint8_t *>(ws + L.xq);
-    uint8_t *xs = reinterpret_cast<uint8_t *>(ws + L.xs);
+    char *fs = ws + L.fscratch;
+    const FfnLayout FL = ffn_layout(P, d, E, dims->I);
     float *yp = reinterpret_cast<float *>(ws + L.yp);
     int32_t *status = reinterpret_cast<int32_t *>(ws + L.status);
 
@@ -261,12 +257,13 @@ lmoe_status lmoe_forward(const uint16_t *x_bf16, const float *Wr, const float *b
     if (e == cudaSuccess) e = launch_topk_softmax(lg, T, E, k, idx, w, st);
     if (e == cudaSuccess) e = mark(1, st);
     if (e == cudaSuccess) e = launch_permute(idx, P, E, counts, offsets, perm, inv, ws + L.pscratch, status, st);
+    if (e == cudaSuccess) e = launch_ffn_schedule(offsets, E, d, dims->I, FL, fs, st);
     if (e == cudaSuccess) e = mark(2, st);
-    if (e == cudaSuccess) e = launch_quant_mxfp8_scatter(x_bf16, T, d, k, inv, xq, xs, st);
+    if (e == cudaSuccess) e = launch_quant_scatter_pad(x_bf16, T, d, k, idx, inv, offsets, FL, fs, st);
     if (e == cudaSuccess) e = mark(3, st);
     if (e == cudaSuccess) {
-        FfnArgs f{xq, xs, W, offsets, perm, w, int(P), d, E, k, dims->I, yp, ws + L.fscratch, status};
-        e = launch_expert_ffn(f, st, g_stage_events_on ? g_stage_events[4] : nullptr);
+        FfnArgs f{W, offsets, perm, w, int(P), d, E, k, dims->I, yp, status};
+        e = launch_expert_gemms(f, FL, fs, st, g_stage_events_on ? g_stage_events[4] : nullptr);
     }
     if (e == cudaSuccess) e = mark(5, st);
     if (e == cudaSuccess) e = launch_combine(yp, inv, T, d, k, y_bf16, st);

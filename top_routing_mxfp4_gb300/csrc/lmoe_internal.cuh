@@ -95,13 +95,6 @@ __host__ __device__ constexpr int64_t round_up(int64_t a, int64_t b) { return ce
 cudaError_t launch_quant_mxfp4(const float *w, int64_t nmat, int rows, int K, uint8_t *q, uint8_t *s, int layout,
                                cudaStream_t st);
 cudaError_t launch_quant_mxfp8(const uint16_t *x, int64_t rows, int K, uint8_t *q, uint8_t *s, cudaStream_t st);
-// x[T][d] -> MXFP8 rows written at the k permuted positions inv[t*k + j].
-cudaError_t launch_quant_mxfp8_scatter(const uint16_t *x, int T, int d, int k, const int32_t *inv, uint8_t *q_sorted,
-                                       uint8_t *s_sorted, cudaStream_t st);
-// rows of xq/xs [T][...] gathered into permuted order (row q <- token perm[q]/k).
-cudaError_t launch_gather_rows(const uint8_t *xq, const uint8_t *xs, int T, int d, int k, const int32_t *perm,
-                               uint8_t *q_sorted, uint8_t *s_sorted, cudaStream_t st);
-
 cudaError_t launch_router_logits(const uint16_t *x, const float *Wr, const float *bias, int T, int d, int E,
                                  float *logits, cudaStream_t st);
 cudaError_t launch_topk_softmax(const float *logits, int T, int E, int k, int32_t *idx, float *w, cudaStream_t st);
@@ -110,19 +103,36 @@ size_t permute_scratch_bytes(int64_t P, int E);
 cudaError_t launch_permute(const int32_t *idx, int64_t P, int E, int32_t *counts, int32_t *offsets, int32_t *perm,
                            int32_t *inv, void *scratch, int32_t *status, cudaStream_t st);
 
+// Expert FFN (tensor cores).  Activations live in a padded token layout
+// inside the FFN scratch: expert e's tokens fill slots of SLOT rows from
+// pad_off[e]; see k_ffn_tc.cu.
+struct FfnLayout {
+    int NT, SLOT;      // token tile and slot rows
+    int64_t rows;      // padded token rows reserved
+    size_t pad_off, tiles_gu, tiles_dn, xq, xs, hq, hs, hs_bytes, total;  // byte offsets / sizes
+};
+FfnLayout ffn_layout(int64_t P, int d, int E, int I);
+
 struct FfnArgs {
-    const uint8_t *xq_sorted, *xs_sorted;  // [P][d], [P][d/32]
     const lmoe_expert_weights *W;
     const int32_t *offsets, *perm;
     const float *topk_w;
     int P, d, E, k, I;
-    float *yp;        // [P][d]
-    void *scratch;    // ffn_scratch_bytes
+    float *yp;  // [P][d] in permuted order
     int32_t *status;
 };
-size_t ffn_scratch_bytes(int64_t P, int d, int E, int I);
-// gate/up GEMM + SwiGLU + MXFP8 of h, then (after `mid`, if not null) the down GEMM.
-cudaError_t launch_expert_ffn(const FfnArgs &a, cudaStream_t st, cudaEvent_t mid = nullptr);
+// slot starts and per-GEMM work-item prefixes from the segment offsets
+cudaError_t launch_ffn_schedule(const int32_t *offsets, int E, int d, int I, const FfnLayout &L, char *scratch,
+                                cudaStream_t st);
+// bf16 x[T][d] -> MXFP8 rows at each routed (expert, slot) position
+cudaError_t launch_quant_scatter_pad(const uint16_t *x, int T, int d, int k, const int32_t *idx, const int32_t *inv,
+                                     const int32_t *offsets, const FfnLayout &L, char *scratch, cudaStream_t st);
+// MXFP8 rows in token order -> padded layout (row q of perm takes token perm[q]/k)
+cudaError_t launch_gather_pad(const uint8_t *xq, const uint8_t *xs, int T, int d, int k, int E, const int32_t *offsets,
+                              const int32_t *perm, const FfnLayout &L, char *scratch, cudaStream_t st);
+// gate/up GEMM (+ SwiGLU, MXFP8 of h), event `mid` (if set), down GEMM (x gate weight)
+cudaError_t launch_expert_gemms(const FfnArgs &a, const FfnLayout &L, char *scratch, cudaStream_t st,
+                                cudaEvent_t mid = nullptr);
 
 cudaError_t launch_combine(const float *yp, const int32_t *inv, int T, int d, int k, uint16_t *y, cudaStream_t st);
 
