@@ -247,7 +247,7 @@ def run_ours(args, ws, rank, local):
     t_gu = stage_ms["gate_up"] / 1e3
     achieved = gateup_bytes / t_gu / 1e9
     layer_weight_gbs = touched * per_expert_w / (ms_per_step / 1e3) / 1e9
-    launches_per_step = 10  # router, top-k, 3 permute passes, scatter, 3 expert-FFN kernels, combine
+    launches_per_step = lmoe.forward_kernel_count(T, wl.d, wl.E, wl.k, wl.I)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,

@@ -121,12 +121,19 @@ lmoe_status lmoe_quant_mxfp4(const float *w, int64_t nmat, int32_t rows, int32_t
 lmoe_status lmoe_quant_mxfp8(const uint16_t *x_bf16, int64_t rows, int32_t K, uint8_t *q, uint8_t *s, void *stream);
 
 /* Router [MoE]: logits[t][e] = fp32(sum_c x[t][c] * Wr[e][c]) (+ bias[e]),
+ * accumulated in fp32 on the tensor cores (Wr split exactly into three bf16
+ * parts whose products with bf16 x are exact in fp32),
  * x bf16 [T][d], Wr fp32 [E][d], bias fp32 [E] or NULL (the skewed
  * workload's popularity bias); then the top-k of each row (larger logit
  * first, ties by smaller id) into topk_idx[T][k] and the softmax over those
  * k logits into topk_w[T][k].  logits [T][E] is a required output. */
 lmoe_status lmoe_route(const uint16_t *x_bf16, const float *Wr, const float *bias, const lmoe_dims *dims,
-                       float *logits, int32_t *topk_idx, float *topk_w, void *stream);
+                       float *logits, int32_t *topk_idx, float *topk_w, void *workspace, size_t ws_bytes,
+                       void *stream);
+
+/* Scratch bytes lmoe_route needs for these dims (the router weights split
+ * into three bf16 parts for the tensor cores, and split-K partial sums). */
+size_t lmoe_route_workspace_size(const lmoe_dims *dims);
 
 /* The top-k + softmax half of lmoe_route on given fp32 logits [T][E]. */
 lmoe_status lmoe_topk_from_logits(const float *logits, const lmoe_dims *dims, int32_t *topk_idx, float *topk_w,
@@ -184,6 +191,10 @@ lmoe_status lmoe_last_device_status(const void *workspace, int32_t *device_statu
 
 /* Clears the status word (enqueued on `stream`). */
 lmoe_status lmoe_clear_device_status(void *workspace, void *stream);
+
+/* Number of CUDA kernels one lmoe_forward call with these dims launches
+ * (0 for invalid dims or T == 0). */
+int32_t lmoe_forward_kernel_count(const lmoe_dims *dims);
 
 /* Profiling hook: when set, lmoe_forward records the n = LMOE_NUM_STAGE_EVENTS
  * CUDA events (cudaEvent_t handles, created by the caller) on its stream at

@@ -66,6 +66,20 @@ def test_forward_decode_sampled(cuda_lib):
     _check(wl, x, y, idx, w, lg, [0, 1, 17, 33, 62, 63])
 
 
+@pytest.mark.parametrize("name", ["prefill", "skewed"])
+def test_forward_prefill_sampled(cuda_lib, name):
+    wl = gen.WORKLOADS[name]
+    x, y, idx, w, lg = _run_forward(cuda_lib, wl)
+    # sampled tokens, including the first and last, and tokens routed to the hottest expert
+    counts = np.bincount(idx.ravel(), minlength=wl.E)
+    hot = int(np.argmax(counts))
+    hot_tokens = np.flatnonzero((idx == hot).any(1))
+    toks = sorted(set([0, 1, wl.T // 2, wl.T - 1, int(hot_tokens[0]), int(hot_tokens[-1])]))
+    _check(wl, x, y, idx, w, lg, toks)
+    if name == "skewed":
+        assert counts.max() / counts.mean() > 5.0
+
+
 @pytest.mark.parametrize("T", [1, 3, 131])
 def test_forward_ragged_token_counts(cuda_lib, T):
     wl = gen.custom(f"ragged{T}", T=T, d=512, I=64)

@@ -17,7 +17,7 @@
 //     G = Wg[e] x^T, U = Wu[e] x^T (two TMEM accumulators), epilogue
 //     h = silu(G) * U, MXFP8-quantised along I (a warp's 32 lanes are one
 //     32-row block of I) -> hq / hs in the padded token layout;
-//   down GEMM, item (expert e, 128 rows of d, token tile):
+//   down GEMM, item (expert e, 256 rows of d, token tile):
 //     Y = Wd[e] h^T, epilogue yp[q][row] = topk_w[perm[q]] * Y.
 //
 // Token layout: the activations of expert e occupy `ntiles(e)` slots of SLOT
@@ -27,10 +27,11 @@
 // 512-byte atoms (128 rows x 4 K-blocks) that one bulk copy moves and one
 // tcgen05.cp puts in TMEM.
 //
-// Persistent, warp-specialised CTA (192 threads, one per SM):
+// Persistent, warp-specialised CTA (224 threads, one per SM):
 //   warp 0     TMA producer (A tiles via the packed-FP4 tensor map that
 //              expands 16 x 4-bit into 16-byte smem units, B tile, scale atoms)
-//   warp 1     TMEM allocator + single-thread MMA issuer
+//   warp 1     TMEM allocator + MMA issuer 0 (gate / first K half of down)
+//   warp 6     MMA issuer 1 (up / second K half of down)
 //   warps 2-5  epilogue (TMEM lane quarter = warp % 4)
 // Every mbarrier wait is bounded; a wait that runs out records
 // LMOE_ERR_TIMEOUT in the status word and the CTA winds down.
@@ -38,6 +39,56 @@
 
 #include "lmoe_internal.cuh"
 #include "tc_ptx.cuh"
+
+#ifdef LMOE_TRACE
+// Diagnostic build only: CTA 0 of each expert GEMM records (tag, item, k chunk,
+// SM clock) at its pipeline events into shared memory (one region per role,
+// plain stores), copied to global memory when the CTA ends;
+// lmoe_debug_trace() returns them.
+constexpr int TRACE_PER_ROLE = 500;
+__device__ uint32_t g_lmoe_trace[2 * 65536];
+__device__ uint32_t g_lmoe_trace_n;
+#define LMOE_TRACE_DECL uint32_t tr_n_ = 0;
+#define LMOE_TRACE_EV(role, tag, item, kc)                                                                   \
+    do {                                                                                                    \
+        if (blockIdx.x == 0 && tr_n_ < TRACE_PER_ROLE) {                                                    \
+            s_trace[2 * ((role) * TRACE_PER_ROLE + tr_n_)] =                                                \
+                (uint32_t(tag) << 24) | ((uint32_t(item) & 0xFFFF) << 8) | (uint32_t(kc) & 0xFF);           \
+            s_trace[2 * ((role) * TRACE_PER_ROLE + tr_n_) + 1] = uint32_t(clock64());                       \
+            ++tr_n_;                                                                                        \
+        }                                                                                                   \
+    } while (0)
+#define LMOE_TRACE_END(role)                                                                                \
+    do {                                                                                                    \
+        if (blockIdx.x == 0 && tr_n_) {                                                                     \
+            const uint32_t base_ = atomicAdd(&g_lmoe_trace_n, tr_n_);                                       \
+            for (uint32_t i_ = 0; i_ < tr_n_ && base_ + i_ < 65536; ++i_) {                                 \
+                g_lmoe_trace[2 * (base_ + i_)] = s_trace[2 * ((role) * TRACE_PER_ROLE + i_)];               \
+                g_lmoe_trace[2 * (base_ + i_) + 1] = s_trace[2 * ((role) * TRACE_PER_ROLE + i_) + 1];       \
+            }                                                                                               \
+        }                                                                                                   \
+    } while (0)
+__shared__ uint32_t s_trace[2 * 3 * TRACE_PER_ROLE];
+extern "C" int lmoe_debug_trace(uint32_t *host, int max_events)
+{
+    uint32_t n = 0;
+    if (cudaMemcpyFromSymbol(&n, g_lmoe_trace_n, sizeof(n)) != cudaSuccess) return -1;
+    if (n > 65536) n = 65536;
+    if (int(n) > max_events) n = uint32_t(max_events);
+    if (n && cudaMemcpyFromSymbol(host, g_lmoe_trace, size_t(n) * 8) != cudaSuccess) return -1;
+    const uint32_t zero = 0;
+    cudaMemcpyToSymbol(g_lmoe_trace_n, &zero, sizeof(zero));
+    return int(n);
+}
+#else
+#define LMOE_TRACE_DECL
+#define LMOE_TRACE_EV(role, tag, item, kc) \
+    do {                                   \
+    } while (0)
+#define LMOE_TRACE_END(role) \
+    do {                     \
+    } while (0)
+#endif
 
 namespace lmoe {
 namespace {
@@ -50,20 +101,21 @@ struct GemmArgs {
     const uint8_t *sfa0, *sfa1;  // weight scale atoms [E][RTa][KC][512]
     const uint8_t *sfb;          // activation scale atoms [rows/128][KC][512]
     const int32_t *offsets;      // [E+1] segment starts in permuted order
-    const int32_t *pad_off;      // [E+1] slot starts in the padded token layout
     const int32_t *tiles;        // [E+1] first work item of each expert
-    const int32_t *perm;
-    const float *topk_w;
+    const float *w_sorted;  // gate weight of each permuted row q (topk_w[perm[q]])
     uint8_t *hq;    // gate/up out: [rows][Ih] e4m3
     uint8_t *hs;    // gate/up out: scale atoms [rows/128][KCh][512]
     float *yp;      // down out: [P][Mtot]
-    int E, Mtot, MT, KC, KCh, Ih;
+    int E, Mtot, MT, MTA, KC, KCh, Ih;  // MT: m tiles per item sequence; MTA: 128-row tiles of A
+    int stages;  // shared-memory pipeline depth (<= Cfg::MAX_STAGES)
     int32_t *status;
 };
 
 template <int MODE, int NT>
 struct Cfg {
-    static constexpr int MATS = MODE == GATEUP ? 2 : 1;
+    // Weight tiles per stage: gate and up rows of the same 128 features, or
+    // two consecutive 128-row tiles of down.
+    static constexpr int MATS = 2;
     static constexpr int SLOT = (NT + 127) / 128 * 128;
     static constexpr int NAT = (NT + 127) / 128;  // B scale atoms per stage
     static constexpr uint32_t A_TILE = 128 * 128;  // smem bytes of one expanded FP4 A tile
@@ -73,15 +125,17 @@ struct Cfg {
     static constexpr uint32_t STAGE_BYTES = (SFB_OFF + NAT * 512 + 1023) / 1024 * 1024;
     // global bytes per stage: packed FP4 tiles count 64 bytes per 128-element row
     static constexpr uint32_t TX_BYTES = MATS * 128 * 64 + B_TILE + MATS * 512 + NAT * 512;
-    static constexpr int ACC_STAGES = (2 * MATS * NT <= 256) ? 2 : 1;
-    static constexpr int SF_COLS = 4 * (MATS + NAT);
-    static constexpr int SMEM_BUDGET = 200 * 1024;
-    static constexpr int STAGES_RAW = SMEM_BUDGET / int(STAGE_BYTES);
-    static constexpr int STAGES = STAGES_RAW > 10 ? 10 : STAGES_RAW;
-    static constexpr int ACC_COLS = ACC_STAGES * MATS * NT;
+    // Two MMA-issuing threads, one per weight tile, each with its own
+    // accumulator.  One thread issues a tcgen05 instruction only every few
+    // dozen cycles, so two issuers keep small-N MMAs from pacing the pipeline.
+    static constexpr int ACC_COLS_ITEM = 2 * NT;
+    static constexpr int ACC_STAGES = (ACC_COLS_ITEM <= 64) ? 4 : (2 * ACC_COLS_ITEM <= 256 ? 2 : 1);
+    static constexpr int ACC_COLS = ACC_STAGES * ACC_COLS_ITEM;
     static constexpr int SF_BASE = (ACC_COLS + 31) / 32 * 32;
-    static_assert(SF_BASE + STAGES * SF_COLS <= 512, "TMEM columns");
-    static_assert(STAGES >= 2, "pipeline depth");
+    static constexpr int SF_COLS_ISSUER = 4 + 4 * NAT;  // this issuer's SFA and SFB copies
+    static constexpr int SF_COLS = 2 * SF_COLS_ISSUER;
+    static constexpr int MAX_STAGES = (512 - SF_BASE) / SF_COLS < 16 ? (512 - SF_BASE) / SF_COLS : 16;
+    static_assert(MAX_STAGES >= 2, "TMEM columns");
 };
 
 struct Item {
@@ -108,36 +162,35 @@ __device__ __forceinline__ Item decode_item(int it, const int32_t *s_tiles, cons
 }
 
 template <int MODE, int NT>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(224, 1)
     k_moe_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                const __grid_constant__ CUtensorMap tmB, const GemmArgs p)
 {
     using C = Cfg<MODE, NT>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int S = p.stages;
     uint8_t *stages = smem;
-    uint64_t *full = reinterpret_cast<uint64_t *>(stages + C::STAGES * C::STAGE_BYTES);
-    uint64_t *empty = full + C::STAGES;
-    uint64_t *acc_full = empty + C::STAGES;
+    uint64_t *full = reinterpret_cast<uint64_t *>(stages + S * C::STAGE_BYTES);
+    uint64_t *empty = full + S;
+    uint64_t *acc_full = empty + S;
     uint64_t *acc_empty = acc_full + C::ACC_STAGES;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_empty + C::ACC_STAGES);
     int32_t *s_tiles = reinterpret_cast<int32_t *>(tmem_slot + 4);
     int32_t *s_off = s_tiles + (p.E + 1);
-    int32_t *s_pad = s_off + (p.E + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int i = threadIdx.x; i <= p.E; i += blockDim.x) {
         s_tiles[i] = p.tiles[i];
         s_off[i] = p.offsets[i];
-        s_pad[i] = p.pad_off[i];
     }
     if (threadIdx.x == 0) {
-        for (int s = 0; s < C::STAGES; ++s) {
+        for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+            mbar_init(&empty[s], 2);  // one commit per MMA issuer
         }
         for (int a = 0; a < C::ACC_STAGES; ++a) {
-            mbar_init(&acc_full[a], 1);
+            mbar_init(&acc_full[a], 2);
             mbar_init(&acc_empty[a], 128);
         }
         mbar_init_fence();
@@ -153,45 +206,58 @@ __global__ void __launch_bounds__(192, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const int total = s_tiles[p.E];
+    // slot start of an expert's first token tile (tiles[e] = slots before e times MT)
+    auto slot_row = [&](int e) { return (s_tiles[e] / p.MT) * C::SLOT; };
 
     if (warp == 0) {
         // ---------------- TMA producer ----------------
         if (lane == 0) {
+            LMOE_TRACE_DECL
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
             for (int it = blockIdx.x; it < total && ok; it += gridDim.x) {
                 const Item w = decode_item(it, s_tiles, s_off, p.E, p.MT, NT);
-                const int R = s_pad[w.e] + w.n_tile * C::SLOT;
-                const int arow = w.e * p.Mtot + w.m_tile * 128;
-                const int64_t sfa_base = (int64_t(w.e) * p.MT + w.m_tile) * p.KC;
+                const int R = slot_row(w.e) + w.n_tile * C::SLOT;
+                // gate/up: tile m of both matrices; down: tiles 2m and 2m+1 (an odd
+                // last tile loads tile 2m twice and the epilogue drops the copy)
+                const int mt0 = MODE == GATEUP ? w.m_tile : 2 * w.m_tile;
+                const int mt1 = MODE == GATEUP ? w.m_tile : (mt0 + 1 < p.MTA ? mt0 + 1 : mt0);
+                const int arow = w.e * p.Mtot + mt0 * 128, arow1 = w.e * p.Mtot + mt1 * 128;
+                const int64_t sfa_base = (int64_t(w.e) * p.MTA + mt0) * p.KC;
+                const int64_t sfa_base1 = (int64_t(w.e) * p.MTA + mt1) * p.KC;
                 for (int kc = 0; kc < p.KC; ++kc) {
                     if (!mbar_wait(&empty[stage], phase ^ 1)) {
                         set_status(p.status, LMOE_ERR_TIMEOUT);
                         ok = false;
                         break;
                     }
+                    LMOE_TRACE_EV(0, 0x10 | MODE, it, kc);  // producer: stage free
                     uint8_t *sb = stages + stage * C::STAGE_BYTES;
                     mbar_arrive_expect_tx(&full[stage], C::TX_BYTES);
                     tma_load_2d(sb, &tmA0, kc * 128, arow, &full[stage]);
-                    if (C::MATS == 2) tma_load_2d(sb + C::A_TILE, &tmA1, kc * 128, arow, &full[stage]);
+                    tma_load_2d(sb + C::A_TILE, &tmA1, kc * 128, arow1, &full[stage]);
                     tma_load_2d(sb + C::MATS * C::A_TILE, &tmB, kc * 128, R, &full[stage]);
                     bulk_load(sb + C::SFA_OFF, p.sfa0 + (sfa_base + kc) * 512, 512, &full[stage]);
-                    if (C::MATS == 2) bulk_load(sb + C::SFA_OFF + 512, p.sfa1 + (sfa_base + kc) * 512, 512, &full[stage]);
+                    bulk_load(sb + C::SFA_OFF + 512, p.sfa1 + (sfa_base1 + kc) * 512, 512, &full[stage]);
 #pragma unroll
                     for (int a = 0; a < C::NAT; ++a)
                         bulk_load(sb + C::SFB_OFF + a * 512, p.sfb + (int64_t(R / 128 + a) * p.KC + kc) * 512, 512,
                                   &full[stage]);
-                    if (++stage == C::STAGES) {
+                    LMOE_TRACE_EV(0, 0x70 | MODE, it, kc);  // producer: copies issued
+                    if (++stage == S) {
                         stage = 0;
                         phase ^= 1;
                     }
                 }
             }
+            LMOE_TRACE_END(0);
         }
-    } else if (warp == 1) {
-        // ---------------- MMA issuer ----------------
+    } else if (warp == 1 || warp == 6) {
+        // ---------------- MMA issuers (warp 1: gate / low K half, warp 6: up / high K half) ----------------
         if (lane == 0) {
+            LMOE_TRACE_DECL
+            const int iss = warp == 1 ? 0 : 1;
             int stage = 0, acc = 0;
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
@@ -203,7 +269,8 @@ __global__ void __launch_bounds__(192, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d0 = tmem + uint32_t(acc * C::MATS * NT);
+                if (iss == 0) LMOE_TRACE_EV(1, 0x20 | MODE, it, 0);  // mma: accumulator free
+                const uint32_t d = tmem + uint32_t(acc * C::ACC_COLS_ITEM + iss * NT);
                 for (int kc = 0; kc < p.KC; ++kc) {
                     if (!mbar_wait(&full[stage], phase)) {
                         set_status(p.status, LMOE_ERR_TIMEOUT);
@@ -211,25 +278,22 @@ __global__ void __launch_bounds__(192, 1)
                         break;
                     }
                     tc_fence_after();
+                    if (iss == 0) LMOE_TRACE_EV(1, 0x30 | MODE, it, kc);  // mma: stage data landed
                     const uint8_t *sb = stages + stage * C::STAGE_BYTES;
-                    const uint32_t sf = tmem + uint32_t(C::SF_BASE + stage * C::SF_COLS);
-                    const uint32_t sfb = sf + 4 * C::MATS;
-                    tc_cp_sf(sf, sdesc_sf(smem_u32(sb + C::SFA_OFF)));
-                    if (C::MATS == 2) tc_cp_sf(sf + 4, sdesc_sf(smem_u32(sb + C::SFA_OFF + 512)));
+                    const uint32_t sfa = tmem + uint32_t(C::SF_BASE + stage * C::SF_COLS + iss * C::SF_COLS_ISSUER);
+                    const uint32_t sfb = sfa + 4;
+                    tc_cp_sf(sfa, sdesc_sf(smem_u32(sb + C::SFA_OFF + iss * 512)));
 #pragma unroll
                     for (int a = 0; a < C::NAT; ++a) tc_cp_sf(sfb + 4 * a, sdesc_sf(smem_u32(sb + C::SFB_OFF + a * 512)));
-                    const uint64_t ad0 = sdesc_k128(smem_u32(sb));
-                    const uint64_t ad1 = sdesc_k128(smem_u32(sb + C::A_TILE));
+                    const uint64_t ad = sdesc_k128(smem_u32(sb + iss * C::A_TILE));
                     const uint64_t bd = sdesc_k128(smem_u32(sb + C::MATS * C::A_TILE));
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint32_t id = idesc_mxf4_e4m3(N, uint32_t(kk));
-                        const uint32_t accum = (kc | kk) ? 1u : 0u;
-                        mma_mxf8f6f4(d0, ad0 + 2 * kk, bd + 2 * kk, id, sf, sfb, accum);
-                        if (C::MATS == 2) mma_mxf8f6f4(d0 + NT, ad1 + 2 * kk, bd + 2 * kk, id, sf + 4, sfb, accum);
-                    }
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_mxf8f6f4(d, ad + 2 * kk, bd + 2 * kk, idesc_mxf4_e4m3(N, uint32_t(kk)), sfa, sfb,
+                                     (kc > 0 || kk > 0) ? 1u : 0u);
                     tc_commit(&empty[stage]);
-                    if (++stage == C::STAGES) {
+                    if (iss == 0) LMOE_TRACE_EV(1, 0x80 | MODE, it, kc);  // mma: stage issued
+                    if (++stage == S) {
                         stage = 0;
                         phase ^= 1;
                     }
@@ -241,75 +305,115 @@ __global__ void __launch_bounds__(192, 1)
                     acc_phase ^= 1;
                 }
             }
+            if (iss == 0) LMOE_TRACE_END(1);
         }
     } else {
-        // ---------------- epilogue ----------------
+        // ---------------- epilogue (warps 2-5) ----------------
         const int q = warp & 3;  // TMEM lane quarter of this warp
+        LMOE_TRACE_DECL
         int acc = 0;
         uint32_t acc_phase = 0;
+        // the next item and its gate weights are fetched one item ahead, so
+        // their load latency overlaps the current item's accumulator wait
+        Item nx{};
+        float wn[(NT + 31) / 32];
+        auto fetch = [&](int it2) {
+            nx = decode_item(it2, s_tiles, s_off, p.E, p.MT, NT);
+            if (MODE == DOWN) {
+                const int qb = s_off[nx.e] + nx.n_tile * NT;
+#pragma unroll
+                for (int i = 0; i < (NT + 31) / 32; ++i)
+                    wn[i] = (32 * i + lane < nx.n_valid) ? __ldg(p.w_sorted + qb + 32 * i + lane) : 0.f;
+            }
+        };
+        if (int(blockIdx.x) < total) fetch(blockIdx.x);
         for (int it = blockIdx.x; it < total; it += gridDim.x) {
-            const Item w = decode_item(it, s_tiles, s_off, p.E, p.MT, NT);
+            const Item w = nx;
+            float wl[(NT + 31) / 32];
+#pragma unroll
+            for (int i = 0; i < (NT + 31) / 32; ++i) wl[i] = wn[i];
+            if (it + int(gridDim.x) < total) fetch(it + gridDim.x);
+            const int qbase = s_off[w.e] + w.n_tile * NT;  // first permuted row of the tile
+            if (threadIdx.x == 64) LMOE_TRACE_EV(2, 0x40 | MODE, it, 0);  // epilogue: waiting
             if (!mbar_wait(&acc_full[acc], acc_phase)) {
                 set_status(p.status, LMOE_ERR_TIMEOUT);
                 break;
             }
             tc_fence_after();
-            const int row0 = w.m_tile * 128 + 32 * q;  // first A row (feature) of this warp
-            const uint32_t tbase = tmem + (uint32_t(32 * q) << 16) + uint32_t(acc * C::MATS * NT);
-            if (row0 < p.Mtot) {
+            if (threadIdx.x == 64) LMOE_TRACE_EV(2, 0x50 | MODE, it, 0);  // epilogue: accumulator ready
+            const uint32_t tbase = tmem + (uint32_t(32 * q) << 16) + uint32_t(acc * C::ACC_COLS_ITEM);
+            if (MODE == GATEUP && w.m_tile * 128 + 32 * q < p.Mtot) {
+                const int row0 = w.m_tile * 128 + 32 * q;  // first row of I held by this warp
                 const int row = row0 + lane;
-                const int64_t Rbase = int64_t(s_pad[w.e]) + int64_t(w.n_tile) * C::SLOT;
-                if (MODE == GATEUP) {
-                    const int blk = row0 / 32;  // MX block of I held by this warp
-                    for (int c0 = 0; c0 < w.n_valid; c0 += 16) {
-                        uint32_t g[16], u[16];
-                        tmem_ld16(tbase + c0, g);
-                        tmem_ld16(tbase + NT + c0, u);
-                        tmem_ld_wait();
+                const int64_t Rbase = int64_t(slot_row(w.e)) + int64_t(w.n_tile) * C::SLOT;
+                for (int c0 = 0; c0 < w.n_valid; c0 += 16) {
+                    uint32_t v0[16], v1[16];
+                    tmem_ld16(tbase + c0, v0);
+                    tmem_ld16(tbase + NT + c0, v1);
+                    tmem_ld_wait();
+                    const int nv = min(16, w.n_valid - c0);
+                    {
+                        // 16 independent columns: SiLU-gated product, block amax over
+                        // the warp's 32 rows of I, E8M0 scale, e4m3 code
+                        const int blk = row0 / 32;  // MX block of I held by this warp
+                        uint32_t code[16], sbv[16];
 #pragma unroll
                         for (int j = 0; j < 16; ++j) {
-                            const int c = c0 + j;
-                            if (c >= w.n_valid) break;
-                            const float gv = __uint_as_float(g[j]), uv = __uint_as_float(u[j]);
-                            const float h = gv / (1.f + expf(-gv)) * uv;
+                            const float gv = __uint_as_float(v0[j]), uv = __uint_as_float(v1[j]);
+                            const float h = __fdividef(gv, 1.f + __expf(-gv)) * uv;
                             uint32_t amax;
                             asm("redux.sync.max.u32 %0, %1, 0xffffffff;" : "=r"(amax) : "r"(__float_as_uint(h) & 0x7FFFFFFFu));
-                            const uint32_t sb = mx_scale_byte(__uint_as_float(amax), 8);
-                            const uint32_t code = e4m3x2(h * mx_inv_scale(sb), 0.f) & 0xFF;
-                            const int64_t R = Rbase + c;
-                            p.hq[R * p.Ih + row] = uint8_t(code);
-                            if (lane == 0) {
-                                const int64_t off = ((R >> 7) * p.KCh + (blk >> 2)) * 512 + (R & 31) * 16 +
-                                                    ((R & 127) >> 5) * 4 + (blk & 3);
-                                p.hs[off] = uint8_t(sb);
-                            }
+                            sbv[j] = mx_scale_byte(__uint_as_float(amax), 8);
+                            code[j] = e4m3x2(h * mx_inv_scale(sbv[j]), 0.f) & 0xFF;
+                        }
+                        uint8_t *hrow = p.hq + (Rbase + c0) * p.Ih + row;
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            if (j < nv) hrow[int64_t(j) * p.Ih] = uint8_t(code[j]);
+                        if (lane < nv) {  // lane j writes column j's scale byte
+                            uint32_t sbl = 0;
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) sbl = (lane == j) ? sbv[j] : sbl;
+                            const int64_t R = Rbase + c0 + lane;
+                            p.hs[((R >> 7) * p.KCh + (blk >> 2)) * 512 + (R & 31) * 16 + ((R & 127) >> 5) * 4 + (blk & 3)] =
+                                uint8_t(sbl);
                         }
                     }
-                } else {
-                    const int qbase = s_off[w.e] + w.n_tile * NT;
+                }
+            }
+            if (MODE == DOWN) {
+                // accumulator h holds output rows (2m + h) * 128 + 32q + lane
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int mt = 2 * w.m_tile + h;
+                    if (mt >= p.MTA) break;  // odd last tile: second accumulator is a copy
+                    const int row = mt * 128 + 32 * q + lane;
                     for (int c0 = 0; c0 < w.n_valid; c0 += 16) {
-                        float wl = 0.f;
-                        if (lane < 16 && c0 + lane < w.n_valid) wl = __ldg(p.topk_w + __ldg(p.perm + qbase + c0 + lane));
-                        uint32_t y[16];
-                        tmem_ld16(tbase + c0, y);
+                        uint32_t v[16];
+                        tmem_ld16(tbase + h * NT + c0, v);
                         tmem_ld_wait();
+                        const int nv = min(16, w.n_valid - c0);
+                        float *yrow = p.yp + int64_t(qbase + c0) * p.Mtot + row;
+                        float wsel = wl[0];
+#pragma unroll
+                        for (int i = 1; i < (NT + 31) / 32; ++i) wsel = (c0 / 32 == i) ? wl[i] : wsel;
 #pragma unroll
                         for (int j = 0; j < 16; ++j) {
-                            const int c = c0 + j;
-                            const float wc = __shfl_sync(0xFFFFFFFFu, wl, j);
-                            if (c >= w.n_valid) break;
-                            p.yp[int64_t(qbase + c) * p.Mtot + row] = wc * __uint_as_float(y[j]);
+                            const float wc = __shfl_sync(0xFFFFFFFFu, wsel, (c0 & 31) + j);
+                            if (j < nv) yrow[int64_t(j) * p.Mtot] = wc * __uint_as_float(v[j]);
                         }
                     }
                 }
             }
             tc_fence_before();
             mbar_arrive(&acc_empty[acc]);
+            if (threadIdx.x == 64) LMOE_TRACE_EV(2, 0x60 | MODE, it, 0);  // epilogue: done
             if (++acc == C::ACC_STAGES) {
                 acc = 0;
                 acc_phase ^= 1;
             }
         }
+        if (threadIdx.x == 64) LMOE_TRACE_END(2);
     }
     tc_fence_before();
     __syncthreads();
@@ -387,8 +491,9 @@ __device__ __forceinline__ int64_t atom_off(int64_t R, int b, int KC)
 // bf16 x[T][d] -> MXFP8 rows at every (expert, slot) position the token is routed to.
 __global__ void k_quant_scatter_pad(const uint16_t *__restrict__ x, int64_t nblocks, int d, int k,
                                     const int32_t *__restrict__ idx, const int32_t *__restrict__ inv,
-                                    const int32_t *__restrict__ offsets, const int32_t *__restrict__ pad_off, int NT,
-                                    int SLOT, uint8_t *__restrict__ xq, uint8_t *__restrict__ xs)
+                                    const float *__restrict__ topk_w, const int32_t *__restrict__ offsets,
+                                    const int32_t *__restrict__ pad_off, int NT, int SLOT, uint8_t *__restrict__ xq,
+                                    uint8_t *__restrict__ xs, float *__restrict__ w_sorted)
 {
     const int nb = d / 32, KC = d / 128;
     for (int64_t g = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; g < nblocks; g += int64_t(gridDim.x) * blockDim.x) {
@@ -415,7 +520,9 @@ __global__ void k_quant_scatter_pad(const uint16_t *__restrict__ x, int64_t nblo
         for (int i = 0; i < 8; ++i) c[i] = e4m3x4(v[4 * i] * iv, v[4 * i + 1] * iv, v[4 * i + 2] * iv, v[4 * i + 3] * iv);
         for (int j = 0; j < k; ++j) {
             const int e = __ldg(idx + t * k + j);
-            const int r = __ldg(inv + t * k + j) - __ldg(offsets + e);
+            const int qrow = __ldg(inv + t * k + j);
+            const int r = qrow - __ldg(offsets + e);
+            if (b == 0) w_sorted[qrow] = __ldg(topk_w + t * k + j);
             const int64_t R = pad_row(r, __ldg(pad_off + e), NT, SLOT);
             uint4 *dst = reinterpret_cast<uint4 *>(xq + R * d + b * 32);
             dst[0] = make_uint4(c[0], c[1], c[2], c[3]);
@@ -428,8 +535,8 @@ __global__ void k_quant_scatter_pad(const uint16_t *__restrict__ x, int64_t nblo
 // MXFP8 rows xq/xs [T][d] (canonical) -> padded layout, row q of perm taking token perm[q]/k.
 __global__ void k_gather_pad(const uint8_t *__restrict__ xq, const uint8_t *__restrict__ xs, int64_t P, int d, int k,
                              int E, const int32_t *__restrict__ offsets, const int32_t *__restrict__ perm,
-                             const int32_t *__restrict__ pad_off, int NT, int SLOT, uint8_t *__restrict__ q_pad,
-                             uint8_t *__restrict__ s_pad)
+                             const float *__restrict__ topk_w, const int32_t *__restrict__ pad_off, int NT, int SLOT,
+                             uint8_t *__restrict__ q_pad, uint8_t *__restrict__ s_pad, float *__restrict__ w_sorted)
 {
     const int cq = d / 16, nb = d / 32, KC = d / 128;
     const int per_row = cq + nb;
@@ -443,7 +550,8 @@ __global__ void k_gather_pad(const uint8_t *__restrict__ xq, const uint8_t *__re
             else hi = mid;
         }
         const int64_t R = pad_row(int(qrow - __ldg(offsets + lo)), __ldg(pad_off + lo), NT, SLOT);
-        const int64_t t = __ldg(perm + qrow) / k;
+        const int64_t pr = __ldg(perm + qrow), t = pr / k;
+        if (c == 0) w_sorted[qrow] = __ldg(topk_w + pr);
         if (c < cq) {
             reinterpret_cast<uint4 *>(q_pad + R * d)[c] = __ldg(reinterpret_cast<const uint4 *>(xq + t * d) + c);
         } else {
@@ -496,22 +604,35 @@ int num_sms()
     return n > 0 ? n : 148;
 }
 
+// Deepest pipeline that fits the per-block shared-memory limit (dynamic part
+// after the kernel's static shared memory) and the TMEM column budget.
 template <int MODE, int NT>
-size_t gemm_smem(int E)
+int gemm_stages(int E, size_t &smem)
 {
     using C = Cfg<MODE, NT>;
-    return 1024 + size_t(C::STAGES) * C::STAGE_BYTES + (2 * C::STAGES + 2 * C::ACC_STAGES) * 8 + 16 +
-           size_t(3) * (E + 1) * 4;
+    int dev = 0, optin = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    cudaFuncAttributes fa{};
+    cudaFuncGetAttributes(&fa, k_moe_gemm<MODE, NT>);
+    const size_t fixed = 1024 + (2 * 16 + 2 * C::ACC_STAGES) * 8 + 16 + size_t(2) * (E + 1) * 4;
+    const long avail = long(optin) - long(fa.sharedSizeBytes) - long(fixed);
+    int st = int(avail / long(C::STAGE_BYTES));
+    if (st > C::MAX_STAGES) st = C::MAX_STAGES;
+    smem = fixed + size_t(st > 0 ? st : 0) * C::STAGE_BYTES;
+    return st;
 }
 
 template <int MODE, int NT>
-cudaError_t launch_gemm(const CUtensorMap &a0, const CUtensorMap &a1, const CUtensorMap &b, const GemmArgs &args,
+cudaError_t launch_gemm(const CUtensorMap &a0, const CUtensorMap &a1, const CUtensorMap &b, GemmArgs args,
                         cudaStream_t st)
 {
-    const size_t smem = gemm_smem<MODE, NT>(args.E);
+    size_t smem = 0;
+    args.stages = gemm_stages<MODE, NT>(args.E, smem);
+    if (args.stages < 2) return cudaErrorInvalidConfiguration;
     cudaError_t e = cudaFuncSetAttribute(k_moe_gemm<MODE, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
-    k_moe_gemm<MODE, NT><<<num_sms(), 192, smem, st>>>(a0, a1, b, args);
+    k_moe_gemm<MODE, NT><<<num_sms(), 224, smem, st>>>(a0, a1, b, args);
     return cudaGetLastError();
 }
 
@@ -520,7 +641,7 @@ cudaError_t launch_gemm(const CUtensorMap &a0, const CUtensorMap &a1, const CUte
 FfnLayout ffn_layout(int64_t P, int d, int E, int I)
 {
     FfnLayout L{};
-    L.NT = (P <= 16 * int64_t(E)) ? 32 : 128;
+    L.NT = P <= 4 * int64_t(E) ? 16 : (P <= 16 * int64_t(E) ? 32 : 128);
     L.SLOT = int(round_up(L.NT, 128));
     const int64_t touched = P < E ? P : E;
     L.rows = (ceil_div(P, L.NT) + touched) * L.SLOT;
@@ -540,6 +661,7 @@ FfnLayout ffn_layout(int64_t P, int d, int E, int I)
     L.hq = take(size_t(L.rows) * I);
     L.hs = take(size_t(atoms) * (Ip / 128) * 512);
     L.hs_bytes = size_t(atoms) * (Ip / 128) * 512;
+    L.w_sorted = take(size_t(P) * 4);
     L.total = off;
     return L;
 }
@@ -547,7 +669,7 @@ FfnLayout ffn_layout(int64_t P, int d, int E, int I)
 cudaError_t launch_ffn_schedule(const int32_t *offsets, int E, int d, int I, const FfnLayout &L, char *scratch,
                                 cudaStream_t st)
 {
-    k_ffn_schedule<<<1, 1024, 0, st>>>(offsets, E, L.NT, L.SLOT, int(ceil_div(I, 128)), d / 128,
+    k_ffn_schedule<<<1, 1024, 0, st>>>(offsets, E, L.NT, L.SLOT, int(ceil_div(I, 128)), int(ceil_div(d / 128, 2)),
                                        reinterpret_cast<int32_t *>(scratch + L.pad_off),
                                        reinterpret_cast<int32_t *>(scratch + L.tiles_gu),
                                        reinterpret_cast<int32_t *>(scratch + L.tiles_dn));
@@ -555,29 +677,33 @@ cudaError_t launch_ffn_schedule(const int32_t *offsets, int E, int d, int I, con
 }
 
 cudaError_t launch_quant_scatter_pad(const uint16_t *x, int T, int d, int k, const int32_t *idx, const int32_t *inv,
-                                     const int32_t *offsets, const FfnLayout &L, char *scratch, cudaStream_t st)
+                                     const float *topk_w, const int32_t *offsets, const FfnLayout &L, char *scratch,
+                                     cudaStream_t st)
 {
     const int64_t nblocks = int64_t(T) * (d / 32);
     if (nblocks == 0) return cudaSuccess;
     const int grid = int(ceil_div(nblocks, 128) < 152 * 32 ? ceil_div(nblocks, 128) : 152 * 32);
-    k_quant_scatter_pad<<<grid, 128, 0, st>>>(x, nblocks, d, k, idx, inv, offsets,
+    k_quant_scatter_pad<<<grid, 128, 0, st>>>(x, nblocks, d, k, idx, inv, topk_w, offsets,
                                               reinterpret_cast<const int32_t *>(scratch + L.pad_off), L.NT, L.SLOT,
                                               reinterpret_cast<uint8_t *>(scratch + L.xq),
-                                              reinterpret_cast<uint8_t *>(scratch + L.xs));
+                                              reinterpret_cast<uint8_t *>(scratch + L.xs),
+                                              reinterpret_cast<float *>(scratch + L.w_sorted));
     return cudaGetLastError();
 }
 
 cudaError_t launch_gather_pad(const uint8_t *xq, const uint8_t *xs, int T, int d, int k, int E, const int32_t *offsets,
-                              const int32_t *perm, const FfnLayout &L, char *scratch, cudaStream_t st)
+                              const int32_t *perm, const float *topk_w, const FfnLayout &L, char *scratch,
+                              cudaStream_t st)
 {
     const int64_t P = int64_t(T) * k;
     const int64_t n = P * (d / 16 + d / 32);
     if (n == 0) return cudaSuccess;
     const int grid = int(ceil_div(n, 256) < 152 * 64 ? ceil_div(n, 256) : 152 * 64);
-    k_gather_pad<<<grid, 256, 0, st>>>(xq, xs, P, d, k, E, offsets, perm,
+    k_gather_pad<<<grid, 256, 0, st>>>(xq, xs, P, d, k, E, offsets, perm, topk_w,
                                        reinterpret_cast<const int32_t *>(scratch + L.pad_off), L.NT, L.SLOT,
                                        reinterpret_cast<uint8_t *>(scratch + L.xq),
-                                       reinterpret_cast<uint8_t *>(scratch + L.xs));
+                                       reinterpret_cast<uint8_t *>(scratch + L.xs),
+                                       reinterpret_cast<float *>(scratch + L.w_sorted));
     return cudaGetLastError();
 }
 
@@ -602,12 +728,9 @@ cudaError_t launch_expert_gemms(const FfnArgs &a, const FfnLayout &L, char *scra
                     make_map(&mx, xq, false, uint64_t(a.d), uint64_t(L.rows), uint64_t(a.d), uint32_t(L.NT)) &&
                     make_map(&mh, hq, false, uint64_t(a.I), uint64_t(L.rows), uint64_t(a.I), uint32_t(L.NT));
     if (!ok) return cudaErrorInvalidValue;
-    const int32_t *pad_off = reinterpret_cast<const int32_t *>(scratch + L.pad_off);
     GemmArgs g{};
     g.offsets = a.offsets;
-    g.pad_off = pad_off;
-    g.perm = a.perm;
-    g.topk_w = a.topk_w;
+    g.w_sorted = reinterpret_cast<const float *>(scratch + L.w_sorted);
     g.E = a.E;
     g.status = a.status;
     // gate/up
@@ -619,10 +742,13 @@ cudaError_t launch_expert_gemms(const FfnArgs &a, const FfnLayout &L, char *scra
     g.hs = hs;
     g.Mtot = a.I;
     g.MT = int(ceil_div(a.I, 128));
+    g.MTA = g.MT;
     g.KC = a.d / 128;
     g.KCh = Ip / 128;
     g.Ih = a.I;
-    cudaError_t e = L.NT == 32 ? launch_gemm<GATEUP, 32>(mg, mu, mx, g, st) : launch_gemm<GATEUP, 128>(mg, mu, mx, g, st);
+    cudaError_t e = L.NT == 16   ? launch_gemm<GATEUP, 16>(mg, mu, mx, g, st)
+                    : L.NT == 32 ? launch_gemm<GATEUP, 32>(mg, mu, mx, g, st)
+                                 : launch_gemm<GATEUP, 128>(mg, mu, mx, g, st);
     if (e != cudaSuccess) return e;
     if (mid) {
         e = cudaEventRecord(mid, st);
@@ -630,14 +756,17 @@ cudaError_t launch_expert_gemms(const FfnArgs &a, const FfnLayout &L, char *scra
     }
     // down
     g.sfa0 = a.W->down_s;
-    g.sfa1 = nullptr;
+    g.sfa1 = a.W->down_s;  // the second tile of a down item is the next tile of the same matrix
     g.sfb = hs;
     g.tiles = reinterpret_cast<const int32_t *>(scratch + L.tiles_dn);
     g.yp = a.yp;
     g.Mtot = a.d;
-    g.MT = a.d / 128;
+    g.MTA = a.d / 128;
+    g.MT = int(ceil_div(g.MTA, 2));  // each down item covers two 128-row tiles
     g.KC = Ip / 128;
-    return L.NT == 32 ? launch_gemm<DOWN, 32>(md, md, mh, g, st) : launch_gemm<DOWN, 128>(md, md, mh, g, st);
+    return L.NT == 16   ? launch_gemm<DOWN, 16>(md, md, mh, g, st)
+           : L.NT == 32 ? launch_gemm<DOWN, 32>(md, md, mh, g, st)
+                        : launch_gemm<DOWN, 128>(md, md, mh, g, st);
 }
 
 }  // namespace lmoe

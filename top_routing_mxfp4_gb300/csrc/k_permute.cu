@@ -139,7 +139,108 @@ __global__ void __launch_bounds__(256) k_perm_scatter(const int32_t *__restrict_
     }
 }
 
+// All of the above in one CTA when the pairs fit one chunk (P <= CHUNK):
+// per-warp histograms -> counts and per-warp starts -> exclusive scan over
+// experts -> ordered scatter.  Used for decode-sized batches, where three
+// launches would cost more than the work.
+__global__ void __launch_bounds__(256) k_perm_single(const int32_t *__restrict__ idx, int P, int E,
+                                                     int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
+                                                     int32_t *__restrict__ perm, int32_t *__restrict__ inv,
+                                                     int32_t *status)
+{
+    extern __shared__ int32_t wh[];  // [WARPS][E]
+    __shared__ int32_t warp_tot[WARPS];
+    int32_t *off_s = wh + WARPS * E;  // [E]
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    for (int i = threadIdx.x; i < WARPS * E; i += blockDim.x) wh[i] = 0;
+    __syncthreads();
+    const int s0 = wid * SUB, s1 = min(P, s0 + SUB);
+    int32_t my[SUB / 32];
+#pragma unroll
+    for (int i = 0; i < SUB / 32; ++i) {
+        const int p = s0 + 32 * i + lane;
+        int e = p < s1 ? __ldg(idx + p) : -1;
+        if (p < s1 && (e < 0 || e >= E)) {
+            set_status(status, LMOE_ERR_DEVICE_CHECK);
+            e = -1;
+        }
+        my[i] = e;
+        if (e >= 0) atomicAdd(&wh[wid * E + e], 1);
+    }
+    __syncthreads();
+    // per expert: total count and each warp's start inside the expert
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int32_t run = 0;
+#pragma unroll
+        for (int w = 0; w < WARPS; ++w) {
+            const int32_t c = wh[w * E + e];
+            wh[w * E + e] = run;
+            run += c;
+        }
+        off_s[e] = run;
+        counts[e] = run;
+    }
+    __syncthreads();
+    // exclusive scan of the counts: thread i owns experts [i*PER, (i+1)*PER)
+    constexpr int PER = MAXE / 256;
+    int32_t v[PER], tsum = 0;
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+        const int e = threadIdx.x * PER + j;
+        v[j] = e < E ? off_s[e] : 0;
+        tsum += v[j];
+    }
+    int32_t incl = tsum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int32_t n = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += n;
+    }
+    if (lane == 31) warp_tot[wid] = incl;
+    __syncthreads();
+    int32_t base = 0;
+    for (int w = 0; w < wid; ++w) base += warp_tot[w];
+    int32_t run = base + incl - tsum;
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+        const int e = threadIdx.x * PER + j;
+        if (e < E) {
+            off_s[e] = run;
+            offsets[e] = run;
+        }
+        run += v[j];
+    }
+    if (threadIdx.x == 255) offsets[E] = run;
+    __syncthreads();
+    for (int i = threadIdx.x; i < WARPS * E; i += blockDim.x) wh[i] += off_s[i % E];
+    __syncthreads();
+    int32_t *cur = wh + wid * E;
+    const unsigned lt = (1u << lane) - 1u;
+#pragma unroll
+    for (int i = 0; i < SUB / 32; ++i) {
+        const int e = my[i];
+        const int p = s0 + 32 * i + lane;
+        const unsigned m = __match_any_sync(0xFFFFFFFFu, e);
+        int32_t pos = -1;
+        if (e >= 0) pos = cur[e] + __popc(m & lt);
+        __syncwarp();
+        if (e >= 0 && (m & lt) == 0) cur[e] += __popc(m);
+        __syncwarp();
+        if (p < s1) {
+            inv[p] = pos;
+            if (pos >= 0) perm[pos] = p;
+        }
+    }
+}
+
 }  // namespace
+
+int permute_kernel_count(int64_t P)
+{
+    const int64_t nblk = ceil_div(P, CHUNK);
+    return nblk == 1 ? 1 : (nblk == 0 ? 1 : 3);
+}
 
 size_t permute_scratch_bytes(int64_t P, int E)
 {
@@ -152,6 +253,15 @@ cudaError_t launch_permute(const int32_t *idx, int64_t P, int E, int32_t *counts
 {
     const int nblk = int(ceil_div(P, CHUNK));
     int32_t *blockhist = static_cast<int32_t *>(scratch);
+    if (nblk == 1) {
+        const size_t smem = size_t(WARPS + 1) * E * sizeof(int32_t);
+        if (smem > 48 * 1024) {
+            cudaError_t e = cudaFuncSetAttribute(k_perm_single, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+            if (e != cudaSuccess) return e;
+        }
+        k_perm_single<<<1, 256, smem, st>>>(idx, int(P), E, counts, offsets, perm, inv, status);
+        return cudaGetLastError();
+    }
     if (nblk > 0) {
         k_perm_hist<<<nblk, 256, 0, st>>>(idx, P, E, blockhist, status);
     }

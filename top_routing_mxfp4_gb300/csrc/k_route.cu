@@ -1,54 +1,13 @@
-// Router: logits = x W_r^T (+ bias), then per token the top-k experts and the
-// softmax over their logits ("SGLang 0.5.17: Kimi K3 原生 MXFP4 推理架构解析",
-// section "MoE 稀疏激活": score all 896 experts, keep the best 16).
+// Router selection ("SGLang 0.5.17: Kimi K3 原生 MXFP4 推理架构解析", section
+// "MoE 稀疏激活": score all 896 experts, keep the best 16): per token the top-k
+// experts by logit and the softmax over their logits.  The logits GEMM itself
+// runs on the tensor cores (k_gemm_bf16.cu).
 #include <float.h>
 
 #include "lmoe_internal.cuh"
 
 namespace lmoe {
 namespace {
-
-// fp32 tiled GEMM, 32 tokens x 32 experts per CTA, K in chunks of 32.
-// Thread (tx, ty): expert column tx, tokens ty*4 .. ty*4+3.
-constexpr int RB = 32;
-
-__global__ void __launch_bounds__(256) k_router_logits(const uint16_t *__restrict__ x, const float *__restrict__ Wr,
-                                                       const float *__restrict__ bias, int T, int d, int E,
-                                                       float *__restrict__ logits)
-{
-    __shared__ float xs[RB][RB + 1];
-    __shared__ float ws[RB][RB + 1];
-    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-    const int e0 = blockIdx.x * RB, t0 = blockIdx.y * RB;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int c0 = 0; c0 < d; c0 += RB) {
-        // 256 threads load 32x32 of x and 32x32 of Wr (4 each)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int r = ty * 4 + i;
-            const int t = t0 + r, e = e0 + r;
-            xs[r][tx] = t < T ? bf16_bits_to_f32(x[int64_t(t) * d + c0 + tx]) : 0.f;
-            ws[r][tx] = e < E ? Wr[int64_t(e) * d + c0 + tx] : 0.f;
-        }
-        __syncthreads();
-#pragma unroll 8
-        for (int c = 0; c < RB; ++c) {
-            const float wv = ws[tx][c];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) acc[i] = fmaf(xs[ty * 4 + i][c], wv, acc[i]);
-        }
-        __syncthreads();
-    }
-    const int e = e0 + tx;
-    if (e < E) {
-        const float b = bias ? bias[e] : 0.f;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int t = t0 + ty * 4 + i;
-            if (t < T) logits[int64_t(t) * E + e] = bias ? acc[i] + b : acc[i];
-        }
-    }
-}
 
 // (value, id) ordering of the selection: larger value first, then smaller id.
 __device__ __forceinline__ bool better(float va, int ia, float vb, int ib)
@@ -108,15 +67,6 @@ __global__ void __launch_bounds__(256) k_topk_softmax(const float *__restrict__ 
 }
 
 }  // namespace
-
-cudaError_t launch_router_logits(const uint16_t *x, const float *Wr, const float *bias, int T, int d, int E,
-                                 float *logits, cudaStream_t st)
-{
-    if (T == 0) return cudaSuccess;
-    dim3 grid(unsigned(ceil_div(E, RB)), unsigned(ceil_div(T, RB)));
-    k_router_logits<<<grid, 256, 0, st>>>(x, Wr, bias, T, d, E, logits);
-    return cudaGetLastError();
-}
 
 cudaError_t launch_topk_softmax(const float *logits, int T, int E, int k, int32_t *idx, float *w, cudaStream_t st)
 {

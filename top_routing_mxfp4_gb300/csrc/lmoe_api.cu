@@ -54,7 +54,7 @@ bool weights_ok(const lmoe_expert_weights *W)
 //   status | logits | idx | w | counts | offsets | perm | inv | permute scratch
 //   | ffn scratch (padded MXFP8 activations, h, schedule) | yp
 struct FwdLayout {
-    size_t status, logits, idx, w, counts, offsets, perm, inv, pscratch, fscratch, yp, total;
+    size_t status, logits, idx, w, counts, offsets, perm, inv, rscratch, pscratch, fscratch, yp, total;
 };
 
 FwdLayout fwd_layout(const lmoe_dims *d)
@@ -75,6 +75,7 @@ FwdLayout fwd_layout(const lmoe_dims *d)
     L.offsets = take(size_t((E + 1) * 4));
     L.perm = take(size_t(P * 4));
     L.inv = take(size_t(P * 4));
+    L.rscratch = take(router_scratch_bytes(int(T), d->d, int(E)));
     L.pscratch = take(permute_scratch_bytes(P, int(E)));
     L.fscratch = take(ffn_layout(P, d->d, int(E), d->I).total);
     L.yp = take(size_t(P * d->d * 4));
@@ -135,14 +136,27 @@ lmoe_status lmoe_quant_mxfp8(const uint16_t *x_bf16, int64_t rows, int32_t K, ui
     return cuda_status(launch_quant_mxfp8(x_bf16, rows, K, q, s, cudaStream_t(stream)));
 }
 
+size_t lmoe_route_workspace_size(const lmoe_dims *dims)
+{
+    if (!dims_ok(dims)) return 0;
+    return kStatusBytes + router_scratch_bytes(dims->T, dims->d, dims->E);
+}
+
 lmoe_status lmoe_route(const uint16_t *x_bf16, const float *Wr, const float *bias, const lmoe_dims *dims,
-                       float *logits, int32_t *topk_idx, float *topk_w, void *stream)
+                       float *logits, int32_t *topk_idx, float *topk_w, void *workspace, size_t ws_bytes,
+                       void *stream)
 {
     if (!dims_ok(dims)) return LMOE_ERR_INVALID_ARG;
     if (dims->T == 0) return LMOE_OK;
-    if (!x_bf16 || !Wr || !logits || !topk_idx || !topk_w) return LMOE_ERR_INVALID_ARG;
+    if (!x_bf16 || !Wr || !logits || !topk_idx || !topk_w || !aligned(x_bf16, 16) || !aligned(Wr, 16))
+        return LMOE_ERR_INVALID_ARG;
+    if (!workspace || ws_bytes < lmoe_route_workspace_size(dims) || !aligned(workspace, 256)) return LMOE_ERR_WORKSPACE;
     cudaStream_t st = cudaStream_t(stream);
-    cudaError_t e = launch_router_logits(x_bf16, Wr, bias, dims->T, dims->d, dims->E, logits, st);
+    char *ws = static_cast<char *>(workspace);
+    int32_t *status = reinterpret_cast<int32_t *>(ws);
+    cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int32_t), st);
+    if (e == cudaSuccess)
+        e = launch_router_logits(x_bf16, Wr, bias, dims->T, dims->d, dims->E, logits, ws + kStatusBytes, status, st);
     if (e == cudaSuccess) e = launch_topk_softmax(logits, dims->T, dims->E, dims->k, topk_idx, topk_w, st);
     return cuda_status(e);
 }
@@ -203,7 +217,8 @@ lmoe_status lmoe_expert_ffn(const uint8_t *xq, const uint8_t *xs, const lmoe_exp
     cudaStream_t st = cudaStream_t(stream);
     cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(int32_t), st);
     if (e == cudaSuccess) e = launch_ffn_schedule(offsets, dims->E, dims->d, dims->I, L, fs, st);
-    if (e == cudaSuccess) e = launch_gather_pad(xq, xs, dims->T, dims->d, dims->k, dims->E, offsets, perm, L, fs, st);
+    if (e == cudaSuccess) e = launch_gather_pad(xq, xs, dims->T, dims->d, dims->k, dims->E, offsets, perm, topk_w, L, fs,
+                                                   st);
     if (e != cudaSuccess) return cuda_status(e);
     FfnArgs f{W, offsets, perm, topk_w, int(P), dims->d, dims->E, dims->k, dims->I, yp, reinterpret_cast<int32_t *>(ws)};
     return cuda_status(launch_expert_gemms(f, L, fs, st));
@@ -231,7 +246,8 @@ lmoe_status lmoe_forward(const uint16_t *x_bf16, const float *Wr, const float *b
     lmoe_status a = act_ok(dims);
     if (a != LMOE_OK) return a;
     if (dims->T == 0) return LMOE_OK;
-    if (!x_bf16 || !Wr || !y_bf16 || !aligned(x_bf16, 16) || !aligned(y_bf16, 16)) return LMOE_ERR_INVALID_ARG;
+    if (!x_bf16 || !Wr || !y_bf16 || !aligned(x_bf16, 16) || !aligned(Wr, 16) || !aligned(y_bf16, 16))
+        return LMOE_ERR_INVALID_ARG;
     if (!weights_ok(W)) return LMOE_ERR_INVALID_ARG;
     const FwdLayout L = fwd_layout(dims);
     if (!workspace || ws_bytes < L.total || !aligned(workspace, 256)) return LMOE_ERR_WORKSPACE;
@@ -253,13 +269,13 @@ lmoe_status lmoe_forward(const uint16_t *x_bf16, const float *Wr, const float *b
 
     cudaError_t e = mark(0, st);
     if (e == cudaSuccess) e = cudaMemsetAsync(status, 0, sizeof(int32_t), st);
-    if (e == cudaSuccess) e = launch_router_logits(x_bf16, Wr, bias, T, d, E, lg, st);
+    if (e == cudaSuccess) e = launch_router_logits(x_bf16, Wr, bias, T, d, E, lg, ws + L.rscratch, status, st);
     if (e == cudaSuccess) e = launch_topk_softmax(lg, T, E, k, idx, w, st);
     if (e == cudaSuccess) e = mark(1, st);
     if (e == cudaSuccess) e = launch_permute(idx, P, E, counts, offsets, perm, inv, ws + L.pscratch, status, st);
     if (e == cudaSuccess) e = launch_ffn_schedule(offsets, E, d, dims->I, FL, fs, st);
     if (e == cudaSuccess) e = mark(2, st);
-    if (e == cudaSuccess) e = launch_quant_scatter_pad(x_bf16, T, d, k, idx, inv, offsets, FL, fs, st);
+    if (e == cudaSuccess) e = launch_quant_scatter_pad(x_bf16, T, d, k, idx, inv, w, offsets, FL, fs, st);
     if (e == cudaSuccess) e = mark(3, st);
     if (e == cudaSuccess) {
         FfnArgs f{W, offsets, perm, w, int(P), d, E, k, dims->I, yp, status};
@@ -269,6 +285,14 @@ lmoe_status lmoe_forward(const uint16_t *x_bf16, const float *Wr, const float *b
     if (e == cudaSuccess) e = launch_combine(yp, inv, T, d, k, y_bf16, st);
     if (e == cudaSuccess) e = mark(6, st);
     return cuda_status(e);
+}
+
+int32_t lmoe_forward_kernel_count(const lmoe_dims *dims)
+{
+    if (!dims_ok(dims) || dims->T == 0) return 0;
+    const int64_t P = int64_t(dims->T) * dims->k;
+    // router (split, GEMM, reduction), top-k, permute, schedule, scatter, two GEMMs, combine
+    return router_kernel_count(dims->T, dims->d, dims->E) + 1 + permute_kernel_count(P) + 1 + 1 + 2 + 1;
 }
 
 lmoe_status lmoe_set_stage_events(void *const *events, int32_t n)

@@ -95,8 +95,16 @@ __host__ __device__ constexpr int64_t round_up(int64_t a, int64_t b) { return ce
 cudaError_t launch_quant_mxfp4(const float *w, int64_t nmat, int rows, int K, uint8_t *q, uint8_t *s, int layout,
                                cudaStream_t st);
 cudaError_t launch_quant_mxfp8(const uint16_t *x, int64_t rows, int K, uint8_t *q, uint8_t *s, cudaStream_t st);
+// Router logits on the tensor cores (fp32 weights split into three bf16 parts).
+size_t router_scratch_bytes(int T, int d, int E);
+int router_kernel_count(int T, int d, int E);
+int permute_kernel_count(int64_t P);
 cudaError_t launch_router_logits(const uint16_t *x, const float *Wr, const float *bias, int T, int d, int E,
-                                 float *logits, cudaStream_t st);
+                                 float *logits, void *scratch, int32_t *status, cudaStream_t st);
+// out[t][n] = bf16(sum_c x[t][c] W[n][c]), bf16 operands, fp32 accumulation.
+size_t linear_scratch_bytes(int T, int K, int N);
+cudaError_t launch_linear_bf16(const uint16_t *x, const uint16_t *W, int T, int K, int N, uint16_t *out, void *scratch,
+                               int32_t *status, cudaStream_t st);
 cudaError_t launch_topk_softmax(const float *logits, int T, int E, int k, int32_t *idx, float *w, cudaStream_t st);
 
 size_t permute_scratch_bytes(int64_t P, int E);
@@ -109,7 +117,7 @@ cudaError_t launch_permute(const int32_t *idx, int64_t P, int E, int32_t *counts
 struct FfnLayout {
     int NT, SLOT;      // token tile and slot rows
     int64_t rows;      // padded token rows reserved
-    size_t pad_off, tiles_gu, tiles_dn, xq, xs, hq, hs, hs_bytes, total;  // byte offsets / sizes
+    size_t pad_off, tiles_gu, tiles_dn, xq, xs, hq, hs, hs_bytes, w_sorted, total;  // byte offsets / sizes
 };
 FfnLayout ffn_layout(int64_t P, int d, int E, int I);
 
@@ -126,10 +134,12 @@ cudaError_t launch_ffn_schedule(const int32_t *offsets, int E, int d, int I, con
                                 cudaStream_t st);
 // bf16 x[T][d] -> MXFP8 rows at each routed (expert, slot) position
 cudaError_t launch_quant_scatter_pad(const uint16_t *x, int T, int d, int k, const int32_t *idx, const int32_t *inv,
-                                     const int32_t *offsets, const FfnLayout &L, char *scratch, cudaStream_t st);
+                                     const float *topk_w, const int32_t *offsets, const FfnLayout &L, char *scratch,
+                                     cudaStream_t st);
 // MXFP8 rows in token order -> padded layout (row q of perm takes token perm[q]/k)
 cudaError_t launch_gather_pad(const uint8_t *xq, const uint8_t *xs, int T, int d, int k, int E, const int32_t *offsets,
-                              const int32_t *perm, const FfnLayout &L, char *scratch, cudaStream_t st);
+                              const int32_t *perm, const float *topk_w, const FfnLayout &L, char *scratch,
+                              cudaStream_t st);
 // gate/up GEMM (+ SwiGLU, MXFP8 of h), event `mid` (if set), down GEMM (x gate weight)
 cudaError_t launch_expert_gemms(const FfnArgs &a, const FfnLayout &L, char *scratch, cudaStream_t st,
                                 cudaEvent_t mid = nullptr);

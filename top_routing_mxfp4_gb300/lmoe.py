@@ -14,7 +14,8 @@ import os
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "liblmoe.so")
+# LMOE_LIBRARY selects another build of the same library (e.g. a trace build)
+LIB_PATH = os.environ.get("LMOE_LIBRARY") or os.path.join(_PKG, "liblmoe.so")
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(f"{LIB_PATH} is missing: build it with `python -c \"import __graft_entry__ as g; g.build()\"` "
@@ -61,7 +62,8 @@ _status_string = _sig("lmoe_status_string", ctypes.c_char_p, ctypes.c_int)
 _mxfp4_bytes = _sig("lmoe_mxfp4_bytes", _sz, _i64, _i32, _i32, _i32, ctypes.POINTER(_sz))
 _quant_mxfp4 = _sig("lmoe_quant_mxfp4", ctypes.c_int, _vp, _i64, _i32, _i32, _vp, _vp, _i32, _vp)
 _quant_mxfp8 = _sig("lmoe_quant_mxfp8", ctypes.c_int, _vp, _i64, _i32, _vp, _vp, _vp)
-_route = _sig("lmoe_route", ctypes.c_int, _vp, _vp, _vp, _DP, _vp, _vp, _vp, _vp)
+_route = _sig("lmoe_route", ctypes.c_int, _vp, _vp, _vp, _DP, _vp, _vp, _vp, _vp, _sz, _vp)
+_route_ws = _sig("lmoe_route_workspace_size", _sz, _DP)
 _topk = _sig("lmoe_topk_from_logits", ctypes.c_int, _vp, _DP, _vp, _vp, _vp)
 _perm_ws = _sig("lmoe_permute_workspace_size", _sz, _DP)
 _permute = _sig("lmoe_permute", ctypes.c_int, _vp, _DP, _vp, _vp, _vp, _vp, _vp, _sz, _vp)
@@ -73,6 +75,12 @@ _forward = _sig("lmoe_forward", ctypes.c_int, _vp, _vp, _vp, _WP, _DP, _vp, _vp,
 _last_status = _sig("lmoe_last_device_status", ctypes.c_int, _vp, ctypes.POINTER(_i32))
 _clear_status = _sig("lmoe_clear_device_status", ctypes.c_int, _vp, _vp)
 _set_events = _sig("lmoe_set_stage_events", ctypes.c_int, ctypes.POINTER(_vp), _i32)
+_kernel_count = _sig("lmoe_forward_kernel_count", _i32, _DP)
+
+
+def forward_kernel_count(T: int, d: int, E: int, k: int, I: int) -> int:
+    D = dims(T, d, E, k, I)
+    return int(_kernel_count(ctypes.byref(D)))
 NUM_STAGE_EVENTS = 7
 STAGES = ("route", "permute", "act_quant", "gate_up", "down", "combine")
 
@@ -222,8 +230,9 @@ def route(x, Wr, k: int, bias=None, stream=None):
     logits = _empty((T, E), torch.float32, x.device)
     idx = _empty((T, k), torch.int32, x.device)
     w = _empty((T, k), torch.float32, x.device)
-    _check(_route(_ptr(x), _ptr(Wr), _ptr(bias), ctypes.byref(D), _ptr(logits), _ptr(idx), _ptr(w),
-                  _stream(stream)), "lmoe_route")
+    ws = workspace(_route_ws(ctypes.byref(D)), x.device)
+    _check(_route(_ptr(x), _ptr(Wr), _ptr(bias), ctypes.byref(D), _ptr(logits), _ptr(idx), _ptr(w), _ptr(ws),
+                  ws.numel(), _stream(stream)), "lmoe_route")
     return logits, idx, w
 
 
