@@ -150,6 +150,24 @@ size_t lmoe_permute_workspace_size(const lmoe_dims *dims);
 lmoe_status lmoe_permute(const int32_t *topk_idx, const lmoe_dims *dims, int32_t *counts, int32_t *offsets,
                          int32_t *perm, int32_t *inv, void *workspace, size_t ws_bytes, void *stream);
 
+/* lmoe_permute for callers that can neither pass a workspace nor let the
+ * library allocate (no counterpart on the pages: this is a deployment aid).
+ * Such callers include plugin code running inside another runtime's memory
+ * pool and serving loops whose device memory is fixed at start-up.  The
+ * block histograms live in a fixed device array inside the library, sized
+ * for at most LMOE_PERMUTE_NOALLOC_MAX_PAIRS = T*k pairs and 2048 experts
+ * (about 1 MB, held on every device that loads the library until the process
+ * exits).  Larger inputs are rejected with LMOE_ERR_INVALID_ARG before any
+ * work is enqueued.  Outputs and their meaning are those of lmoe_permute.
+ * `device_status` (nullable, a device int32) receives the device-side check
+ * result (LMOE_OK or LMOE_ERR_DEVICE_CHECK).  The first call on a device
+ * looks up the array's device address; make it before any stream capture.
+ * All calls share the array, so calls that overlap on the GPU race: the
+ * caller serialises them.  Nothing is allocated. */
+#define LMOE_PERMUTE_NOALLOC_MAX_PAIRS 524288
+lmoe_status lmoe_permute_noalloc(const int32_t *topk_idx, const lmoe_dims *dims, int32_t *counts, int32_t *offsets,
+                                 int32_t *perm, int32_t *inv, int32_t *device_status, void *stream);
+
 /* Scratch bytes lmoe_expert_ffn needs for these dims. */
 size_t lmoe_expert_ffn_workspace_size(const lmoe_dims *dims);
 

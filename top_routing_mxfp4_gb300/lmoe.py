@@ -67,6 +67,8 @@ _route_ws = _sig("lmoe_route_workspace_size", _sz, _DP)
 _topk = _sig("lmoe_topk_from_logits", ctypes.c_int, _vp, _DP, _vp, _vp, _vp)
 _perm_ws = _sig("lmoe_permute_workspace_size", _sz, _DP)
 _permute = _sig("lmoe_permute", ctypes.c_int, _vp, _DP, _vp, _vp, _vp, _vp, _vp, _sz, _vp)
+_permute_noalloc = _sig("lmoe_permute_noalloc", ctypes.c_int, _vp, _DP, _vp, _vp, _vp, _vp, _vp, _vp)
+PERMUTE_NOALLOC_MAX_PAIRS = 524288
 _ffn_ws = _sig("lmoe_expert_ffn_workspace_size", _sz, _DP)
 _ffn = _sig("lmoe_expert_ffn", ctypes.c_int, _vp, _vp, _WP, _vp, _vp, _vp, _DP, _vp, _vp, _sz, _vp)
 _combine = _sig("lmoe_combine", ctypes.c_int, _vp, _vp, _DP, _vp, _vp)
@@ -264,6 +266,24 @@ def permute(idx, E: int, ws=None, stream=None):
     _check(_permute(_ptr(idx), ctypes.byref(D), _ptr(counts), _ptr(offsets), _ptr(perm), _ptr(inv), _ptr(ws),
                     ws.numel(), _stream(stream)), "lmoe_permute")
     return counts, offsets, perm, inv, ws
+
+
+def permute_noalloc(idx, E: int, out=None, stream=None):
+    """lmoe_permute_noalloc: the permute with no workspace (the library's fixed
+    device array holds the scratch).  `out` may pass preallocated
+    (counts, offsets, perm, inv, device_status) tensors, so the call itself
+    allocates nothing."""
+    T, k = idx.shape
+    _need(idx, torch.int32, (T, k), "topk_idx")
+    D = dims(T, 128, E, k, 32)
+    dev = idx.device
+    if out is None:
+        out = (_empty(E, torch.int32, dev), _empty(E + 1, torch.int32, dev), _empty(T * k, torch.int32, dev),
+               _empty(T * k, torch.int32, dev), _empty(1, torch.int32, dev))
+    counts, offsets, perm, inv, status = out
+    _check(_permute_noalloc(_ptr(idx), ctypes.byref(D), _ptr(counts), _ptr(offsets), _ptr(perm), _ptr(inv),
+                            _ptr(status), _stream(stream)), "lmoe_permute_noalloc")
+    return counts, offsets, perm, inv, status
 
 
 def expert_ffn(xq, xs, bank: ExpertBank, offsets, perm, topk_w, k: int, ws=None, stream=None):
