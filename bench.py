@@ -55,6 +55,34 @@ def dist_env():
     return ws, rank, local
 
 
+def gemm_source_hash() -> str:
+    import hashlib
+    csrc = os.path.join(ROOT, "top_routing_mxfp4_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in ("k_ffn_tc.cu", "tc_ptx.cuh", "lmoe_internal.cuh"):
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per gate/up launch from the committed ncu summary of this
+    workload, or None when the GEMM source has changed since the capture."""
+    path = os.path.join(ROOT, "profiles", f"k_moe_gemm_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    meta = {}
+    for line in open(path):
+        if ":" in line and line.split(":")[0].strip() in ("gemm_source_sha256_16", "traffic_bytes_per_launch"):
+            k, v = line.split(":", 1)
+            meta[k.strip()] = v.strip()
+    if meta.get("gemm_source_sha256_16") != gemm_source_hash():
+        return None
+    for kv in meta.get("traffic_bytes_per_launch", "").split():
+        if kv.startswith("gate_up="):
+            return int(kv.split("=")[1])
+    return None
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -258,7 +286,8 @@ def run_ours(args, ws, rank, local):
                          f"of weights read per step (L2 129 MB)"},
         "roofline": {"bound": "hbm", "kernel": "gate/up expert GEMM", "achieved": achieved,
                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                     "traffic": None, "peak_source": peaks["source"],
+                     "traffic": profiled_traffic(wl.name), "traffic_unit": "bytes per launch (ncu)",
+                     "algorithmic_bytes": gateup_bytes, "peak_source": peaks["source"],
                      "layer_weight_gbs": layer_weight_gbs, "layer_frac": layer_weight_gbs / peaks["hbm_gbs"]},
         "stage_ms": stage_ms, "touched_experts": touched,
         "e2e": {"value": ws * T / (e2e_ms / K / 1e3), "unit": UNIT, "h2d_bytes_per_step": xh.numel() * 2,

@@ -199,6 +199,27 @@ lmoe_status lmoe_forward(const uint16_t *x_bf16, const float *Wr, const float *b
                          const lmoe_dims *dims, uint16_t *y_bf16, int32_t *topk_idx, float *topk_w, float *logits,
                          void *workspace, size_t ws_bytes, void *stream);
 
+/* ---- full block around the layer ([L1] section 一: LatentMoE compresses the
+ * hidden state to the latent space, routes and computes experts there) ---- */
+
+/* out[r][n] = bf16( sum_c x[r][c] * W[n][c] ), x bf16 [rows][K], W bf16 [N][K],
+ * fp32 accumulation on the tensor cores, round to nearest even.
+ * K % 64 == 0, N % 16 == 0. */
+lmoe_status lmoe_linear_bf16(const uint16_t *x, const uint16_t *W, int64_t rows, int32_t K, int32_t N, uint16_t *out,
+                             void *stream);
+
+/* Scratch bytes lmoe_forward_block needs for these dims and hidden width. */
+size_t lmoe_block_workspace_size(const lmoe_dims *dims, int32_t hidden);
+
+/* lat = bf16(x_h W_in^T) [T][d]; y = lmoe_forward(lat) [T][d];
+ * out = bf16(y W_out^T) [T][hidden].  x_h bf16 [T][hidden], W_in bf16
+ * [d][hidden], W_out bf16 [hidden][d]; hidden % 64 == 0.  Optional outputs
+ * (NULL to skip): lat and y (bf16 [T][d]), topk_idx, topk_w, logits. */
+lmoe_status lmoe_forward_block(const uint16_t *x_h, const uint16_t *W_in, const float *Wr, const float *bias,
+                               const lmoe_expert_weights *W, const uint16_t *W_out, const lmoe_dims *dims,
+                               int32_t hidden, uint16_t *out, uint16_t *lat, uint16_t *y, int32_t *topk_idx,
+                               float *topk_w, float *logits, void *workspace, size_t ws_bytes, void *stream);
+
 /* ---- helpers --------------------------------------------------------------- */
 
 /* Reads (synchronously, after all prior work on the device) the status word

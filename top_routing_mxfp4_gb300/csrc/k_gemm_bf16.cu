@@ -246,12 +246,13 @@ __global__ void k_split_bf16x3(const float *__restrict__ w, int64_t n, __nv_bflo
     }
 }
 
-// out[t][m] = sum_{s < KS} part[s][t][m] (+ bias[m]), fixed order.
+// logits[t][m] = sum_{s < KS} part[s][t][m] (+ bias[m]), slices in fixed order.
 __global__ void k_splitk_reduce(const float *__restrict__ part, int KS, int64_t TM, int M, const float *__restrict__ bias,
                                 float *__restrict__ out)
 {
     for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < TM; i += int64_t(gridDim.x) * blockDim.x) {
         float acc = 0.f;
+#pragma unroll 8
         for (int s = 0; s < KS; ++s) acc += __ldg(part + int64_t(s) * TM + i);
         out[i] = bias ? acc + __ldg(bias + i % M) : acc;
     }
@@ -334,7 +335,7 @@ int router_kernel_count(int T, int d, int E)
 {
     int NB, KS;
     plan(T, E, d, NB, KS);
-    return KS > 1 ? 3 : 2;  // split, GEMM (+ split-K reduction)
+    return KS > 1 ? 4 : 3;  // split, GEMM, (split-K reduction), top-k
 }
 
 size_t router_scratch_bytes(int T, int d, int E)
@@ -344,8 +345,8 @@ size_t router_scratch_bytes(int T, int d, int E)
     return size_t(round_up(int64_t(3) * E * d * 2, 256)) + (KS > 1 ? size_t(round_up(int64_t(KS) * T * E * 4, 256)) : 0);
 }
 
-cudaError_t launch_router_logits(const uint16_t *x, const float *Wr, const float *bias, int T, int d, int E,
-                                 float *logits, void *scratch, int32_t *status, cudaStream_t st)
+cudaError_t launch_route(const uint16_t *x, const float *Wr, const float *bias, int T, int d, int E, int k,
+                         float *logits, int32_t *idx, float *w, void *scratch, int32_t *status, cudaStream_t st)
 {
     if (T == 0) return cudaSuccess;
     __nv_bfloat16 *w3 = static_cast<__nv_bfloat16 *>(scratch);
@@ -361,7 +362,11 @@ cudaError_t launch_router_logits(const uint16_t *x, const float *Wr, const float
         !make_bf16_map(&mb, x, uint64_t(d), uint64_t(T), uint32_t(NB)))
         return cudaErrorInvalidValue;
     DenseArgs a{E, T, d, int(ceil_div(E, 128)), int(ceil_div(T, NB)), KS, d / 64 / KS, bias, logits, status};
-    if (KS == 1) return dispatch<3, OUT_F32>(NB, ma, mb, a, st);
+    if (KS == 1) {
+        e = dispatch<3, OUT_F32>(NB, ma, mb, a, st);
+        if (e != cudaSuccess) return e;
+        return launch_topk_softmax(logits, T, E, k, idx, w, st);
+    }
     a.out = partial;
     a.bias = nullptr;
     e = dispatch<3, OUT_PARTIAL>(NB, ma, mb, a, st);
@@ -369,7 +374,9 @@ cudaError_t launch_router_logits(const uint16_t *x, const float *Wr, const float
     const int64_t TM = int64_t(T) * E;
     k_splitk_reduce<<<int(ceil_div(TM, 256) < 152 * 8 ? ceil_div(TM, 256) : 152 * 8), 256, 0, st>>>(partial, KS, TM, E,
                                                                                                     bias, logits);
-    return cudaGetLastError();
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return launch_topk_softmax(logits, T, E, k, idx, w, st);
 }
 
 size_t linear_scratch_bytes(int T, int K, int N)

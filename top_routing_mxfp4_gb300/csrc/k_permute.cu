@@ -142,27 +142,38 @@ __global__ void __launch_bounds__(256) k_perm_scatter(const int32_t *__restrict_
 // All of the above in one CTA when the pairs fit one chunk (P <= CHUNK):
 // per-warp histograms -> counts and per-warp starts -> exclusive scan over
 // experts -> ordered scatter.  Used for decode-sized batches, where three
-// launches would cost more than the work.
+// launches would cost more than the work.  The P pairs are split over the 8
+// warps in consecutive runs of `sub` (a multiple of 32), so every warp
+// works; all expert ids are loaded before the shared-memory atomics.
 __global__ void __launch_bounds__(256) k_perm_single(const int32_t *__restrict__ idx, int P, int E,
                                                      int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
                                                      int32_t *__restrict__ perm, int32_t *__restrict__ inv,
                                                      int32_t *status)
 {
-    extern __shared__ int32_t wh[];  // [WARPS][E]
+    extern __shared__ int4 wh_raw[];
+    int32_t *wh = reinterpret_cast<int32_t *>(wh_raw);  // [WARPS][E]
     __shared__ int32_t warp_tot[WARPS];
-    int32_t *off_s = wh + WARPS * E;  // [E]
+    int32_t *off_s = wh + WARPS * E;                    // [E]
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    for (int i = threadIdx.x; i < WARPS * E; i += blockDim.x) wh[i] = 0;
-    __syncthreads();
-    const int s0 = wid * SUB, s1 = min(P, s0 + SUB);
+    for (int i = threadIdx.x; i < (WARPS * E) / 4; i += blockDim.x) wh_raw[i] = make_int4(0, 0, 0, 0);
+    const int sub = (P + WARPS * 32 - 1) / (WARPS * 32) * 32;  // pairs per warp, <= SUB
+    const int steps = sub / 32;
+    const int s0 = wid * sub, s1 = min(P, s0 + sub);
     int32_t my[SUB / 32];
 #pragma unroll
     for (int i = 0; i < SUB / 32; ++i) {
         const int p = s0 + 32 * i + lane;
-        int e = p < s1 ? __ldg(idx + p) : -1;
-        if (p < s1 && (e < 0 || e >= E)) {
+        my[i] = (i < steps && p < s1) ? __ldg(idx + p) : -1;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < SUB / 32; ++i) {
+        int e = my[i];
+        if (e >= E) {
             set_status(status, LMOE_ERR_DEVICE_CHECK);
             e = -1;
+        } else if (e < 0 && i < steps && s0 + 32 * i + lane < s1) {
+            set_status(status, LMOE_ERR_DEVICE_CHECK);
         }
         my[i] = e;
         if (e >= 0) atomicAdd(&wh[wid * E + e], 1);
@@ -199,9 +210,9 @@ __global__ void __launch_bounds__(256) k_perm_single(const int32_t *__restrict__
     if (lane == 31) warp_tot[wid] = incl;
     __syncthreads();
     int32_t base = 0;
-    for (int w = 0; w < wid; ++w) base += warp_tot[w];
+#pragma unroll
+    for (int w = 0; w < WARPS; ++w) base += (w < wid) ? warp_tot[w] : 0;
     int32_t run = base + incl - tsum;
-    __syncthreads();
 #pragma unroll
     for (int j = 0; j < PER; ++j) {
         const int e = threadIdx.x * PER + j;
@@ -213,12 +224,17 @@ __global__ void __launch_bounds__(256) k_perm_single(const int32_t *__restrict__
     }
     if (threadIdx.x == 255) offsets[E] = run;
     __syncthreads();
-    for (int i = threadIdx.x; i < WARPS * E; i += blockDim.x) wh[i] += off_s[i % E];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        const int32_t o = off_s[e];
+#pragma unroll
+        for (int w = 0; w < WARPS; ++w) wh[w * E + e] += o;
+    }
     __syncthreads();
     int32_t *cur = wh + wid * E;
     const unsigned lt = (1u << lane) - 1u;
 #pragma unroll
     for (int i = 0; i < SUB / 32; ++i) {
+        if (i >= steps) break;
         const int e = my[i];
         const int p = s0 + 32 * i + lane;
         const unsigned m = __match_any_sync(0xFFFFFFFFu, e);
@@ -254,7 +270,7 @@ cudaError_t launch_permute(const int32_t *idx, int64_t P, int E, int32_t *counts
     const int nblk = int(ceil_div(P, CHUNK));
     int32_t *blockhist = static_cast<int32_t *>(scratch);
     if (nblk == 1) {
-        const size_t smem = size_t(WARPS + 1) * E * sizeof(int32_t);
+        const size_t smem = size_t(WARPS + 1) * E * sizeof(int32_t) + 16;
         if (smem > 48 * 1024) {
             cudaError_t e = cudaFuncSetAttribute(k_perm_single, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
             if (e != cudaSuccess) return e;

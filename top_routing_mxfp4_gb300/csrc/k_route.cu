@@ -3,6 +3,7 @@
 // experts by logit and the softmax over their logits.  The logits GEMM itself
 // runs on the tensor cores (k_gemm_bf16.cu).
 #include <float.h>
+#include <math.h>
 
 #include "lmoe_internal.cuh"
 
@@ -15,36 +16,54 @@ __device__ __forceinline__ bool better(float va, int ia, float vb, int ib)
     return va > vb || (va == vb && ia < ib);
 }
 
-// One warp per token.  Lane l holds experts l, l+32, ... (NV values).
+// Best (value, slot) of a lane's NV values by a pairwise tournament: depth
+// log2(NV) instead of an NV-long dependent chain.  Equal values keep the
+// smaller slot, i.e. the smaller expert id (id = lane + 32 * slot).
 template <int NV>
-__global__ void __launch_bounds__(256) k_topk_softmax(const float *__restrict__ logits, int T, int E, int k,
-                                                      int32_t *__restrict__ idx, float *__restrict__ w)
+__device__ __forceinline__ void lane_best(const float *v, float &bv, int &bs)
+{
+    float tv[NV];
+    int ts[NV];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        tv[i] = v[i];
+        ts[i] = i;
+    }
+#pragma unroll
+    for (int width = 1; width < NV; width *= 2) {
+#pragma unroll
+        for (int i = 0; i + width < NV; i += 2 * width) {
+            // tv[i] holds the best of [i, i+width), tv[i+width] of [i+width, i+2*width)
+            const bool take = tv[i + width] > tv[i];  // ties keep the left (smaller slot)
+            tv[i] = take ? tv[i + width] : tv[i];
+            ts[i] = take ? ts[i + width] : ts[i];
+        }
+    }
+    bv = tv[0];
+    bs = ts[0];
+}
+
+// One warp per token.  Lane l holds experts l, l+32, ... (NV values); a taken
+// or absent expert holds -inf.
+// The selection of one token by one warp from its logits row `row` (any
+// memory space): slots j = 0..k-1 of idx / w.
+template <int NV>
+__device__ __forceinline__ void select_topk(const float *row, int E, int k, int32_t *idx_t, float *w_t)
 {
     const int lane = threadIdx.x & 31;
-    const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    if (t >= T) return;
-    const float *row = logits + int64_t(t) * E;
     float v[NV];
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
         const int e = lane + 32 * i;
-        v[i] = e < E ? row[e] : -FLT_MAX;
+        v[i] = e < E ? row[e] : -INFINITY;
     }
-    uint64_t taken = 0;
     float sel_v = 0.f, top_v = 0.f;
     int sel_id = 0;
     for (int j = 0; j < k; ++j) {
-        float bv = -FLT_MAX;
-        int bi = INT32_MAX, bslot = -1;
-#pragma unroll
-        for (int i = 0; i < NV; ++i) {
-            const int e = lane + 32 * i;
-            if (e < E && !((taken >> i) & 1) && better(v[i], e, bv, bi)) {
-                bv = v[i];
-                bi = e;
-                bslot = i;
-            }
-        }
+        float bv;
+        int bs;
+        lane_best<NV>(v, bv, bs);
+        int bi = bv == -INFINITY ? INT32_MAX : lane + 32 * bs;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
             const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
@@ -52,7 +71,11 @@ __global__ void __launch_bounds__(256) k_topk_softmax(const float *__restrict__ 
             if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
         }
         // the owner marks the winner taken
-        if (bslot >= 0 && lane + 32 * bslot == bi) taken |= (1ull << bslot);
+        if ((bi & 31) == lane) {
+            const int slot = bi >> 5;
+#pragma unroll
+            for (int i = 0; i < NV; ++i) v[i] = (i == slot) ? -INFINITY : v[i];
+        }
         if (j == 0) top_v = bv;
         if (lane == j) { sel_v = bv; sel_id = bi; }
     }
@@ -61,9 +84,19 @@ __global__ void __launch_bounds__(256) k_topk_softmax(const float *__restrict__ 
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
     if (lane < k) {
-        idx[int64_t(t) * k + lane] = sel_id;
-        w[int64_t(t) * k + lane] = ex / sum;
+        idx_t[lane] = sel_id;
+        w_t[lane] = ex / sum;
     }
+}
+
+// One warp per token, logits in global memory.
+template <int NV>
+__global__ void __launch_bounds__(256) k_topk_softmax(const float *__restrict__ logits, int T, int E, int k,
+                                                      int32_t *__restrict__ idx, float *__restrict__ w)
+{
+    const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (t >= T) return;
+    select_topk<NV>(logits + int64_t(t) * E, E, k, idx + int64_t(t) * k, w + int64_t(t) * k);
 }
 
 }  // namespace

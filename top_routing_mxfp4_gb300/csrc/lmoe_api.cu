@@ -156,8 +156,8 @@ lmoe_status lmoe_route(const uint16_t *x_bf16, const float *Wr, const float *bia
     int32_t *status = reinterpret_cast<int32_t *>(ws);
     cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int32_t), st);
     if (e == cudaSuccess)
-        e = launch_router_logits(x_bf16, Wr, bias, dims->T, dims->d, dims->E, logits, ws + kStatusBytes, status, st);
-    if (e == cudaSuccess) e = launch_topk_softmax(logits, dims->T, dims->E, dims->k, topk_idx, topk_w, st);
+        e = launch_route(x_bf16, Wr, bias, dims->T, dims->d, dims->E, dims->k, logits, topk_idx, topk_w,
+                         ws + kStatusBytes, status, st);
     return cuda_status(e);
 }
 
@@ -269,8 +269,7 @@ lmoe_status lmoe_forward(const uint16_t *x_bf16, const float *Wr, const float *b
 
     cudaError_t e = mark(0, st);
     if (e == cudaSuccess) e = cudaMemsetAsync(status, 0, sizeof(int32_t), st);
-    if (e == cudaSuccess) e = launch_router_logits(x_bf16, Wr, bias, T, d, E, lg, ws + L.rscratch, status, st);
-    if (e == cudaSuccess) e = launch_topk_softmax(lg, T, E, k, idx, w, st);
+    if (e == cudaSuccess) e = launch_route(x_bf16, Wr, bias, T, d, E, k, lg, idx, w, ws + L.rscratch, status, st);
     if (e == cudaSuccess) e = mark(1, st);
     if (e == cudaSuccess) e = launch_permute(idx, P, E, counts, offsets, perm, inv, ws + L.pscratch, status, st);
     if (e == cudaSuccess) e = launch_ffn_schedule(offsets, E, d, dims->I, FL, fs, st);
@@ -287,12 +286,57 @@ lmoe_status lmoe_forward(const uint16_t *x_bf16, const float *Wr, const float *b
     return cuda_status(e);
 }
 
+lmoe_status lmoe_linear_bf16(const uint16_t *x, const uint16_t *W, int64_t rows, int32_t K, int32_t N, uint16_t *out,
+                             void *stream)
+{
+    if (rows < 0 || rows > INT32_MAX || K <= 0 || K % 64 != 0 || N <= 0 || N % 16 != 0) return LMOE_ERR_INVALID_ARG;
+    if (rows == 0) return LMOE_OK;
+    if (!x || !W || !out || !aligned(x, 16) || !aligned(W, 16) || !aligned(out, 16)) return LMOE_ERR_INVALID_ARG;
+    return cuda_status(launch_linear_bf16(x, W, int(rows), K, N, out, nullptr, nullptr, cudaStream_t(stream)));
+}
+
+size_t lmoe_block_workspace_size(const lmoe_dims *dims, int32_t hidden)
+{
+    if (!dims_ok(dims) || hidden <= 0 || hidden % 64 != 0) return 0;
+    const size_t lat = size_t(round_up(int64_t(dims->T) * dims->d * 2, 256));
+    return 2 * lat + lmoe_workspace_size(dims);
+}
+
+lmoe_status lmoe_forward_block(const uint16_t *x_h, const uint16_t *W_in, const float *Wr, const float *bias,
+                               const lmoe_expert_weights *W, const uint16_t *W_out, const lmoe_dims *dims,
+                               int32_t hidden, uint16_t *out, uint16_t *lat, uint16_t *y, int32_t *topk_idx,
+                               float *topk_w, float *logits, void *workspace, size_t ws_bytes, void *stream)
+{
+    if (!dims_ok(dims) || hidden <= 0 || hidden % 64 != 0) return LMOE_ERR_INVALID_ARG;
+    lmoe_status a = act_ok(dims);
+    if (a != LMOE_OK) return a;
+    if (dims->T == 0) return LMOE_OK;
+    if (!x_h || !W_in || !W_out || !out || !aligned(x_h, 16) || !aligned(W_in, 16) || !aligned(W_out, 16) ||
+        !aligned(out, 16) || (lat && !aligned(lat, 16)) || (y && !aligned(y, 16)))
+        return LMOE_ERR_INVALID_ARG;
+    if (!Wr || !aligned(Wr, 16) || !weights_ok(W)) return LMOE_ERR_INVALID_ARG;
+    const size_t need = lmoe_block_workspace_size(dims, hidden);
+    if (!workspace || ws_bytes < need || !aligned(workspace, 256)) return LMOE_ERR_WORKSPACE;
+    char *ws = static_cast<char *>(workspace);
+    const size_t latb = size_t(round_up(int64_t(dims->T) * dims->d * 2, 256));
+    uint16_t *lat_buf = lat ? lat : reinterpret_cast<uint16_t *>(ws);
+    uint16_t *y_buf = y ? y : reinterpret_cast<uint16_t *>(ws + latb);
+    void *fws = ws + 2 * latb;
+    cudaStream_t st = cudaStream_t(stream);
+    cudaError_t e = launch_linear_bf16(x_h, W_in, dims->T, hidden, dims->d, lat_buf, nullptr, nullptr, st);
+    if (e != cudaSuccess) return cuda_status(e);
+    lmoe_status s = lmoe_forward(lat_buf, Wr, bias, W, dims, y_buf, topk_idx, topk_w, logits, fws,
+                                 ws_bytes - 2 * latb, stream);
+    if (s != LMOE_OK) return s;
+    return cuda_status(launch_linear_bf16(y_buf, W_out, dims->T, dims->d, hidden, out, nullptr, nullptr, st));
+}
+
 int32_t lmoe_forward_kernel_count(const lmoe_dims *dims)
 {
     if (!dims_ok(dims) || dims->T == 0) return 0;
     const int64_t P = int64_t(dims->T) * dims->k;
-    // router (split, GEMM, reduction), top-k, permute, schedule, scatter, two GEMMs, combine
-    return router_kernel_count(dims->T, dims->d, dims->E) + 1 + permute_kernel_count(P) + 1 + 1 + 2 + 1;
+    // router (split, GEMM, top-k), permute, schedule, scatter, two GEMMs, combine
+    return router_kernel_count(dims->T, dims->d, dims->E) + permute_kernel_count(P) + 1 + 1 + 2 + 1;
 }
 
 lmoe_status lmoe_set_stage_events(void *const *events, int32_t n)

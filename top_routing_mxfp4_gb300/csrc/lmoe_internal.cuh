@@ -97,15 +97,17 @@ cudaError_t launch_quant_mxfp4(const float *w, int64_t nmat, int rows, int K, ui
 cudaError_t launch_quant_mxfp8(const uint16_t *x, int64_t rows, int K, uint8_t *q, uint8_t *s, cudaStream_t st);
 // Router logits on the tensor cores (fp32 weights split into three bf16 parts).
 size_t router_scratch_bytes(int T, int d, int E);
-int router_kernel_count(int T, int d, int E);
+int router_kernel_count(int T, int d, int E);  // kernels of launch_route, top-k included
 int permute_kernel_count(int64_t P);
-cudaError_t launch_router_logits(const uint16_t *x, const float *Wr, const float *bias, int T, int d, int E,
-                                 float *logits, void *scratch, int32_t *status, cudaStream_t st);
 // out[t][n] = bf16(sum_c x[t][c] W[n][c]), bf16 operands, fp32 accumulation.
 size_t linear_scratch_bytes(int T, int K, int N);
 cudaError_t launch_linear_bf16(const uint16_t *x, const uint16_t *W, int T, int K, int N, uint16_t *out, void *scratch,
                                int32_t *status, cudaStream_t st);
+// Top-k + softmax of fp32 logits [T][E].
 cudaError_t launch_topk_softmax(const float *logits, int T, int E, int k, int32_t *idx, float *w, cudaStream_t st);
+// Router logits + top-k + softmax (split, GEMM, split-K reduction, selection).
+cudaError_t launch_route(const uint16_t *x, const float *Wr, const float *bias, int T, int d, int E, int k,
+                         float *logits, int32_t *idx, float *w, void *scratch, int32_t *status, cudaStream_t st);
 
 size_t permute_scratch_bytes(int64_t P, int E);
 cudaError_t launch_permute(const int32_t *idx, int64_t P, int E, int32_t *counts, int32_t *offsets, int32_t *perm,

@@ -74,6 +74,10 @@ _ffn = _sig("lmoe_expert_ffn", ctypes.c_int, _vp, _vp, _WP, _vp, _vp, _vp, _DP, 
 _combine = _sig("lmoe_combine", ctypes.c_int, _vp, _vp, _DP, _vp, _vp)
 _ws_size = _sig("lmoe_workspace_size", _sz, _DP)
 _forward = _sig("lmoe_forward", ctypes.c_int, _vp, _vp, _vp, _WP, _DP, _vp, _vp, _vp, _vp, _vp, _sz, _vp)
+_linear = _sig("lmoe_linear_bf16", ctypes.c_int, _vp, _vp, _i64, _i32, _i32, _vp, _vp)
+_block_ws = _sig("lmoe_block_workspace_size", _sz, _DP, _i32)
+_forward_block = _sig("lmoe_forward_block", ctypes.c_int, _vp, _vp, _vp, _vp, _WP, _vp, _DP, _i32, _vp, _vp, _vp, _vp,
+                      _vp, _vp, _vp, _sz, _vp)
 _last_status = _sig("lmoe_last_device_status", ctypes.c_int, _vp, ctypes.POINTER(_i32))
 _clear_status = _sig("lmoe_clear_device_status", ctypes.c_int, _vp, _vp)
 _set_events = _sig("lmoe_set_stage_events", ctypes.c_int, ctypes.POINTER(_vp), _i32)
@@ -346,6 +350,43 @@ class Layer:
 
     def device_status(self) -> int:
         return last_device_status(self._ws)
+
+
+def linear_bf16(x, W, out=None, stream=None):
+    """out = bf16(x W^T): x bf16 [rows, K], W bf16 [N, K]."""
+    rows, K = x.shape
+    N = W.shape[0]
+    _need(x, torch.bfloat16, (rows, K), "x")
+    _need(W, torch.bfloat16, (N, K), "W")
+    out = _empty((rows, N), torch.bfloat16, x.device) if out is None else out
+    _check(_linear(_ptr(x), _ptr(W), rows, K, N, _ptr(out), _stream(stream)), "lmoe_linear_bf16")
+    return out
+
+
+class Block:
+    """hidden -> latent projection, the LatentMoE layer, latent -> hidden."""
+
+    def __init__(self, W_in: torch.Tensor, layer: Layer, W_out: torch.Tensor):
+        self.W_in, self.layer, self.W_out = W_in, layer, W_out
+        self._ws = None
+
+    def forward(self, x_h, out=None, lat=None, y=None, topk_idx=None, topk_w=None, logits=None, stream=None):
+        T, hidden = x_h.shape
+        bank, k = self.layer.bank, self.layer.k
+        _need(x_h, torch.bfloat16, (T, hidden), "x_h")
+        _need(self.W_in, torch.bfloat16, (bank.d, hidden), "W_in")
+        _need(self.W_out, torch.bfloat16, (hidden, bank.d), "W_out")
+        D = dims(T, bank.d, bank.E, k, bank.I)
+        need = int(_block_ws(ctypes.byref(D), hidden))
+        if self._ws is None or self._ws.numel() < need:
+            self._ws = workspace(need, x_h.device)
+        out = _empty((T, hidden), torch.bfloat16, x_h.device) if out is None else out
+        W = bank.struct()
+        _check(_forward_block(_ptr(x_h), _ptr(self.W_in), _ptr(self.layer.Wr), _ptr(self.layer.bias), ctypes.byref(W),
+                              _ptr(self.W_out), ctypes.byref(D), hidden, _ptr(out), _ptr(lat), _ptr(y), _ptr(topk_idx),
+                              _ptr(topk_w), _ptr(logits), _ptr(self._ws), self._ws.numel(), _stream(stream)),
+               "lmoe_forward_block")
+        return out
 
 
 def last_device_status(ws) -> int:
