@@ -113,9 +113,11 @@ struct GemmArgs {
 
 template <int MODE, int NT>
 struct Cfg {
-    // Weight tiles per stage: gate and up rows of the same 128 features, or
-    // two consecutive 128-row tiles of down.
-    static constexpr int MATS = 2;
+    // Weight tiles per stage: gate and up rows of the same 128 features; for
+    // down, two consecutive 128-row tiles when token tiles are small (more
+    // bytes per pipeline stage), one tile when they are large (so the
+    // accumulators can be double-buffered in TMEM).
+    static constexpr int MATS = (MODE == GATEUP || NT <= 32) ? 2 : 1;
     static constexpr int SLOT = (NT + 127) / 128 * 128;
     static constexpr int NAT = (NT + 127) / 128;  // B scale atoms per stage
     static constexpr uint32_t A_TILE = 128 * 128;  // smem bytes of one expanded FP4 A tile
@@ -125,15 +127,15 @@ struct Cfg {
     static constexpr uint32_t STAGE_BYTES = (SFB_OFF + NAT * 512 + 1023) / 1024 * 1024;
     // global bytes per stage: packed FP4 tiles count 64 bytes per 128-element row
     static constexpr uint32_t TX_BYTES = MATS * 128 * 64 + B_TILE + MATS * 512 + NAT * 512;
-    // Two MMA-issuing threads, one per weight tile, each with its own
-    // accumulator.  One thread issues a tcgen05 instruction only every few
-    // dozen cycles, so two issuers keep small-N MMAs from pacing the pipeline.
-    static constexpr int ACC_COLS_ITEM = 2 * NT;
+    // One MMA-issuing thread per weight tile, each with its own accumulator.
+    // One thread issues a tcgen05 instruction only every few dozen cycles, so
+    // two issuers keep small-N MMAs from pacing the pipeline.
+    static constexpr int ACC_COLS_ITEM = MATS * NT;
     static constexpr int ACC_STAGES = (ACC_COLS_ITEM <= 64) ? 4 : (2 * ACC_COLS_ITEM <= 256 ? 2 : 1);
     static constexpr int ACC_COLS = ACC_STAGES * ACC_COLS_ITEM;
     static constexpr int SF_BASE = (ACC_COLS + 31) / 32 * 32;
     static constexpr int SF_COLS_ISSUER = 4 + 4 * NAT;  // this issuer's SFA and SFB copies
-    static constexpr int SF_COLS = 2 * SF_COLS_ISSUER;
+    static constexpr int SF_COLS = MATS * SF_COLS_ISSUER;
     static constexpr int MAX_STAGES = (512 - SF_BASE) / SF_COLS < 16 ? (512 - SF_BASE) / SF_COLS : 16;
     static_assert(MAX_STAGES >= 2, "TMEM columns");
 };
@@ -187,10 +189,10 @@ __global__ void __launch_bounds__(224, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 2);  // one commit per MMA issuer
+            mbar_init(&empty[s], C::MATS);  // one commit per MMA issuer
         }
         for (int a = 0; a < C::ACC_STAGES; ++a) {
-            mbar_init(&acc_full[a], 2);
+            mbar_init(&acc_full[a], C::MATS);
             mbar_init(&acc_empty[a], 128);
         }
         mbar_init_fence();
@@ -221,7 +223,7 @@ __global__ void __launch_bounds__(224, 1)
                 const int R = slot_row(w.e) + w.n_tile * C::SLOT;
                 // gate/up: tile m of both matrices; down: tiles 2m and 2m+1 (an odd
                 // last tile loads tile 2m twice and the epilogue drops the copy)
-                const int mt0 = MODE == GATEUP ? w.m_tile : 2 * w.m_tile;
+                const int mt0 = MODE == GATEUP ? w.m_tile : C::MATS * w.m_tile;
                 const int mt1 = MODE == GATEUP ? w.m_tile : (mt0 + 1 < p.MTA ? mt0 + 1 : mt0);
                 const int arow = w.e * p.Mtot + mt0 * 128, arow1 = w.e * p.Mtot + mt1 * 128;
                 const int64_t sfa_base = (int64_t(w.e) * p.MTA + mt0) * p.KC;
@@ -236,10 +238,10 @@ __global__ void __launch_bounds__(224, 1)
                     uint8_t *sb = stages + stage * C::STAGE_BYTES;
                     mbar_arrive_expect_tx(&full[stage], C::TX_BYTES);
                     tma_load_2d(sb, &tmA0, kc * 128, arow, &full[stage]);
-                    tma_load_2d(sb + C::A_TILE, &tmA1, kc * 128, arow1, &full[stage]);
+                    if (C::MATS == 2) tma_load_2d(sb + C::A_TILE, &tmA1, kc * 128, arow1, &full[stage]);
                     tma_load_2d(sb + C::MATS * C::A_TILE, &tmB, kc * 128, R, &full[stage]);
                     bulk_load(sb + C::SFA_OFF, p.sfa0 + (sfa_base + kc) * 512, 512, &full[stage]);
-                    bulk_load(sb + C::SFA_OFF + 512, p.sfa1 + (sfa_base1 + kc) * 512, 512, &full[stage]);
+                    if (C::MATS == 2) bulk_load(sb + C::SFA_OFF + 512, p.sfa1 + (sfa_base1 + kc) * 512, 512, &full[stage]);
 #pragma unroll
                     for (int a = 0; a < C::NAT; ++a)
                         bulk_load(sb + C::SFB_OFF + a * 512, p.sfb + (int64_t(R / 128 + a) * p.KC + kc) * 512, 512,
@@ -254,8 +256,8 @@ __global__ void __launch_bounds__(224, 1)
             LMOE_TRACE_END(0);
         }
     } else if (warp == 1 || warp == 6) {
-        // ---------------- MMA issuers (warp 1: gate / low K half, warp 6: up / high K half) ----------------
-        if (lane == 0) {
+        // ---------------- MMA issuers (warp 1: gate / first tile, warp 6: up / second tile) ----------------
+        if (lane == 0 && (warp == 1 || C::MATS == 2)) {
             LMOE_TRACE_DECL
             const int iss = warp == 1 ? 0 : 1;
             int stage = 0, acc = 0;
@@ -382,10 +384,10 @@ __global__ void __launch_bounds__(224, 1)
                 }
             }
             if (MODE == DOWN) {
-                // accumulator h holds output rows (2m + h) * 128 + 32q + lane
+                // accumulator h holds output rows (MATS m + h) * 128 + 32q + lane
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int mt = 2 * w.m_tile + h;
+                for (int h = 0; h < C::MATS; ++h) {
+                    const int mt = C::MATS * w.m_tile + h;
                     if (mt >= p.MTA) break;  // odd last tile: second accumulator is a copy
                     const int row = mt * 128 + 32 * q + lane;
                     for (int c0 = 0; c0 < w.n_valid; c0 += 16) {
@@ -488,11 +490,11 @@ __device__ __forceinline__ int64_t atom_off(int64_t R, int b, int KC)
     return ((R >> 7) * KC + (b >> 2)) * 512 + (R & 31) * 16 + ((R & 127) >> 5) * 4 + (b & 3);
 }
 
-// bf16 x[T][d] -> MXFP8 rows at every (expert, slot) position the token is routed to.
+// bf16 x[T][d] -> MXFP8 rows at every padded row the token's pairs go to
+// (dst_row, written by the permute).
 __global__ void k_quant_scatter_pad(const uint16_t *__restrict__ x, int64_t nblocks, int d, int k,
-                                    const int32_t *__restrict__ idx, const int32_t *__restrict__ inv,
-                                    const float *__restrict__ topk_w, const int32_t *__restrict__ offsets,
-                                    const int32_t *__restrict__ pad_off, int NT, int SLOT, uint8_t *__restrict__ xq,
+                                    const int32_t *__restrict__ dst_row, const int32_t *__restrict__ inv,
+                                    const float *__restrict__ topk_w, uint8_t *__restrict__ xq,
                                     uint8_t *__restrict__ xs, float *__restrict__ w_sorted)
 {
     const int nb = d / 32, KC = d / 128;
@@ -518,12 +520,10 @@ __global__ void k_quant_scatter_pad(const uint16_t *__restrict__ x, int64_t nblo
         uint32_t c[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) c[i] = e4m3x4(v[4 * i] * iv, v[4 * i + 1] * iv, v[4 * i + 2] * iv, v[4 * i + 3] * iv);
+#pragma unroll 4
         for (int j = 0; j < k; ++j) {
-            const int e = __ldg(idx + t * k + j);
-            const int qrow = __ldg(inv + t * k + j);
-            const int r = qrow - __ldg(offsets + e);
-            if (b == 0) w_sorted[qrow] = __ldg(topk_w + t * k + j);
-            const int64_t R = pad_row(r, __ldg(pad_off + e), NT, SLOT);
+            if (b == 0) w_sorted[__ldg(inv + t * k + j)] = __ldg(topk_w + t * k + j);
+            const int64_t R = __ldg(dst_row + t * k + j);
             uint4 *dst = reinterpret_cast<uint4 *>(xq + R * d + b * 32);
             dst[0] = make_uint4(c[0], c[1], c[2], c[3]);
             dst[1] = make_uint4(c[4], c[5], c[6], c[7]);
@@ -638,6 +638,9 @@ cudaError_t launch_gemm(const CUtensorMap &a0, const CUtensorMap &a1, const CUte
 
 }  // namespace
 
+// 128-row weight tiles per down-GEMM item (Cfg<DOWN, NT>::MATS).
+static int down_tiles_per_item(int NT) { return NT <= 32 ? 2 : 1; }
+
 FfnLayout ffn_layout(int64_t P, int d, int E, int I)
 {
     FfnLayout L{};
@@ -662,6 +665,7 @@ FfnLayout ffn_layout(int64_t P, int d, int E, int I)
     L.hs = take(size_t(atoms) * (Ip / 128) * 512);
     L.hs_bytes = size_t(atoms) * (Ip / 128) * 512;
     L.w_sorted = take(size_t(P) * 4);
+    L.dst_row = take(size_t(P) * 4);
     L.total = off;
     return L;
 }
@@ -669,23 +673,36 @@ FfnLayout ffn_layout(int64_t P, int d, int E, int I)
 cudaError_t launch_ffn_schedule(const int32_t *offsets, int E, int d, int I, const FfnLayout &L, char *scratch,
                                 cudaStream_t st)
 {
-    k_ffn_schedule<<<1, 1024, 0, st>>>(offsets, E, L.NT, L.SLOT, int(ceil_div(I, 128)), int(ceil_div(d / 128, 2)),
+    k_ffn_schedule<<<1, 1024, 0, st>>>(offsets, E, L.NT, L.SLOT, int(ceil_div(I, 128)),
+                                       int(ceil_div(d / 128, down_tiles_per_item(L.NT))),
                                        reinterpret_cast<int32_t *>(scratch + L.pad_off),
                                        reinterpret_cast<int32_t *>(scratch + L.tiles_gu),
                                        reinterpret_cast<int32_t *>(scratch + L.tiles_dn));
     return cudaGetLastError();
 }
 
-cudaError_t launch_quant_scatter_pad(const uint16_t *x, int T, int d, int k, const int32_t *idx, const int32_t *inv,
-                                     const float *topk_w, const int32_t *offsets, const FfnLayout &L, char *scratch,
-                                     cudaStream_t st)
+FfnSched ffn_sched(const FfnLayout &L, int d, int I, char *scratch)
+{
+    FfnSched sc;
+    sc.NT = L.NT;
+    sc.SLOT = L.SLOT;
+    sc.MT_gu = int(ceil_div(I, 128));
+    sc.MT_dn = int(ceil_div(d / 128, down_tiles_per_item(L.NT)));
+    sc.pad_off = reinterpret_cast<int32_t *>(scratch + L.pad_off);
+    sc.tiles_gu = reinterpret_cast<int32_t *>(scratch + L.tiles_gu);
+    sc.tiles_dn = reinterpret_cast<int32_t *>(scratch + L.tiles_dn);
+    sc.dst_row = reinterpret_cast<int32_t *>(scratch + L.dst_row);
+    return sc;
+}
+
+cudaError_t launch_quant_scatter_pad(const uint16_t *x, int T, int d, int k, const int32_t *inv, const float *topk_w,
+                                     const FfnLayout &L, char *scratch, cudaStream_t st)
 {
     const int64_t nblocks = int64_t(T) * (d / 32);
     if (nblocks == 0) return cudaSuccess;
     const int grid = int(ceil_div(nblocks, 128) < 152 * 32 ? ceil_div(nblocks, 128) : 152 * 32);
-    k_quant_scatter_pad<<<grid, 128, 0, st>>>(x, nblocks, d, k, idx, inv, topk_w, offsets,
-                                              reinterpret_cast<const int32_t *>(scratch + L.pad_off), L.NT, L.SLOT,
-                                              reinterpret_cast<uint8_t *>(scratch + L.xq),
+    k_quant_scatter_pad<<<grid, 128, 0, st>>>(x, nblocks, d, k, reinterpret_cast<const int32_t *>(scratch + L.dst_row),
+                                              inv, topk_w, reinterpret_cast<uint8_t *>(scratch + L.xq),
                                               reinterpret_cast<uint8_t *>(scratch + L.xs),
                                               reinterpret_cast<float *>(scratch + L.w_sorted));
     return cudaGetLastError();
@@ -762,7 +779,7 @@ cudaError_t launch_expert_gemms(const FfnArgs &a, const FfnLayout &L, char *scra
     g.yp = a.yp;
     g.Mtot = a.d;
     g.MTA = a.d / 128;
-    g.MT = int(ceil_div(g.MTA, 2));  // each down item covers two 128-row tiles
+    g.MT = int(ceil_div(g.MTA, down_tiles_per_item(L.NT)));
     g.KC = Ip / 128;
     return L.NT == 16   ? launch_gemm<DOWN, 16>(md, md, mh, g, st)
            : L.NT == 32 ? launch_gemm<DOWN, 32>(md, md, mh, g, st)

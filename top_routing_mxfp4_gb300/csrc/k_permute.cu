@@ -38,9 +38,68 @@ __global__ void __launch_bounds__(256) k_perm_hist(const int32_t *__restrict__ i
     for (int e = threadIdx.x; e < E; e += blockDim.x) blockhist[int64_t(blockIdx.x) * E + e] = h[e];
 }
 
+// Exclusive scan of v[0..n) (n <= 2048) into out[0..n], out[n] = total, by a
+// block of nthreads (256 or 1024) threads; each thread owns MAXE/nthreads
+// consecutive entries.  Ends with __syncthreads().
+template <int NTHREADS>
+__device__ void block_scan(const int32_t *v, int n, int32_t *out, int32_t *warp_tot)
+{
+    constexpr int PER = MAXE / NTHREADS;
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    int32_t x[PER], tsum = 0;
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+        const int e = threadIdx.x * PER + j;
+        x[j] = e < n ? v[e] : 0;
+        tsum += x[j];
+    }
+    int32_t incl = tsum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += t;
+    }
+    if (lane == 31) warp_tot[wid] = incl;
+    __syncthreads();
+    int32_t base = 0;
+    for (int w = 0; w < wid; ++w) base += warp_tot[w];
+    int32_t run = base + incl - tsum;
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+        const int e = threadIdx.x * PER + j;
+        if (e < n) out[e] = run;
+        run += x[j];
+    }
+    if (threadIdx.x == NTHREADS - 1) out[n] = run;
+    __syncthreads();
+}
+
+// The FFN schedule from per-expert counts (shared memory, E entries):
+// token tiles per expert, exclusive scan, slot rows and work-item starts.
+template <int NTHREADS>
+__device__ void ffn_schedule_from_counts(const int32_t *cnt_s, int E, const FfnSched &sc, int32_t *tmp_s,
+                                         int32_t *scan_s, int32_t *warp_tot)
+{
+    for (int e = threadIdx.x; e < E; e += NTHREADS) tmp_s[e] = (cnt_s[e] + sc.NT - 1) / sc.NT;
+    __syncthreads();
+    block_scan<NTHREADS>(tmp_s, E, scan_s, warp_tot);
+    for (int e = threadIdx.x; e <= E; e += NTHREADS) {
+        sc.pad_off[e] = scan_s[e] * sc.SLOT;
+        sc.tiles_gu[e] = scan_s[e] * sc.MT_gu;
+        sc.tiles_dn[e] = scan_s[e] * sc.MT_dn;
+    }
+}
+
+__device__ __forceinline__ int32_t padded_row(int32_t pos, int32_t off_e, int32_t pad_e, int NT, int SLOT)
+{
+    const int32_t r = pos - off_e;
+    return pad_e + (r / NT) * SLOT + r % NT;
+}
+
 // Single CTA of 1024 threads.
 __global__ void __launch_bounds__(1024) k_perm_scan(int32_t *__restrict__ blockhist, int nblk, int E,
-                                                    int32_t *__restrict__ counts, int32_t *__restrict__ offsets)
+                                                    int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
+                                                    FfnSched sc)
 {
     __shared__ int32_t cnt[MAXE];
     __shared__ int32_t warp_tot[32];
@@ -87,11 +146,16 @@ __global__ void __launch_bounds__(1024) k_perm_scan(int32_t *__restrict__ blockh
         const int32_t base = offsets[e];
         for (int bb = 0; bb < nblk; ++bb) blockhist[int64_t(bb) * E + e] += base;
     }
+    if (sc.pad_off) {
+        __shared__ int32_t tmp[MAXE], scn[MAXE + 1];
+        ffn_schedule_from_counts<1024>(cnt, E, sc, tmp, scn, warp_tot);
+    }
 }
 
 __global__ void __launch_bounds__(256) k_perm_scatter(const int32_t *__restrict__ idx, int64_t P, int E,
                                                       const int32_t *__restrict__ blockstart,
-                                                      int32_t *__restrict__ perm, int32_t *__restrict__ inv)
+                                                      int32_t *__restrict__ perm, int32_t *__restrict__ inv,
+                                                      const int32_t *__restrict__ offsets, FfnSched sc)
 {
     extern __shared__ int32_t wh[];  // [WARPS][E] per-warp counts, then cursors
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
@@ -135,6 +199,8 @@ __global__ void __launch_bounds__(256) k_perm_scatter(const int32_t *__restrict_
         if (p < s1) {
             inv[p] = pos;
             if (pos >= 0) perm[pos] = int32_t(p);
+            if (sc.dst_row && pos >= 0)
+                sc.dst_row[p] = padded_row(pos, __ldg(offsets + e), __ldg(sc.pad_off + e), sc.NT, sc.SLOT);
         }
     }
 }
@@ -148,7 +214,7 @@ __global__ void __launch_bounds__(256) k_perm_scatter(const int32_t *__restrict_
 __global__ void __launch_bounds__(256) k_perm_single(const int32_t *__restrict__ idx, int P, int E,
                                                      int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
                                                      int32_t *__restrict__ perm, int32_t *__restrict__ inv,
-                                                     int32_t *status)
+                                                     int32_t *status, FfnSched sc)
 {
     extern __shared__ int4 wh_raw[];
     int32_t *wh = reinterpret_cast<int32_t *>(wh_raw);  // [WARPS][E]
@@ -230,6 +296,15 @@ __global__ void __launch_bounds__(256) k_perm_single(const int32_t *__restrict__
         for (int w = 0; w < WARPS; ++w) wh[w * E + e] += o;
     }
     __syncthreads();
+    int32_t *pad_s = nullptr;
+    if (sc.pad_off) {
+        // counts are offsets[e+1] - offsets[e]; reuse the shared tail for the schedule
+        __shared__ int32_t tmp[MAXE], scn[MAXE + 1], wt2[WARPS];
+        for (int e = threadIdx.x; e < E; e += blockDim.x) tmp[e] = counts[e];
+        __syncthreads();
+        ffn_schedule_from_counts<256>(tmp, E, sc, tmp, scn, wt2);
+        pad_s = scn;  // slot index of each expert (times SLOT = pad_off)
+    }
     int32_t *cur = wh + wid * E;
     const unsigned lt = (1u << lane) - 1u;
 #pragma unroll
@@ -246,6 +321,7 @@ __global__ void __launch_bounds__(256) k_perm_single(const int32_t *__restrict__
         if (p < s1) {
             inv[p] = pos;
             if (pos >= 0) perm[pos] = p;
+            if (pad_s && pos >= 0) sc.dst_row[p] = padded_row(pos, off_s[e], pad_s[e] * sc.SLOT, sc.NT, sc.SLOT);
         }
     }
 }
@@ -265,30 +341,30 @@ size_t permute_scratch_bytes(int64_t P, int E)
 }
 
 cudaError_t launch_permute(const int32_t *idx, int64_t P, int E, int32_t *counts, int32_t *offsets, int32_t *perm,
-                           int32_t *inv, void *scratch, int32_t *status, cudaStream_t st)
+                           int32_t *inv, void *scratch, int32_t *status, cudaStream_t st, const FfnSched &sched)
 {
     const int nblk = int(ceil_div(P, CHUNK));
     int32_t *blockhist = static_cast<int32_t *>(scratch);
     if (nblk == 1) {
+        // dynamic part; the kernel also has ~16 KB of static shared memory, so
+        // the limit is raised explicitly
         const size_t smem = size_t(WARPS + 1) * E * sizeof(int32_t) + 16;
-        if (smem > 48 * 1024) {
-            cudaError_t e = cudaFuncSetAttribute(k_perm_single, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-            if (e != cudaSuccess) return e;
-        }
-        k_perm_single<<<1, 256, smem, st>>>(idx, int(P), E, counts, offsets, perm, inv, status);
+        cudaError_t e = cudaFuncSetAttribute(k_perm_single, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+        if (e != cudaSuccess) return e;
+        k_perm_single<<<1, 256, smem, st>>>(idx, int(P), E, counts, offsets, perm, inv, status, sched);
         return cudaGetLastError();
     }
     if (nblk > 0) {
         k_perm_hist<<<nblk, 256, 0, st>>>(idx, P, E, blockhist, status);
     }
-    k_perm_scan<<<1, 1024, 0, st>>>(blockhist, nblk, E, counts, offsets);
+    k_perm_scan<<<1, 1024, 0, st>>>(blockhist, nblk, E, counts, offsets, sched);
     if (nblk > 0) {
         const size_t smem = size_t(WARPS) * E * sizeof(int32_t);
         if (smem > 48 * 1024) {  // above the default dynamic shared-memory limit (E > 1536)
             cudaError_t e = cudaFuncSetAttribute(k_perm_scatter, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
             if (e != cudaSuccess) return e;
         }
-        k_perm_scatter<<<nblk, 256, smem, st>>>(idx, P, E, blockhist, perm, inv);
+        k_perm_scatter<<<nblk, 256, smem, st>>>(idx, P, E, blockhist, perm, inv, offsets, sched);
     }
     return cudaGetLastError();
 }

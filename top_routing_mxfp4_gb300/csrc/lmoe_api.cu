@@ -271,10 +271,11 @@ lmoe_status lmoe_forward(const uint16_t *x_bf16, const float *Wr, const float *b
     if (e == cudaSuccess) e = cudaMemsetAsync(status, 0, sizeof(int32_t), st);
     if (e == cudaSuccess) e = launch_route(x_bf16, Wr, bias, T, d, E, k, lg, idx, w, ws + L.rscratch, status, st);
     if (e == cudaSuccess) e = mark(1, st);
-    if (e == cudaSuccess) e = launch_permute(idx, P, E, counts, offsets, perm, inv, ws + L.pscratch, status, st);
-    if (e == cudaSuccess) e = launch_ffn_schedule(offsets, E, d, dims->I, FL, fs, st);
+    if (e == cudaSuccess)
+        e = launch_permute(idx, P, E, counts, offsets, perm, inv, ws + L.pscratch, status, st,
+                           ffn_sched(FL, d, dims->I, fs));
     if (e == cudaSuccess) e = mark(2, st);
-    if (e == cudaSuccess) e = launch_quant_scatter_pad(x_bf16, T, d, k, idx, inv, w, offsets, FL, fs, st);
+    if (e == cudaSuccess) e = launch_quant_scatter_pad(x_bf16, T, d, k, inv, w, FL, fs, st);
     if (e == cudaSuccess) e = mark(3, st);
     if (e == cudaSuccess) {
         FfnArgs f{W, offsets, perm, w, int(P), d, E, k, dims->I, yp, status};
@@ -335,8 +336,8 @@ int32_t lmoe_forward_kernel_count(const lmoe_dims *dims)
 {
     if (!dims_ok(dims) || dims->T == 0) return 0;
     const int64_t P = int64_t(dims->T) * dims->k;
-    // router (split, GEMM, top-k), permute, schedule, scatter, two GEMMs, combine
-    return router_kernel_count(dims->T, dims->d, dims->E) + permute_kernel_count(P) + 1 + 1 + 2 + 1;
+    // router (split, GEMM, (reduction), top-k), permute (with the GEMM schedule), scatter, two GEMMs, combine
+    return router_kernel_count(dims->T, dims->d, dims->E) + permute_kernel_count(P) + 1 + 2 + 1;
 }
 
 lmoe_status lmoe_set_stage_events(void *const *events, int32_t n)

@@ -109,9 +109,18 @@ cudaError_t launch_topk_softmax(const float *logits, int T, int E, int k, int32_
 cudaError_t launch_route(const uint16_t *x, const float *Wr, const float *bias, int T, int d, int E, int k,
                          float *logits, int32_t *idx, float *w, void *scratch, int32_t *status, cudaStream_t st);
 
+// Optional by-products of the permute for the expert GEMMs: per expert the
+// first slot row in the padded token layout (pad_off, E+1) and the first work
+// item of each GEMM (tiles_gu / tiles_dn, E+1), and per pair p its padded
+// token row (dst_row, T*k).  pad_off == nullptr disables them.
+struct FfnSched {
+    int NT = 0, SLOT = 0, MT_gu = 0, MT_dn = 0;
+    int32_t *pad_off = nullptr, *tiles_gu = nullptr, *tiles_dn = nullptr, *dst_row = nullptr;
+};
 size_t permute_scratch_bytes(int64_t P, int E);
 cudaError_t launch_permute(const int32_t *idx, int64_t P, int E, int32_t *counts, int32_t *offsets, int32_t *perm,
-                           int32_t *inv, void *scratch, int32_t *status, cudaStream_t st);
+                           int32_t *inv, void *scratch, int32_t *status, cudaStream_t st,
+                           const FfnSched &sched = FfnSched());
 
 // Expert FFN (tensor cores).  Activations live in a padded token layout
 // inside the FFN scratch: expert e's tokens fill slots of SLOT rows from
@@ -119,9 +128,11 @@ cudaError_t launch_permute(const int32_t *idx, int64_t P, int E, int32_t *counts
 struct FfnLayout {
     int NT, SLOT;      // token tile and slot rows
     int64_t rows;      // padded token rows reserved
-    size_t pad_off, tiles_gu, tiles_dn, xq, xs, hq, hs, hs_bytes, w_sorted, total;  // byte offsets / sizes
+    size_t pad_off, tiles_gu, tiles_dn, xq, xs, hq, hs, hs_bytes, w_sorted, dst_row, total;  // byte offsets / sizes
 };
 FfnLayout ffn_layout(int64_t P, int d, int E, int I);
+// The permute by-products the forward asks for, pointing into the FFN scratch.
+FfnSched ffn_sched(const FfnLayout &L, int d, int I, char *scratch);
 
 struct FfnArgs {
     const lmoe_expert_weights *W;
@@ -134,10 +145,10 @@ struct FfnArgs {
 // slot starts and per-GEMM work-item prefixes from the segment offsets
 cudaError_t launch_ffn_schedule(const int32_t *offsets, int E, int d, int I, const FfnLayout &L, char *scratch,
                                 cudaStream_t st);
-// bf16 x[T][d] -> MXFP8 rows at each routed (expert, slot) position
-cudaError_t launch_quant_scatter_pad(const uint16_t *x, int T, int d, int k, const int32_t *idx, const int32_t *inv,
-                                     const float *topk_w, const int32_t *offsets, const FfnLayout &L, char *scratch,
-                                     cudaStream_t st);
+// bf16 x[T][d] -> MXFP8 rows at each routed pair's padded row (dst_row from
+// the permute); also the gate weights in permuted order.
+cudaError_t launch_quant_scatter_pad(const uint16_t *x, int T, int d, int k, const int32_t *inv, const float *topk_w,
+                                     const FfnLayout &L, char *scratch, cudaStream_t st);
 // MXFP8 rows in token order -> padded layout (row q of perm takes token perm[q]/k)
 cudaError_t launch_gather_pad(const uint8_t *xq, const uint8_t *xs, int T, int d, int k, int E, const int32_t *offsets,
                               const int32_t *perm, const float *topk_w, const FfnLayout &L, char *scratch,
