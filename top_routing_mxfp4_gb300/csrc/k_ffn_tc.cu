@@ -17,8 +17,8 @@
 //     G = Wg[e] x^T, U = Wu[e] x^T (two TMEM accumulators), epilogue
 //     h = silu(G) * U, MXFP8-quantised along I (a warp's 32 lanes are one
 //     32-row block of I) -> hq / hs in the padded token layout;
-//   down GEMM, item (expert e, 256 rows of d, token tile):
-//     Y = Wd[e] h^T, epilogue yp[q][row] = topk_w[perm[q]] * Y.
+//   down GEMM, item (expert e, 128 or 256 rows of d, token tile):
+//     Y = Wd[e] h^T, epilogue yp[q][row] = topk_w[perm[q]] * Y (fp32).
 //
 // Token layout: the activations of expert e occupy `ntiles(e)` slots of SLOT
 // = roundup(NT, 128) rows starting at pad_off[e] (a multiple of 128); token r
@@ -27,12 +27,13 @@
 // 512-byte atoms (128 rows x 4 K-blocks) that one bulk copy moves and one
 // tcgen05.cp puts in TMEM.
 //
-// Persistent, warp-specialised CTA (224 threads, one per SM):
+// Persistent, warp-specialised CTA (224 or 352 threads, one per SM):
 //   warp 0     TMA producer (A tiles via the packed-FP4 tensor map that
 //              expands 16 x 4-bit into 16-byte smem units, B tile, scale atoms)
-//   warp 1     TMEM allocator + MMA issuer 0 (gate / first K half of down)
-//   warp 6     MMA issuer 1 (up / second K half of down)
-//   warps 2-5  epilogue (TMEM lane quarter = warp % 4)
+//   warp 1     TMEM allocator + MMA issuer 0 (gate / first weight tile of down)
+//   warps 2..  epilogue, 4 or 8 warps: TMEM lane quarter = warp % 4; with 8,
+//              two warps per quarter take alternate column chunks
+//   last warp  MMA issuer 1 (up / second weight tile of down)
 // Every mbarrier wait is bounded; a wait that runs out records
 // LMOE_ERR_TIMEOUT in the status word and the CTA winds down.
 #include <cuda.h>
@@ -138,6 +139,20 @@ struct Cfg {
     static constexpr int SF_COLS = MATS * SF_COLS_ISSUER;
     static constexpr int MAX_STAGES = (512 - SF_BASE) / SF_COLS < 16 ? (512 - SF_BASE) / SF_COLS : 16;
     static_assert(MAX_STAGES >= 2, "TMEM columns");
+    // Epilogue.  Large token tiles: 8 warps (two per TMEM lane quarter, on
+    // alternate column chunks) that transpose each chunk through a per-warp
+    // shared-memory tile (down: CW tokens x 32 fp32, 36-float row stride;
+    // gate/up: 16 tokens x 32 e4m3 codes) so that every lane stores 16
+    // contiguous bytes.  Small tiles (decode): 4 warps storing straight from
+    // registers, leaving the shared memory to the pipeline stages.
+    static constexpr bool STAGED = NT >= 64;
+    static constexpr int EPI_WARPS = STAGED ? 8 : 4;
+    static constexpr int NW = EPI_WARPS / 4;  // epilogue warps per lane quarter
+    static constexpr int THREADS = 32 * (3 + EPI_WARPS);
+    static constexpr int CW = NT < 32 ? NT : 32;  // accumulator columns per TMEM load (down)
+    static constexpr int STG_STRIDE = 36;
+    static constexpr uint32_t EPI_WARP_BYTES = !STAGED ? 0 : (MODE == DOWN ? CW * STG_STRIDE * 4 : 16 * 32);
+    static constexpr uint32_t EPI_BYTES = EPI_WARPS * EPI_WARP_BYTES;
 };
 
 struct Item {
@@ -164,7 +179,7 @@ __device__ __forceinline__ Item decode_item(int it, const int32_t *s_tiles, cons
 }
 
 template <int MODE, int NT>
-__global__ void __launch_bounds__(224, 1)
+__global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
     k_moe_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                const __grid_constant__ CUtensorMap tmB, const GemmArgs p)
 {
@@ -173,7 +188,8 @@ __global__ void __launch_bounds__(224, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int S = p.stages;
     uint8_t *stages = smem;
-    uint64_t *full = reinterpret_cast<uint64_t *>(stages + S * C::STAGE_BYTES);
+    uint8_t *epi_stage = stages + S * C::STAGE_BYTES;
+    uint64_t *full = reinterpret_cast<uint64_t *>(epi_stage + C::EPI_BYTES);
     uint64_t *empty = full + S;
     uint64_t *acc_full = empty + S;
     uint64_t *acc_empty = acc_full + C::ACC_STAGES;
@@ -193,7 +209,7 @@ __global__ void __launch_bounds__(224, 1)
         }
         for (int a = 0; a < C::ACC_STAGES; ++a) {
             mbar_init(&acc_full[a], C::MATS);
-            mbar_init(&acc_empty[a], 128);
+            mbar_init(&acc_empty[a], 32 * C::EPI_WARPS);
         }
         mbar_init_fence();
     }
@@ -255,8 +271,8 @@ __global__ void __launch_bounds__(224, 1)
             }
             LMOE_TRACE_END(0);
         }
-    } else if (warp == 1 || warp == 6) {
-        // ---------------- MMA issuers (warp 1: gate / first tile, warp 6: up / second tile) ----------------
+    } else if (warp == 1 || warp == 2 + C::EPI_WARPS) {
+        // ---------------- MMA issuers (warp 1: gate / first tile, last warp: up / second tile) ----------------
         if (lane == 0 && (warp == 1 || C::MATS == 2)) {
             LMOE_TRACE_DECL
             const int iss = warp == 1 ? 0 : 1;
@@ -310,8 +326,10 @@ __global__ void __launch_bounds__(224, 1)
             if (iss == 0) LMOE_TRACE_END(1);
         }
     } else {
-        // ---------------- epilogue (warps 2-5) ----------------
-        const int q = warp & 3;  // TMEM lane quarter of this warp
+        // ---------------- epilogue (warps 2 .. 1 + EPI_WARPS) ----------------
+        const int q = warp & 3;             // TMEM lane quarter of this warp
+        const int half = (warp - 2) >> 2;   // which of the quarter's NW warps
+        [[maybe_unused]] uint8_t *stg = epi_stage + (warp - 2) * C::EPI_WARP_BYTES;
         LMOE_TRACE_DECL
         int acc = 0;
         uint32_t acc_phase = 0;
@@ -335,7 +353,7 @@ __global__ void __launch_bounds__(224, 1)
 #pragma unroll
             for (int i = 0; i < (NT + 31) / 32; ++i) wl[i] = wn[i];
             if (it + int(gridDim.x) < total) fetch(it + gridDim.x);
-            const int qbase = s_off[w.e] + w.n_tile * NT;  // first permuted row of the tile
+            [[maybe_unused]] const int qbase = s_off[w.e] + w.n_tile * NT;  // first permuted row of the tile (down)
             if (threadIdx.x == 64) LMOE_TRACE_EV(2, 0x40 | MODE, it, 0);  // epilogue: waiting
             if (!mbar_wait(&acc_full[acc], acc_phase)) {
                 set_status(p.status, LMOE_ERR_TIMEOUT);
@@ -346,63 +364,97 @@ __global__ void __launch_bounds__(224, 1)
             const uint32_t tbase = tmem + (uint32_t(32 * q) << 16) + uint32_t(acc * C::ACC_COLS_ITEM);
             if (MODE == GATEUP && w.m_tile * 128 + 32 * q < p.Mtot) {
                 const int row0 = w.m_tile * 128 + 32 * q;  // first row of I held by this warp
-                const int row = row0 + lane;
+                const int blk = row0 / 32;                 // MX block of I held by this warp
                 const int64_t Rbase = int64_t(slot_row(w.e)) + int64_t(w.n_tile) * C::SLOT;
-                for (int c0 = 0; c0 < w.n_valid; c0 += 16) {
+                for (int c0 = 16 * half; c0 < w.n_valid; c0 += 16 * C::NW) {
                     uint32_t v0[16], v1[16];
                     tmem_ld16(tbase + c0, v0);
                     tmem_ld16(tbase + NT + c0, v1);
                     tmem_ld_wait();
-                    const int nv = min(16, w.n_valid - c0);
-                    {
-                        // 16 independent columns: SiLU-gated product, block amax over
-                        // the warp's 32 rows of I, E8M0 scale, e4m3 code
-                        const int blk = row0 / 32;  // MX block of I held by this warp
-                        uint32_t code[16], sbv[16];
+                    // 16 independent columns: SiLU-gated product, block amax over
+                    // the warp's 32 rows of I, E8M0 scale, e4m3 code
+                    uint32_t sbv[16], code[16];
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const float gv = __uint_as_float(v0[j]), uv = __uint_as_float(v1[j]);
-                            const float h = __fdividef(gv, 1.f + __expf(-gv)) * uv;
-                            uint32_t amax;
-                            asm("redux.sync.max.u32 %0, %1, 0xffffffff;" : "=r"(amax) : "r"(__float_as_uint(h) & 0x7FFFFFFFu));
-                            sbv[j] = mx_scale_byte(__uint_as_float(amax), 8);
-                            code[j] = e4m3x2(h * mx_inv_scale(sbv[j]), 0.f) & 0xFF;
-                        }
-                        uint8_t *hrow = p.hq + (Rbase + c0) * p.Ih + row;
+                    for (int j = 0; j < 16; ++j) {
+                        const float gv = __uint_as_float(v0[j]), uv = __uint_as_float(v1[j]);
+                        const float h = __fdividef(gv, 1.f + __expf(-gv)) * uv;
+                        uint32_t amax;
+                        asm("redux.sync.max.u32 %0, %1, 0xffffffff;" : "=r"(amax) : "r"(__float_as_uint(h) & 0x7FFFFFFFu));
+                        sbv[j] = mx_scale_byte(__uint_as_float(amax), 8);
+                        code[j] = e4m3x2(h * mx_inv_scale(sbv[j]), 0.f) & 0xFF;
+                    }
+                    if constexpr (C::STAGED) {
+                        __syncwarp();  // the previous chunk's staged codes have been read
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) stg[j * 32 + lane] = uint8_t(code[j]);
+                        __syncwarp();
+                        // lane l stores 16 codes of token column l/2 (rows 16*(l&1) ..)
+                        const int c = lane >> 1;
+                        if (c0 + c < w.n_valid)
+                            *reinterpret_cast<uint4 *>(p.hq + (Rbase + c0 + c) * p.Ih + row0 + 16 * (lane & 1)) =
+                                *reinterpret_cast<const uint4 *>(stg + 16 * lane);
+                    } else {
+                        uint8_t *hrow = p.hq + (Rbase + c0) * p.Ih + row0 + lane;
 #pragma unroll
                         for (int j = 0; j < 16; ++j)
-                            if (j < nv) hrow[int64_t(j) * p.Ih] = uint8_t(code[j]);
-                        if (lane < nv) {  // lane j writes column j's scale byte
-                            uint32_t sbl = 0;
+                            if (c0 + j < w.n_valid) hrow[int64_t(j) * p.Ih] = uint8_t(code[j]);
+                    }
+                    if (c0 + lane < w.n_valid && lane < 16) {  // lane j writes column j's scale byte
+                        uint32_t sbl = 0;
 #pragma unroll
-                            for (int j = 0; j < 16; ++j) sbl = (lane == j) ? sbv[j] : sbl;
-                            const int64_t R = Rbase + c0 + lane;
-                            p.hs[((R >> 7) * p.KCh + (blk >> 2)) * 512 + (R & 31) * 16 + ((R & 127) >> 5) * 4 + (blk & 3)] =
-                                uint8_t(sbl);
-                        }
+                        for (int j = 0; j < 16; ++j) sbl = (lane == j) ? sbv[j] : sbl;
+                        const int64_t R = Rbase + c0 + lane;
+                        p.hs[((R >> 7) * p.KCh + (blk >> 2)) * 512 + (R & 31) * 16 + ((R & 127) >> 5) * 4 + (blk & 3)] =
+                            uint8_t(sbl);
                     }
                 }
             }
             if (MODE == DOWN) {
-                // accumulator h holds output rows (MATS m + h) * 128 + 32q + lane
-#pragma unroll
-                for (int h = 0; h < C::MATS; ++h) {
+                // accumulator h holds output rows (MATS m + h) * 128 + 32q + lane;
+                // work units (h, column chunk) alternate between the quarter's NW warps
+                constexpr int CW = C::CW;
+                [[maybe_unused]] float *sf = reinterpret_cast<float *>(stg);
+                const int nch = (w.n_valid + CW - 1) / CW;
+                for (int u = half; u < C::MATS * nch; u += C::NW) {
+                    const int h = u / nch, c0 = (u - h * nch) * CW;
                     const int mt = C::MATS * w.m_tile + h;
-                    if (mt >= p.MTA) break;  // odd last tile: second accumulator is a copy
-                    const int row = mt * 128 + 32 * q + lane;
-                    for (int c0 = 0; c0 < w.n_valid; c0 += 16) {
-                        uint32_t v[16];
-                        tmem_ld16(tbase + h * NT + c0, v);
-                        tmem_ld_wait();
-                        const int nv = min(16, w.n_valid - c0);
-                        float *yrow = p.yp + int64_t(qbase + c0) * p.Mtot + row;
-                        float wsel = wl[0];
+                    if (mt >= p.MTA) continue;  // odd last tile: second accumulator is a copy
+                    uint32_t v[CW];
+                    tmem_ld_cols<CW>(tbase + h * NT + c0, v);
+                    tmem_ld_wait();
+                    // gate weights of this chunk's columns: column c's weight is lane (c0 & 31) + c of wl[c0 / 32]
+                    float wsel = wl[0];
 #pragma unroll
-                        for (int i = 1; i < (NT + 31) / 32; ++i) wsel = (c0 / 32 == i) ? wl[i] : wsel;
+                    for (int i = 1; i < (NT + 31) / 32; ++i) wsel = (c0 / 32 == i) ? wl[i] : wsel;
+                    if constexpr (C::STAGED) {
+                        // transpose through shared memory: sf[c][row], row stride STG_STRIDE
+                        __syncwarp();
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) {
+                        for (int j = 0; j < CW; ++j) sf[j * C::STG_STRIDE + lane] = __uint_as_float(v[j]);
+                        __syncwarp();
+                        // lane l: token column c = 4 pp + l / 8, 4 rows starting at 4 (l % 8)
+                        const int f4 = 4 * (lane & 7);
+                        float *ybase = p.yp + int64_t(qbase + c0) * p.Mtot + mt * 128 + 32 * q + f4;
+#pragma unroll
+                        for (int pp = 0; pp < CW / 4; ++pp) {
+                            const int c = 4 * pp + (lane >> 3);
+                            const float wc = __shfl_sync(0xFFFFFFFFu, wsel, (c0 & 31) + c);
+                            if (c0 + c < w.n_valid) {
+                                float4 a = *reinterpret_cast<const float4 *>(sf + c * C::STG_STRIDE + f4);
+                                a.x *= wc;
+                                a.y *= wc;
+                                a.z *= wc;
+                                a.w *= wc;
+                                *reinterpret_cast<float4 *>(ybase + int64_t(c) * p.Mtot) = a;
+                            }
+                        }
+                    } else {
+                        // lane = output row; each column's 32 rows are one 128-byte store
+                        float *yrow = p.yp + int64_t(qbase + c0) * p.Mtot + mt * 128 + 32 * q + lane;
+#pragma unroll
+                        for (int j = 0; j < CW; ++j) {
                             const float wc = __shfl_sync(0xFFFFFFFFu, wsel, (c0 & 31) + j);
-                            if (j < nv) yrow[int64_t(j) * p.Mtot] = wc * __uint_as_float(v[j]);
+                            if (c0 + j < w.n_valid) yrow[int64_t(j) * p.Mtot] = wc * __uint_as_float(v[j]);
                         }
                     }
                 }
@@ -615,7 +667,7 @@ int gemm_stages(int E, size_t &smem)
     cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     cudaFuncAttributes fa{};
     cudaFuncGetAttributes(&fa, k_moe_gemm<MODE, NT>);
-    const size_t fixed = 1024 + (2 * 16 + 2 * C::ACC_STAGES) * 8 + 16 + size_t(2) * (E + 1) * 4;
+    const size_t fixed = 1024 + C::EPI_BYTES + (2 * 16 + 2 * C::ACC_STAGES) * 8 + 16 + size_t(2) * (E + 1) * 4;
     const long avail = long(optin) - long(fa.sharedSizeBytes) - long(fixed);
     int st = int(avail / long(C::STAGE_BYTES));
     if (st > C::MAX_STAGES) st = C::MAX_STAGES;
@@ -632,7 +684,7 @@ cudaError_t launch_gemm(const CUtensorMap &a0, const CUtensorMap &a1, const CUte
     if (args.stages < 2) return cudaErrorInvalidConfiguration;
     cudaError_t e = cudaFuncSetAttribute(k_moe_gemm<MODE, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
-    k_moe_gemm<MODE, NT><<<num_sms(), 224, smem, st>>>(a0, a1, b, args);
+    k_moe_gemm<MODE, NT><<<num_sms(), Cfg<MODE, NT>::THREADS, smem, st>>>(a0, a1, b, args);
     return cudaGetLastError();
 }
 

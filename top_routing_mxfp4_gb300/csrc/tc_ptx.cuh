@@ -169,6 +169,13 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t *r)
           "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
 }
+// CW (a multiple of 16) consecutive columns; complete with tmem_ld_wait().
+template <int CW>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t *r)
+{
+#pragma unroll
+    for (int i = 0; i < CW / 16; ++i) tmem_ld16(taddr + uint32_t(16 * i), r + 16 * i);
+}
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 }  // namespace tc
