@@ -93,6 +93,24 @@ def test_forward_ragged_shapes(cuda_lib):
     _check(wl, x, y, idx, w, lg, list(range(0, 45, 4)))
 
 
+@pytest.mark.parametrize("T,E,k", [(600, 8, 4), (301, 10, 6)])
+def test_forward_fused_combine_all_tokens(cuda_lib, T, E, k):
+    """Batches with more than 16 routed pairs per expert use 128-token tiles,
+    and the down GEMM's epilogue adds each pair's weighted output straight
+    into its token's fp32 row (fp32 atomics; the k terms in an unspecified
+    order).  Every token is checked: several ragged token tiles per expert,
+    d = 3 weight tiles, I = 160 (a ragged last K chunk)."""
+    wl = gen.custom(f"fused{T}", T=T, d=384, I=160, E=E, k=k)
+    assert wl.P > 16 * wl.E
+    x, y, idx, w, lg = _run_forward(cuda_lib, wl)
+    err = _check(wl, x, y, idx, w, lg, list(range(T)))
+    assert np.bincount(idx.ravel(), minlength=E).max() > 128  # experts span several token tiles
+    assert err.max() <= TOL
+    # a zero batch accumulates to exactly zero
+    _, y0, _, _, _ = _run_forward(cuda_lib, wl, np.zeros((T, wl.d), np.uint16))
+    assert np.all((y0 & 0x7FFF) == 0)
+
+
 def test_forward_zero_input_gives_zero(cuda_lib):
     wl = gen.WORKLOADS["tiny"]
     x = np.zeros((4, wl.d), np.uint16)

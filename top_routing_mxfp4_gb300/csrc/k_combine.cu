@@ -31,7 +31,31 @@ __global__ void __launch_bounds__(128) k_combine(const float *__restrict__ yp, c
     }
 }
 
+// fused combine's last step: the fp32 per-token sums rounded to bf16
+__global__ void __launch_bounds__(256) k_acc_to_bf16(const float4 *__restrict__ acc, int64_t n4, uint2 *__restrict__ y)
+{
+    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < n4; i += int64_t(gridDim.x) * blockDim.x) {
+        const float4 v = __ldg(acc + i);
+        __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y);
+        __nv_bfloat162 hi = __floats2bfloat162_rn(v.z, v.w);
+        uint2 out;
+        out.x = *reinterpret_cast<uint32_t *>(&lo);
+        out.y = *reinterpret_cast<uint32_t *>(&hi);
+        y[i] = out;
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_acc_to_bf16(const float *acc, int64_t n, uint16_t *y, cudaStream_t st)
+{
+    const int64_t n4 = n / 4;
+    if (n4 == 0) return cudaSuccess;
+    const int64_t blocks = ceil_div(n4, 256);
+    k_acc_to_bf16<<<int(blocks < 152 * 16 ? blocks : 152 * 16), 256, 0, st>>>(reinterpret_cast<const float4 *>(acc), n4,
+                                                                             reinterpret_cast<uint2 *>(y));
+    return cudaGetLastError();
+}
 
 cudaError_t launch_combine(const float *yp, const int32_t *inv, int T, int d, int k, uint16_t *y, cudaStream_t st)
 {

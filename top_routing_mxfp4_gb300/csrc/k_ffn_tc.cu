@@ -18,7 +18,10 @@
 //     h = silu(G) * U, MXFP8-quantised along I (a warp's 32 lanes are one
 //     32-row block of I) -> hq / hs in the padded token layout;
 //   down GEMM, item (expert e, 128 or 256 rows of d, token tile):
-//     Y = Wd[e] h^T, epilogue yp[q][row] = topk_w[perm[q]] * Y (fp32).
+//     Y = Wd[e] h^T, epilogue yp[q][row] = topk_w[perm[q]] * Y (fp32), or,
+//     with the combine fused (large token tiles), yacc[perm[q] / k][row] +=
+//     topk_w[perm[q]] * Y by fp32 vector atomics in L2 (the k terms of a
+//     token are then summed in fp32 in an unspecified order).
 //
 // Token layout: the activations of expert e occupy `ntiles(e)` slots of SLOT
 // = roundup(NT, 128) rows starting at pad_off[e] (a multiple of 128); token r
@@ -107,6 +110,9 @@ struct GemmArgs {
     uint8_t *hq;    // gate/up out: [rows][Ih] e4m3
     uint8_t *hs;    // gate/up out: scale atoms [rows/128][KCh][512]
     float *yp;      // down out: [P][Mtot]
+    float *yacc;    // down out when set (fused combine): [T][Mtot] fp32 sums, zeroed by the caller
+    const int32_t *perm;  // [P] pair of each permuted row (token = perm / k)
+    int k;
     int E, Mtot, MT, MTA, KC, KCh, Ih;  // MT: m tiles per item sequence; MTA: 128-row tiles of A
     int stages;  // shared-memory pipeline depth (<= Cfg::MAX_STAGES)
     int32_t *status;
@@ -337,21 +343,29 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
         // their load latency overlaps the current item's accumulator wait
         Item nx{};
         float wn[(NT + 31) / 32];
+        int tn[(NT + 31) / 32];  // token of each column (fused combine)
         auto fetch = [&](int it2) {
             nx = decode_item(it2, s_tiles, s_off, p.E, p.MT, NT);
             if (MODE == DOWN) {
                 const int qb = s_off[nx.e] + nx.n_tile * NT;
 #pragma unroll
-                for (int i = 0; i < (NT + 31) / 32; ++i)
-                    wn[i] = (32 * i + lane < nx.n_valid) ? __ldg(p.w_sorted + qb + 32 * i + lane) : 0.f;
+                for (int i = 0; i < (NT + 31) / 32; ++i) {
+                    const bool v = 32 * i + lane < nx.n_valid;
+                    wn[i] = v ? __ldg(p.w_sorted + qb + 32 * i + lane) : 0.f;
+                    tn[i] = (v && p.yacc) ? __ldg(p.perm + qb + 32 * i + lane) / p.k : 0;
+                }
             }
         };
         if (int(blockIdx.x) < total) fetch(blockIdx.x);
         for (int it = blockIdx.x; it < total; it += gridDim.x) {
             const Item w = nx;
             float wl[(NT + 31) / 32];
+            int tl[(NT + 31) / 32];
 #pragma unroll
-            for (int i = 0; i < (NT + 31) / 32; ++i) wl[i] = wn[i];
+            for (int i = 0; i < (NT + 31) / 32; ++i) {
+                wl[i] = wn[i];
+                tl[i] = tn[i];
+            }
             if (it + int(gridDim.x) < total) fetch(it + gridDim.x);
             [[maybe_unused]] const int qbase = s_off[w.e] + w.n_tile * NT;  // first permuted row of the tile (down)
             if (threadIdx.x == 64) LMOE_TRACE_EV(2, 0x40 | MODE, it, 0);  // epilogue: waiting
@@ -424,8 +438,12 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
                     tmem_ld_wait();
                     // gate weights of this chunk's columns: column c's weight is lane (c0 & 31) + c of wl[c0 / 32]
                     float wsel = wl[0];
+                    int tsel = tl[0];
 #pragma unroll
-                    for (int i = 1; i < (NT + 31) / 32; ++i) wsel = (c0 / 32 == i) ? wl[i] : wsel;
+                    for (int i = 1; i < (NT + 31) / 32; ++i) {
+                        wsel = (c0 / 32 == i) ? wl[i] : wsel;
+                        tsel = (c0 / 32 == i) ? tl[i] : tsel;
+                    }
                     if constexpr (C::STAGED) {
                         // transpose through shared memory: sf[c][row], row stride STG_STRIDE
                         __syncwarp();
@@ -434,18 +452,22 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
                         __syncwarp();
                         // lane l: token column c = 4 pp + l / 8, 4 rows starting at 4 (l % 8)
                         const int f4 = 4 * (lane & 7);
-                        float *ybase = p.yp + int64_t(qbase + c0) * p.Mtot + mt * 128 + 32 * q + f4;
+                        const int col = mt * 128 + 32 * q + f4;
 #pragma unroll
                         for (int pp = 0; pp < CW / 4; ++pp) {
                             const int c = 4 * pp + (lane >> 3);
                             const float wc = __shfl_sync(0xFFFFFFFFu, wsel, (c0 & 31) + c);
+                            const int tc = __shfl_sync(0xFFFFFFFFu, tsel, (c0 & 31) + c);
                             if (c0 + c < w.n_valid) {
                                 float4 a = *reinterpret_cast<const float4 *>(sf + c * C::STG_STRIDE + f4);
                                 a.x *= wc;
                                 a.y *= wc;
                                 a.z *= wc;
                                 a.w *= wc;
-                                *reinterpret_cast<float4 *>(ybase + int64_t(c) * p.Mtot) = a;
+                                if (p.yacc)
+                                    atomicAdd(reinterpret_cast<float4 *>(p.yacc + int64_t(tc) * p.Mtot + col), a);
+                                else
+                                    *reinterpret_cast<float4 *>(p.yp + int64_t(qbase + c0 + c) * p.Mtot + col) = a;
                             }
                         }
                     } else {
@@ -697,6 +719,7 @@ FfnLayout ffn_layout(int64_t P, int d, int E, int I)
 {
     FfnLayout L{};
     L.NT = P <= 4 * int64_t(E) ? 16 : (P <= 16 * int64_t(E) ? 32 : 128);
+    L.fused = L.NT >= 64;  // Cfg<DOWN, NT>::STAGED
     L.SLOT = int(round_up(L.NT, 128));
     const int64_t touched = P < E ? P : E;
     L.rows = (ceil_div(P, L.NT) + touched) * L.SLOT;
@@ -779,6 +802,7 @@ cudaError_t launch_gather_pad(const uint8_t *xq, const uint8_t *xs, int T, int d
 cudaError_t launch_expert_gemms(const FfnArgs &a, const FfnLayout &L, char *scratch, cudaStream_t st, cudaEvent_t mid)
 {
     if (a.P == 0) return cudaSuccess;
+    if (a.yacc && !L.fused) return cudaErrorInvalidValue;  // the fused combine needs the staged epilogue
     const int Ip = int(round_up(a.I, 128));
     uint8_t *xq = reinterpret_cast<uint8_t *>(scratch + L.xq);
     uint8_t *xs = reinterpret_cast<uint8_t *>(scratch + L.xs);
@@ -829,6 +853,9 @@ cudaError_t launch_expert_gemms(const FfnArgs &a, const FfnLayout &L, char *scra
     g.sfb = hs;
     g.tiles = reinterpret_cast<const int32_t *>(scratch + L.tiles_dn);
     g.yp = a.yp;
+    g.yacc = a.yacc;
+    g.perm = a.perm;
+    g.k = a.k;
     g.Mtot = a.d;
     g.MTA = a.d / 128;
     g.MT = int(ceil_div(g.MTA, down_tiles_per_item(L.NT)));

@@ -52,7 +52,8 @@ bool weights_ok(const lmoe_expert_weights *W)
 
 // Workspace layout of lmoe_forward (each region 256-byte aligned):
 //   status | logits | idx | w | counts | offsets | perm | inv | permute scratch
-//   | ffn scratch (padded MXFP8 activations, h, schedule) | yp
+//   | ffn scratch (padded MXFP8 activations, h, schedule)
+//   | yp (per-pair outputs [T*k][d]) or, with the fused combine, yacc ([T][d] fp32 sums)
 struct FwdLayout {
     size_t status, logits, idx, w, counts, offsets, perm, inv, rscratch, pscratch, fscratch, yp, total;
 };
@@ -78,7 +79,7 @@ FwdLayout fwd_layout(const lmoe_dims *d)
     L.rscratch = take(router_scratch_bytes(int(T), d->d, int(E)));
     L.pscratch = take(permute_scratch_bytes(P, int(E)));
     L.fscratch = take(ffn_layout(P, d->d, int(E), d->I).total);
-    L.yp = take(size_t(P * d->d * 4));
+    L.yp = take(size_t((ffn_layout(P, d->d, int(E), d->I).fused ? T : P) * d->d * 4));
     L.total = off;
     return L;
 }
@@ -220,7 +221,7 @@ lmoe_status lmoe_expert_ffn(const uint8_t *xq, const uint8_t *xs, const lmoe_exp
     if (e == cudaSuccess) e = launch_gather_pad(xq, xs, dims->T, dims->d, dims->k, dims->E, offsets, perm, topk_w, L, fs,
                                                    st);
     if (e != cudaSuccess) return cuda_status(e);
-    FfnArgs f{W, offsets, perm, topk_w, int(P), dims->d, dims->E, dims->k, dims->I, yp, reinterpret_cast<int32_t *>(ws)};
+    FfnArgs f{W, offsets, perm, topk_w, int(P), dims->d, dims->E, dims->k, dims->I, yp, nullptr, reinterpret_cast<int32_t *>(ws)};
     return cuda_status(launch_expert_gemms(f, L, fs, st));
 }
 
@@ -266,6 +267,10 @@ lmoe_status lmoe_forward(const uint16_t *x_bf16, const float *Wr, const float *b
     const FfnLayout FL = ffn_layout(P, d, E, dims->I);
     float *yp = reinterpret_cast<float *>(ws + L.yp);
     int32_t *status = reinterpret_cast<int32_t *>(ws + L.status);
+    // Large batches fuse the combine into the down GEMM: its epilogue adds
+    // each pair's weighted output into the token's fp32 row (zeroed here),
+    // which one pass then rounds to bf16.
+    float *yacc = FL.fused ? yp : nullptr;
 
     cudaError_t e = mark(0, st);
     if (e == cudaSuccess) e = cudaMemsetAsync(status, 0, sizeof(int32_t), st);
@@ -276,13 +281,15 @@ lmoe_status lmoe_forward(const uint16_t *x_bf16, const float *Wr, const float *b
                            ffn_sched(FL, d, dims->I, fs));
     if (e == cudaSuccess) e = mark(2, st);
     if (e == cudaSuccess) e = launch_quant_scatter_pad(x_bf16, T, d, k, inv, w, FL, fs, st);
+    if (e == cudaSuccess && yacc) e = cudaMemsetAsync(yacc, 0, size_t(T) * d * sizeof(float), st);
     if (e == cudaSuccess) e = mark(3, st);
     if (e == cudaSuccess) {
-        FfnArgs f{W, offsets, perm, w, int(P), d, E, k, dims->I, yp, status};
+        FfnArgs f{W, offsets, perm, w, int(P), d, E, k, dims->I, yp, yacc, status};
         e = launch_expert_gemms(f, FL, fs, st, g_stage_events_on ? g_stage_events[4] : nullptr);
     }
     if (e == cudaSuccess) e = mark(5, st);
-    if (e == cudaSuccess) e = launch_combine(yp, inv, T, d, k, y_bf16, st);
+    if (e == cudaSuccess)
+        e = yacc ? launch_acc_to_bf16(yacc, int64_t(T) * d, y_bf16, st) : launch_combine(yp, inv, T, d, k, y_bf16, st);
     if (e == cudaSuccess) e = mark(6, st);
     return cuda_status(e);
 }

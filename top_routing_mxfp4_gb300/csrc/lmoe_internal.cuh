@@ -129,6 +129,7 @@ struct FfnLayout {
     int NT, SLOT;      // token tile and slot rows
     int64_t rows;      // padded token rows reserved
     size_t pad_off, tiles_gu, tiles_dn, xq, xs, hq, hs, hs_bytes, w_sorted, dst_row, total;  // byte offsets / sizes
+    bool fused;  // large token tiles: the down GEMM can accumulate into the per-token output (FfnArgs::yacc)
 };
 FfnLayout ffn_layout(int64_t P, int d, int E, int I);
 // The permute by-products the forward asks for, pointing into the FFN scratch.
@@ -139,7 +140,8 @@ struct FfnArgs {
     const int32_t *offsets, *perm;
     const float *topk_w;
     int P, d, E, k, I;
-    float *yp;  // [P][d] in permuted order
+    float *yp;    // [P][d] in permuted order
+    float *yacc;  // when set (FfnLayout::fused only): [T][d] fp32 sums over the k pairs instead of yp
     int32_t *status;
 };
 // slot starts and per-GEMM work-item prefixes from the segment offsets
@@ -158,5 +160,7 @@ cudaError_t launch_expert_gemms(const FfnArgs &a, const FfnLayout &L, char *scra
                                 cudaEvent_t mid = nullptr);
 
 cudaError_t launch_combine(const float *yp, const int32_t *inv, int T, int d, int k, uint16_t *y, cudaStream_t st);
+// y = bf16(acc), n elements (n % 4 == 0)
+cudaError_t launch_acc_to_bf16(const float *acc, int64_t n, uint16_t *y, cudaStream_t st);
 
 }  // namespace lmoe
