@@ -83,6 +83,31 @@ def profiled_traffic(workload: str):
     return None
 
 
+def barrier(ws: int) -> None:
+    """All ranks meet (no-op for a single process)."""
+    if ws > 1:
+        import torch.distributed as tdist
+        tdist.barrier()
+
+
+def max_over_ranks(value: float, ws: int, device) -> float:
+    """The largest of the ranks' values (the slowest rank's time): one
+    all-reduce of a scalar on `device` (the GPU under NCCL, the CPU under gloo)."""
+    if ws == 1:
+        return value
+    import torch
+    import torch.distributed as tdist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(tokens_per_rank: int, ws: int, ms_per_step: float) -> float:
+    """Tokens per second of all ranks together: every rank processes its own
+    batch (weak scaling, replicas), timed by the slowest rank."""
+    return ws * tokens_per_rank / (ms_per_step / 1e3)
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -185,7 +210,6 @@ def cpu_baseline(wl, ntok: int):
 def run_ours(args, ws, rank, local):
     import numpy as np
     import torch
-    import torch.distributed as tdist
 
     import lmoe_inputs as gen
     from top_routing_mxfp4_gb300 import build as lbuild
@@ -221,8 +245,7 @@ def run_ours(args, ws, rank, local):
         for e in row:
             e.record(st)
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if ws > 1:
-        tdist.barrier()
+    barrier(ws)
     torch.cuda.synchronize()
     t_start.record(st)
     for i in range(K):
@@ -230,18 +253,14 @@ def run_ours(args, ws, rank, local):
         layer.forward(xd, y=y, topk_idx=idx)
     t_end.record(st)
     torch.cuda.synchronize()
-    if ws > 1:
-        tdist.barrier()
+    barrier(ws)
     lmoe.set_stage_events(None)
     clocks = sampler.stop()
     elapsed_ms = t_start.elapsed_time(t_end)
     stage_ms = {name: sum(e[j].elapsed_time(e[j + 1]) for e in evs) / K for j, name in enumerate(lmoe.STAGES)}
-    if ws > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, ws, dev)
     ms_per_step = elapsed_ms / K
-    value = ws * T / (ms_per_step / 1e3)
+    value = whole_job_rate(T, ws, ms_per_step)
 
     # end to end through host buffers: H2D of x from pinned memory, forward, D2H of y
     xh = torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -252,8 +271,7 @@ def run_ours(args, ws, rank, local):
         layer.forward(xdev, y=y)
         yh.copy_(y, non_blocking=True)
     torch.cuda.synchronize()
-    if ws > 1:
-        tdist.barrier()
+    barrier(ws)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(st)
     for _ in range(K):
@@ -262,12 +280,8 @@ def run_ours(args, ws, rank, local):
         yh.copy_(y, non_blocking=True)
     e1.record(st)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if ws > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-        tdist.barrier()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), ws, dev)
+    barrier(ws)
 
     peaks = load_peaks()
     per_expert_w = 3 * wl.I * wl.d * MXFP4_B           # gate + up + down bytes of one expert
@@ -306,7 +320,7 @@ def run_ours(args, ws, rank, local):
                          f"of weights read per step (L2 129 MB)"},
         "roofline": roofline,
         "stage_ms": stage_ms, "touched_experts": touched,
-        "e2e": {"value": ws * T / (e2e_ms / K / 1e3), "unit": UNIT, "h2d_bytes_per_step": xh.numel() * 2,
+        "e2e": {"value": whole_job_rate(T, ws, e2e_ms / K), "unit": UNIT, "h2d_bytes_per_step": xh.numel() * 2,
                 "d2h_bytes_per_step": yh.numel() * 2},
         "gpu_launches": K * launches_per_step, "clocks": clocks,
     }
