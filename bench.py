@@ -240,24 +240,34 @@ def run_ours(args, ws, rank, local):
     sampler.start()
     time.sleep(0.3)
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(lmoe.NUM_STAGE_EVENTS)] for _ in range(K)]
-    for row in evs:  # torch creates the CUDA event objects on first record
-        for e in row:
-            e.record(st)
+    # headline: K back-to-back forward passes, nothing else on the stream (the
+    # kernels of consecutive stages overlap their launch through programmatic
+    # dependent launch, which an event between them would serialise)
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(ws)
     torch.cuda.synchronize()
     t_start.record(st)
     for i in range(K):
-        lmoe.set_stage_events(evs[i])
         layer.forward(xd, y=y, topk_idx=idx)
     t_end.record(st)
     torch.cuda.synchronize()
     barrier(ws)
+    elapsed_ms = t_start.elapsed_time(t_end)
+    # stage breakdown (and the gate/up GEMM time of the roofline): a second
+    # live pass with CUDA events at the stage boundaries
+    K2 = min(K, 50)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(lmoe.NUM_STAGE_EVENTS)] for _ in range(K2)]
+    for row in evs:  # torch creates the CUDA event objects on first record
+        for e in row:
+            e.record(st)
+    torch.cuda.synchronize()
+    for i in range(K2):
+        lmoe.set_stage_events(evs[i])
+        layer.forward(xd, y=y, topk_idx=idx)
+    torch.cuda.synchronize()
     lmoe.set_stage_events(None)
     clocks = sampler.stop()
-    elapsed_ms = t_start.elapsed_time(t_end)
-    stage_ms = {name: sum(e[j].elapsed_time(e[j + 1]) for e in evs) / K for j, name in enumerate(lmoe.STAGES)}
+    stage_ms = {name: sum(e[j].elapsed_time(e[j + 1]) for e in evs) / K2 for j, name in enumerate(lmoe.STAGES)}
     elapsed_ms = max_over_ranks(elapsed_ms, ws, dev)
     ms_per_step = elapsed_ms / K
     value = whole_job_rate(T, ws, ms_per_step)
@@ -319,7 +329,10 @@ def run_ours(args, ws, rank, local):
                    "l2": f"inputs larger than L2: {touched} touched experts = {touched * per_expert_w / 1e9:.2f} GB "
                          f"of weights read per step (L2 129 MB)"},
         "roofline": roofline,
-        "stage_ms": stage_ms, "touched_experts": touched,
+        "stage_ms": stage_ms,
+        "stage_ms_note": f"second live pass of {K2} steps with CUDA events at the stage boundaries (the events "
+                         "serialise the launches, so the stages add up to more than ms_per_step)",
+        "touched_experts": touched,
         "e2e": {"value": whole_job_rate(T, ws, e2e_ms / K), "unit": UNIT, "h2d_bytes_per_step": xh.numel() * 2,
                 "d2h_bytes_per_step": yh.numel() * 2},
         "gpu_launches": K * launches_per_step, "clocks": clocks,

@@ -11,6 +11,7 @@ namespace {
 __global__ void __launch_bounds__(128) k_combine(const float *__restrict__ yp, const int32_t *__restrict__ inv, int T,
                                                  int d, int k, uint16_t *__restrict__ y)
 {
+    pdl_enter();
     __shared__ int32_t rows[32];
     const int t = blockIdx.x;
     if (threadIdx.x < k) rows[threadIdx.x] = __ldg(inv + int64_t(t) * k + threadIdx.x);
@@ -34,6 +35,7 @@ __global__ void __launch_bounds__(128) k_combine(const float *__restrict__ yp, c
 // fused combine's last step: the fp32 per-token sums rounded to bf16
 __global__ void __launch_bounds__(256) k_acc_to_bf16(const float4 *__restrict__ acc, int64_t n4, uint2 *__restrict__ y)
 {
+    pdl_enter();
     for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < n4; i += int64_t(gridDim.x) * blockDim.x) {
         const float4 v = __ldg(acc + i);
         __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y);
@@ -52,17 +54,15 @@ cudaError_t launch_acc_to_bf16(const float *acc, int64_t n, uint16_t *y, cudaStr
     const int64_t n4 = n / 4;
     if (n4 == 0) return cudaSuccess;
     const int64_t blocks = ceil_div(n4, 256);
-    k_acc_to_bf16<<<int(blocks < 152 * 16 ? blocks : 152 * 16), 256, 0, st>>>(reinterpret_cast<const float4 *>(acc), n4,
-                                                                             reinterpret_cast<uint2 *>(y));
-    return cudaGetLastError();
+    return launch_pdl(k_acc_to_bf16, dim3(unsigned(blocks < 152 * 16 ? blocks : 152 * 16)), dim3(256), 0, st,
+                      reinterpret_cast<const float4 *>(acc), n4, reinterpret_cast<uint2 *>(y));
 }
 
 cudaError_t launch_combine(const float *yp, const int32_t *inv, int T, int d, int k, uint16_t *y, cudaStream_t st)
 {
     if (T == 0) return cudaSuccess;
     const int ysplit = T >= 1024 ? 1 : (T >= 128 ? 2 : 7);  // enough CTAs for small T
-    k_combine<<<dim3(T, ysplit), 128, 0, st>>>(yp, inv, T, d, k, y);
-    return cudaGetLastError();
+    return launch_pdl(k_combine, dim3(T, ysplit), dim3(128), 0, st, yp, inv, T, d, k, y);
 }
 
 }  // namespace lmoe

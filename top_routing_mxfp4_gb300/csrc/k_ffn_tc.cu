@@ -204,9 +204,11 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
     int32_t *s_off = s_tiles + (p.E + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // the schedule is an output of an earlier kernel than the previous one
+    // (complete before this grid starts); read through L2
     for (int i = threadIdx.x; i <= p.E; i += blockDim.x) {
-        s_tiles[i] = p.tiles[i];
-        s_off[i] = p.offsets[i];
+        s_tiles[i] = __ldcg(p.tiles + i);
+        s_off[i] = __ldcg(p.offsets + i);
     }
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -232,6 +234,24 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
     const int total = s_tiles[p.E];
     // slot start of an expert's first token tile (tiles[e] = slots before e times MT)
     auto slot_row = [&](int e) { return (s_tiles[e] / p.MT) * C::SLOT; };
+    // Before the previous kernel has finished: the producer asks L2 for the
+    // weight tiles of its first stages (the weights and the schedule are
+    // inputs of earlier kernels), then every thread waits for it.
+    if (warp == 0 && lane == 0) {
+        int it = blockIdx.x, kc = 0;
+        for (int s = 0; s < p.stages && it < total; ++s) {
+            const Item w = decode_item(it, s_tiles, s_off, p.E, p.MT, NT);
+            const int mt0 = MODE == GATEUP ? w.m_tile : C::MATS * w.m_tile;
+            const int mt1 = MODE == GATEUP ? w.m_tile : (mt0 + 1 < p.MTA ? mt0 + 1 : mt0);
+            tma_prefetch_2d(&tmA0, kc * 128, w.e * p.Mtot + mt0 * 128);
+            if (C::MATS == 2) tma_prefetch_2d(&tmA1, kc * 128, w.e * p.Mtot + mt1 * 128);
+            if (++kc == p.KC) {
+                kc = 0;
+                it += gridDim.x;
+            }
+        }
+    }
+    pdl_enter();
 
     if (warp == 0) {
         // ---------------- TMA producer ----------------
@@ -535,6 +555,7 @@ __global__ void __launch_bounds__(1024) k_ffn_schedule(const int32_t *__restrict
                                                       int MT_gu, int MT_dn, int32_t *pad_off, int32_t *tiles_gu,
                                                       int32_t *tiles_dn)
 {
+    pdl_enter();
     __shared__ int32_t v[2048], o[2048], warp_tot[32], tot;
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
         const int n = offsets[e + 1] - offsets[e];
@@ -571,6 +592,7 @@ __global__ void k_quant_scatter_pad(const uint16_t *__restrict__ x, int64_t nblo
                                     const float *__restrict__ topk_w, uint8_t *__restrict__ xq,
                                     uint8_t *__restrict__ xs, float *__restrict__ w_sorted)
 {
+    pdl_enter();
     const int nb = d / 32, KC = d / 128;
     for (int64_t g = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; g < nblocks; g += int64_t(gridDim.x) * blockDim.x) {
         const int64_t t = g / nb;
@@ -612,6 +634,7 @@ __global__ void k_gather_pad(const uint8_t *__restrict__ xq, const uint8_t *__re
                              const float *__restrict__ topk_w, const int32_t *__restrict__ pad_off, int NT, int SLOT,
                              uint8_t *__restrict__ q_pad, uint8_t *__restrict__ s_pad, float *__restrict__ w_sorted)
 {
+    pdl_enter();
     const int cq = d / 16, nb = d / 32, KC = d / 128;
     const int per_row = cq + nb;
     for (int64_t g = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; g < P * per_row; g += int64_t(gridDim.x) * blockDim.x) {
@@ -706,7 +729,10 @@ cudaError_t launch_gemm(const CUtensorMap &a0, const CUtensorMap &a1, const CUte
     if (args.stages < 2) return cudaErrorInvalidConfiguration;
     cudaError_t e = cudaFuncSetAttribute(k_moe_gemm<MODE, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
-    k_moe_gemm<MODE, NT><<<num_sms(), Cfg<MODE, NT>::THREADS, smem, st>>>(a0, a1, b, args);
+    {
+        const cudaError_t le_ = launch_pdl(k_moe_gemm<MODE, NT>, dim3(num_sms()), dim3(Cfg<MODE, NT>::THREADS), smem, st, a0, a1, b, args);
+        if (le_ != cudaSuccess) return le_;
+    }
     return cudaGetLastError();
 }
 
@@ -748,11 +774,10 @@ FfnLayout ffn_layout(int64_t P, int d, int E, int I)
 cudaError_t launch_ffn_schedule(const int32_t *offsets, int E, int d, int I, const FfnLayout &L, char *scratch,
                                 cudaStream_t st)
 {
-    k_ffn_schedule<<<1, 1024, 0, st>>>(offsets, E, L.NT, L.SLOT, int(ceil_div(I, 128)),
-                                       int(ceil_div(d / 128, down_tiles_per_item(L.NT))),
-                                       reinterpret_cast<int32_t *>(scratch + L.pad_off),
-                                       reinterpret_cast<int32_t *>(scratch + L.tiles_gu),
-                                       reinterpret_cast<int32_t *>(scratch + L.tiles_dn));
+    {
+        const cudaError_t le_ = launch_pdl(k_ffn_schedule, dim3(1), dim3(1024), 0, st, offsets, E, L.NT, L.SLOT, int(ceil_div(I, 128)), int(ceil_div(d / 128, down_tiles_per_item(L.NT))), reinterpret_cast<int32_t *>(scratch + L.pad_off), reinterpret_cast<int32_t *>(scratch + L.tiles_gu), reinterpret_cast<int32_t *>(scratch + L.tiles_dn));
+        if (le_ != cudaSuccess) return le_;
+    }
     return cudaGetLastError();
 }
 
@@ -776,10 +801,10 @@ cudaError_t launch_quant_scatter_pad(const uint16_t *x, int T, int d, int k, con
     const int64_t nblocks = int64_t(T) * (d / 32);
     if (nblocks == 0) return cudaSuccess;
     const int grid = int(ceil_div(nblocks, 128) < 152 * 32 ? ceil_div(nblocks, 128) : 152 * 32);
-    k_quant_scatter_pad<<<grid, 128, 0, st>>>(x, nblocks, d, k, reinterpret_cast<const int32_t *>(scratch + L.dst_row),
-                                              inv, topk_w, reinterpret_cast<uint8_t *>(scratch + L.xq),
-                                              reinterpret_cast<uint8_t *>(scratch + L.xs),
-                                              reinterpret_cast<float *>(scratch + L.w_sorted));
+    {
+        const cudaError_t le_ = launch_pdl(k_quant_scatter_pad, dim3(grid), dim3(128), 0, st, x, nblocks, d, k, reinterpret_cast<const int32_t *>(scratch + L.dst_row), inv, topk_w, reinterpret_cast<uint8_t *>(scratch + L.xq), reinterpret_cast<uint8_t *>(scratch + L.xs), reinterpret_cast<float *>(scratch + L.w_sorted));
+        if (le_ != cudaSuccess) return le_;
+    }
     return cudaGetLastError();
 }
 
@@ -791,11 +816,10 @@ cudaError_t launch_gather_pad(const uint8_t *xq, const uint8_t *xs, int T, int d
     const int64_t n = P * (d / 16 + d / 32);
     if (n == 0) return cudaSuccess;
     const int grid = int(ceil_div(n, 256) < 152 * 64 ? ceil_div(n, 256) : 152 * 64);
-    k_gather_pad<<<grid, 256, 0, st>>>(xq, xs, P, d, k, E, offsets, perm, topk_w,
-                                       reinterpret_cast<const int32_t *>(scratch + L.pad_off), L.NT, L.SLOT,
-                                       reinterpret_cast<uint8_t *>(scratch + L.xq),
-                                       reinterpret_cast<uint8_t *>(scratch + L.xs),
-                                       reinterpret_cast<float *>(scratch + L.w_sorted));
+    {
+        const cudaError_t le_ = launch_pdl(k_gather_pad, dim3(grid), dim3(256), 0, st, xq, xs, P, d, k, E, offsets, perm, topk_w, reinterpret_cast<const int32_t *>(scratch + L.pad_off), L.NT, L.SLOT, reinterpret_cast<uint8_t *>(scratch + L.xq), reinterpret_cast<uint8_t *>(scratch + L.xs), reinterpret_cast<float *>(scratch + L.w_sorted));
+        if (le_ != cudaSuccess) return le_;
+    }
     return cudaGetLastError();
 }
 

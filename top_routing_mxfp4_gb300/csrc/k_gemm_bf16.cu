@@ -102,6 +102,7 @@ __global__ void __launch_bounds__(192, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const int total = p.MT * p.NTL * p.KS;
+    pdl_enter();
 
     // item -> (k slice, token tile, m tile); m fastest so neighbouring CTAs share the token tile
     if (warp == 0) {
@@ -229,6 +230,7 @@ __global__ void __launch_bounds__(192, 1)
 // fp32 -> three bf16 parts (hi, mid, lo), each part a contiguous [n] block.
 __global__ void k_split_bf16x3(const float *__restrict__ w, int64_t n, __nv_bfloat16 *__restrict__ out)
 {
+    pdl_enter();
     for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < n / 4; i += int64_t(gridDim.x) * blockDim.x) {
         const float4 v = __ldg(reinterpret_cast<const float4 *>(w) + i);
         const float a[4] = {v.x, v.y, v.z, v.w};
@@ -250,6 +252,7 @@ __global__ void k_split_bf16x3(const float *__restrict__ w, int64_t n, __nv_bflo
 __global__ void k_splitk_reduce(const float *__restrict__ part, int KS, int64_t TM, int M, const float *__restrict__ bias,
                                 float *__restrict__ out)
 {
+    pdl_enter();
     for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < TM; i += int64_t(gridDim.x) * blockDim.x) {
         float acc = 0.f;
 #pragma unroll 8
@@ -301,7 +304,10 @@ cudaError_t run(const CUtensorMap &a, const CUtensorMap &b, const DenseArgs &arg
     if (e != cudaSuccess) return e;
     const int total = args.MT * args.NTL * args.KS;
     const int grid = total < sm_count() ? total : sm_count();
-    k_gemm_bf16<NPARTS, NB, OUT><<<grid, 192, smem, st>>>(a, b, args);
+    {
+        const cudaError_t le_ = launch_pdl(k_gemm_bf16<NPARTS, NB, OUT>, dim3(grid), dim3(192), smem, st, a, b, args);
+        if (le_ != cudaSuccess) return le_;
+    }
     return cudaGetLastError();
 }
 
@@ -352,7 +358,10 @@ cudaError_t launch_route(const uint16_t *x, const float *Wr, const float *bias, 
     __nv_bfloat16 *w3 = static_cast<__nv_bfloat16 *>(scratch);
     float *partial = reinterpret_cast<float *>(static_cast<char *>(scratch) + round_up(int64_t(3) * E * d * 2, 256));
     const int64_t n = int64_t(E) * d;
-    k_split_bf16x3<<<int(ceil_div(n / 4, 256) < 152 * 16 ? ceil_div(n / 4, 256) : 152 * 16), 256, 0, st>>>(Wr, n, w3);
+    {
+        const cudaError_t le_ = launch_pdl(k_split_bf16x3, dim3(int(ceil_div(n / 4, 256) < 152 * 16 ? ceil_div(n / 4, 256) : 152 * 16)), dim3(256), 0, st, Wr, n, w3);
+        if (le_ != cudaSuccess) return le_;
+    }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     int NB, KS;
@@ -372,8 +381,10 @@ cudaError_t launch_route(const uint16_t *x, const float *Wr, const float *bias, 
     e = dispatch<3, OUT_PARTIAL>(NB, ma, mb, a, st);
     if (e != cudaSuccess) return e;
     const int64_t TM = int64_t(T) * E;
-    k_splitk_reduce<<<int(ceil_div(TM, 256) < 152 * 8 ? ceil_div(TM, 256) : 152 * 8), 256, 0, st>>>(partial, KS, TM, E,
-                                                                                                    bias, logits);
+    {
+        const cudaError_t le_ = launch_pdl(k_splitk_reduce, dim3(int(ceil_div(TM, 256) < 152 * 8 ? ceil_div(TM, 256) : 152 * 8)), dim3(256), 0, st, partial, KS, TM, E, bias, logits);
+        if (le_ != cudaSuccess) return le_;
+    }
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     return launch_topk_softmax(logits, T, E, k, idx, w, st);

@@ -24,6 +24,7 @@ constexpr int MAXE = 2048;
 __global__ void __launch_bounds__(256) k_perm_hist(const int32_t *__restrict__ idx, int64_t P, int E,
                                                    int32_t *__restrict__ blockhist, int32_t *status)
 {
+    pdl_enter();
     __shared__ int32_t h[MAXE];
     for (int e = threadIdx.x; e < E; e += blockDim.x) h[e] = 0;
     __syncthreads();
@@ -101,6 +102,7 @@ __global__ void __launch_bounds__(1024) k_perm_scan(int32_t *__restrict__ blockh
                                                     int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
                                                     FfnSched sc)
 {
+    pdl_enter();
     __shared__ int32_t cnt[MAXE];
     __shared__ int32_t warp_tot[32];
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
@@ -157,6 +159,7 @@ __global__ void __launch_bounds__(256) k_perm_scatter(const int32_t *__restrict_
                                                       int32_t *__restrict__ perm, int32_t *__restrict__ inv,
                                                       const int32_t *__restrict__ offsets, FfnSched sc)
 {
+    pdl_enter();
     extern __shared__ int32_t wh[];  // [WARPS][E] per-warp counts, then cursors
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     for (int i = threadIdx.x; i < WARPS * E; i += blockDim.x) wh[i] = 0;
@@ -216,6 +219,7 @@ __global__ void __launch_bounds__(256) k_perm_single(const int32_t *__restrict__
                                                      int32_t *__restrict__ perm, int32_t *__restrict__ inv,
                                                      int32_t *status, FfnSched sc)
 {
+    pdl_enter();
     extern __shared__ int4 wh_raw[];
     int32_t *wh = reinterpret_cast<int32_t *>(wh_raw);  // [WARPS][E]
     __shared__ int32_t warp_tot[WARPS];
@@ -351,20 +355,32 @@ cudaError_t launch_permute(const int32_t *idx, int64_t P, int E, int32_t *counts
         const size_t smem = size_t(WARPS + 1) * E * sizeof(int32_t) + 16;
         cudaError_t e = cudaFuncSetAttribute(k_perm_single, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
         if (e != cudaSuccess) return e;
-        k_perm_single<<<1, 256, smem, st>>>(idx, int(P), E, counts, offsets, perm, inv, status, sched);
+        {
+            const cudaError_t le_ = launch_pdl(k_perm_single, dim3(1), dim3(256), smem, st, idx, int(P), E, counts, offsets, perm, inv, status, sched);
+            if (le_ != cudaSuccess) return le_;
+        }
         return cudaGetLastError();
     }
     if (nblk > 0) {
-        k_perm_hist<<<nblk, 256, 0, st>>>(idx, P, E, blockhist, status);
+        {
+            const cudaError_t le_ = launch_pdl(k_perm_hist, dim3(nblk), dim3(256), 0, st, idx, P, E, blockhist, status);
+            if (le_ != cudaSuccess) return le_;
+        }
     }
-    k_perm_scan<<<1, 1024, 0, st>>>(blockhist, nblk, E, counts, offsets, sched);
+    {
+        const cudaError_t le_ = launch_pdl(k_perm_scan, dim3(1), dim3(1024), 0, st, blockhist, nblk, E, counts, offsets, sched);
+        if (le_ != cudaSuccess) return le_;
+    }
     if (nblk > 0) {
         const size_t smem = size_t(WARPS) * E * sizeof(int32_t);
         if (smem > 48 * 1024) {  // above the default dynamic shared-memory limit (E > 1536)
             cudaError_t e = cudaFuncSetAttribute(k_perm_scatter, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
             if (e != cudaSuccess) return e;
         }
-        k_perm_scatter<<<nblk, 256, smem, st>>>(idx, P, E, blockhist, perm, inv, offsets, sched);
+        {
+            const cudaError_t le_ = launch_pdl(k_perm_scatter, dim3(nblk), dim3(256), smem, st, idx, P, E, blockhist, perm, inv, offsets, sched);
+            if (le_ != cudaSuccess) return le_;
+        }
     }
     return cudaGetLastError();
 }

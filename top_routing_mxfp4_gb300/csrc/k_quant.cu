@@ -21,6 +21,7 @@ __device__ __forceinline__ int64_t tc_scale_offset(int64_t m, int r, int b, int 
 __global__ void k_quant_mxfp4(const float *__restrict__ w, int64_t nblocks, int rows, int K, uint8_t *__restrict__ q,
                               uint8_t *__restrict__ s, int layout, int Kp, int RT, int KC)
 {
+    pdl_enter();
     const int nb = K / 32;
     for (int64_t g = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; g < nblocks; g += int64_t(gridDim.x) * blockDim.x) {
         const int64_t row = g / nb;  // row over all matrices
@@ -86,6 +87,7 @@ __device__ __forceinline__ uint32_t quant_block_e4m3(const uint16_t *src, uint4 
 __global__ void k_quant_mxfp8(const uint16_t *__restrict__ x, int64_t nblocks, int K, uint8_t *__restrict__ q,
                               uint8_t *__restrict__ s)
 {
+    pdl_enter();
     const int nb = K / 32;
     for (int64_t g = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; g < nblocks; g += int64_t(gridDim.x) * blockDim.x) {
         const int64_t row = g / nb;
@@ -121,7 +123,10 @@ cudaError_t launch_quant_mxfp4(const float *w, int64_t nmat, int rows, int K, ui
         if (e != cudaSuccess) return e;
     }
     if (nblocks == 0) return cudaSuccess;
-    k_quant_mxfp4<<<grid_for(nblocks, 256), 256, 0, st>>>(w, nblocks, rows, K, q, s, layout, Kp, RT, KC);
+    {
+        const cudaError_t le_ = launch_pdl(k_quant_mxfp4, dim3(grid_for(nblocks, 256)), dim3(256), 0, st, w, nblocks, rows, K, q, s, layout, Kp, RT, KC);
+        if (le_ != cudaSuccess) return le_;
+    }
     return cudaGetLastError();
 }
 
@@ -129,7 +134,10 @@ cudaError_t launch_quant_mxfp8(const uint16_t *x, int64_t rows, int K, uint8_t *
 {
     const int64_t nblocks = rows * (K / 32);
     if (nblocks == 0) return cudaSuccess;
-    k_quant_mxfp8<<<grid_for(nblocks, 256), 256, 0, st>>>(x, nblocks, K, q, s);
+    {
+        const cudaError_t le_ = launch_pdl(k_quant_mxfp8, dim3(grid_for(nblocks, 256)), dim3(256), 0, st, x, nblocks, K, q, s);
+        if (le_ != cudaSuccess) return le_;
+    }
     return cudaGetLastError();
 }
 

@@ -94,6 +94,7 @@ template <int NV>
 __global__ void __launch_bounds__(256) k_topk_softmax(const float *__restrict__ logits, int T, int E, int k,
                                                       int32_t *__restrict__ idx, float *__restrict__ w)
 {
+    pdl_enter();
     const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (t >= T) return;
     select_topk<NV>(logits + int64_t(t) * E, E, k, idx + int64_t(t) * k, w + int64_t(t) * k);
@@ -105,9 +106,9 @@ cudaError_t launch_topk_softmax(const float *logits, int T, int E, int k, int32_
 {
     if (T == 0) return cudaSuccess;
     const int grid = int(ceil_div(T, 8));
-    if (E <= 256) k_topk_softmax<8><<<grid, 256, 0, st>>>(logits, T, E, k, idx, w);
-    else if (E <= 896) k_topk_softmax<28><<<grid, 256, 0, st>>>(logits, T, E, k, idx, w);
-    else k_topk_softmax<64><<<grid, 256, 0, st>>>(logits, T, E, k, idx, w);
+    if (E <= 256) { const cudaError_t le_ = launch_pdl(k_topk_softmax<8>, dim3(grid), dim3(256), 0, st, logits, T, E, k, idx, w); if (le_ != cudaSuccess) return le_; }
+    else if (E <= 896) { const cudaError_t le_ = launch_pdl(k_topk_softmax<28>, dim3(grid), dim3(256), 0, st, logits, T, E, k, idx, w); if (le_ != cudaSuccess) return le_; }
+    else { const cudaError_t le_ = launch_pdl(k_topk_softmax<64>, dim3(grid), dim3(256), 0, st, logits, T, E, k, idx, w); if (le_ != cudaSuccess) return le_; }
     return cudaGetLastError();
 }
 

@@ -9,6 +9,39 @@
 
 namespace lmoe {
 
+// ---- programmatic dependent launch -------------------------------------------------------
+// Every kernel of the library is launched with programmatic stream
+// serialisation: it may be scheduled while the previous kernel of the stream
+// drains.  Before reading that kernel's outputs or writing global memory it
+// calls pdl_wait() (returns once the previous grid has completed and its
+// writes are visible), and only then allows its own dependents to be
+// scheduled (pdl_trigger), so at most the immediately preceding kernel can
+// still be running while a kernel does its pre-wait work; outputs of earlier
+// kernels are complete.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_enter()
+{
+    pdl_wait();
+    pdl_trigger();
+}
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args... args)
+{
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // ---- status word (first 4 bytes of a workspace) ---------------------------------
 // Kernels record the first error they see; the host reads it back with
 // lmoe_last_device_status.
