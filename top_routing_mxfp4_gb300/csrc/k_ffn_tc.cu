@@ -234,23 +234,8 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
     const int total = s_tiles[p.E];
     // slot start of an expert's first token tile (tiles[e] = slots before e times MT)
     auto slot_row = [&](int e) { return (s_tiles[e] / p.MT) * C::SLOT; };
-    // Before the previous kernel has finished: the producer asks L2 for the
-    // weight tiles of its first stages (the weights and the schedule are
-    // inputs of earlier kernels), then every thread waits for it.
-    if (warp == 0 && lane == 0) {
-        int it = blockIdx.x, kc = 0;
-        for (int s = 0; s < p.stages && it < total; ++s) {
-            const Item w = decode_item(it, s_tiles, s_off, p.E, p.MT, NT);
-            const int mt0 = MODE == GATEUP ? w.m_tile : C::MATS * w.m_tile;
-            const int mt1 = MODE == GATEUP ? w.m_tile : (mt0 + 1 < p.MTA ? mt0 + 1 : mt0);
-            tma_prefetch_2d(&tmA0, kc * 128, w.e * p.Mtot + mt0 * 128);
-            if (C::MATS == 2) tma_prefetch_2d(&tmA1, kc * 128, w.e * p.Mtot + mt1 * 128);
-            if (++kc == p.KC) {
-                kc = 0;
-                it += gridDim.x;
-            }
-        }
-    }
+    // Everything above reads only inputs of earlier kernels; the previous
+    // kernel's outputs are read after this wait.
     pdl_enter();
 
     if (warp == 0) {
