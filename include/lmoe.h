@@ -120,19 +120,28 @@ lmoe_status lmoe_quant_mxfp4(const float *w, int64_t nmat, int32_t rows, int32_t
  * round-to-nearest-even of x / 2^(byte-127), saturated at 448. */
 lmoe_status lmoe_quant_mxfp8(const uint16_t *x_bf16, int64_t rows, int32_t K, uint8_t *q, uint8_t *s, void *stream);
 
+/* Router weights in the form the router GEMM reads (load-time conversion, as
+ * for the expert weights): the fp32 weights Wr [E][d] written as three bf16
+ * planes Wr3 [3][E][d] (hi = bf16(Wr), mid = bf16(Wr - hi), lo = bf16(Wr -
+ * hi - mid), each rounded to nearest even) whose sum is Wr exactly (24
+ * significand bits).  d % 64 == 0.  Wr3 must hold
+ * lmoe_router_prepared_bytes(E, d) bytes (0 for invalid sizes). */
+size_t lmoe_router_prepared_bytes(int32_t E, int32_t d);
+lmoe_status lmoe_prepare_router(const float *Wr, int32_t E, int32_t d, uint16_t *Wr3, void *stream);
+
 /* Router [MoE]: logits[t][e] = fp32(sum_c x[t][c] * Wr[e][c]) (+ bias[e]),
- * accumulated in fp32 on the tensor cores (Wr split exactly into three bf16
- * parts whose products with bf16 x are exact in fp32),
- * x bf16 [T][d], Wr fp32 [E][d], bias fp32 [E] or NULL (the skewed
- * workload's popularity bias); then the top-k of each row (larger logit
- * first, ties by smaller id) into topk_idx[T][k] and the softmax over those
- * k logits into topk_w[T][k].  logits [T][E] is a required output. */
-lmoe_status lmoe_route(const uint16_t *x_bf16, const float *Wr, const float *bias, const lmoe_dims *dims,
+ * accumulated in fp32 on the tensor cores: each bf16 x times each bf16 plane
+ * of Wr is exact in fp32 and the three planes accumulate into one sum.
+ * x bf16 [T][d], Wr3 the prepared router weights (lmoe_prepare_router), bias
+ * fp32 [E] or NULL (the skewed workload's popularity bias); then the top-k of
+ * each row (larger logit first, ties by smaller id) into topk_idx[T][k] and
+ * the softmax over those k logits into topk_w[T][k].  logits [T][E] is a
+ * required output. */
+lmoe_status lmoe_route(const uint16_t *x_bf16, const uint16_t *Wr3, const float *bias, const lmoe_dims *dims,
                        float *logits, int32_t *topk_idx, float *topk_w, void *workspace, size_t ws_bytes,
                        void *stream);
 
-/* Scratch bytes lmoe_route needs for these dims (the router weights split
- * into three bf16 parts for the tensor cores, and split-K partial sums). */
+/* Scratch bytes lmoe_route needs for these dims (split-K partial sums). */
 size_t lmoe_route_workspace_size(const lmoe_dims *dims);
 
 /* The top-k + softmax half of lmoe_route on given fp32 logits [T][E]. */
@@ -193,9 +202,10 @@ lmoe_status lmoe_combine(const float *yp, const int32_t *inv, const lmoe_dims *d
 size_t lmoe_workspace_size(const lmoe_dims *dims);
 
 /* route -> permute -> MXFP8 activations -> expert FFN -> combine, all on
- * `stream`.  y bf16 [T][d].  Optional outputs (NULL to skip): topk_idx
- * [T][k], topk_w [T][k], logits [T][E]. */
-lmoe_status lmoe_forward(const uint16_t *x_bf16, const float *Wr, const float *bias, const lmoe_expert_weights *W,
+ * `stream`.  Wr3: prepared router weights (lmoe_prepare_router).  y bf16
+ * [T][d].  Optional outputs (NULL to skip): topk_idx [T][k], topk_w [T][k],
+ * logits [T][E]. */
+lmoe_status lmoe_forward(const uint16_t *x_bf16, const uint16_t *Wr3, const float *bias, const lmoe_expert_weights *W,
                          const lmoe_dims *dims, uint16_t *y_bf16, int32_t *topk_idx, float *topk_w, float *logits,
                          void *workspace, size_t ws_bytes, void *stream);
 
@@ -215,7 +225,7 @@ size_t lmoe_block_workspace_size(const lmoe_dims *dims, int32_t hidden);
  * out = bf16(y W_out^T) [T][hidden].  x_h bf16 [T][hidden], W_in bf16
  * [d][hidden], W_out bf16 [hidden][d]; hidden % 64 == 0.  Optional outputs
  * (NULL to skip): lat and y (bf16 [T][d]), topk_idx, topk_w, logits. */
-lmoe_status lmoe_forward_block(const uint16_t *x_h, const uint16_t *W_in, const float *Wr, const float *bias,
+lmoe_status lmoe_forward_block(const uint16_t *x_h, const uint16_t *W_in, const uint16_t *Wr3, const float *bias,
                                const lmoe_expert_weights *W, const uint16_t *W_out, const lmoe_dims *dims,
                                int32_t hidden, uint16_t *out, uint16_t *lat, uint16_t *y, int32_t *topk_idx,
                                float *topk_w, float *logits, void *workspace, size_t ws_bytes, void *stream);

@@ -154,6 +154,22 @@ def test_permute_flags_out_of_range_ids(cuda_lib):
     assert int(inv[3 * 16 + 5]) == -1 and int(offsets[-1]) == 159
 
 
+def test_prepare_router_planes_sum_to_fp32(cuda_lib):
+    """lmoe_prepare_router: hi = bf16_rne(W), then the two residual planes; the
+    three bf16 planes add up to the fp32 weights exactly (24 significand
+    bits), across a wide exponent range."""
+    lmoe = cuda_lib
+    rng = np.random.default_rng(5)
+    E, d = 40, 192
+    W = (rng.standard_normal((E, d)) * np.exp2(rng.integers(-60, 60, (E, d)))).astype(np.float32)
+    W3 = lmoe.prepare_router(torch.from_numpy(W).to(DEV))
+    torch.cuda.synchronize()
+    planes = bf16_to_f64(from_dev_bf16(W3)).reshape(3, E, d)
+    np.testing.assert_array_equal(planes.sum(0), W.astype(np.float64))
+    hi = torch.from_numpy(W).to(torch.bfloat16).float().numpy().astype(np.float64)  # RNE
+    np.testing.assert_array_equal(planes[0], hi)
+
+
 def test_combine_slot_order_fp32(cuda_lib):
     lmoe = cuda_lib
     rng = np.random.default_rng(12)

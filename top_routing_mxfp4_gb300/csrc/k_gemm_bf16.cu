@@ -341,29 +341,31 @@ int router_kernel_count(int T, int d, int E)
 {
     int NB, KS;
     plan(T, E, d, NB, KS);
-    return KS > 1 ? 4 : 3;  // split, GEMM, (split-K reduction), top-k
+    return KS > 1 ? 3 : 2;  // GEMM, (split-K reduction), top-k
 }
 
 size_t router_scratch_bytes(int T, int d, int E)
 {
     int NB, KS;
     plan(T, E, d, NB, KS);
-    return size_t(round_up(int64_t(3) * E * d * 2, 256)) + (KS > 1 ? size_t(round_up(int64_t(KS) * T * E * 4, 256)) : 0);
+    return KS > 1 ? size_t(round_up(int64_t(KS) * T * E * 4, 256)) : 0;
 }
 
-cudaError_t launch_route(const uint16_t *x, const float *Wr, const float *bias, int T, int d, int E, int k,
+cudaError_t launch_split_router(const float *Wr, int E, int d, uint16_t *Wr3, cudaStream_t st)
+{
+    const int64_t n = int64_t(E) * d;
+    const int64_t blocks = ceil_div(n / 4, 256);
+    return launch_pdl(k_split_bf16x3, dim3(unsigned(blocks < 152 * 16 ? blocks : 152 * 16)), dim3(256), 0, st, Wr, n,
+                      reinterpret_cast<__nv_bfloat16 *>(Wr3));
+}
+
+cudaError_t launch_route(const uint16_t *x, const uint16_t *Wr3, const float *bias, int T, int d, int E, int k,
                          float *logits, int32_t *idx, float *w, void *scratch, int32_t *status, cudaStream_t st)
 {
     if (T == 0) return cudaSuccess;
-    __nv_bfloat16 *w3 = static_cast<__nv_bfloat16 *>(scratch);
-    float *partial = reinterpret_cast<float *>(static_cast<char *>(scratch) + round_up(int64_t(3) * E * d * 2, 256));
-    const int64_t n = int64_t(E) * d;
-    {
-        const cudaError_t le_ = launch_pdl(k_split_bf16x3, dim3(int(ceil_div(n / 4, 256) < 152 * 16 ? ceil_div(n / 4, 256) : 152 * 16)), dim3(256), 0, st, Wr, n, w3);
-        if (le_ != cudaSuccess) return le_;
-    }
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    const __nv_bfloat16 *w3 = reinterpret_cast<const __nv_bfloat16 *>(Wr3);
+    float *partial = static_cast<float *>(scratch);
+    cudaError_t e = cudaSuccess;
     int NB, KS;
     plan(T, E, d, NB, KS);
     CUtensorMap ma, mb;

@@ -143,13 +143,26 @@ size_t lmoe_route_workspace_size(const lmoe_dims *dims)
     return kStatusBytes + router_scratch_bytes(dims->T, dims->d, dims->E);
 }
 
-lmoe_status lmoe_route(const uint16_t *x_bf16, const float *Wr, const float *bias, const lmoe_dims *dims,
+size_t lmoe_router_prepared_bytes(int32_t E, int32_t d)
+{
+    if (E <= 0 || d <= 0 || d % 64 != 0) return 0;
+    return size_t(3) * size_t(E) * size_t(d) * 2;
+}
+
+lmoe_status lmoe_prepare_router(const float *Wr, int32_t E, int32_t d, uint16_t *Wr3, void *stream)
+{
+    if (E <= 0 || d <= 0 || d % 64 != 0 || !Wr || !Wr3 || !aligned(Wr, 16) || !aligned(Wr3, 16))
+        return LMOE_ERR_INVALID_ARG;
+    return cuda_status(launch_split_router(Wr, E, d, Wr3, cudaStream_t(stream)));
+}
+
+lmoe_status lmoe_route(const uint16_t *x_bf16, const uint16_t *Wr3, const float *bias, const lmoe_dims *dims,
                        float *logits, int32_t *topk_idx, float *topk_w, void *workspace, size_t ws_bytes,
                        void *stream)
 {
     if (!dims_ok(dims)) return LMOE_ERR_INVALID_ARG;
     if (dims->T == 0) return LMOE_OK;
-    if (!x_bf16 || !Wr || !logits || !topk_idx || !topk_w || !aligned(x_bf16, 16) || !aligned(Wr, 16))
+    if (!x_bf16 || !Wr3 || !logits || !topk_idx || !topk_w || !aligned(x_bf16, 16) || !aligned(Wr3, 16))
         return LMOE_ERR_INVALID_ARG;
     if (!workspace || ws_bytes < lmoe_route_workspace_size(dims) || !aligned(workspace, 256)) return LMOE_ERR_WORKSPACE;
     cudaStream_t st = cudaStream_t(stream);
@@ -157,7 +170,7 @@ lmoe_status lmoe_route(const uint16_t *x_bf16, const float *Wr, const float *bia
     int32_t *status = reinterpret_cast<int32_t *>(ws);
     cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int32_t), st);
     if (e == cudaSuccess)
-        e = launch_route(x_bf16, Wr, bias, dims->T, dims->d, dims->E, dims->k, logits, topk_idx, topk_w,
+        e = launch_route(x_bf16, Wr3, bias, dims->T, dims->d, dims->E, dims->k, logits, topk_idx, topk_w,
                          ws + kStatusBytes, status, st);
     return cuda_status(e);
 }
@@ -239,7 +252,7 @@ size_t lmoe_workspace_size(const lmoe_dims *dims)
     return fwd_layout(dims).total;
 }
 
-lmoe_status lmoe_forward(const uint16_t *x_bf16, const float *Wr, const float *bias, const lmoe_expert_weights *W,
+lmoe_status lmoe_forward(const uint16_t *x_bf16, const uint16_t *Wr3, const float *bias, const lmoe_expert_weights *W,
                          const lmoe_dims *dims, uint16_t *y_bf16, int32_t *topk_idx, float *topk_w, float *logits,
                          void *workspace, size_t ws_bytes, void *stream)
 {
@@ -247,7 +260,7 @@ lmoe_status lmoe_forward(const uint16_t *x_bf16, const float *Wr, const float *b
     lmoe_status a = act_ok(dims);
     if (a != LMOE_OK) return a;
     if (dims->T == 0) return LMOE_OK;
-    if (!x_bf16 || !Wr || !y_bf16 || !aligned(x_bf16, 16) || !aligned(Wr, 16) || !aligned(y_bf16, 16))
+    if (!x_bf16 || !Wr3 || !y_bf16 || !aligned(x_bf16, 16) || !aligned(Wr3, 16) || !aligned(y_bf16, 16))
         return LMOE_ERR_INVALID_ARG;
     if (!weights_ok(W)) return LMOE_ERR_INVALID_ARG;
     const FwdLayout L = fwd_layout(dims);
@@ -274,7 +287,7 @@ lmoe_status lmoe_forward(const uint16_t *x_bf16, const float *Wr, const float *b
 
     cudaError_t e = mark(0, st);
     if (e == cudaSuccess) e = cudaMemsetAsync(status, 0, sizeof(int32_t), st);
-    if (e == cudaSuccess) e = launch_route(x_bf16, Wr, bias, T, d, E, k, lg, idx, w, ws + L.rscratch, status, st);
+    if (e == cudaSuccess) e = launch_route(x_bf16, Wr3, bias, T, d, E, k, lg, idx, w, ws + L.rscratch, status, st);
     if (e == cudaSuccess) e = mark(1, st);
     if (e == cudaSuccess)
         e = launch_permute(idx, P, E, counts, offsets, perm, inv, ws + L.pscratch, status, st,
@@ -310,7 +323,7 @@ size_t lmoe_block_workspace_size(const lmoe_dims *dims, int32_t hidden)
     return 2 * lat + lmoe_workspace_size(dims);
 }
 
-lmoe_status lmoe_forward_block(const uint16_t *x_h, const uint16_t *W_in, const float *Wr, const float *bias,
+lmoe_status lmoe_forward_block(const uint16_t *x_h, const uint16_t *W_in, const uint16_t *Wr3, const float *bias,
                                const lmoe_expert_weights *W, const uint16_t *W_out, const lmoe_dims *dims,
                                int32_t hidden, uint16_t *out, uint16_t *lat, uint16_t *y, int32_t *topk_idx,
                                float *topk_w, float *logits, void *workspace, size_t ws_bytes, void *stream)
@@ -322,7 +335,7 @@ lmoe_status lmoe_forward_block(const uint16_t *x_h, const uint16_t *W_in, const 
     if (!x_h || !W_in || !W_out || !out || !aligned(x_h, 16) || !aligned(W_in, 16) || !aligned(W_out, 16) ||
         !aligned(out, 16) || (lat && !aligned(lat, 16)) || (y && !aligned(y, 16)))
         return LMOE_ERR_INVALID_ARG;
-    if (!Wr || !aligned(Wr, 16) || !weights_ok(W)) return LMOE_ERR_INVALID_ARG;
+    if (!Wr3 || !aligned(Wr3, 16) || !weights_ok(W)) return LMOE_ERR_INVALID_ARG;
     const size_t need = lmoe_block_workspace_size(dims, hidden);
     if (!workspace || ws_bytes < need || !aligned(workspace, 256)) return LMOE_ERR_WORKSPACE;
     char *ws = static_cast<char *>(workspace);
@@ -333,7 +346,7 @@ lmoe_status lmoe_forward_block(const uint16_t *x_h, const uint16_t *W_in, const 
     cudaStream_t st = cudaStream_t(stream);
     cudaError_t e = launch_linear_bf16(x_h, W_in, dims->T, hidden, dims->d, lat_buf, nullptr, nullptr, st);
     if (e != cudaSuccess) return cuda_status(e);
-    lmoe_status s = lmoe_forward(lat_buf, Wr, bias, W, dims, y_buf, topk_idx, topk_w, logits, fws,
+    lmoe_status s = lmoe_forward(lat_buf, Wr3, bias, W, dims, y_buf, topk_idx, topk_w, logits, fws,
                                  ws_bytes - 2 * latb, stream);
     if (s != LMOE_OK) return s;
     return cuda_status(launch_linear_bf16(y_buf, W_out, dims->T, dims->d, hidden, out, nullptr, nullptr, st));

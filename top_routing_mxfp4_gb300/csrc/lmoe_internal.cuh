@@ -139,7 +139,9 @@ cudaError_t launch_linear_bf16(const uint16_t *x, const uint16_t *W, int T, int 
 // Top-k + softmax of fp32 logits [T][E].
 cudaError_t launch_topk_softmax(const float *logits, int T, int E, int k, int32_t *idx, float *w, cudaStream_t st);
 // Router logits + top-k + softmax (split, GEMM, split-K reduction, selection).
-cudaError_t launch_route(const uint16_t *x, const float *Wr, const float *bias, int T, int d, int E, int k,
+// fp32 router weights [E][d] -> three bf16 planes [3][E][d] whose sum is exact
+cudaError_t launch_split_router(const float *Wr, int E, int d, uint16_t *Wr3, cudaStream_t st);
+cudaError_t launch_route(const uint16_t *x, const uint16_t *Wr3, const float *bias, int T, int d, int E, int k,
                          float *logits, int32_t *idx, float *w, void *scratch, int32_t *status, cudaStream_t st);
 
 // Optional by-products of the permute for the expert GEMMs: per expert the

@@ -63,6 +63,8 @@ _mxfp4_bytes = _sig("lmoe_mxfp4_bytes", _sz, _i64, _i32, _i32, _i32, ctypes.POIN
 _quant_mxfp4 = _sig("lmoe_quant_mxfp4", ctypes.c_int, _vp, _i64, _i32, _i32, _vp, _vp, _i32, _vp)
 _quant_mxfp8 = _sig("lmoe_quant_mxfp8", ctypes.c_int, _vp, _i64, _i32, _vp, _vp, _vp)
 _route = _sig("lmoe_route", ctypes.c_int, _vp, _vp, _vp, _DP, _vp, _vp, _vp, _vp, _sz, _vp)
+_router_bytes = _sig("lmoe_router_prepared_bytes", _sz, _i32, _i32)
+_prepare_router = _sig("lmoe_prepare_router", ctypes.c_int, _vp, _i32, _i32, _vp, _vp)
 _route_ws = _sig("lmoe_route_workspace_size", _sz, _DP)
 _topk = _sig("lmoe_topk_from_logits", ctypes.c_int, _vp, _DP, _vp, _vp, _vp)
 _perm_ws = _sig("lmoe_permute_workspace_size", _sz, _DP)
@@ -225,11 +227,27 @@ class ExpertBank:
 
 # ---- stages ------------------------------------------------------------------------
 
-def route(x, Wr, k: int, bias=None, stream=None):
-    T, d = x.shape
-    E = Wr.shape[0]
-    _need(x, torch.bfloat16, (T, d), "x")
+def prepare_router(Wr, stream=None):
+    """fp32 router weights [E, d] -> the three bf16 planes [3, E, d] the router
+    GEMM reads (their sum is Wr exactly)."""
+    E, d = Wr.shape
     _need(Wr, torch.float32, (E, d), "Wr")
+    if int(_router_bytes(E, d)) == 0:
+        raise ValueError(f"router weights [{E}, {d}]: d must be a multiple of 64")
+    Wr3 = _empty((3, E, d), torch.bfloat16, Wr.device)
+    _check(_prepare_router(_ptr(Wr), E, d, _ptr(Wr3), _stream(stream)), "lmoe_prepare_router")
+    return Wr3
+
+
+def route(x, Wr, k: int, bias=None, stream=None, Wr3=None):
+    """Router + top-k + softmax.  Wr: fp32 [E, d] (prepared on the fly) or
+    Wr3: prepared planes [3, E, d]."""
+    T, d = x.shape
+    if Wr3 is None:
+        Wr3 = prepare_router(Wr, stream)
+    E = Wr3.shape[1]
+    _need(x, torch.bfloat16, (T, d), "x")
+    _need(Wr3, torch.bfloat16, (3, E, d), "Wr3")
     if bias is not None:
         _need(bias, torch.float32, (E,), "bias")
     D = dims(T, d, E, k, 32)
@@ -237,7 +255,7 @@ def route(x, Wr, k: int, bias=None, stream=None):
     idx = _empty((T, k), torch.int32, x.device)
     w = _empty((T, k), torch.float32, x.device)
     ws = workspace(_route_ws(ctypes.byref(D)), x.device)
-    _check(_route(_ptr(x), _ptr(Wr), _ptr(bias), ctypes.byref(D), _ptr(logits), _ptr(idx), _ptr(w), _ptr(ws),
+    _check(_route(_ptr(x), _ptr(Wr3), _ptr(bias), ctypes.byref(D), _ptr(logits), _ptr(idx), _ptr(w), _ptr(ws),
                   ws.numel(), _stream(stream)), "lmoe_route")
     return logits, idx, w
 
@@ -324,10 +342,12 @@ def workspace_size(T: int, d: int, E: int, k: int, I: int) -> int:
 
 
 class Layer:
-    """A LatentMoE layer: router weights, optional logit bias, expert bank."""
+    """A LatentMoE layer: router weights (fp32, prepared once into the form the
+    router GEMM reads), optional logit bias, expert bank."""
 
     def __init__(self, Wr: torch.Tensor, bank: ExpertBank, k: int = 16, bias=None):
         self.Wr, self.bank, self.k, self.bias = Wr, bank, k, bias
+        self.Wr3 = prepare_router(Wr)
         self._ws = None
 
     def workspace(self, T: int) -> torch.Tensor:
@@ -343,7 +363,7 @@ class Layer:
         y = _empty((T, d), torch.bfloat16, x.device) if y is None else y
         ws = self.workspace(T)
         W = self.bank.struct()
-        _check(_forward(_ptr(x), _ptr(self.Wr), _ptr(self.bias), ctypes.byref(W), ctypes.byref(D), _ptr(y),
+        _check(_forward(_ptr(x), _ptr(self.Wr3), _ptr(self.bias), ctypes.byref(W), ctypes.byref(D), _ptr(y),
                         _ptr(topk_idx), _ptr(topk_w), _ptr(logits), _ptr(ws), ws.numel(), _stream(stream)),
                "lmoe_forward")
         return y
@@ -382,7 +402,7 @@ class Block:
             self._ws = workspace(need, x_h.device)
         out = _empty((T, hidden), torch.bfloat16, x_h.device) if out is None else out
         W = bank.struct()
-        _check(_forward_block(_ptr(x_h), _ptr(self.W_in), _ptr(self.layer.Wr), _ptr(self.layer.bias), ctypes.byref(W),
+        _check(_forward_block(_ptr(x_h), _ptr(self.W_in), _ptr(self.layer.Wr3), _ptr(self.layer.bias), ctypes.byref(W),
                               _ptr(self.W_out), ctypes.byref(D), hidden, _ptr(out), _ptr(lat), _ptr(y), _ptr(topk_idx),
                               _ptr(topk_w), _ptr(logits), _ptr(self._ws), self._ws.numel(), _stream(stream)),
                "lmoe_forward_block")
