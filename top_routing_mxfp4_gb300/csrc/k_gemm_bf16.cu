@@ -248,19 +248,6 @@ __global__ void k_split_bf16x3(const float *__restrict__ w, int64_t n, __nv_bflo
     }
 }
 
-// logits[t][m] = sum_{s < KS} part[s][t][m] (+ bias[m]), slices in fixed order.
-__global__ void k_splitk_reduce(const float *__restrict__ part, int KS, int64_t TM, int M, const float *__restrict__ bias,
-                                float *__restrict__ out)
-{
-    pdl_enter();
-    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < TM; i += int64_t(gridDim.x) * blockDim.x) {
-        float acc = 0.f;
-#pragma unroll 8
-        for (int s = 0; s < KS; ++s) acc += __ldg(part + int64_t(s) * TM + i);
-        out[i] = bias ? acc + __ldg(bias + i % M) : acc;
-    }
-}
-
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -341,7 +328,7 @@ int router_kernel_count(int T, int d, int E)
 {
     int NB, KS;
     plan(T, E, d, NB, KS);
-    return KS > 1 ? 3 : 2;  // GEMM, (split-K reduction), top-k
+    return 2;  // GEMM, top-k (with the split-K reduction when K is split)
 }
 
 size_t router_scratch_bytes(int T, int d, int E)
@@ -382,14 +369,7 @@ cudaError_t launch_route(const uint16_t *x, const uint16_t *Wr3, const float *bi
     a.bias = nullptr;
     e = dispatch<3, OUT_PARTIAL>(NB, ma, mb, a, st);
     if (e != cudaSuccess) return e;
-    const int64_t TM = int64_t(T) * E;
-    {
-        const cudaError_t le_ = launch_pdl(k_splitk_reduce, dim3(int(ceil_div(TM, 256) < 152 * 8 ? ceil_div(TM, 256) : 152 * 8)), dim3(256), 0, st, partial, KS, TM, E, bias, logits);
-        if (le_ != cudaSuccess) return le_;
-    }
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    return launch_topk_softmax(logits, T, E, k, idx, w, st);
+    return launch_reduce_topk(partial, KS, T, E, bias, logits, k, idx, w, st);
 }
 
 size_t linear_scratch_bytes(int T, int K, int N)

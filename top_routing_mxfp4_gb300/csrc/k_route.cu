@@ -100,7 +100,43 @@ __global__ void __launch_bounds__(256) k_topk_softmax(const float *__restrict__ 
     select_topk<NV>(logits + int64_t(t) * E, E, k, idx + int64_t(t) * k, w + int64_t(t) * k);
 }
 
+// Split-K partial logits summed in slice order (then + bias), written to
+// `logits` and kept in shared memory, where warp 0 selects the top-k: one CTA
+// per token (one thread per expert), one launch instead of a reduction pass
+// and a selection pass.
+template <int NV>
+__global__ void __launch_bounds__(1024) k_reduce_topk(const float *__restrict__ part, int KS, int T, int E,
+                                                     const float *__restrict__ bias, float *__restrict__ logits, int k,
+                                                     int32_t *__restrict__ idx, float *__restrict__ w)
+{
+    pdl_enter();
+    extern __shared__ float row[];  // [E]
+    const int t = blockIdx.x;
+    const int64_t TM = int64_t(T) * E, base = int64_t(t) * E;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        float acc = 0.f;
+#pragma unroll 8
+        for (int s = 0; s < KS; ++s) acc += __ldcg(part + int64_t(s) * TM + base + e);
+        const float v = bias ? acc + __ldg(bias + e) : acc;
+        row[e] = v;
+        logits[base + e] = v;
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) select_topk<NV>(row, E, k, idx + int64_t(t) * k, w + int64_t(t) * k);
+}
+
 }  // namespace
+
+cudaError_t launch_reduce_topk(const float *part, int KS, int T, int E, const float *bias, float *logits, int k,
+                               int32_t *idx, float *w, cudaStream_t st)
+{
+    if (T == 0) return cudaSuccess;
+    const size_t smem = size_t(E) * sizeof(float);  // E <= 2048: within the default 48 KB
+    const dim3 block(unsigned(E < 1024 ? round_up(E, 32) : 1024));  // one thread per expert: KS loads each
+    if (E <= 256) return launch_pdl(k_reduce_topk<8>, dim3(T), block, smem, st, part, KS, T, E, bias, logits, k, idx, w);
+    if (E <= 896) return launch_pdl(k_reduce_topk<28>, dim3(T), block, smem, st, part, KS, T, E, bias, logits, k, idx, w);
+    return launch_pdl(k_reduce_topk<64>, dim3(T), block, smem, st, part, KS, T, E, bias, logits, k, idx, w);
+}
 
 cudaError_t launch_topk_softmax(const float *logits, int T, int E, int k, int32_t *idx, float *w, cudaStream_t st)
 {

@@ -138,6 +138,9 @@ cudaError_t launch_linear_bf16(const uint16_t *x, const uint16_t *W, int T, int 
                                int32_t *status, cudaStream_t st);
 // Top-k + softmax of fp32 logits [T][E].
 cudaError_t launch_topk_softmax(const float *logits, int T, int E, int k, int32_t *idx, float *w, cudaStream_t st);
+// split-K partial logits [KS][T][E] -> logits (+ bias) and their top-k + softmax, one launch
+cudaError_t launch_reduce_topk(const float *part, int KS, int T, int E, const float *bias, float *logits, int k,
+                               int32_t *idx, float *w, cudaStream_t st);
 // Router logits + top-k + softmax (split, GEMM, split-K reduction, selection).
 // fp32 router weights [E][d] -> three bf16 planes [3][E][d] whose sum is exact
 cudaError_t launch_split_router(const float *Wr, int E, int d, uint16_t *Wr3, cudaStream_t st);
