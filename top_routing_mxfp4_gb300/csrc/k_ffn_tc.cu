@@ -73,6 +73,22 @@ __device__ uint32_t g_lmoe_trace_n;
         }                                                                                                   \
     } while (0)
 __shared__ uint32_t s_trace[2 * 3 * TRACE_PER_ROLE];
+// Every CTA's start and end (%globaltimer, ns) per GEMM mode: [mode][cta][2].
+__device__ unsigned long long g_lmoe_cta_ns[2][1024][2];
+__device__ __forceinline__ unsigned long long lmoe_globaltimer()
+{
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+#define LMOE_TRACE_CTA(mode, which) \
+    do {                            \
+        if (threadIdx.x == 0 && blockIdx.x < 1024) g_lmoe_cta_ns[mode][blockIdx.x][which] = lmoe_globaltimer(); \
+    } while (0)
+extern "C" int lmoe_debug_cta_times(unsigned long long *host)
+{
+    return cudaMemcpyFromSymbol(host, g_lmoe_cta_ns, sizeof(g_lmoe_cta_ns)) == cudaSuccess ? 0 : -1;
+}
 extern "C" int lmoe_debug_trace(uint32_t *host, int max_events)
 {
     uint32_t n = 0;
@@ -92,12 +108,23 @@ extern "C" int lmoe_debug_trace(uint32_t *host, int max_events)
 #define LMOE_TRACE_END(role) \
     do {                     \
     } while (0)
+#define LMOE_TRACE_CTA(mode, which) \
+    do {                            \
+    } while (0)
 #endif
 
 namespace lmoe {
 namespace {
 
 using namespace tc;
+
+// Four consecutive fp32 adds to global memory as one vector reduction that
+// returns nothing (the issuing thread never waits for it); 16-byte aligned.
+__device__ __forceinline__ void red_add_v4(float *dst, float4 v)
+{
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
+                 : "memory");
+}
 
 enum { GATEUP = 0, DOWN = 1 };
 
@@ -204,6 +231,7 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
     int32_t *s_off = s_tiles + (p.E + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    LMOE_TRACE_CTA(MODE, 0);
     // the schedule is an output of an earlier kernel than the previous one
     // (complete before this grid starts); read through L2
     for (int i = threadIdx.x; i <= p.E; i += blockDim.x) {
@@ -344,39 +372,29 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
         LMOE_TRACE_DECL
         int acc = 0;
         uint32_t acc_phase = 0;
-        // the next item and its gate weights are fetched one item ahead, so
-        // their load latency overlaps the current item's accumulator wait
-        Item nx{};
-        float wn[(NT + 31) / 32];
-        int tn[(NT + 31) / 32];  // token of each column (fused combine)
-        auto fetch = [&](int it2) {
+        // The gate weights and tokens of an item are loaded two items ahead
+        // (their latency under the output traffic is several microseconds),
+        // into two register sets used alternately, so no register waits on an
+        // outstanding load before its item comes up.
+        constexpr int NV = (NT + 31) / 32;
+        auto fetch = [&](int it2, Item &nx, float (&wn)[NV], int (&tn)[NV]) {
             nx = decode_item(it2, s_tiles, s_off, p.E, p.MT, NT);
             if (MODE == DOWN) {
                 const int qb = s_off[nx.e] + nx.n_tile * NT;
 #pragma unroll
-                for (int i = 0; i < (NT + 31) / 32; ++i) {
+                for (int i = 0; i < NV; ++i) {
                     const bool v = 32 * i + lane < nx.n_valid;
                     wn[i] = v ? __ldg(p.w_sorted + qb + 32 * i + lane) : 0.f;
                     tn[i] = (v && p.yacc) ? __ldg(p.perm + qb + 32 * i + lane) / p.k : 0;
                 }
             }
         };
-        if (int(blockIdx.x) < total) fetch(blockIdx.x);
-        for (int it = blockIdx.x; it < total; it += gridDim.x) {
-            const Item w = nx;
-            float wl[(NT + 31) / 32];
-            int tl[(NT + 31) / 32];
-#pragma unroll
-            for (int i = 0; i < (NT + 31) / 32; ++i) {
-                wl[i] = wn[i];
-                tl[i] = tn[i];
-            }
-            if (it + int(gridDim.x) < total) fetch(it + gridDim.x);
+        auto process = [&](int it, const Item &w, const float (&wl)[NV], const int (&tl)[NV]) -> bool {
             [[maybe_unused]] const int qbase = s_off[w.e] + w.n_tile * NT;  // first permuted row of the tile (down)
             if (threadIdx.x == 64) LMOE_TRACE_EV(2, 0x40 | MODE, it, 0);  // epilogue: waiting
             if (!mbar_wait(&acc_full[acc], acc_phase)) {
                 set_status(p.status, LMOE_ERR_TIMEOUT);
-                break;
+                return false;
             }
             tc_fence_after();
             if (threadIdx.x == 64) LMOE_TRACE_EV(2, 0x50 | MODE, it, 0);  // epilogue: accumulator ready
@@ -470,7 +488,7 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
                                 a.z *= wc;
                                 a.w *= wc;
                                 if (p.yacc)
-                                    atomicAdd(reinterpret_cast<float4 *>(p.yacc + int64_t(tc) * p.Mtot + col), a);
+                                    red_add_v4(p.yacc + int64_t(tc) * p.Mtot + col, a);
                                 else
                                     *reinterpret_cast<float4 *>(p.yp + int64_t(qbase + c0 + c) * p.Mtot + col) = a;
                             }
@@ -493,12 +511,27 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
                 acc = 0;
                 acc_phase ^= 1;
             }
+            return true;
+        };
+        Item nA{}, nB{};
+        float wA[NV], wB[NV];
+        int tA[NV], tB[NV];
+        const int G = int(gridDim.x);
+        if (int(blockIdx.x) < total) fetch(blockIdx.x, nA, wA, tA);
+        if (int(blockIdx.x) + G < total) fetch(blockIdx.x + G, nB, wB, tB);
+        for (int it = blockIdx.x; it < total; it += 2 * G) {
+            if (!process(it, nA, wA, tA)) break;
+            if (it + 2 * G < total) fetch(it + 2 * G, nA, wA, tA);
+            if (it + G >= total) break;
+            if (!process(it + G, nB, wB, tB)) break;
+            if (it + 3 * G < total) fetch(it + 3 * G, nB, wB, tB);
         }
         if (threadIdx.x == 64) LMOE_TRACE_END(2);
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    LMOE_TRACE_CTA(MODE, 1);
     if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
