@@ -148,10 +148,10 @@ struct GemmArgs {
 template <int MODE, int NT>
 struct Cfg {
     // Weight tiles per stage: gate and up rows of the same 128 features; for
-    // down, two consecutive 128-row tiles when token tiles are small (more
-    // bytes per pipeline stage), one tile when they are large (so the
-    // accumulators can be double-buffered in TMEM).
-    static constexpr int MATS = (MODE == GATEUP || NT <= 32) ? 2 : 1;
+    // down, two consecutive 128-row tiles sharing the stage's token tile (more
+    // weight bytes per stage, half the h traffic) up to 96-token tiles, one
+    // tile beyond (so the accumulators still fit twice in TMEM).
+    static constexpr int MATS = (MODE == GATEUP || NT <= 96) ? 2 : 1;
     static constexpr int SLOT = (NT + 127) / 128 * 128;
     static constexpr int NAT = (NT + 127) / 128;  // B scale atoms per stage
     static constexpr uint32_t A_TILE = 128 * 128;  // smem bytes of one expanded FP4 A tile
@@ -165,11 +165,15 @@ struct Cfg {
     // One thread issues a tcgen05 instruction only every few dozen cycles, so
     // two issuers keep small-N MMAs from pacing the pipeline.
     static constexpr int ACC_COLS_ITEM = MATS * NT;
-    static constexpr int ACC_STAGES = (ACC_COLS_ITEM <= 64) ? 4 : (2 * ACC_COLS_ITEM <= 256 ? 2 : 1);
-    static constexpr int ACC_COLS = ACC_STAGES * ACC_COLS_ITEM;
-    static constexpr int SF_BASE = (ACC_COLS + 31) / 32 * 32;
     static constexpr int SF_COLS_ISSUER = 4 + 4 * NAT;  // this issuer's SFA and SFB copies
     static constexpr int SF_COLS = MATS * SF_COLS_ISSUER;
+    // accumulator stages: double-buffered (the epilogue of one item overlaps
+    // the next item's MMAs) whenever two items and 4 stages of scale factors
+    // fit the 512 TMEM columns
+    static constexpr int ACC_STAGES =
+        (ACC_COLS_ITEM <= 64) ? 4 : (2 * ACC_COLS_ITEM + 4 * SF_COLS <= 512 ? 2 : 1);
+    static constexpr int ACC_COLS = ACC_STAGES * ACC_COLS_ITEM;
+    static constexpr int SF_BASE = (ACC_COLS + 31) / 32 * 32;
     static constexpr int MAX_STAGES = (512 - SF_BASE) / SF_COLS < 16 ? (512 - SF_BASE) / SF_COLS : 16;
     static_assert(MAX_STAGES >= 2, "TMEM columns");
     // Epilogue.  Large token tiles: 8 warps (two per TMEM lane quarter, on
@@ -757,12 +761,12 @@ cudaError_t launch_gemm(const CUtensorMap &a0, const CUtensorMap &a1, const CUte
 }  // namespace
 
 // 128-row weight tiles per down-GEMM item (Cfg<DOWN, NT>::MATS).
-static int down_tiles_per_item(int NT) { return NT <= 32 ? 2 : 1; }
+static int down_tiles_per_item(int NT) { return NT <= 96 ? 2 : 1; }
 
 FfnLayout ffn_layout(int64_t P, int d, int E, int I)
 {
     FfnLayout L{};
-    L.NT = P <= 4 * int64_t(E) ? 16 : (P <= 16 * int64_t(E) ? 32 : 128);
+    L.NT = P <= 4 * int64_t(E) ? 16 : (P <= 16 * int64_t(E) ? 32 : 96);
     L.fused = L.NT >= 64;  // Cfg<DOWN, NT>::STAGED
     L.SLOT = int(round_up(L.NT, 128));
     const int64_t touched = P < E ? P : E;
@@ -883,7 +887,7 @@ cudaError_t launch_expert_gemms(const FfnArgs &a, const FfnLayout &L, char *scra
     g.Ih = a.I;
     cudaError_t e = L.NT == 16   ? launch_gemm<GATEUP, 16>(mg, mu, mx, g, st)
                     : L.NT == 32 ? launch_gemm<GATEUP, 32>(mg, mu, mx, g, st)
-                                 : launch_gemm<GATEUP, 128>(mg, mu, mx, g, st);
+                                 : launch_gemm<GATEUP, 96>(mg, mu, mx, g, st);
     if (e != cudaSuccess) return e;
     if (mid) {
         e = cudaEventRecord(mid, st);
@@ -904,7 +908,7 @@ cudaError_t launch_expert_gemms(const FfnArgs &a, const FfnLayout &L, char *scra
     g.KC = Ip / 128;
     return L.NT == 16   ? launch_gemm<DOWN, 16>(md, md, mh, g, st)
            : L.NT == 32 ? launch_gemm<DOWN, 32>(md, md, mh, g, st)
-                        : launch_gemm<DOWN, 128>(md, md, mh, g, st);
+                        : launch_gemm<DOWN, 96>(md, md, mh, g, st);
 }
 
 }  // namespace lmoe
