@@ -119,10 +119,12 @@ namespace {
 using namespace tc;
 
 // Four consecutive fp32 adds to global memory as one vector reduction that
-// returns nothing (the issuing thread never waits for it); 16-byte aligned.
-__device__ __forceinline__ void red_add_v4(float *dst, float4 v)
+// returns nothing (the issuing thread never waits for it); 16-byte aligned;
+// `policy` is the L2 cache policy of the line.
+__device__ __forceinline__ void red_add_v4(float *dst, float4 v, uint64_t policy)
 {
-    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
+    asm volatile("red.global.add.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(dst), "f"(v.x), "f"(v.y),
+                 "f"(v.z), "f"(v.w), "l"(policy)
                  : "memory");
 }
 
@@ -372,6 +374,9 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
         // ---------------- epilogue (warps 2 .. 1 + EPI_WARPS) ----------------
         const int q = warp & 3;             // TMEM lane quarter of this warp
         const int half = (warp - 2) >> 2;   // which of the quarter's NW warps
+        // the fused combine's per-token fp32 rows take every pair's reduction:
+        // keep them in L2 in preference to the streamed weights
+        [[maybe_unused]] const uint64_t keep_policy = l2_policy_evict_last();
         [[maybe_unused]] uint8_t *stg = epi_stage + (warp - 2) * C::EPI_WARP_BYTES;
         LMOE_TRACE_DECL
         int acc = 0;
@@ -492,7 +497,7 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
                                 a.z *= wc;
                                 a.w *= wc;
                                 if (p.yacc)
-                                    red_add_v4(p.yacc + int64_t(tc) * p.Mtot + col, a);
+                                    red_add_v4(p.yacc + int64_t(tc) * p.Mtot + col, a, keep_policy);
                                 else
                                     *reinterpret_cast<float4 *>(p.yp + int64_t(qbase + c0 + c) * p.Mtot + col) = a;
                             }
