@@ -643,6 +643,15 @@ __global__ void k_quant_scatter_pad(const uint16_t *__restrict__ x, int64_t nblo
         uint32_t c[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) c[i] = e4m3x4(v[4 * i] * iv, v[4 * i + 1] * iv, v[4 * i + 2] * iv, v[4 * i + 3] * iv);
+        // the 4 scale bytes of blocks 4c .. 4c+3 (adjacent in the atom) go out as
+        // one 32-bit store by the group's first lane: groups of 4 consecutive
+        // blocks are aligned (d / 32 and every thread's start are multiples of
+        // 4), so a group is either wholly active or wholly inactive
+        const unsigned mask = __activemask();
+        uint32_t sb4 = sb;
+        sb4 |= __shfl_down_sync(mask, sb, 1) << 8;
+        sb4 |= __shfl_down_sync(mask, sb, 2) << 16;
+        sb4 |= __shfl_down_sync(mask, sb, 3) << 24;
 #pragma unroll 4
         for (int j = 0; j < k; ++j) {
             if (b == 0) w_sorted[__ldg(inv + t * k + j)] = __ldg(topk_w + t * k + j);
@@ -650,7 +659,7 @@ __global__ void k_quant_scatter_pad(const uint16_t *__restrict__ x, int64_t nblo
             uint4 *dst = reinterpret_cast<uint4 *>(xq + R * d + b * 32);
             dst[0] = make_uint4(c[0], c[1], c[2], c[3]);
             dst[1] = make_uint4(c[4], c[5], c[6], c[7]);
-            xs[atom_off(R, b, KC)] = uint8_t(sb);
+            if ((b & 3) == 0) *reinterpret_cast<uint32_t *>(xs + atom_off(R, b, KC)) = sb4;
         }
     }
 }
