@@ -198,20 +198,45 @@ struct Item {
     int e, n_tile, m_tile, n_valid;
 };
 
+// Work item `it` -> (expert, token tile, weight tile).  s_tiles[e] counts the
+// items before expert e (token tiles before e times MT).  Items run in
+// (expert, token tile, weight tile) order, weight tile fastest, so the
+// weight-tile items of one token tile run together and share its activation
+// rows in L2.  Down with large token tiles (the fused combine): the weight
+// tiles are split into two bands (the first and second half of the output
+// columns) and all items of the first band come first, so that only half of
+// the per-token fp32 rows is being written at a time (less of them evicted
+// to DRAM); each weight tile is still read once.
+template <int MODE, int NT>
 __device__ __forceinline__ Item decode_item(int it, const int32_t *s_tiles, const int32_t *s_off, int E, int MT, int nt)
 {
-    int lo = 0, hi = E;  // s_tiles[lo] <= it < s_tiles[hi]
+    int key = it, m0 = 0, mt = MT;  // band of weight tiles [m0, m0 + mt)
+    if (MODE == DOWN && NT >= 64) {
+        const int TT = s_tiles[E] / MT;  // token tiles
+        const int MT0 = (MT + 1) / 2;    // weight tiles of the first band
+        const int first = TT * MT0;      // items of the first band
+        if (it >= first) {
+            m0 = MT0;
+            mt = MT - MT0;
+            it -= first;
+        } else {
+            mt = MT0;
+        }
+        const int r = it / mt;           // token tile
+        key = r * MT + (it - r * mt);    // as if in the one-band order, weight tile m0 + (it - r mt)
+    }
+    int lo = 0, hi = E;  // s_tiles[lo] <= key < s_tiles[hi]
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
-        if (s_tiles[mid] <= it) lo = mid;
+        if (s_tiles[mid] <= key) lo = mid;
         else hi = mid;
     }
     // skip experts with no items (equal starts)
     Item r;
     r.e = lo;
-    const int local = it - s_tiles[lo];
+    const int local = key - s_tiles[lo];
     r.n_tile = local / MT;
-    r.m_tile = local - r.n_tile * MT;
+    r.m_tile = m0 + (local - r.n_tile * MT);
     const int n_e = s_off[lo + 1] - s_off[lo];
     r.n_valid = min(nt, n_e - r.n_tile * nt);
     return r;
@@ -280,7 +305,7 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
             uint32_t phase = 0;
             bool ok = true;
             for (int it = blockIdx.x; it < total && ok; it += gridDim.x) {
-                const Item w = decode_item(it, s_tiles, s_off, p.E, p.MT, NT);
+                const Item w = decode_item<MODE, NT>(it, s_tiles, s_off, p.E, p.MT, NT);
                 const int R = slot_row(w.e) + w.n_tile * C::SLOT;
                 // gate/up: tile m of both matrices; down: tiles 2m and 2m+1 (an odd
                 // last tile loads tile 2m twice and the epilogue drops the copy)
@@ -325,7 +350,7 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
             for (int it = blockIdx.x; it < total && ok; it += gridDim.x) {
-                const Item w = decode_item(it, s_tiles, s_off, p.E, p.MT, NT);
+                const Item w = decode_item<MODE, NT>(it, s_tiles, s_off, p.E, p.MT, NT);
                 const uint32_t N = uint32_t((w.n_valid + 15) & ~15);
                 if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1)) {
                     set_status(p.status, LMOE_ERR_TIMEOUT);
@@ -387,7 +412,7 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
         // outstanding load before its item comes up.
         constexpr int NV = (NT + 31) / 32;
         auto fetch = [&](int it2, Item &nx, float (&wn)[NV], int (&tn)[NV]) {
-            nx = decode_item(it2, s_tiles, s_off, p.E, p.MT, NT);
+            nx = decode_item<MODE, NT>(it2, s_tiles, s_off, p.E, p.MT, NT);
             if (MODE == DOWN) {
                 const int qb = s_off[nx.e] + nx.n_tile * NT;
 #pragma unroll
