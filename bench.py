@@ -224,10 +224,27 @@ def run_ours(args, ws, rank, local):
     st = torch.cuda.current_stream()
     idx = torch.empty((T, wl.k), dtype=torch.int32, device=dev)
     y = torch.empty((T, wl.d), dtype=torch.bfloat16, device=dev)
+    if wl.hidden:
+        # the block: bf16 hidden -> latent projection, the layer, latent -> hidden
+        def dev_bf16(a):
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+        blk = lmoe.Block(dev_bf16(gen.proj_in_bf16(wl)), layer, dev_bf16(gen.proj_out_bf16(wl)))
+        x = gen.hidden_bf16(wl)
+        xin = dev_bf16(x)
+        out = torch.empty((T, wl.hidden), dtype=torch.bfloat16, device=dev)
+
+        def fwd(xi):
+            blk.forward(xi, out=out, topk_idx=idx)
+    else:
+        xin, out = xd, y
+
+        def fwd(xi):
+            layer.forward(xi, y=y, topk_idx=idx)
     for _ in range(max(3, args.warmup)):
-        layer.forward(xd, y=y, topk_idx=idx)
+        fwd(xin)
     torch.cuda.synchronize()
-    assert layer.device_status() == 0
+    if not wl.hidden:
+        assert layer.device_status() == 0
     counts = torch.bincount(idx.view(-1).long(), minlength=wl.E)
     touched = int((counts > 0).sum())
 
@@ -248,7 +265,7 @@ def run_ours(args, ws, rank, local):
     torch.cuda.synchronize()
     t_start.record(st)
     for i in range(K):
-        layer.forward(xd, y=y, topk_idx=idx)
+        fwd(xin)
     t_end.record(st)
     torch.cuda.synchronize()
     barrier(ws)
@@ -263,7 +280,7 @@ def run_ours(args, ws, rank, local):
     torch.cuda.synchronize()
     for i in range(K2):
         lmoe.set_stage_events(evs[i])
-        layer.forward(xd, y=y, topk_idx=idx)
+        fwd(xin)
     torch.cuda.synchronize()
     lmoe.set_stage_events(None)
     clocks = sampler.stop()
@@ -272,22 +289,22 @@ def run_ours(args, ws, rank, local):
     ms_per_step = elapsed_ms / K
     value = whole_job_rate(T, ws, ms_per_step)
 
-    # end to end through host buffers: H2D of x from pinned memory, forward, D2H of y
+    # end to end through host buffers: H2D of the input from pinned memory, forward, D2H of the output
     xh = torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16).pin_memory()
-    yh = torch.empty((T, wl.d), dtype=torch.bfloat16).pin_memory()
-    xdev = torch.empty_like(xd)
+    yh = torch.empty(tuple(out.shape), dtype=torch.bfloat16).pin_memory()
+    xdev = torch.empty_like(xin)
     for _ in range(3):
         xdev.copy_(xh, non_blocking=True)
-        layer.forward(xdev, y=y)
-        yh.copy_(y, non_blocking=True)
+        fwd(xdev)
+        yh.copy_(out, non_blocking=True)
     torch.cuda.synchronize()
     barrier(ws)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(st)
     for _ in range(K):
         xdev.copy_(xh, non_blocking=True)
-        layer.forward(xdev, y=y)
-        yh.copy_(y, non_blocking=True)
+        fwd(xdev)
+        yh.copy_(out, non_blocking=True)
     e1.record(st)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), ws, dev)
@@ -298,7 +315,7 @@ def run_ours(args, ws, rank, local):
     gateup_bytes = touched * 2 * wl.I * wl.d * MXFP4_B  # weights the gate/up GEMM must stream once
     t_gu = stage_ms["gate_up"] / 1e3
     layer_weight_gbs = touched * per_expert_w / (ms_per_step / 1e3) / 1e9
-    launches_per_step = lmoe.forward_kernel_count(T, wl.d, wl.E, wl.k, wl.I)
+    launches_per_step = lmoe.forward_kernel_count(T, wl.d, wl.E, wl.k, wl.I) + (2 if wl.hidden else 0)
     P = T * wl.k
     if P >= 16 * wl.E:
         # prefill-shaped: the expert GEMMs are compute-bound; the block-scaled
@@ -306,13 +323,18 @@ def run_ours(args, ws, rank, local):
         fp8_peak = 2.0 * peaks["bf16_tflops"]
         gu_flops = 2.0 * 2 * P * wl.d * wl.I            # gate + up GEMMs
         expert_flops = 2.0 * 3 * P * wl.d * wl.I        # gate + up + down
+        proj_flops = 2.0 * 2 * T * wl.d * wl.hidden     # block: the two bf16 projections
+        ideal_s = expert_flops / (fp8_peak * 1e12) + proj_flops / (peaks["bf16_tflops"] * 1e12)
         roofline = {"bound": "tensor", "kernel": "gate/up expert GEMM", "achieved": gu_flops / t_gu / 1e12,
                     "peak": fp8_peak, "unit": "TFLOP/s", "frac": gu_flops / t_gu / 1e12 / fp8_peak,
                     "traffic": profiled_traffic(wl.name), "traffic_unit": "bytes per launch (ncu)",
                     "algorithmic_flops": gu_flops,
                     "peak_source": f"{peaks['source']} bf16 burst x 2 (nominal fp8 / bf16 ratio)",
-                    "layer_tflops": expert_flops / (ms_per_step / 1e3) / 1e12,
-                    "layer_frac": expert_flops / (ms_per_step / 1e3) / 1e12 / fp8_peak}
+                    "layer_tflops": (expert_flops + proj_flops) / (ms_per_step / 1e3) / 1e12,
+                    "layer_frac": ideal_s / (ms_per_step / 1e3),
+                    "layer_frac_note": "expert FLOPs at the FP8-rate peak"
+                                       + (" + projection FLOPs at the bf16 peak" if wl.hidden else "")
+                                       + ", as ideal time / measured step"}
     else:
         achieved = gateup_bytes / t_gu / 1e9
         roofline = {"bound": "hbm", "kernel": "gate/up expert GEMM", "achieved": achieved,
@@ -324,14 +346,15 @@ def run_ours(args, ws, rank, local):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "mxfp4 x mxfp8 -> f32 acc", "data": "synthetic (seeded counter-based generator)",
-        "config": {"workload": wl.name, "T": T, "d": wl.d, "E": wl.E, "k": wl.k, "I": wl.I,
+        "config": {"workload": wl.name, "T": T, "d": wl.d, "E": wl.E, "k": wl.k, "I": wl.I, "hidden": wl.hidden,
                    "per_gpu_batch_tokens": T, "parallelism": f"replicas x{ws}",
                    "l2": f"inputs larger than L2: {touched} touched experts = {touched * per_expert_w / 1e9:.2f} GB "
                          f"of weights read per step (L2 129 MB)"},
         "roofline": roofline,
         "stage_ms": stage_ms,
-        "stage_ms_note": f"second live pass of {K2} steps with CUDA events at the stage boundaries (the events "
-                         "serialise the launches, so the stages add up to more than ms_per_step)",
+        "stage_ms_note": f"second live pass of {K2} steps with CUDA events at the layer's stage boundaries (the "
+                         "events serialise the launches, so the stages add up to more than the layer's share of "
+                         "ms_per_step)" + ("; the block's two projections are not in these stages" if wl.hidden else ""),
         "touched_experts": touched,
         "e2e": {"value": whole_job_rate(T, ws, e2e_ms / K), "unit": UNIT, "h2d_bytes_per_step": xh.numel() * 2,
                 "d2h_bytes_per_step": yh.numel() * 2},
