@@ -10,12 +10,6 @@
 namespace lmoe {
 namespace {
 
-// (value, id) ordering of the selection: larger value first, then smaller id.
-__device__ __forceinline__ bool better(float va, int ia, float vb, int ib)
-{
-    return va > vb || (va == vb && ia < ib);
-}
-
 // Best (value, slot) of a lane's NV values by a pairwise tournament: depth
 // log2(NV) instead of an NV-long dependent chain.  Equal values keep the
 // smaller slot, i.e. the smaller expert id (id = lane + 32 * slot).
@@ -43,8 +37,24 @@ __device__ __forceinline__ void lane_best(const float *v, float &bv, int &bs)
     bs = ts[0];
 }
 
+// Order-preserving 32-bit key of a float: larger value, larger key; -0 and +0
+// share one key (they compare equal).
+__device__ __forceinline__ uint32_t order_key(float v)
+{
+    uint32_t b = __float_as_uint(v);
+    if (b == 0x80000000u) b = 0;
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(uint32_t k)
+{
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
 // One warp per token.  Lane l holds experts l, l+32, ... (NV values); a taken
-// or absent expert holds -inf.
+// or absent expert holds -inf.  Each round: every lane's best (value, slot),
+// then the warp's largest value (redux max over the keys) and, among the lanes
+// holding it, the smallest expert id (redux min) -- the (value desc, id asc)
+// order.
 // The selection of one token by one warp from its logits row `row` (any
 // memory space): slots j = 0..k-1 of idx / w.
 template <int NV>
@@ -63,21 +73,20 @@ __device__ __forceinline__ void select_topk(const float *row, int E, int k, int3
         float bv;
         int bs;
         lane_best<NV>(v, bv, bs);
-        int bi = bv == -INFINITY ? INT32_MAX : lane + 32 * bs;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
-            const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
-            if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
-        }
+        const uint32_t key = order_key(bv);
+        uint32_t kmax, bi;
+        asm volatile("redux.sync.max.u32 %0, %1, 0xffffffff;" : "=r"(kmax) : "r"(key));
+        const uint32_t cand = (key == kmax && bv != -INFINITY) ? uint32_t(lane + 32 * bs) : 0xFFFFFFFFu;
+        asm volatile("redux.sync.min.u32 %0, %1, 0xffffffff;" : "=r"(bi) : "r"(cand));
+        const float wv = key_value(kmax);
         // the owner marks the winner taken
-        if ((bi & 31) == lane) {
-            const int slot = bi >> 5;
+        if (int(bi & 31) == lane) {
+            const int slot = int(bi >> 5);
 #pragma unroll
             for (int i = 0; i < NV; ++i) v[i] = (i == slot) ? -INFINITY : v[i];
         }
-        if (j == 0) top_v = bv;
-        if (lane == j) { sel_v = bv; sel_id = bi; }
+        if (j == 0) top_v = wv;
+        if (lane == j) { sel_v = wv; sel_id = int(bi); }
     }
     const float ex = lane < k ? expf(sel_v - top_v) : 0.f;
     float sum = ex;
