@@ -649,6 +649,11 @@ __global__ void k_quant_scatter_pad(const uint16_t *__restrict__ x, int64_t nblo
     for (int64_t g = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; g < nblocks; g += int64_t(gridDim.x) * blockDim.x) {
         const int64_t t = g / nb;
         const int b = int(g - t * nb);
+        // destination rows first: their loads overlap the quantisation below
+        constexpr int KR = 16;
+        int32_t rows[KR];
+#pragma unroll
+        for (int j = 0; j < KR; ++j) rows[j] = j < k ? __ldg(dst_row + t * k + j) : 0;
         const uint4 *src = reinterpret_cast<const uint4 *>(x + t * d + b * 32);
         uint4 raw[4];
 #pragma unroll
@@ -680,7 +685,10 @@ __global__ void k_quant_scatter_pad(const uint16_t *__restrict__ x, int64_t nblo
 #pragma unroll 4
         for (int j = 0; j < k; ++j) {
             if (b == 0) w_sorted[__ldg(inv + t * k + j)] = __ldg(topk_w + t * k + j);
-            const int64_t R = __ldg(dst_row + t * k + j);
+            int32_t Rj = 0;
+#pragma unroll
+            for (int i = 0; i < KR; ++i) Rj = (i == j) ? rows[i] : Rj;
+            const int64_t R = j < KR ? Rj : __ldg(dst_row + t * k + j);
             uint4 *dst = reinterpret_cast<uint4 *>(xq + R * d + b * 32);
             dst[0] = make_uint4(c[0], c[1], c[2], c[3]);
             dst[1] = make_uint4(c[4], c[5], c[6], c[7]);
