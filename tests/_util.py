@@ -28,6 +28,132 @@ def row_rel_err(y_gpu_bf16: np.ndarray, y_ref_bf16: np.ndarray) -> np.ndarray:
     return np.abs(g - r).max(1) / np.maximum(rms, 1e-30)
 
 
+_E4M3_GRID = None
+
+
+def _e4m3_grid() -> np.ndarray:
+    """Magnitudes of the finite e4m3 codes, ascending (0 .. 448)."""
+    global _E4M3_GRID
+    if _E4M3_GRID is None:
+        import oracle
+        _E4M3_GRID = np.array(sorted({abs(oracle.e4m3_value(c)) for c in range(127)}))
+    return _E4M3_GRID
+
+
+def _round_e4m3(a: np.ndarray) -> np.ndarray:
+    """Nearest e4m3 magnitude of each a >= 0, saturating at 448 (ties: either)."""
+    g = _e4m3_grid()
+    a = np.minimum(a, g[-1])
+    i = np.clip(np.searchsorted(g, a), 1, len(g) - 1)
+    lo, hi = g[i - 1], g[i]
+    return np.where(a - lo <= hi - a, lo, hi)
+
+
+def h_decision_envelope(x_row, idx_row, w_row, ob, d: int, I: int) -> np.ndarray:
+    """Per output element of one token, a bound on how far the MXFP8 decisions
+    on the intermediate h may move the layer output when h is computed in fp32.
+
+    The GPU accumulates g = Wg x and u = Wu x in fp32, one 32-element block
+    (its products exact, its two scales shared) at a time; adding the d / 32
+    block sums in order is within 2^-24 times the sum of the running sums'
+    magnitudes of the exact value (taken 4 times, a margin for rounding
+    inside a block).  Carried
+    through h = silu(g) u (first order, plus a few fp32 ulps for the SiLU),
+    that gives an interval around each fp64 h.  Where the interval holds a
+    block-scale boundary (a power of two of the block amax) or an e4m3
+    rounding midpoint, both decisions are correct fp32 results; the bound adds,
+    per element of h, the largest change of its decoded value over the
+    decisions reachable in the interval, times |w_j Wd[:, i]|.  Elements whose
+    interval holds no boundary contribute exactly zero."""
+    import oracle
+    E = ob.arrays[0].size // (I * (d // 2))
+    gq, gs = ob.arrays[0].reshape(E, I, d // 2), ob.arrays[1].reshape(E, I, d // 32)
+    uq, us = ob.arrays[2].reshape(E, I, d // 2), ob.arrays[3].reshape(E, I, d // 32)
+    dq, ds = ob.arrays[4].reshape(E, d, I // 2), ob.arrays[5].reshape(E, d, I // 32)
+    xq, xs = oracle.quant_mxfp8(np.asarray(x_row, np.uint16)[None])
+    xh = oracle.dequant_mxfp8(xq, xs)[0]
+    env = np.zeros(d)
+
+    def sum_and_bound(W):
+        # block partial sums (32 products sharing two scales) added in K order
+        # into an fp32 accumulator: error <= 2^-24 * sum of |running sums|
+        part = (W * xh).reshape(I, d // 32, 32).sum(2)
+        run = np.cumsum(part, axis=1)
+        return run[:, -1], 2.0 ** -24 * np.abs(run[:, 1:]).sum(1)
+
+    for e, wj in zip(idx_row, w_row):
+        g, dg = sum_and_bound(oracle.dequant_mxfp4(gq[e], gs[e]))
+        u, du = sum_and_bound(oracle.dequant_mxfp4(uq[e], us[e]))
+        dg, du = 4 * dg, 4 * du  # margin for the order of the products inside a block
+        sg = 1.0 / (1.0 + np.exp(-g))
+        silu = g * sg
+        h = silu * u
+        dh = np.abs(sg * (1.0 + g * (1.0 - sg)) * u) * dg + np.abs(silu) * du + 2.0 ** -20 * np.abs(h)
+        hq, hs = oracle.quant_mxfp8_f64(h[None])
+        hh = np.abs(oracle.dequant_mxfp8(hq, hs)[0])
+        dev = np.zeros(I)
+        for b in range(I // 32):
+            sl = slice(32 * b, 32 * b + 32)
+            a, da = np.abs(h[sl]), dh[sl]
+            flip_sign = a <= da
+            s_lo = oracle.scale_byte(float(np.maximum(a - da, 0.0).max()), 8)
+            s_hi = oracle.scale_byte(float((a + da).max()), 8)
+            for sb in range(s_lo, s_hi + 1):
+                sc = 2.0 ** (sb - 127)
+                lo = _round_e4m3(np.maximum(a - da, 0.0) / sc) * sc
+                hi = _round_e4m3((a + da) / sc) * sc
+                m = np.maximum(np.abs(lo - hh[sl]), np.abs(hi - hh[sl]))
+                m = np.where(flip_sign, hh[sl] + hi, m)
+                dev[sl] = np.maximum(dev[sl], m)
+        if dev.any():
+            env += abs(float(wj)) * (np.abs(oracle.dequant_mxfp4(dq[e], ds[e])) @ dev)
+    return env
+
+
+def half_ulp_bf16(v: np.ndarray) -> np.ndarray:
+    """Half the spacing of bf16 values at each (bf16) value v: the largest
+    error of rounding a real number to v."""
+    a = np.maximum(np.abs(np.asarray(v, np.float64)), 2.0 ** -126)
+    return 2.0 ** (np.floor(np.log2(a)) - 8)
+
+
+def assert_layer_rows(y_gpu_bf16, y_ref_f64, x_rows, idx_rows, w_rows, ob, d: int, I: int, tol: float):
+    """Layer output rows against the oracle's fp64 values: max|y - y_ref| <=
+    tol * rms(y_ref) per row.  The GPU's own final rounding to bf16 (half a
+    bf16 ulp of each output) is not the layer's error, and where h sits at an
+    MXFP8 boundary both decisions are correct fp32 results: a row over the
+    bar passes only if every element is within tol * rms plus its half ulp
+    plus the decision envelope of h.  Returns, per row, the error beyond the
+    output's rounding, max(|y - y_ref| - half ulp(y)) / rms."""
+    g, r = bf16_to_f64(y_gpu_bf16), np.asarray(y_ref_f64, np.float64)
+    rms = np.maximum(np.sqrt((r ** 2).mean(1)), 1e-30)
+    beyond = np.maximum(np.abs(g - r) - half_ulp_bf16(g), 0.0)
+    err = beyond.max(1) / rms
+    for n in np.nonzero(err > tol)[0]:
+        env = h_decision_envelope(x_rows[n], idx_rows[n], w_rows[n], ob, d, I)
+        excess = beyond[n] - tol * rms[n] - env
+        assert excess.max() <= 0, (f"row {n}: error {err[n]:.3e} of rms, beyond the bar by "
+                                   f"{excess.max() / rms[n]:.3e} of rms after the output's half ulp and the "
+                                   f"h decision envelope (envelope max {env.max() / rms[n]:.3e} of rms)")
+    return err
+
+
+def pair_row_err(yp_row, ref_row, x_row, e: int, wj: float, ob, d: int, I: int, tol: float) -> float:
+    """One routed pair's weighted expert output (fp32 from the GPU) against the
+    oracle's fp64 value: max|diff| / rms(ref); above `tol` it must lie within
+    tol * rms plus the MXFP8 decision envelope of this pair's h."""
+    ref = np.asarray(ref_row, np.float64)
+    diff = np.abs(np.asarray(yp_row, np.float64) - ref)
+    rms = np.sqrt((ref ** 2).mean())
+    err = diff.max() / rms
+    if err > tol:
+        env = h_decision_envelope(x_row, [e], [wj], ob, d, I)
+        excess = diff - tol * rms - env
+        assert excess.max() <= 0, (f"pair of expert {e}: error {err:.3e} of rms, beyond the bar by "
+                                   f"{excess.max() / rms:.3e} after the h decision envelope")
+    return float(err)
+
+
 def canonical_to_tc(q: np.ndarray, s: np.ndarray, nmat: int, rows: int, K: int):
     """Canonical MXFP4 arrays -> the tensor-core layout (include/lmoe.h):
     codes with K padded to a multiple of 128; scales in 512-byte atoms of

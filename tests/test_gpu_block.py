@@ -15,7 +15,7 @@ import torch
 
 import lmoe_inputs as gen
 import oracle
-from _util import bf16_to_f64, device_bank, from_dev_bf16, row_rel_err, to_dev_bf16
+from _util import assert_layer_rows, bf16_to_f64, device_bank, from_dev_bf16, to_dev_bf16
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -68,8 +68,8 @@ def _block_case(lmoe, wl, tokens):
     np.testing.assert_array_equal(idx_h, ridx)
     np.testing.assert_allclose(w_h, rw, rtol=1e-6, atol=1e-9)
     ob = oracle.quantize_experts(wl, experts=np.unique(ridx[tok]))
-    yref = oracle.moe_tokens(lat_h, ridx, rw, ob, wl.d, wl.E, wl.I, tokens=tok)
-    assert row_rel_err(y_h[tok], yref).max() <= 1e-2
+    _, y64 = oracle.moe_tokens(lat_h, ridx, rw, ob, wl.d, wl.E, wl.I, tokens=tok, want_f64=True)
+    assert_layer_rows(y_h[tok], y64, lat_h[tok], ridx[tok], rw[tok], ob, wl.d, wl.I, 1e-2)
     # S7': up-projection of the GPU's layer output
     assert_within_one_bf16_ulp(out_h[tok], oracle.linear_bf16(y_h[tok], W_out), y_h[tok], W_out)
 

@@ -11,7 +11,7 @@ import torch
 
 import lmoe_inputs as gen
 import oracle
-from _util import device_bank, from_dev_bf16, row_rel_err, to_dev_bf16
+from _util import assert_layer_rows, device_bank, from_dev_bf16, to_dev_bf16
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -48,10 +48,10 @@ def _check(wl, x, y, idx, w, logits, tokens):
     np.testing.assert_array_equal(idx, ridx)
     np.testing.assert_allclose(w, rw, rtol=1e-6, atol=1e-9)
     ob = oracle.quantize_experts(wl, experts=np.unique(ridx[tokens]))
-    yref = oracle.moe_tokens(x, ridx, rw, ob, wl.d, wl.E, wl.I, tokens=np.asarray(tokens, np.int32))
-    err = row_rel_err(y[tokens], yref)
-    assert err.max() <= TOL, f"max row error {err.max():.3e}"
-    return err
+    _, y64 = oracle.moe_tokens(x, ridx, rw, ob, wl.d, wl.E, wl.I, tokens=np.asarray(tokens, np.int32),
+                               want_f64=True)
+    tok = np.asarray(tokens)
+    return assert_layer_rows(y[tok], y64, x[tok], ridx[tok], rw[tok], ob, wl.d, wl.I, TOL)
 
 
 def test_forward_tiny_all_tokens(cuda_lib):
@@ -93,22 +93,48 @@ def test_forward_ragged_shapes(cuda_lib):
     _check(wl, x, y, idx, w, lg, list(range(0, 45, 4)))
 
 
-@pytest.mark.parametrize("T,E,k", [(600, 8, 4), (301, 10, 6)])
+def _token_tile(wl):
+    """Token tile the library picks for a batch (by the mean pairs per expert)."""
+    return 16 if wl.P <= 4 * wl.E else 32 if wl.P <= 16 * wl.E else 96
+
+
+@pytest.mark.parametrize("T,E,k", [(600, 24, 4), (301, 15, 6), (600, 8, 4), (301, 10, 6)])
 def test_forward_fused_combine_all_tokens(cuda_lib, T, E, k):
-    """Batches with more than 16 routed pairs per expert use 128-token tiles,
+    """Batches with more than 16 routed pairs per expert use 96-token tiles,
     and the down GEMM's epilogue adds each pair's weighted output straight
     into its token's fp32 row (fp32 atomics; the k terms in an unspecified
-    order).  Every token is checked: several ragged token tiles per expert,
-    d = 3 weight tiles, I = 160 (a ragged last K chunk)."""
-    wl = gen.custom(f"fused{T}", T=T, d=384, I=160, E=E, k=k)
+    order).  Every token is checked: one to four ragged token tiles per
+    expert, d = 3 weight tiles, I = 160 (a ragged last K chunk)."""
+    wl = gen.custom(f"fused{T}_{E}", T=T, d=384, I=160, E=E, k=k)
     assert wl.P > 16 * wl.E
     x, y, idx, w, lg = _run_forward(cuda_lib, wl)
-    err = _check(wl, x, y, idx, w, lg, list(range(T)))
-    assert np.bincount(idx.ravel(), minlength=E).max() > 128  # experts span several token tiles
-    assert err.max() <= TOL
+    _check(wl, x, y, idx, w, lg, list(range(T)))
+    assert np.bincount(idx.ravel(), minlength=E).max() > _token_tile(wl)  # experts span several token tiles
     # a zero batch accumulates to exactly zero
     _, y0, _, _, _ = _run_forward(cuda_lib, wl, np.zeros((T, wl.d), np.uint16))
     assert np.all((y0 & 0x7FFF) == 0)
+
+
+@pytest.mark.parametrize("d,E", [(256, 12), (128, 6)])
+def test_forward_fused_combine_single_weight_band(cuda_lib, d, E):
+    """Fused path whose down GEMM has one item per token tile (two 128-row
+    weight tiles per item: d = 256, or d = 128 where the item's second tile
+    is a copy the epilogue drops), so the second output-column band is empty;
+    every token checked."""
+    wl = gen.custom(f"fused_d{d}", T=300, d=d, I=96, E=E, k=4)
+    assert _token_tile(wl) == 96
+    x, y, idx, w, lg = _run_forward(cuda_lib, wl)
+    _check(wl, x, y, idx, w, lg, list(range(wl.T)))
+
+
+def test_forward_32_token_tiles_all_experts(cuda_lib):
+    """Between 4 and 16 pairs per expert (T = 512 over 896 experts): 32-token
+    tiles, two weight tiles per down stage, per-pair outputs and the
+    slot-order combine."""
+    wl = gen.custom("mid512", T=512, d=512, I=64)
+    assert 4 * wl.E < wl.P <= 16 * wl.E
+    x, y, idx, w, lg = _run_forward(cuda_lib, wl)
+    _check(wl, x, y, idx, w, lg, [0, 1, 100, 255, 256, 400, 511])
 
 
 def test_forward_zero_input_gives_zero(cuda_lib):
