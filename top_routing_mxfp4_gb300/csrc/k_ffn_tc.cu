@@ -418,8 +418,9 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
 #pragma unroll
                 for (int i = 0; i < NV; ++i) {
                     const bool v = 32 * i + lane < nx.n_valid;
+                    // raw pair ids: dividing here would wait for the load
                     wn[i] = v ? __ldg(p.w_sorted + qb + 32 * i + lane) : 0.f;
-                    tn[i] = (v && p.yacc) ? __ldg(p.perm + qb + 32 * i + lane) / p.k : 0;
+                    tn[i] = (v && p.yacc) ? __ldg(p.perm + qb + 32 * i + lane) : 0;
                 }
             }
         };
@@ -501,6 +502,7 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
                         wsel = (c0 / 32 == i) ? wl[i] : wsel;
                         tsel = (c0 / 32 == i) ? tl[i] : tsel;
                     }
+                    tsel /= p.k;  // pair -> token
                     if constexpr (C::STAGED) {
                         // transpose through shared memory: sf[c][row], row stride STG_STRIDE
                         __syncwarp();
