@@ -30,13 +30,15 @@
 // 512-byte atoms (128 rows x 4 K-blocks) that one bulk copy moves and one
 // tcgen05.cp puts in TMEM.
 //
-// Persistent, warp-specialised CTA (224 or 352 threads, one per SM):
-//   warp 0     TMA producer (A tiles via the packed-FP4 tensor map that
-//              expands 16 x 4-bit into 16-byte smem units, B tile, scale atoms)
+// Persistent, warp-specialised CTA (256 or 384 threads, one per SM):
+//   warp 0     TMA producer 0 (first A tile via the packed-FP4 tensor map that
+//              expands 16 x 4-bit into 16-byte smem units, its scale atom, the
+//              B tile)
 //   warp 1     TMEM allocator + MMA issuer 0 (gate / first weight tile of down)
 //   warps 2..  epilogue, 4 or 8 warps: TMEM lane quarter = warp % 4; with 8,
 //              two warps per quarter take alternate column chunks
-//   last warp  MMA issuer 1 (up / second weight tile of down)
+//   next warp  MMA issuer 1 (up / second weight tile of down)
+//   last warp  TMA producer 1 (second A tile, its scale atom, B scale atoms)
 // Every mbarrier wait is bounded; a wait that runs out records
 // LMOE_ERR_TIMEOUT in the status word and the CTA winds down.
 #include <cuda.h>
@@ -161,8 +163,13 @@ struct Cfg {
     static constexpr uint32_t SFA_OFF = MATS * A_TILE + B_TILE;
     static constexpr uint32_t SFB_OFF = SFA_OFF + MATS * 512;
     static constexpr uint32_t STAGE_BYTES = (SFB_OFF + NAT * 512 + 1023) / 1024 * 1024;
-    // global bytes per stage: packed FP4 tiles count 64 bytes per 128-element row
-    static constexpr uint32_t TX_BYTES = MATS * 128 * 64 + B_TILE + MATS * 512 + NAT * 512;
+    // global bytes per stage: packed FP4 tiles count 64 bytes per 128-element row.
+    // Two producer threads share a stage's copies (one thread issues an async
+    // copy only every ~80 cycles): producer 0 the first weight tile, its scale
+    // atom and the token tile; producer 1 the second weight tile, its scales
+    // and the token scale atoms.
+    static constexpr uint32_t TX_BYTES0 = 128 * 64 + 512 + B_TILE;
+    static constexpr uint32_t TX_BYTES1 = (MATS - 1) * (128 * 64 + 512) + NAT * 512;
     // One MMA-issuing thread per weight tile, each with its own accumulator.
     // One thread issues a tcgen05 instruction only every few dozen cycles, so
     // two issuers keep small-N MMAs from pacing the pipeline.
@@ -187,7 +194,7 @@ struct Cfg {
     static constexpr bool STAGED = NT >= 64;
     static constexpr int EPI_WARPS = STAGED ? 8 : 4;
     static constexpr int NW = EPI_WARPS / 4;  // epilogue warps per lane quarter
-    static constexpr int THREADS = 32 * (3 + EPI_WARPS);
+    static constexpr int THREADS = 32 * (4 + EPI_WARPS);
     static constexpr int CW = NT < 32 ? NT : 32;  // accumulator columns per TMEM load (down)
     static constexpr int STG_STRIDE = 36;
     static constexpr uint32_t EPI_WARP_BYTES = !STAGED ? 0 : (MODE == DOWN ? CW * STG_STRIDE * 4 : 16 * 32);
@@ -271,7 +278,7 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
     }
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(&full[s], 1);
+            mbar_init(&full[s], 2);  // one expect_tx arrival per producer
             mbar_init(&empty[s], C::MATS);  // one commit per MMA issuer
         }
         for (int a = 0; a < C::ACC_STAGES; ++a) {
@@ -297,9 +304,10 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
     // kernel's outputs are read after this wait.
     pdl_enter();
 
-    if (warp == 0) {
-        // ---------------- TMA producer ----------------
+    if (warp == 0 || warp == 3 + C::EPI_WARPS) {
+        // ---------------- TMA producers (warp 0 and the last warp) ----------------
         if (lane == 0) {
+            const int pr = warp == 0 ? 0 : 1;
             LMOE_TRACE_DECL
             int stage = 0;
             uint32_t phase = 0;
@@ -311,35 +319,42 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
                 // last tile loads tile 2m twice and the epilogue drops the copy)
                 const int mt0 = MODE == GATEUP ? w.m_tile : C::MATS * w.m_tile;
                 const int mt1 = MODE == GATEUP ? w.m_tile : (mt0 + 1 < p.MTA ? mt0 + 1 : mt0);
-                const int arow = w.e * p.Mtot + mt0 * 128, arow1 = w.e * p.Mtot + mt1 * 128;
-                const int64_t sfa_base = (int64_t(w.e) * p.MTA + mt0) * p.KC;
-                const int64_t sfa_base1 = (int64_t(w.e) * p.MTA + mt1) * p.KC;
+                const int arow = w.e * p.Mtot + (pr == 0 ? mt0 : mt1) * 128;
+                const int64_t sfa_base = (int64_t(w.e) * p.MTA + (pr == 0 ? mt0 : mt1)) * p.KC;
+                const CUtensorMap *tmA = pr == 0 ? &tmA0 : &tmA1;
+                const uint8_t *sfa = pr == 0 ? p.sfa0 : p.sfa1;
                 for (int kc = 0; kc < p.KC; ++kc) {
                     if (!mbar_wait(&empty[stage], phase ^ 1)) {
                         set_status(p.status, LMOE_ERR_TIMEOUT);
                         ok = false;
                         break;
                     }
-                    LMOE_TRACE_EV(0, 0x10 | MODE, it, kc);  // producer: stage free
+                    if (pr == 0) LMOE_TRACE_EV(0, 0x10 | MODE, it, kc);  // producer: stage free
                     uint8_t *sb = stages + stage * C::STAGE_BYTES;
-                    mbar_arrive_expect_tx(&full[stage], C::TX_BYTES);
-                    tma_load_2d(sb, &tmA0, kc * 128, arow, &full[stage]);
-                    if (C::MATS == 2) tma_load_2d(sb + C::A_TILE, &tmA1, kc * 128, arow1, &full[stage]);
-                    tma_load_2d(sb + C::MATS * C::A_TILE, &tmB, kc * 128, R, &full[stage]);
-                    bulk_load(sb + C::SFA_OFF, p.sfa0 + (sfa_base + kc) * 512, 512, &full[stage]);
-                    if (C::MATS == 2) bulk_load(sb + C::SFA_OFF + 512, p.sfa1 + (sfa_base1 + kc) * 512, 512, &full[stage]);
+                    if (pr == 0) {
+                        mbar_arrive_expect_tx(&full[stage], C::TX_BYTES0);
+                        tma_load_2d(sb, tmA, kc * 128, arow, &full[stage]);
+                        tma_load_2d(sb + C::MATS * C::A_TILE, &tmB, kc * 128, R, &full[stage]);
+                        bulk_load(sb + C::SFA_OFF, sfa + (sfa_base + kc) * 512, 512, &full[stage]);
+                    } else {
+                        mbar_arrive_expect_tx(&full[stage], C::TX_BYTES1);
+                        if (C::MATS == 2) {
+                            tma_load_2d(sb + C::A_TILE, tmA, kc * 128, arow, &full[stage]);
+                            bulk_load(sb + C::SFA_OFF + 512, sfa + (sfa_base + kc) * 512, 512, &full[stage]);
+                        }
 #pragma unroll
-                    for (int a = 0; a < C::NAT; ++a)
-                        bulk_load(sb + C::SFB_OFF + a * 512, p.sfb + (int64_t(R / 128 + a) * p.KC + kc) * 512, 512,
-                                  &full[stage]);
-                    LMOE_TRACE_EV(0, 0x70 | MODE, it, kc);  // producer: copies issued
+                        for (int a = 0; a < C::NAT; ++a)
+                            bulk_load(sb + C::SFB_OFF + a * 512, p.sfb + (int64_t(R / 128 + a) * p.KC + kc) * 512, 512,
+                                      &full[stage]);
+                    }
+                    if (pr == 0) LMOE_TRACE_EV(0, 0x70 | MODE, it, kc);  // producer: copies issued
                     if (++stage == S) {
                         stage = 0;
                         phase ^= 1;
                     }
                 }
             }
-            LMOE_TRACE_END(0);
+            if (pr == 0) LMOE_TRACE_END(0);
         }
     } else if (warp == 1 || warp == 2 + C::EPI_WARPS) {
         // ---------------- MMA issuers (warp 1: gate / first tile, last warp: up / second tile) ----------------
@@ -414,13 +429,16 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
         auto fetch = [&](int it2, Item &nx, float (&wn)[NV], int (&tn)[NV]) {
             nx = decode_item<MODE, NT>(it2, s_tiles, s_off, p.E, p.MT, NT);
             if (MODE == DOWN) {
+                // Unconditional loads at clamped rows (entries past the tile are
+                // never used) of raw pair ids: a select or a division here would
+                // wait for the load.
                 const int qb = s_off[nx.e] + nx.n_tile * NT;
+                const int qlast = s_off[p.E] - 1;
 #pragma unroll
                 for (int i = 0; i < NV; ++i) {
-                    const bool v = 32 * i + lane < nx.n_valid;
-                    // raw pair ids: dividing here would wait for the load
-                    wn[i] = v ? __ldg(p.w_sorted + qb + 32 * i + lane) : 0.f;
-                    tn[i] = (v && p.yacc) ? __ldg(p.perm + qb + 32 * i + lane) : 0;
+                    const int q = min(qb + 32 * i + lane, qlast);
+                    wn[i] = __ldg(p.w_sorted + q);
+                    tn[i] = __ldg(p.perm + q);
                 }
             }
         };
@@ -640,22 +658,31 @@ __device__ __forceinline__ int64_t atom_off(int64_t R, int b, int KC)
 }
 
 // bf16 x[T][d] -> MXFP8 rows at every padded row the token's pairs go to
-// (dst_row, written by the permute).
-__global__ void k_quant_scatter_pad(const uint16_t *__restrict__ x, int64_t nblocks, int d, int k,
+// (dst_row, written by the permute).  Work unit (token t, destination group,
+// block b): block b of token t quantised and stored to the group's up to
+// SCATTER_KG destination rows; a token's groups are separate units, so more
+// threads (and stores) are in flight per token.  b runs fastest, so a warp's
+// stores to one destination row are contiguous.
+constexpr int SCATTER_KG = 8;
+__global__ void k_quant_scatter_pad(const uint16_t *__restrict__ x, int64_t nunits, int d, int k,
                                     const int32_t *__restrict__ dst_row, const int32_t *__restrict__ inv,
                                     const float *__restrict__ topk_w, uint8_t *__restrict__ xq,
                                     uint8_t *__restrict__ xs, float *__restrict__ w_sorted)
 {
     pdl_enter();
     const int nb = d / 32, KC = d / 128;
-    for (int64_t g = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; g < nblocks; g += int64_t(gridDim.x) * blockDim.x) {
-        const int64_t t = g / nb;
-        const int b = int(g - t * nb);
+    const int ng = (k + SCATTER_KG - 1) / SCATTER_KG;
+    for (int64_t g = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; g < nunits; g += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t tg = g / nb;  // t * ng + group
+        const int b = int(g - tg * nb);
+        const int64_t t = tg / ng;
+        const int j0 = int(tg - t * ng) * SCATTER_KG;
+        const int nj = min(SCATTER_KG, k - j0);
+        const int64_t p0 = t * k + j0;  // first pair of the group
         // destination rows first: their loads overlap the quantisation below
-        constexpr int KR = 16;
-        int32_t rows[KR];
+        int32_t rows[SCATTER_KG];
 #pragma unroll
-        for (int j = 0; j < KR; ++j) rows[j] = j < k ? __ldg(dst_row + t * k + j) : 0;
+        for (int j = 0; j < SCATTER_KG; ++j) rows[j] = j < nj ? __ldg(dst_row + p0 + j) : 0;
         const uint4 *src = reinterpret_cast<const uint4 *>(x + t * d + b * 32);
         uint4 raw[4];
 #pragma unroll
@@ -684,13 +711,11 @@ __global__ void k_quant_scatter_pad(const uint16_t *__restrict__ x, int64_t nblo
         sb4 |= __shfl_down_sync(mask, sb, 1) << 8;
         sb4 |= __shfl_down_sync(mask, sb, 2) << 16;
         sb4 |= __shfl_down_sync(mask, sb, 3) << 24;
-#pragma unroll 4
-        for (int j = 0; j < k; ++j) {
-            if (b == 0) w_sorted[__ldg(inv + t * k + j)] = __ldg(topk_w + t * k + j);
-            int32_t Rj = 0;
 #pragma unroll
-            for (int i = 0; i < KR; ++i) Rj = (i == j) ? rows[i] : Rj;
-            const int64_t R = j < KR ? Rj : __ldg(dst_row + t * k + j);
+        for (int j = 0; j < SCATTER_KG; ++j) {
+            if (j >= nj) break;
+            if (b == 0) w_sorted[__ldg(inv + p0 + j)] = __ldg(topk_w + p0 + j);
+            const int64_t R = rows[j];
             uint4 *dst = reinterpret_cast<uint4 *>(xq + R * d + b * 32);
             dst[0] = make_uint4(c[0], c[1], c[2], c[3]);
             dst[1] = make_uint4(c[4], c[5], c[6], c[7]);
@@ -869,11 +894,11 @@ FfnSched ffn_sched(const FfnLayout &L, int d, int I, char *scratch)
 cudaError_t launch_quant_scatter_pad(const uint16_t *x, int T, int d, int k, const int32_t *inv, const float *topk_w,
                                      const FfnLayout &L, char *scratch, cudaStream_t st)
 {
-    const int64_t nblocks = int64_t(T) * (d / 32);
-    if (nblocks == 0) return cudaSuccess;
-    const int grid = int(ceil_div(nblocks, 128) < 152 * 32 ? ceil_div(nblocks, 128) : 152 * 32);
+    const int64_t nunits = int64_t(T) * ceil_div(k, SCATTER_KG) * (d / 32);
+    if (nunits == 0) return cudaSuccess;
+    const int grid = int(ceil_div(nunits, 128) < 152 * 32 ? ceil_div(nunits, 128) : 152 * 32);
     {
-        const cudaError_t le_ = launch_pdl(k_quant_scatter_pad, dim3(grid), dim3(128), 0, st, x, nblocks, d, k, reinterpret_cast<const int32_t *>(scratch + L.dst_row), inv, topk_w, reinterpret_cast<uint8_t *>(scratch + L.xq), reinterpret_cast<uint8_t *>(scratch + L.xs), reinterpret_cast<float *>(scratch + L.w_sorted));
+        const cudaError_t le_ = launch_pdl(k_quant_scatter_pad, dim3(grid), dim3(128), 0, st, x, nunits, d, k, reinterpret_cast<const int32_t *>(scratch + L.dst_row), inv, topk_w, reinterpret_cast<uint8_t *>(scratch + L.xq), reinterpret_cast<uint8_t *>(scratch + L.xs), reinterpret_cast<float *>(scratch + L.w_sorted));
         if (le_ != cudaSuccess) return le_;
     }
     return cudaGetLastError();
