@@ -136,7 +136,9 @@ struct GemmArgs {
     const uint8_t *sfa0, *sfa1;  // weight scale atoms [E][RTa][KC][512]
     const uint8_t *sfb;          // activation scale atoms [rows/128][KC][512]
     const int32_t *offsets;      // [E+1] segment starts in permuted order
-    const int32_t *tiles;        // [E+1] first work item of each expert
+    const int32_t *tiles;        // [E+1] first work item of each expert (tiles[E]: the item count)
+    const int32_t *pad_off;      // [E+1] first padded token row of each expert
+    const int2 *items;           // work-item table in execution order (fill_item_tables)
     const float *w_sorted;  // gate weight of each permuted row q (topk_w[perm[q]])
     uint8_t *hq;    // gate/up out: [rows][Ih] e4m3
     uint8_t *hs;    // gate/up out: scale atoms [rows/128][KCh][512]
@@ -144,7 +146,7 @@ struct GemmArgs {
     float *yacc;    // down out when set (fused combine): [T][Mtot] fp32 sums, zeroed by the caller
     const int32_t *perm;  // [P] pair of each permuted row (token = perm / k)
     int k;
-    int E, Mtot, MT, MTA, KC, KCh, Ih;  // MT: m tiles per item sequence; MTA: 128-row tiles of A
+    int E, Mtot, MTA, KC, KCh, Ih;  // MTA: 128-row tiles of A
     int stages;  // shared-memory pipeline depth (<= Cfg::MAX_STAGES)
     int32_t *status;
 };
@@ -205,47 +207,21 @@ struct Item {
     int e, n_tile, m_tile, n_valid;
 };
 
-// Work item `it` -> (expert, token tile, weight tile).  s_tiles[e] counts the
-// items before expert e (token tiles before e times MT).  Items run in
-// (expert, token tile, weight tile) order, weight tile fastest, so the
-// weight-tile items of one token tile run together and share its activation
-// rows in L2.  Down with large token tiles (the fused combine): the weight
-// tiles are split into two bands (the first and second half of the output
-// columns) and all items of the first band come first, so that only half of
-// the per-token fp32 rows is being written at a time (less of them evicted
-// to DRAM); each weight tile is still read once.
-template <int MODE, int NT>
-__device__ __forceinline__ Item decode_item(int it, const int32_t *s_tiles, const int32_t *s_off, int E, int MT, int nt)
+// Work-item table entry -> (expert, token tile, weight tile, valid tokens).
+// The table (written with the schedule) fixes the execution order: weight
+// tile fastest within a token tile, so the weight-tile items of one token
+// tile run together and share its activation rows in L2; for the down GEMM
+// with large token tiles (the fused combine), the first half of the weight
+// tiles of every token tile before the second half.  Each role loads its
+// entries an item or two ahead (a table load is a global-memory round trip;
+// a search of the per-expert prefix in shared memory took ~1,400 cycles).
+__device__ __forceinline__ Item item_at(int2 v, const int32_t *s_off, int nt)
 {
-    int key = it, m0 = 0, mt = MT;  // band of weight tiles [m0, m0 + mt)
-    if (MODE == DOWN && NT >= 64) {
-        const int TT = s_tiles[E] / MT;  // token tiles
-        const int MT0 = (MT + 1) / 2;    // weight tiles of the first band
-        const int first = TT * MT0;      // items of the first band
-        if (it >= first) {
-            m0 = MT0;
-            mt = MT - MT0;
-            it -= first;
-        } else {
-            mt = MT0;
-        }
-        const int r = it / mt;           // token tile
-        key = r * MT + (it - r * mt);    // as if in the one-band order, weight tile m0 + (it - r mt)
-    }
-    int lo = 0, hi = E;  // s_tiles[lo] <= key < s_tiles[hi]
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (s_tiles[mid] <= key) lo = mid;
-        else hi = mid;
-    }
-    // skip experts with no items (equal starts)
     Item r;
-    r.e = lo;
-    const int local = key - s_tiles[lo];
-    r.n_tile = local / MT;
-    r.m_tile = m0 + (local - r.n_tile * MT);
-    const int n_e = s_off[lo + 1] - s_off[lo];
-    r.n_valid = min(nt, n_e - r.n_tile * nt);
+    r.e = v.x & 0xFFFF;
+    r.m_tile = int(uint32_t(v.x) >> 16);
+    r.n_tile = v.y;
+    r.n_valid = min(nt, s_off[r.e + 1] - s_off[r.e] - r.n_tile * nt);
     return r;
 }
 
@@ -265,16 +241,27 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
     uint64_t *acc_full = empty + S;
     uint64_t *acc_empty = acc_full + C::ACC_STAGES;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_empty + C::ACC_STAGES);
-    int32_t *s_tiles = reinterpret_cast<int32_t *>(tmem_slot + 4);
-    int32_t *s_off = s_tiles + (p.E + 1);
+    int32_t *s_pad = reinterpret_cast<int32_t *>(tmem_slot + 4);
+    int32_t *s_off = s_pad + (p.E + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     LMOE_TRACE_CTA(MODE, 0);
     // the schedule is an output of an earlier kernel than the previous one
     // (complete before this grid starts); read through L2
     for (int i = threadIdx.x; i <= p.E; i += blockDim.x) {
-        s_tiles[i] = __ldcg(p.tiles + i);
+        s_pad[i] = __ldcg(p.pad_off + i);
         s_off[i] = __ldcg(p.offsets + i);
+    }
+    const int total = __ldcg(p.tiles + p.E);
+    const int G = int(gridDim.x);
+    // this CTA's item-table entries at index i (clamped: entries past the end
+    // are loaded but never used)
+    auto entry = [&](int i) { return __ldcg(p.items + (i < total ? i : total - 1)); };
+    // first two entries, loaded before the wait (the table is complete)
+    int2 ent0 = make_int2(0, 0), ent1 = make_int2(0, 0);
+    if (int(blockIdx.x) < total) {
+        ent0 = entry(blockIdx.x);
+        ent1 = entry(blockIdx.x + G);
     }
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -297,9 +284,7 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const int total = s_tiles[p.E];
-    // slot start of an expert's first token tile (tiles[e] = slots before e times MT)
-    auto slot_row = [&](int e) { return (s_tiles[e] / p.MT) * C::SLOT; };
+    auto slot_row = [&](int e) { return s_pad[e]; };  // first padded row of expert e
     // Everything above reads only inputs of earlier kernels; the previous
     // kernel's outputs are read after this wait.
     pdl_enter();
@@ -312,8 +297,11 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
-            for (int it = blockIdx.x; it < total && ok; it += gridDim.x) {
-                const Item w = decode_item<MODE, NT>(it, s_tiles, s_off, p.E, p.MT, NT);
+            int2 ent = ent0, ent_next = ent1;
+            for (int it = blockIdx.x; it < total && ok; it += G) {
+                const Item w = item_at(ent, s_off, NT);
+                ent = ent_next;
+                ent_next = entry(it + 2 * G);
                 const int R = slot_row(w.e) + w.n_tile * C::SLOT;
                 // gate/up: tile m of both matrices; down: tiles 2m and 2m+1 (an odd
                 // last tile loads tile 2m twice and the epilogue drops the copy)
@@ -364,8 +352,11 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
             int stage = 0, acc = 0;
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
-            for (int it = blockIdx.x; it < total && ok; it += gridDim.x) {
-                const Item w = decode_item<MODE, NT>(it, s_tiles, s_off, p.E, p.MT, NT);
+            int2 ent = ent0, ent_next = ent1;
+            for (int it = blockIdx.x; it < total && ok; it += G) {
+                const Item w = item_at(ent, s_off, NT);
+                ent = ent_next;
+                ent_next = entry(it + 2 * G);
                 const uint32_t N = uint32_t((w.n_valid + 15) & ~15);
                 if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1)) {
                     set_status(p.status, LMOE_ERR_TIMEOUT);
@@ -424,10 +415,11 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
         // The gate weights and tokens of an item are loaded two items ahead
         // (their latency under the output traffic is several microseconds),
         // into two register sets used alternately, so no register waits on an
-        // outstanding load before its item comes up.
+        // outstanding load before its item comes up; the item's table entry
+        // was loaded two items before that.
         constexpr int NV = (NT + 31) / 32;
-        auto fetch = [&](int it2, Item &nx, float (&wn)[NV], int (&tn)[NV]) {
-            nx = decode_item<MODE, NT>(it2, s_tiles, s_off, p.E, p.MT, NT);
+        auto fetch = [&](int2 ent, Item &nx, float (&wn)[NV], int (&tn)[NV]) {
+            nx = item_at(ent, s_off, NT);
             if (MODE == DOWN) {
                 // Unconditional loads at clamped rows (entries past the tile are
                 // never used) of raw pair ids: a select or a division here would
@@ -570,15 +562,21 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
         Item nA{}, nB{};
         float wA[NV], wB[NV];
         int tA[NV], tB[NV];
-        const int G = int(gridDim.x);
-        if (int(blockIdx.x) < total) fetch(blockIdx.x, nA, wA, tA);
-        if (int(blockIdx.x) + G < total) fetch(blockIdx.x + G, nB, wB, tB);
+        if (int(blockIdx.x) < total) fetch(ent0, nA, wA, tA);
+        if (int(blockIdx.x) + G < total) fetch(ent1, nB, wB, tB);
+        int2 eA = entry(blockIdx.x + 2 * G), eB = entry(blockIdx.x + 3 * G);  // next entries of the two sets
         for (int it = blockIdx.x; it < total; it += 2 * G) {
             if (!process(it, nA, wA, tA)) break;
-            if (it + 2 * G < total) fetch(it + 2 * G, nA, wA, tA);
+            if (it + 2 * G < total) {
+                fetch(eA, nA, wA, tA);
+                eA = entry(it + 4 * G);
+            }
             if (it + G >= total) break;
             if (!process(it + G, nB, wB, tB)) break;
-            if (it + 3 * G < total) fetch(it + 3 * G, nB, wB, tB);
+            if (it + 3 * G < total) {
+                fetch(eB, nB, wB, tB);
+                eB = entry(it + 5 * G);
+            }
         }
         if (threadIdx.x == 64) LMOE_TRACE_END(2);
     }
@@ -623,28 +621,24 @@ __device__ void block_exclusive_scan(const int32_t *v, int n, int32_t *out, int3
     __syncthreads();
 }
 
-__global__ void __launch_bounds__(1024) k_ffn_schedule(const int32_t *__restrict__ offsets, int E, int NT, int SLOT,
-                                                      int MT_gu, int MT_dn, int32_t *pad_off, int32_t *tiles_gu,
-                                                      int32_t *tiles_dn)
+__global__ void __launch_bounds__(1024) k_ffn_schedule(const int32_t *__restrict__ offsets, int E, FfnSched sc)
 {
     pdl_enter();
-    __shared__ int32_t v[2048], o[2048], warp_tot[32], tot;
+    __shared__ int32_t v[2048], o[2049], warp_tot[32], tot;
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
         const int n = offsets[e + 1] - offsets[e];
-        v[e] = (n + NT - 1) / NT;  // token tiles of expert e
+        v[e] = (n + sc.NT - 1) / sc.NT;  // token tiles of expert e
     }
     __syncthreads();
     block_exclusive_scan(v, E, o, &tot, warp_tot);
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        pad_off[e] = o[e] * SLOT;
-        tiles_gu[e] = o[e] * MT_gu;
-        tiles_dn[e] = o[e] * MT_dn;
+    if (threadIdx.x == 0) o[E] = tot;
+    __syncthreads();
+    for (int e = threadIdx.x; e <= E; e += blockDim.x) {
+        sc.pad_off[e] = o[e] * sc.SLOT;
+        sc.tiles_gu[e] = o[e] * sc.MT_gu;
+        sc.tiles_dn[e] = o[e] * sc.MT_dn;
     }
-    if (threadIdx.x == 0) {
-        pad_off[E] = tot * SLOT;
-        tiles_gu[E] = tot * MT_gu;
-        tiles_dn[E] = tot * MT_dn;
-    }
+    fill_item_tables(o, E, sc, blockDim.x);
 }
 
 // ---- activations into the padded token layout ------------------------------------------
@@ -856,6 +850,10 @@ FfnLayout ffn_layout(int64_t P, int d, int E, int I)
     L.pad_off = take(size_t(E + 1) * 4);
     L.tiles_gu = take(size_t(E + 1) * 4);
     L.tiles_dn = take(size_t(E + 1) * 4);
+    const int64_t max_tiles = L.rows / L.SLOT;
+    L.items_gu = take(size_t(max_tiles * ceil_div(I, 128)) * sizeof(int2));
+    L.items_dn = take(size_t(max_tiles * ceil_div(d / 128, down_tiles_per_item(L.NT))) * sizeof(int2));
+    L.tile_e = take(size_t(max_tiles) * 4);
     L.xq = take(size_t(L.rows) * d);
     L.xs = take(size_t(atoms) * (d / 128) * 512);
     L.hq = take(size_t(L.rows) * I);
@@ -871,7 +869,8 @@ cudaError_t launch_ffn_schedule(const int32_t *offsets, int E, int d, int I, con
                                 cudaStream_t st)
 {
     {
-        const cudaError_t le_ = launch_pdl(k_ffn_schedule, dim3(1), dim3(1024), 0, st, offsets, E, L.NT, L.SLOT, int(ceil_div(I, 128)), int(ceil_div(d / 128, down_tiles_per_item(L.NT))), reinterpret_cast<int32_t *>(scratch + L.pad_off), reinterpret_cast<int32_t *>(scratch + L.tiles_gu), reinterpret_cast<int32_t *>(scratch + L.tiles_dn));
+        const cudaError_t le_ =
+            launch_pdl(k_ffn_schedule, dim3(1), dim3(1024), 0, st, offsets, E, ffn_sched(L, d, I, scratch));
         if (le_ != cudaSuccess) return le_;
     }
     return cudaGetLastError();
@@ -887,6 +886,10 @@ FfnSched ffn_sched(const FfnLayout &L, int d, int I, char *scratch)
     sc.pad_off = reinterpret_cast<int32_t *>(scratch + L.pad_off);
     sc.tiles_gu = reinterpret_cast<int32_t *>(scratch + L.tiles_gu);
     sc.tiles_dn = reinterpret_cast<int32_t *>(scratch + L.tiles_dn);
+    sc.items_gu = reinterpret_cast<int2 *>(scratch + L.items_gu);
+    sc.items_dn = reinterpret_cast<int2 *>(scratch + L.items_dn);
+    sc.tile_e = reinterpret_cast<int32_t *>(scratch + L.tile_e);
+    sc.band = L.NT >= 64 ? 1 : 0;  // Cfg<DOWN, NT>::STAGED
     sc.dst_row = reinterpret_cast<int32_t *>(scratch + L.dst_row);
     return sc;
 }
@@ -951,11 +954,12 @@ cudaError_t launch_expert_gemms(const FfnArgs &a, const FfnLayout &L, char *scra
     g.sfa1 = a.W->up_s;
     g.sfb = xs;
     g.tiles = reinterpret_cast<const int32_t *>(scratch + L.tiles_gu);
+    g.pad_off = reinterpret_cast<const int32_t *>(scratch + L.pad_off);
+    g.items = reinterpret_cast<const int2 *>(scratch + L.items_gu);
     g.hq = hq;
     g.hs = hs;
     g.Mtot = a.I;
-    g.MT = int(ceil_div(a.I, 128));
-    g.MTA = g.MT;
+    g.MTA = int(ceil_div(a.I, 128));
     g.KC = a.d / 128;
     g.KCh = Ip / 128;
     g.Ih = a.I;
@@ -972,13 +976,13 @@ cudaError_t launch_expert_gemms(const FfnArgs &a, const FfnLayout &L, char *scra
     g.sfa1 = a.W->down_s;  // the second tile of a down item is the next tile of the same matrix
     g.sfb = hs;
     g.tiles = reinterpret_cast<const int32_t *>(scratch + L.tiles_dn);
+    g.items = reinterpret_cast<const int2 *>(scratch + L.items_dn);
     g.yp = a.yp;
     g.yacc = a.yacc;
     g.perm = a.perm;
     g.k = a.k;
     g.Mtot = a.d;
     g.MTA = a.d / 128;
-    g.MT = int(ceil_div(g.MTA, down_tiles_per_item(L.NT)));
     g.KC = Ip / 128;
     return L.NT == 16   ? launch_gemm<DOWN, 16>(md, md, mh, g, st)
            : L.NT == 32 ? launch_gemm<DOWN, 32>(md, md, mh, g, st)

@@ -149,12 +149,51 @@ cudaError_t launch_route(const uint16_t *x, const uint16_t *Wr3, const float *bi
 
 // Optional by-products of the permute for the expert GEMMs: per expert the
 // first slot row in the padded token layout (pad_off, E+1) and the first work
-// item of each GEMM (tiles_gu / tiles_dn, E+1), and per pair p its padded
-// token row (dst_row, T*k).  pad_off == nullptr disables them.
+// item of each GEMM (tiles_gu / tiles_dn, E+1), the work-item tables of the
+// two GEMMs (items_gu / items_dn, see fill_item_tables), and per pair p its
+// padded token row (dst_row, T*k).  pad_off == nullptr disables them.
 struct FfnSched {
     int NT = 0, SLOT = 0, MT_gu = 0, MT_dn = 0;
+    int band = 0;  // the down GEMM runs its items in two output-column bands
     int32_t *pad_off = nullptr, *tiles_gu = nullptr, *tiles_dn = nullptr, *dst_row = nullptr;
+    int2 *items_gu = nullptr, *items_dn = nullptr;
+    int32_t *tile_e = nullptr;  // expert of each token tile (scratch of fill_item_tables)
 };
+
+// Work-item tables of the two expert GEMMs, in execution order: entry i is
+// item i as {expert | weight tile << 16, token tile within the expert}.
+// `scan` holds the token tiles before each expert (E + 1 entries, in shared
+// memory).  gate/up: items in (token tile, weight tile) order, weight tile
+// fastest.  down: the same, or with `band`, every item of the first half of
+// the weight tiles before the second half (each half in that order), so that
+// only half of the per-token output rows take reductions at a time.  Called
+// by every thread of the block: the expert of each token tile goes to
+// sc.tile_e first, then consecutive threads write consecutive entries.
+__device__ __forceinline__ void fill_item_tables(const int32_t *scan, int E, const FfnSched &sc, int nthreads)
+{
+    const int TT = scan[E];
+    for (int e = threadIdx.x; e < E; e += nthreads)
+        for (int R = scan[e]; R < scan[e + 1]; ++R) sc.tile_e[R] = e;
+    __syncthreads();
+    const int MT0 = sc.band ? (sc.MT_dn + 1) / 2 : sc.MT_dn, MT1 = sc.MT_dn - MT0;
+    const int n_gu = TT * sc.MT_gu, n_dn0 = TT * MT0, n_dn = TT * sc.MT_dn;
+    for (int it = threadIdx.x; it < n_gu; it += nthreads) {
+        const int R = it / sc.MT_gu, m = it - R * sc.MT_gu, e = sc.tile_e[R];
+        sc.items_gu[it] = make_int2(e | (m << 16), R - scan[e]);
+    }
+    for (int it = threadIdx.x; it < n_dn; it += nthreads) {
+        int R, m;
+        if (it < n_dn0) {
+            R = it / MT0;
+            m = it - R * MT0;
+        } else {
+            R = (it - n_dn0) / MT1;
+            m = MT0 + (it - n_dn0 - R * MT1);
+        }
+        const int e = sc.tile_e[R];
+        sc.items_dn[it] = make_int2(e | (m << 16), R - scan[e]);
+    }
+}
 size_t permute_scratch_bytes(int64_t P, int E);
 cudaError_t launch_permute(const int32_t *idx, int64_t P, int E, int32_t *counts, int32_t *offsets, int32_t *perm,
                            int32_t *inv, void *scratch, int32_t *status, cudaStream_t st,
@@ -166,7 +205,8 @@ cudaError_t launch_permute(const int32_t *idx, int64_t P, int E, int32_t *counts
 struct FfnLayout {
     int NT, SLOT;      // token tile and slot rows
     int64_t rows;      // padded token rows reserved
-    size_t pad_off, tiles_gu, tiles_dn, xq, xs, hq, hs, hs_bytes, w_sorted, dst_row, total;  // byte offsets / sizes
+    size_t pad_off, tiles_gu, tiles_dn, items_gu, items_dn, tile_e, xq, xs, hq, hs, hs_bytes, w_sorted, dst_row,
+        total;  // byte offsets / sizes
     bool fused;  // large token tiles: the down GEMM can accumulate into the per-token output (FfnArgs::yacc)
 };
 FfnLayout ffn_layout(int64_t P, int d, int E, int I);
