@@ -138,7 +138,7 @@ struct GemmArgs {
     const int32_t *offsets;      // [E+1] segment starts in permuted order
     const int32_t *tiles;        // [E+1] first work item of each expert (tiles[E]: the item count)
     const int32_t *pad_off;      // [E+1] first padded token row of each expert
-    const int2 *items;           // work-item table in execution order (fill_item_tables)
+    const int2 *items;           // work-item table in execution order (fill_item_entries)
     const float *w_sorted;  // gate weight of each permuted row q (topk_w[perm[q]])
     uint8_t *hq;    // gate/up out: [rows][Ih] e4m3
     uint8_t *hs;    // gate/up out: scale atoms [rows/128][KCh][512]
@@ -255,14 +255,8 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
     const int total = __ldcg(p.tiles + p.E);
     const int G = int(gridDim.x);
     // this CTA's item-table entries at index i (clamped: entries past the end
-    // are loaded but never used)
+    // are loaded but never used); the table may come from the previous kernel
     auto entry = [&](int i) { return __ldcg(p.items + (i < total ? i : total - 1)); };
-    // first two entries, loaded before the wait (the table is complete)
-    int2 ent0 = make_int2(0, 0), ent1 = make_int2(0, 0);
-    if (int(blockIdx.x) < total) {
-        ent0 = entry(blockIdx.x);
-        ent1 = entry(blockIdx.x + G);
-    }
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 2);  // one expect_tx arrival per producer
@@ -288,6 +282,11 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
     // Everything above reads only inputs of earlier kernels; the previous
     // kernel's outputs are read after this wait.
     pdl_enter();
+    int2 ent0 = make_int2(0, 0), ent1 = make_int2(0, 0);  // the first two entries
+    if (int(blockIdx.x) < total) {
+        ent0 = entry(blockIdx.x);
+        ent1 = entry(blockIdx.x + G);
+    }
 
     if (warp == 0 || warp == 3 + C::EPI_WARPS) {
         // ---------------- TMA producers (warp 0 and the last warp) ----------------
@@ -638,7 +637,9 @@ __global__ void __launch_bounds__(1024) k_ffn_schedule(const int32_t *__restrict
         sc.tiles_gu[e] = o[e] * sc.MT_gu;
         sc.tiles_dn[e] = o[e] * sc.MT_dn;
     }
-    fill_item_tables(o, E, sc, blockDim.x);
+    fill_tile_info(o, E, sc, blockDim.x);
+    __syncthreads();
+    fill_item_entries(sc, tot * sc.MT_gu, tot * sc.MT_dn, threadIdx.x, blockDim.x);
 }
 
 // ---- activations into the padded token layout ------------------------------------------
@@ -661,9 +662,12 @@ constexpr int SCATTER_KG = 8;
 __global__ void k_quant_scatter_pad(const uint16_t *__restrict__ x, int64_t nunits, int d, int k,
                                     const int32_t *__restrict__ dst_row, const int32_t *__restrict__ inv,
                                     const float *__restrict__ topk_w, uint8_t *__restrict__ xq,
-                                    uint8_t *__restrict__ xs, float *__restrict__ w_sorted)
+                                    uint8_t *__restrict__ xs, float *__restrict__ w_sorted, FfnSched sc, int E)
 {
     pdl_enter();
+    // the expert GEMMs' work-item tables, from the permute's tile_info
+    fill_item_entries(sc, sc.tiles_gu[E], sc.tiles_dn[E], blockIdx.x * int64_t(blockDim.x) + threadIdx.x,
+                      int64_t(gridDim.x) * blockDim.x);
     const int nb = d / 32, KC = d / 128;
     const int ng = (k + SCATTER_KG - 1) / SCATTER_KG;
     for (int64_t g = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; g < nunits; g += int64_t(gridDim.x) * blockDim.x) {
@@ -853,7 +857,7 @@ FfnLayout ffn_layout(int64_t P, int d, int E, int I)
     const int64_t max_tiles = L.rows / L.SLOT;
     L.items_gu = take(size_t(max_tiles * ceil_div(I, 128)) * sizeof(int2));
     L.items_dn = take(size_t(max_tiles * ceil_div(d / 128, down_tiles_per_item(L.NT))) * sizeof(int2));
-    L.tile_e = take(size_t(max_tiles) * 4);
+    L.tile_info = take(size_t(max_tiles) * sizeof(int2));
     L.xq = take(size_t(L.rows) * d);
     L.xs = take(size_t(atoms) * (d / 128) * 512);
     L.hq = take(size_t(L.rows) * I);
@@ -888,20 +892,20 @@ FfnSched ffn_sched(const FfnLayout &L, int d, int I, char *scratch)
     sc.tiles_dn = reinterpret_cast<int32_t *>(scratch + L.tiles_dn);
     sc.items_gu = reinterpret_cast<int2 *>(scratch + L.items_gu);
     sc.items_dn = reinterpret_cast<int2 *>(scratch + L.items_dn);
-    sc.tile_e = reinterpret_cast<int32_t *>(scratch + L.tile_e);
+    sc.tile_info = reinterpret_cast<int2 *>(scratch + L.tile_info);
     sc.band = L.NT >= 64 ? 1 : 0;  // Cfg<DOWN, NT>::STAGED
     sc.dst_row = reinterpret_cast<int32_t *>(scratch + L.dst_row);
     return sc;
 }
 
-cudaError_t launch_quant_scatter_pad(const uint16_t *x, int T, int d, int k, const int32_t *inv, const float *topk_w,
-                                     const FfnLayout &L, char *scratch, cudaStream_t st)
+cudaError_t launch_quant_scatter_pad(const uint16_t *x, int T, int d, int k, int E, int I, const int32_t *inv,
+                                     const float *topk_w, const FfnLayout &L, char *scratch, cudaStream_t st)
 {
     const int64_t nunits = int64_t(T) * ceil_div(k, SCATTER_KG) * (d / 32);
     if (nunits == 0) return cudaSuccess;
     const int grid = int(ceil_div(nunits, 128) < 152 * 32 ? ceil_div(nunits, 128) : 152 * 32);
     {
-        const cudaError_t le_ = launch_pdl(k_quant_scatter_pad, dim3(grid), dim3(128), 0, st, x, nunits, d, k, reinterpret_cast<const int32_t *>(scratch + L.dst_row), inv, topk_w, reinterpret_cast<uint8_t *>(scratch + L.xq), reinterpret_cast<uint8_t *>(scratch + L.xs), reinterpret_cast<float *>(scratch + L.w_sorted));
+        const cudaError_t le_ = launch_pdl(k_quant_scatter_pad, dim3(grid), dim3(128), 0, st, x, nunits, d, k, reinterpret_cast<const int32_t *>(scratch + L.dst_row), inv, topk_w, reinterpret_cast<uint8_t *>(scratch + L.xq), reinterpret_cast<uint8_t *>(scratch + L.xs), reinterpret_cast<float *>(scratch + L.w_sorted), ffn_sched(L, d, I, scratch), E);
         if (le_ != cudaSuccess) return le_;
     }
     return cudaGetLastError();

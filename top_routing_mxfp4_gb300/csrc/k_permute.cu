@@ -77,7 +77,7 @@ __device__ void block_scan(const int32_t *v, int n, int32_t *out, int32_t *warp_
 
 // The FFN schedule from per-expert counts (shared memory, E entries):
 // token tiles per expert, exclusive scan, slot rows, work-item starts and the
-// work-item tables.
+// expert of each token tile.
 template <int NTHREADS>
 __device__ void ffn_schedule_from_counts(const int32_t *cnt_s, int E, const FfnSched &sc, int32_t *tmp_s,
                                          int32_t *scan_s, int32_t *warp_tot)
@@ -90,7 +90,7 @@ __device__ void ffn_schedule_from_counts(const int32_t *cnt_s, int E, const FfnS
         sc.tiles_gu[e] = scan_s[e] * sc.MT_gu;
         sc.tiles_dn[e] = scan_s[e] * sc.MT_dn;
     }
-    fill_item_tables(scan_s, E, sc, NTHREADS);
+    fill_tile_info(scan_s, E, sc, NTHREADS);
 }
 
 __device__ __forceinline__ int32_t padded_row(int32_t pos, int32_t off_e, int32_t pad_e, int NT, int SLOT)

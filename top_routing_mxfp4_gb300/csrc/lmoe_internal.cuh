@@ -149,49 +149,59 @@ cudaError_t launch_route(const uint16_t *x, const uint16_t *Wr3, const float *bi
 
 // Optional by-products of the permute for the expert GEMMs: per expert the
 // first slot row in the padded token layout (pad_off, E+1) and the first work
-// item of each GEMM (tiles_gu / tiles_dn, E+1), the work-item tables of the
-// two GEMMs (items_gu / items_dn, see fill_item_tables), and per pair p its
-// padded token row (dst_row, T*k).  pad_off == nullptr disables them.
+// item of each GEMM (tiles_gu / tiles_dn, E+1), the expert of each token tile
+// (tile_info; the activation scatter turns it into the GEMMs' work-item
+// tables items_gu / items_dn), and per pair p its padded token row (dst_row,
+// T*k).  pad_off == nullptr disables them.
 struct FfnSched {
     int NT = 0, SLOT = 0, MT_gu = 0, MT_dn = 0;
     int band = 0;  // the down GEMM runs its items in two output-column bands
     int32_t *pad_off = nullptr, *tiles_gu = nullptr, *tiles_dn = nullptr, *dst_row = nullptr;
     int2 *items_gu = nullptr, *items_dn = nullptr;
-    int32_t *tile_e = nullptr;  // expert of each token tile (scratch of fill_item_tables)
+    int2 *tile_info = nullptr;  // per token tile: {expert, token tile within the expert}
 };
 
 // Work-item tables of the two expert GEMMs, in execution order: entry i is
 // item i as {expert | weight tile << 16, token tile within the expert}.
-// `scan` holds the token tiles before each expert (E + 1 entries, in shared
-// memory).  gate/up: items in (token tile, weight tile) order, weight tile
-// fastest.  down: the same, or with `band`, every item of the first half of
-// the weight tiles before the second half (each half in that order), so that
-// only half of the per-token output rows take reductions at a time.  Called
-// by every thread of the block: the expert of each token tile goes to
-// sc.tile_e first, then consecutive threads write consecutive entries.
-__device__ __forceinline__ void fill_item_tables(const int32_t *scan, int E, const FfnSched &sc, int nthreads)
+// gate/up: items in (token tile, weight tile) order, weight tile fastest.
+// down: the same, or with `band`, every item of the first half of the weight
+// tiles before the second half (each half in that order), so that only half
+// of the per-token output rows take reductions at a time.
+// Two steps: tile_info[R] = {expert, token tile within the expert} for every
+// token tile R (from the scan of token tiles per expert, E + 1 entries; one
+// block), then any grid writes the entries, consecutive threads consecutive
+// entries (the table sizes are tiles_gu[E] and tiles_dn[E]).
+__device__ __forceinline__ void fill_tile_info(const int32_t *scan, int E, const FfnSched &sc, int nthreads)
 {
-    const int TT = scan[E];
     for (int e = threadIdx.x; e < E; e += nthreads)
-        for (int R = scan[e]; R < scan[e + 1]; ++R) sc.tile_e[R] = e;
-    __syncthreads();
+        for (int R = scan[e]; R < scan[e + 1]; ++R) sc.tile_info[R] = make_int2(e, R - scan[e]);
+}
+// Entries [g0, n_gu + n_dn) with stride `step` (gate/up entries first).
+__device__ __forceinline__ void fill_item_entries(const FfnSched &sc, int n_gu, int n_dn, int64_t g0, int64_t step)
+{
+    const int TT = n_gu / sc.MT_gu;
     const int MT0 = sc.band ? (sc.MT_dn + 1) / 2 : sc.MT_dn, MT1 = sc.MT_dn - MT0;
-    const int n_gu = TT * sc.MT_gu, n_dn0 = TT * MT0, n_dn = TT * sc.MT_dn;
-    for (int it = threadIdx.x; it < n_gu; it += nthreads) {
-        const int R = it / sc.MT_gu, m = it - R * sc.MT_gu, e = sc.tile_e[R];
-        sc.items_gu[it] = make_int2(e | (m << 16), R - scan[e]);
-    }
-    for (int it = threadIdx.x; it < n_dn; it += nthreads) {
+    const int n_dn0 = TT * MT0;
+    for (int64_t g = g0; g < int64_t(n_gu) + n_dn; g += step) {
         int R, m;
-        if (it < n_dn0) {
-            R = it / MT0;
-            m = it - R * MT0;
+        int2 *dst;
+        if (g < n_gu) {
+            R = int(g) / sc.MT_gu;
+            m = int(g) - R * sc.MT_gu;
+            dst = sc.items_gu + g;
         } else {
-            R = (it - n_dn0) / MT1;
-            m = MT0 + (it - n_dn0 - R * MT1);
+            const int it = int(g - n_gu);
+            if (it < n_dn0) {
+                R = it / MT0;
+                m = it - R * MT0;
+            } else {
+                R = (it - n_dn0) / MT1;
+                m = MT0 + (it - n_dn0 - R * MT1);
+            }
+            dst = sc.items_dn + it;
         }
-        const int e = sc.tile_e[R];
-        sc.items_dn[it] = make_int2(e | (m << 16), R - scan[e]);
+        const int2 ti = sc.tile_info[R];
+        *dst = make_int2(ti.x | (m << 16), ti.y);
     }
 }
 size_t permute_scratch_bytes(int64_t P, int E);
@@ -205,7 +215,7 @@ cudaError_t launch_permute(const int32_t *idx, int64_t P, int E, int32_t *counts
 struct FfnLayout {
     int NT, SLOT;      // token tile and slot rows
     int64_t rows;      // padded token rows reserved
-    size_t pad_off, tiles_gu, tiles_dn, items_gu, items_dn, tile_e, xq, xs, hq, hs, hs_bytes, w_sorted, dst_row,
+    size_t pad_off, tiles_gu, tiles_dn, items_gu, items_dn, tile_info, xq, xs, hq, hs, hs_bytes, w_sorted, dst_row,
         total;  // byte offsets / sizes
     bool fused;  // large token tiles: the down GEMM can accumulate into the per-token output (FfnArgs::yacc)
 };
@@ -227,8 +237,9 @@ cudaError_t launch_ffn_schedule(const int32_t *offsets, int E, int d, int I, con
                                 cudaStream_t st);
 // bf16 x[T][d] -> MXFP8 rows at each routed pair's padded row (dst_row from
 // the permute); also the gate weights in permuted order.
-cudaError_t launch_quant_scatter_pad(const uint16_t *x, int T, int d, int k, const int32_t *inv, const float *topk_w,
-                                     const FfnLayout &L, char *scratch, cudaStream_t st);
+// (also writes the expert GEMMs' work-item tables from the permute's tile_info)
+cudaError_t launch_quant_scatter_pad(const uint16_t *x, int T, int d, int k, int E, int I, const int32_t *inv,
+                                     const float *topk_w, const FfnLayout &L, char *scratch, cudaStream_t st);
 // MXFP8 rows in token order -> padded layout (row q of perm takes token perm[q]/k)
 cudaError_t launch_gather_pad(const uint8_t *xq, const uint8_t *xs, int T, int d, int k, int E, const int32_t *offsets,
                               const int32_t *perm, const float *topk_w, const FfnLayout &L, char *scratch,
