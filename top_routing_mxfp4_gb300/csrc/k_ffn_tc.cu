@@ -670,9 +670,14 @@ __global__ void k_quant_scatter_pad(const uint16_t *__restrict__ x, int64_t nuni
                       int64_t(gridDim.x) * blockDim.x);
     const int nb = d / 32, KC = d / 128;
     const int ng = (k + SCATTER_KG - 1) / SCATTER_KG;
-    for (int64_t g = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; g < nunits; g += int64_t(gridDim.x) * blockDim.x) {
-        const int64_t tg = g / nb;  // t * ng + group
-        const int b = int(g - tg * nb);
+    // unit g = half h (16 elements) of block b: lanes 2i and 2i+1 share a
+    // block (its amax by one shuffle), and a warp's store to a destination
+    // row is 512 contiguous bytes, 16 per lane
+    for (int64_t g = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; g < 2 * nunits; g += int64_t(gridDim.x) * blockDim.x) {
+        const int h = int(g & 1);
+        const int64_t gb = g >> 1;
+        const int64_t tg = gb / nb;  // t * ng + group
+        const int b = int(gb - tg * nb);
         const int64_t t = tg / ng;
         const int j0 = int(tg - t * ng) * SCATTER_KG;
         const int nj = min(SCATTER_KG, k - j0);
@@ -681,43 +686,45 @@ __global__ void k_quant_scatter_pad(const uint16_t *__restrict__ x, int64_t nuni
         int32_t rows[SCATTER_KG];
 #pragma unroll
         for (int j = 0; j < SCATTER_KG; ++j) rows[j] = j < nj ? __ldg(dst_row + p0 + j) : 0;
-        const uint4 *src = reinterpret_cast<const uint4 *>(x + t * d + b * 32);
-        uint4 raw[4];
+        const uint4 *src = reinterpret_cast<const uint4 *>(x + t * d + b * 32 + h * 16);
+        uint4 raw[2];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) raw[i] = __ldg(src + i);
+        for (int i = 0; i < 2; ++i) raw[i] = __ldg(src + i);
         const uint32_t *rw = reinterpret_cast<const uint32_t *>(raw);
-        float v[32];
+        float v[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
+        for (int i = 0; i < 8; ++i) {
             v[2 * i] = __uint_as_float(rw[i] << 16);
             v[2 * i + 1] = __uint_as_float(rw[i] & 0xFFFF0000u);
         }
         uint32_t amax = 0;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) amax = max(amax, __float_as_uint(v[i]) & 0x7FFFFFFFu);
+        for (int i = 0; i < 16; ++i) amax = max(amax, __float_as_uint(v[i]) & 0x7FFFFFFFu);
+        // pairs of lanes are wholly active or inactive (2 * nunits is even and
+        // every thread's start is even)
+        const unsigned mask = __activemask();
+        amax = max(amax, __shfl_xor_sync(mask, amax, 1));
         const uint32_t sb = mx_scale_byte(__uint_as_float(amax), 8);
         const float iv = mx_inv_scale(sb);
-        uint32_t c[8];
+        uint32_t c[4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) c[i] = e4m3x4(v[4 * i] * iv, v[4 * i + 1] * iv, v[4 * i + 2] * iv, v[4 * i + 3] * iv);
+        for (int i = 0; i < 4; ++i) c[i] = e4m3x4(v[4 * i] * iv, v[4 * i + 1] * iv, v[4 * i + 2] * iv, v[4 * i + 3] * iv);
         // the 4 scale bytes of blocks 4c .. 4c+3 (adjacent in the atom) go out as
-        // one 32-bit store by the group's first lane: groups of 4 consecutive
-        // blocks are aligned (d / 32 and every thread's start are multiples of
-        // 4), so a group is either wholly active or wholly inactive
-        const unsigned mask = __activemask();
+        // one 32-bit store by the first lane of the group's 8: groups of 4
+        // consecutive blocks are aligned (d / 32 and every thread's start are
+        // multiples of 4 blocks), so a group is either wholly active or wholly
+        // inactive
         uint32_t sb4 = sb;
-        sb4 |= __shfl_down_sync(mask, sb, 1) << 8;
-        sb4 |= __shfl_down_sync(mask, sb, 2) << 16;
-        sb4 |= __shfl_down_sync(mask, sb, 3) << 24;
+        sb4 |= __shfl_down_sync(mask, sb, 2) << 8;
+        sb4 |= __shfl_down_sync(mask, sb, 4) << 16;
+        sb4 |= __shfl_down_sync(mask, sb, 6) << 24;
 #pragma unroll
         for (int j = 0; j < SCATTER_KG; ++j) {
             if (j >= nj) break;
-            if (b == 0) w_sorted[__ldg(inv + p0 + j)] = __ldg(topk_w + p0 + j);
+            if (b == 0 && h == 0) w_sorted[__ldg(inv + p0 + j)] = __ldg(topk_w + p0 + j);
             const int64_t R = rows[j];
-            uint4 *dst = reinterpret_cast<uint4 *>(xq + R * d + b * 32);
-            dst[0] = make_uint4(c[0], c[1], c[2], c[3]);
-            dst[1] = make_uint4(c[4], c[5], c[6], c[7]);
-            if ((b & 3) == 0) *reinterpret_cast<uint32_t *>(xs + atom_off(R, b, KC)) = sb4;
+            *reinterpret_cast<uint4 *>(xq + R * d + b * 32 + h * 16) = make_uint4(c[0], c[1], c[2], c[3]);
+            if ((b & 3) == 0 && h == 0) *reinterpret_cast<uint32_t *>(xs + atom_off(R, b, KC)) = sb4;
         }
     }
 }
@@ -903,7 +910,7 @@ cudaError_t launch_quant_scatter_pad(const uint16_t *x, int T, int d, int k, int
 {
     const int64_t nunits = int64_t(T) * ceil_div(k, SCATTER_KG) * (d / 32);
     if (nunits == 0) return cudaSuccess;
-    const int grid = int(ceil_div(nunits, 128) < 152 * 32 ? ceil_div(nunits, 128) : 152 * 32);
+    const int grid = int(ceil_div(2 * nunits, 128) < 152 * 32 ? ceil_div(2 * nunits, 128) : 152 * 32);
     {
         const cudaError_t le_ = launch_pdl(k_quant_scatter_pad, dim3(grid), dim3(128), 0, st, x, nunits, d, k, reinterpret_cast<const int32_t *>(scratch + L.dst_row), inv, topk_w, reinterpret_cast<uint8_t *>(scratch + L.xq), reinterpret_cast<uint8_t *>(scratch + L.xs), reinterpret_cast<float *>(scratch + L.w_sorted), ffn_sched(L, d, I, scratch), E);
         if (le_ != cudaSuccess) return le_;
