@@ -84,10 +84,17 @@ def _route_case(lmoe, wl):
     return x, Wr, bias, logits.cpu().numpy(), idx.cpu().numpy(), w.cpu().numpy()
 
 
-@pytest.mark.parametrize("name", ["tiny", "decode", "skewed_small"])
+WIDE = {  # more than 896 experts: 64 logits per lane in the selecting warp
+    "wide_small_T": gen.custom("wide_small_T", T=40, d=512, I=64, E=1536),   # split-K + reduce/top-k
+    "wide_large_T": gen.custom("wide_large_T", T=2048, d=512, I=64, E=1536),  # one-pass GEMM + top-k
+}
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode", "skewed_small", "wide_small_T", "wide_large_T"])
 def test_route_topk_exact_given_logits(cuda_lib, name):
     lmoe = cuda_lib
-    wl = gen.WORKLOADS.get(name) or gen.custom(name, T=512, d=3584, I=512, zipf_s=1.2, zipf_beta=0.18)
+    wl = gen.WORKLOADS.get(name) or WIDE.get(name) or gen.custom(name, T=512, d=3584, I=512, zipf_s=1.2,
+                                                                   zipf_beta=0.18)
     x, Wr, bias, lg, idx, w = _route_case(lmoe, wl)
     # the GPU's fp32 logits are close to the oracle's (fp32 accumulation order only)
     ref = oracle.router_logits(x, Wr, bias)

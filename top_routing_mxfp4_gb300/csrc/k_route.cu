@@ -113,8 +113,8 @@ __global__ void __launch_bounds__(256) k_topk_softmax(const float *__restrict__ 
 // `logits` and kept in shared memory, where warp 0 selects the top-k: one CTA
 // per token (one thread per expert), one launch instead of a reduction pass
 // and a selection pass.
-template <int NV>
-__global__ void __launch_bounds__(1024) k_reduce_topk(const float *__restrict__ part, int KS, int T, int E,
+template <int NV, int NTHREADS>
+__global__ void __launch_bounds__(NTHREADS) k_reduce_topk(const float *__restrict__ part, int KS, int T, int E,
                                                      const float *__restrict__ bias, float *__restrict__ logits, int k,
                                                      int32_t *__restrict__ idx, float *__restrict__ w)
 {
@@ -141,10 +141,15 @@ cudaError_t launch_reduce_topk(const float *part, int KS, int T, int E, const fl
 {
     if (T == 0) return cudaSuccess;
     const size_t smem = size_t(E) * sizeof(float);  // E <= 2048: within the default 48 KB
-    const dim3 block(unsigned(E < 1024 ? round_up(E, 32) : 1024));  // one thread per expert: KS loads each
-    if (E <= 256) return launch_pdl(k_reduce_topk<8>, dim3(T), block, smem, st, part, KS, T, E, bias, logits, k, idx, w);
-    if (E <= 896) return launch_pdl(k_reduce_topk<28>, dim3(T), block, smem, st, part, KS, T, E, bias, logits, k, idx, w);
-    return launch_pdl(k_reduce_topk<64>, dim3(T), block, smem, st, part, KS, T, E, bias, logits, k, idx, w);
+    // one thread per expert (KS loads each) up to 896 experts; beyond, 256
+    // threads, so that the selecting warp may keep its 64 values per lane in
+    // registers (a 1024-thread block allows 64 registers a thread)
+    const dim3 block(unsigned(E <= 896 ? round_up(E, 32) : 256));
+    if (E <= 256)
+        return launch_pdl(k_reduce_topk<8, 1024>, dim3(T), block, smem, st, part, KS, T, E, bias, logits, k, idx, w);
+    if (E <= 896)
+        return launch_pdl(k_reduce_topk<28, 1024>, dim3(T), block, smem, st, part, KS, T, E, bias, logits, k, idx, w);
+    return launch_pdl(k_reduce_topk<64, 256>, dim3(T), block, smem, st, part, KS, T, E, bias, logits, k, idx, w);
 }
 
 cudaError_t launch_topk_softmax(const float *logits, int T, int E, int k, int32_t *idx, float *w, cudaStream_t st)
