@@ -45,6 +45,9 @@ def test_host_side_argument_checks(lib):
         assert ws_size(ctypes.byref(bad)) == 0
     fwd = lib.lmoe_forward
     fwd.restype = ctypes.c_int
+    vp = ctypes.c_void_p
+    fwd.argtypes = [vp, vp, vp, ctypes.POINTER(lmoe.ExpertWeights), ctypes.POINTER(D), vp, vp, vp, vp, vp,
+                    ctypes.c_size_t, vp]
     good = D(8, 512, 896, 16, 64, 1)
     # null weights / null pointers / bad dims are refused before any launch
     assert fwd(None, None, None, None, ctypes.byref(good), None, None, None, None, None, 0, None) == lmoe.ERR_INVALID_ARG
@@ -64,6 +67,39 @@ def test_host_side_argument_checks(lib):
     # empty batch is a no-op
     assert fwd(None, None, None, None, ctypes.byref(D(0, 512, 896, 16, 64, 1)), None, None, None, None, None, 0,
                None) == lmoe.OK
+
+
+def test_expert_ffn_argument_checks(lib):
+    """The stage entry point refuses null or misaligned operands and a short
+    workspace before any launch."""
+    from top_routing_mxfp4_gb300 import lmoe
+    D = lmoe.Dims
+    good = D(64, 3584, 896, 16, 512, 1)
+    size = lib.lmoe_expert_ffn_workspace_size
+    size.restype = ctypes.c_size_t
+    size.argtypes = [ctypes.POINTER(D)]
+    need = size(ctypes.byref(good))
+    assert need > 0
+    # a larger batch never needs less scratch
+    assert size(ctypes.byref(D(8192, 3584, 896, 16, 512, 1))) > need
+    ffn = lib.lmoe_expert_ffn
+    ffn.restype = ctypes.c_int
+    vp = ctypes.c_void_p
+    ffn.argtypes = [vp, vp, ctypes.POINTER(lmoe.ExpertWeights), vp, vp, vp, ctypes.POINTER(D), vp, vp,
+                    ctypes.c_size_t, vp]
+    W = lmoe.ExpertWeights(256, 256, 256, 256, 256, 256, lmoe.LAYOUT_TC)
+    p = ctypes.c_void_p(4096)
+
+    def call(xq=p, xs=p, ws=p, ws_bytes=need, dims=good):
+        return ffn(xq, xs, ctypes.byref(W), p, p, p, ctypes.byref(dims), p, ws, ws_bytes, None)
+
+    assert call(xq=None) == lmoe.ERR_INVALID_ARG
+    assert call(xs=None) == lmoe.ERR_INVALID_ARG
+    assert call(xq=ctypes.c_void_p(4104)) == lmoe.ERR_INVALID_ARG   # codes not 16-byte aligned
+    assert call(xs=ctypes.c_void_p(4100)) == lmoe.ERR_INVALID_ARG   # scales not 16-byte aligned
+    assert call(ws_bytes=need - 1) == lmoe.ERR_WORKSPACE
+    assert call(ws=ctypes.c_void_p(4096 + 16)) == lmoe.ERR_WORKSPACE  # workspace not 256-byte aligned
+    assert call(dims=D(0, 3584, 896, 16, 512, 1)) == lmoe.OK          # empty batch: nothing to do
 
 
 def test_mxfp4_byte_counts(lib):

@@ -219,7 +219,8 @@ lmoe_status lmoe_expert_ffn(const uint8_t *xq, const uint8_t *xs, const lmoe_exp
     lmoe_status a = act_ok(dims);
     if (a != LMOE_OK) return a;
     if (dims->T == 0) return LMOE_OK;
-    if (!xq || !xs || !offsets || !perm || !topk_w || !yp || !aligned(xq, 16) || !aligned(yp, 16))
+    if (!xq || !xs || !offsets || !perm || !topk_w || !yp || !aligned(xq, 16) || !aligned(xs, 16) ||
+        !aligned(yp, 16))
         return LMOE_ERR_INVALID_ARG;
     if (!weights_ok(W)) return LMOE_ERR_INVALID_ARG;
     if (!workspace || ws_bytes < lmoe_expert_ffn_workspace_size(dims) || !aligned(workspace, 256))
