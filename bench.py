@@ -3,7 +3,7 @@
 experts on MXFP4 weights) on GB300, one process per GPU.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload decode|tiny|prefill|skewed] [--no-cpu-baseline]
+                  [--workload decode|decode1|decode16|tiny|prefill|skewed|block] [--no-cpu-baseline]
 
 A step is one lmoe_forward call (route -> permute -> MXFP8 activations ->
 gate/up GEMM + SwiGLU -> down GEMM -> combine) over one batch of seeded
@@ -188,6 +188,7 @@ def cpu_baseline(wl, ntok: int):
 
     import lmoe_inputs as gen
     import oracle
+    ntok = min(ntok, wl.T)
     x = gen.x_bf16(wl, 0, ntok)
     Wr = gen.router_f32(wl)
     bias = gen.router_bias(wl)
@@ -247,6 +248,13 @@ def run_ours(args, ws, rank, local):
         assert layer.device_status() == 0
     counts = torch.bincount(idx.view(-1).long(), minlength=wl.E)
     touched = int((counts > 0).sum())
+    per_expert_w = 3 * wl.I * wl.d * MXFP4_B           # gate + up + down bytes of one expert
+    # Batches whose touched weights could stay in L2 between steps (batch-1
+    # decode: 16 experts = 47 MB) get L2 written over before every step, and
+    # each step is timed alone with events after the flush.
+    l2_bytes = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or 129 * 2 ** 20)
+    flush = touched * per_expert_w < 2 * l2_bytes
+    scrub = torch.empty(2 * l2_bytes // 4, dtype=torch.float32, device=dev) if flush else None
 
     try:
         uuid = str(torch.cuda.get_device_properties(dev).uuid)
@@ -263,13 +271,24 @@ def run_ours(args, ws, rank, local):
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(ws)
     torch.cuda.synchronize()
-    t_start.record(st)
-    for i in range(K):
-        fwd(xin)
-    t_end.record(st)
-    torch.cuda.synchronize()
-    barrier(ws)
-    elapsed_ms = t_start.elapsed_time(t_end)
+    if flush:
+        step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        for a, b in step_ev:
+            scrub.zero_()
+            a.record(st)
+            fwd(xin)
+            b.record(st)
+        torch.cuda.synchronize()
+        barrier(ws)
+        elapsed_ms = sum(a.elapsed_time(b) for a, b in step_ev)
+    else:
+        t_start.record(st)
+        for i in range(K):
+            fwd(xin)
+        t_end.record(st)
+        torch.cuda.synchronize()
+        barrier(ws)
+        elapsed_ms = t_start.elapsed_time(t_end)
     # stage breakdown (and the gate/up GEMM time of the roofline): a second
     # live pass with CUDA events at the stage boundaries
     K2 = min(K, 50)
@@ -279,6 +298,8 @@ def run_ours(args, ws, rank, local):
             e.record(st)
     torch.cuda.synchronize()
     for i in range(K2):
+        if flush:
+            scrub.zero_()
         lmoe.set_stage_events(evs[i])
         fwd(xin)
     torch.cuda.synchronize()
@@ -299,19 +320,30 @@ def run_ours(args, ws, rank, local):
         yh.copy_(out, non_blocking=True)
     torch.cuda.synchronize()
     barrier(ws)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(st)
-    for _ in range(K):
-        xdev.copy_(xh, non_blocking=True)
-        fwd(xdev)
-        yh.copy_(out, non_blocking=True)
-    e1.record(st)
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1), ws, dev)
+    if flush:
+        e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        for a, b in e2e_ev:
+            scrub.zero_()
+            a.record(st)
+            xdev.copy_(xh, non_blocking=True)
+            fwd(xdev)
+            yh.copy_(out, non_blocking=True)
+            b.record(st)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in e2e_ev), ws, dev)
+    else:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        for _ in range(K):
+            xdev.copy_(xh, non_blocking=True)
+            fwd(xdev)
+            yh.copy_(out, non_blocking=True)
+        e1.record(st)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1), ws, dev)
     barrier(ws)
 
     peaks = load_peaks()
-    per_expert_w = 3 * wl.I * wl.d * MXFP4_B           # gate + up + down bytes of one expert
     gateup_bytes = touched * 2 * wl.I * wl.d * MXFP4_B  # weights the gate/up GEMM must stream once
     t_gu = stage_ms["gate_up"] / 1e3
     layer_weight_gbs = touched * per_expert_w / (ms_per_step / 1e3) / 1e9
@@ -348,8 +380,10 @@ def run_ours(args, ws, rank, local):
         "dtype": "mxfp4 x mxfp8 -> f32 acc", "data": "synthetic (seeded counter-based generator)",
         "config": {"workload": wl.name, "T": T, "d": wl.d, "E": wl.E, "k": wl.k, "I": wl.I, "hidden": wl.hidden,
                    "per_gpu_batch_tokens": T, "parallelism": f"replicas x{ws}",
-                   "l2": f"inputs larger than L2: {touched} touched experts = {touched * per_expert_w / 1e9:.2f} GB "
-                         f"of weights read per step (L2 129 MB)"},
+                   "l2": (f"L2 flushed before every step ({scrub.numel() * 4 / 1e6:.0f} MB written, not timed); "
+                          if flush else "inputs larger than L2: ")
+                         + f"{touched} touched experts = {touched * per_expert_w / 1e9:.2f} GB of weights read "
+                           f"per step (L2 {l2_bytes / 2 ** 20:.0f} MB)"},
         "roofline": roofline,
         "stage_ms": stage_ms,
         "stage_ms_note": f"second live pass of {K2} steps with CUDA events at the layer's stage boundaries (the "

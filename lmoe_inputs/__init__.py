@@ -143,6 +143,8 @@ class Workload:
 WORKLOADS = {
     "tiny": Workload("tiny", T=8, d=512, I=64, note="T=8, d=512, I=64"),
     "decode": Workload("decode", T=64, d=3584, I=512, note="T=64 decode-shaped batch"),
+    "decode1": Workload("decode1", T=1, d=3584, I=512, note="T=1 batch-1 decode step (16 experts)"),
+    "decode16": Workload("decode16", T=16, d=3584, I=512, note="T=16 small-batch decode step"),
     "prefill": Workload("prefill", T=8192, d=3584, I=512, note="T=8192 prefill chunk"),
     "skewed": Workload("skewed", T=8192, d=3584, I=512, zipf_s=1.2, zipf_beta=0.18,
                        note="T=8192, Zipf(1.2) popularity bias, beta=0.18"),

@@ -54,6 +54,15 @@ def test_zipf_bias_is_log_popularity():
     np.testing.assert_allclose(b, 0.18 * np.log(p), rtol=1e-6)
 
 
+def test_small_decode_workloads():
+    for name, T in (("decode1", 1), ("decode16", 16)):
+        wl = gen.WORKLOADS[name]
+        assert (wl.T, wl.d, wl.E, wl.k, wl.I) == (T, 3584, 896, 16, 512)
+        assert wl.P <= 4 * wl.E  # 16-token tiles
+        # the same tokens as the first T of the 64-token decode batch (one seed, one stream)
+        np.testing.assert_array_equal(gen.x_bf16(wl), gen.x_bf16(gen.WORKLOADS["decode"], 0, T))
+
+
 def test_workload_shapes():
     wl = gen.WORKLOADS["tiny"]
     assert gen.x_bf16(wl).shape == (8, 512)
