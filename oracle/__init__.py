@@ -17,6 +17,10 @@ itself; the tests named live in tests/test_oracle_pins.py):
   permute                -- numpy stable argsort + invariants
   MoE tokens (sparse)    -- dense brute force over all experts; numpy
                             float64 SwiGLU on decoded weights; k = E = 1 case
+  bf16 rounding          -- torch's fp32 -> bf16 conversion on every kind of
+                            fp32 input (no double rounding possible), typed
+                            ties / carries / overflow / subnormals (golden),
+                            doubles between fp32 neighbours of a midpoint
   linear bf16            -- numpy float64 matmul + bf16 rounding
 """
 from __future__ import annotations
@@ -79,6 +83,7 @@ def _load():
     lib.oracle_expert_ffn_token.argtypes = [vp, ctypes.POINTER(_Experts), i32, i32, i32, vp]
     lib.oracle_moe_dense.argtypes = [vp, vp, vp, ctypes.POINTER(_Experts), i32, i32, i32, i32, i32, vp, i32, vp]
     lib.oracle_linear_bf16.argtypes = [vp, vp, i64, i32, i32, vp]
+    lib.oracle_round_bf16.argtypes = [vp, i64, vp]
     _lib = lib
     return lib
 
@@ -237,6 +242,14 @@ def expert_ffn_token(x_row_bf16, experts: Experts, e: int, d: int, I: int) -> np
     x = _c(x_row_bf16, np.uint16)
     out = np.empty(d, np.float64)
     _load().oracle_expert_ffn_token(_p(x), ctypes.byref(experts.struct), e, d, I, _p(out))
+    return out
+
+
+def round_bf16(v) -> np.ndarray:
+    """bf16 bits of float64 values, rounded once to nearest even."""
+    v = _c(v, np.float64)
+    out = np.empty(v.shape, np.uint16)
+    _load().oracle_round_bf16(_p(v), v.size, _p(out))
     return out
 
 

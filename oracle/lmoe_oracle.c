@@ -140,6 +140,11 @@ static uint16_t double_to_bf16(double v)
     return out;
 }
 
+void oracle_round_bf16(const double *v, int64_t n, uint16_t *out)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = double_to_bf16(v[i]);
+}
+
 void oracle_quant_mxfp4(const float *w, int64_t rows, int K, uint8_t *q, uint8_t *s)
 {
     const int nb = K / 32;

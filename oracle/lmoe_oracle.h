@@ -81,6 +81,11 @@ void oracle_expert_ffn_token(const uint16_t *x_bf16_row, const oracle_experts *W
 void oracle_moe_dense(const uint16_t *x_bf16, const int32_t *idx, const float *w, const oracle_experts *W, int T,
                       int d, int E, int k, int I, const int32_t *tokens, int ntok, double *y_f64);
 
+/* out[i] = bf16 bits of v[i] rounded to nearest even (ties to the even
+ * significand, overflow past the largest finite bf16 to infinity, bf16
+ * subnormals below 2^-126), rounded once from the double value. */
+void oracle_round_bf16(const double *v, int64_t n, uint16_t *out);
+
 /* out[r][n] = bf16( sum_c x[r][c] * W[n][c] ), all bf16 bits, fp64 accumulation. */
 void oracle_linear_bf16(const uint16_t *x, const uint16_t *W, int64_t rows, int K, int N, uint16_t *out);
 

@@ -88,25 +88,6 @@ def bf16_to_f64(b):
     return (np.asarray(b, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
-def f64_to_bf16_exact(v):
-    """bf16 RNE of float64 values directly (no rounding through fp32)."""
-    out = np.empty(np.shape(v), np.uint16)
-    for i, x in enumerate(np.asarray(v, np.float64).ravel()):
-        if x == 0:
-            out.flat[i] = 0x8000 if math.copysign(1, x) < 0 else 0
-            continue
-        m, e = math.frexp(abs(x))
-        ulp = max(e - 1 - 7, -133)
-        q = abs(x) / 2.0 ** ulp
-        fl = math.floor(q)
-        fr = q - fl
-        r = fl + (1 if (fr > 0.5 or (fr == 0.5 and fl % 2 == 1)) else 0)
-        f = np.float32(r * 2.0 ** ulp)
-        b = int(np.array(f, np.float32).view(np.uint32)) >> 16
-        out.flat[i] = b | (0x8000 if x < 0 else 0)
-    return out
-
-
 # ---- codecs ---------------------------------------------------------------------
 
 def test_e2m1_decode_matches_typed_table():
@@ -361,7 +342,7 @@ def test_moe_matches_numpy_restatement():
     ref = np_swiglu_layer(x, idx, w, bank, wl, range(wl.T))
     scale = np.sqrt((ref ** 2).mean(1, keepdims=True))
     assert np.max(np.abs(yf - ref) / scale) < 1e-12
-    np.testing.assert_array_equal(y16, f64_to_bf16_exact(yf))
+    np.testing.assert_array_equal(y16, oracle.round_bf16(yf))
 
 
 def test_single_expert_reduces_to_dense_swiglu_ffn():
@@ -385,6 +366,62 @@ def test_linear_bf16_matches_numpy():
     rng = np.random.default_rng(8)
     x = gen.normal_bf16(0, 90, 0, 6 * 96, 1.0).reshape(6, 96)
     W = gen.normal_bf16(0, 91, 0, 40 * 96, 0.1).reshape(40, 96)
-    ref = f64_to_bf16_exact(bf16_to_f64(x) @ bf16_to_f64(W).T)
+    ref = oracle.round_bf16(bf16_to_f64(x) @ bf16_to_f64(W).T)
     np.testing.assert_array_equal(oracle.linear_bf16(x, W), ref)
     del rng
+
+
+# ---- bf16 rounding of the layer output and the projections ------------------------
+
+def test_round_bf16_typed_cases():
+    """Ties, carries, overflow, subnormals and signed zeros worked out from
+    the bf16 format definition (tests/golden/bf16_rounding.txt), including
+    doubles just off a midpoint that an fp32 pass would turn into a tie."""
+    rows = [l.split() for l in open(os.path.join(GOLDEN, "bf16_rounding.txt"))
+            if l.strip() and not l.startswith("#")]
+    assert len(rows) >= 30
+    v = np.array([float.fromhex(r[0]) for r in rows])
+    want = np.array([int(r[1], 16) for r in rows], np.uint16)
+    got = oracle.round_bf16(v)
+    bad = [(rows[i][0], rows[i][1], f"{got[i]:04x}") for i in np.nonzero(got != want)[0]]
+    assert not bad, bad
+
+
+def test_round_bf16_matches_torch_on_every_kind_of_fp32_input():
+    """On inputs that are fp32 values, rounding the double once equals
+    torch's fp32 -> bf16 conversion (round to nearest even; no double
+    rounding is possible): random bit patterns over the whole finite range,
+    every bf16 midpoint and its fp32 neighbours, fp32 subnormals, +-0."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(2024)
+    pats = [rng.integers(0, 2 ** 32, size=3_000_000, dtype=np.uint64).astype(np.uint32)]
+    b = np.arange(0, 0x10000, dtype=np.uint32)
+    mid = (b << 16) | 0x8000
+    pats += [mid, mid - 1, mid + 1]
+    pats.append(rng.integers(0, 0x800000, size=200_000, dtype=np.uint64).astype(np.uint32))  # subnormals
+    pats.append(np.array([0, 0x80000000, 1, 0x80000001, 0x7F7F7FFF, 0x7F7F8000, 0xFF7F8000], np.uint32))
+    u = np.concatenate(pats)
+    u = u[(u & 0x7F800000) != 0x7F800000]  # finite inputs only
+    f = u.view(np.float32)
+    want = torch.from_numpy(f.copy()).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = oracle.round_bf16(f.astype(np.float64))
+    bad = np.nonzero(got != want)[0]
+    assert bad.size == 0, [(f"{u[i]:08x}", f"{got[i]:04x}", f"{want[i]:04x}") for i in bad[:10]]
+
+
+def test_round_bf16_of_doubles_is_not_rounded_through_fp32():
+    """Doubles strictly between a bf16 midpoint and its fp32 neighbours round
+    to the bf16 value on their own side of the midpoint; a rounding that went
+    through fp32 first would land on the tie and pick the even side for
+    half of them."""
+    rng = np.random.default_rng(7)
+    b = rng.integers(0x0080, 0x7F7F, size=20_000).astype(np.uint32)  # positive normal bf16, not the largest
+    lo = ((b << 16)).view(np.float32).astype(np.float64)
+    hi = (((b + 1) << 16)).view(np.float32).astype(np.float64)
+    mid = (lo + hi) / 2
+    tiny = (hi - lo) * 2.0 ** -30  # far below an fp32 ulp there
+    up = oracle.round_bf16(mid + tiny)
+    down = oracle.round_bf16(mid - tiny)
+    np.testing.assert_array_equal(up, (b + 1).astype(np.uint16))
+    np.testing.assert_array_equal(down, b.astype(np.uint16))
+    np.testing.assert_array_equal(oracle.round_bf16(-(mid + tiny)), ((b + 1) | 0x8000).astype(np.uint16))
