@@ -170,7 +170,8 @@ lmoe_status lmoe_permute(const int32_t *topk_idx, const lmoe_dims *dims, int32_t
  * work is enqueued.  Outputs and their meaning are those of lmoe_permute.
  * `device_status` (nullable, a device int32) receives the device-side check
  * result (LMOE_OK or LMOE_ERR_DEVICE_CHECK).  The first call on a device
- * looks up the array's device address; make it before any stream capture.
+ * looks up the array's device address (the first call after a device reset
+ * looks it up again, in the new context); make it before any stream capture.
  * All calls share the array, so calls that overlap on the GPU race: the
  * caller serialises them.  Nothing is allocated. */
 #define LMOE_PERMUTE_NOALLOC_MAX_PAIRS 524288
@@ -253,6 +254,37 @@ int32_t lmoe_forward_kernel_count(const lmoe_dims *dims);
  * setting is process-wide and not thread-safe; it only adds event records. */
 #define LMOE_NUM_STAGE_EVENTS 7
 lmoe_status lmoe_set_stage_events(void *const *events, int32_t n);
+
+/* ---- diagnostics (used by the parity tests; not needed to run the layer) ---- */
+
+/* Where lmoe_forward keeps the expert GEMMs' MXFP8 operands inside its
+ * workspace, as byte offsets from the workspace start, for these dims:
+ *   xq  [rows][d]  e4m3 codes of x, one padded row per routed pair,
+ *   xs  scale atoms of x: 512 bytes per 128 rows x 4 blocks of 32 along d,
+ *       row R (R = 128*a + 32*j + i) block b at byte ((a*(d/128) + b/4)*512
+ *       + 16*i + 4*j + b%4) (the expert weights' scale layout),
+ *   hq  [rows][I]  e4m3 codes of the gated product h of each pair,
+ *   hs  scale atoms of h (the same layout with roundup(I,128)/128 atoms per
+ *       128 rows),
+ *   dst_row  int32 [T*k]: the padded row of pair p = t*k + j;
+ * rows = padded rows reserved, tile_tokens = tokens per expert-GEMM tile,
+ * slot_rows = rows per tile slot.  Valid after an lmoe_forward call with the
+ * same dims has completed; rows no pair maps to hold no defined data. */
+typedef struct {
+    int64_t xq, xs, hq, hs, dst_row;
+    int64_t rows;
+    int32_t tile_tokens, slot_rows;
+} lmoe_ffn_views;
+lmoe_status lmoe_forward_workspace_views(const lmoe_dims *dims, lmoe_ffn_views *views);
+
+/* When h_f32 is set (device buffer of `bytes` bytes, 16-byte aligned), every
+ * later lmoe_forward / lmoe_expert_ffn call also writes the fp32 value of
+ * each h its gate/up GEMM rounds to MXFP8 at h_f32[R][i] (R the pair's
+ * padded row as in lmoe_ffn_views, I floats per row), so a test can check
+ * the rounding bit for bit.  Calls return LMOE_ERR_INVALID_ARG while the
+ * buffer is smaller than rows * I * 4 bytes.  NULL clears the hook.  The
+ * setting is process-wide and not thread-safe. */
+lmoe_status lmoe_set_h_capture(float *h_f32, size_t bytes);
 
 const char *lmoe_status_string(lmoe_status s);
 

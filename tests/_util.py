@@ -117,16 +117,19 @@ def half_ulp_bf16(v: np.ndarray) -> np.ndarray:
     return 2.0 ** (np.floor(np.log2(a)) - 8)
 
 
-def assert_layer_rows(y_gpu_bf16, y_ref_f64, x_rows, idx_rows, w_rows, ob, d: int, I: int, tol: float):
+def check_layer_rows(y_gpu_bf16, y_ref_f64, x_rows, idx_rows, w_rows, ob, d: int, I: int, tol: float):
     """Layer output rows against the oracle's fp64 values: max|y - y_ref| <=
     tol * rms(y_ref) per row.  The GPU's own final rounding to bf16 (half a
     bf16 ulp of each output) is not the layer's error, and where h sits at an
     MXFP8 boundary both decisions are correct fp32 results: a row over the
     bar passes only if every element is within tol * rms plus its half ulp
-    plus the decision envelope of h.  Returns, per row, the error beyond the
-    output's rounding, max(|y - y_ref| - half ulp(y)) / rms."""
+    plus the decision envelope of h.  Returns (per-row error, rows that
+    passed only through those allowances): the error is measured against the
+    exact value, max|y - y_ref| / rms, and a row uses an allowance when that
+    is above the bar."""
     g, r = bf16_to_f64(y_gpu_bf16), np.asarray(y_ref_f64, np.float64)
     rms = np.maximum(np.sqrt((r ** 2).mean(1)), 1e-30)
+    raw = np.abs(g - r).max(1) / rms
     beyond = np.maximum(np.abs(g - r) - half_ulp_bf16(g), 0.0)
     err = beyond.max(1) / rms
     for n in np.nonzero(err > tol)[0]:
@@ -135,7 +138,63 @@ def assert_layer_rows(y_gpu_bf16, y_ref_f64, x_rows, idx_rows, w_rows, ob, d: in
         assert excess.max() <= 0, (f"row {n}: error {err[n]:.3e} of rms, beyond the bar by "
                                    f"{excess.max() / rms[n]:.3e} of rms after the output's half ulp and the "
                                    f"h decision envelope (envelope max {env.max() / rms[n]:.3e} of rms)")
-    return err
+    return raw, int((raw > tol).sum())
+
+
+def assert_layer_rows(y_gpu_bf16, y_ref_f64, x_rows, idx_rows, w_rows, ob, d: int, I: int, tol: float):
+    """check_layer_rows; returns, per row, the error beyond the output's
+    rounding, max(|y - y_ref| - half ulp(y)) / rms (0 where no allowance was
+    needed to pass)."""
+    check_layer_rows(y_gpu_bf16, y_ref_f64, x_rows, idx_rows, w_rows, ob, d, I, tol)
+    g, r = bf16_to_f64(y_gpu_bf16), np.asarray(y_ref_f64, np.float64)
+    rms = np.maximum(np.sqrt((r ** 2).mean(1)), 1e-30)
+    return np.maximum(np.abs(g - r) - half_ulp_bf16(g), 0.0).max(1) / rms
+
+
+def allowance_budget(rows: int) -> int:
+    """Rows a GPU test may pass only through the rounding allowances: 1 % of
+    the rows checked (at least one)."""
+    return max(1, rows // 100)
+
+
+def _threads() -> int:
+    import os
+    return max(1, min(32, os.cpu_count() or 1))
+
+
+def quantize_experts_parallel(wl, experts):
+    """oracle.quantize_experts for the listed experts, the experts spread over
+    threads (the oracle's C calls release the interpreter lock)."""
+    import concurrent.futures as cf
+
+    import oracle
+    E, I, d = wl.E, wl.I, wl.d
+    gq = np.zeros((E, I, d // 2), np.uint8); gs = np.zeros((E, I, d // 32), np.uint8)
+    uq = np.zeros((E, I, d // 2), np.uint8); us = np.zeros((E, I, d // 32), np.uint8)
+    dq = np.zeros((E, d, I // 2), np.uint8); ds = np.zeros((E, d, I // 32), np.uint8)
+
+    def one(e):
+        gq[e], gs[e] = oracle.quant_mxfp4(gen.expert_f32(wl, "gate", e, e + 1)[0])
+        uq[e], us[e] = oracle.quant_mxfp4(gen.expert_f32(wl, "up", e, e + 1)[0])
+        dq[e], ds[e] = oracle.quant_mxfp4(gen.expert_f32(wl, "down", e, e + 1)[0])
+
+    with cf.ThreadPoolExecutor(_threads()) as ex:
+        list(ex.map(one, sorted(set(int(e) for e in experts))))
+    return oracle.Experts(gq, gs, uq, us, dq, ds)
+
+
+def oracle_rows_parallel(x_bf16, idx, w, ob, d: int, E: int, I: int, tokens):
+    """oracle.moe_tokens (fp64 outputs) on the listed tokens, in chunks of
+    tokens over threads; rows in the order of `tokens`."""
+    import concurrent.futures as cf
+
+    import oracle
+    tokens = np.asarray(tokens, np.int32)
+    chunks = [c for c in np.array_split(tokens, min(len(tokens), 4 * _threads())) if c.size]
+    with cf.ThreadPoolExecutor(_threads()) as ex:
+        parts = list(ex.map(lambda c: oracle.moe_tokens(x_bf16, idx, w, ob, d, E, I, tokens=c, want_f64=True)[1],
+                            chunks))
+    return np.concatenate(parts, 0)
 
 
 def pair_row_err(yp_row, ref_row, x_row, e: int, wj: float, ob, d: int, I: int, tol: float) -> float:

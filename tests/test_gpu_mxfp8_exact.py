@@ -1,0 +1,90 @@
+"""Every MXFP8 quantisation on lmoe_forward's path, bit for bit.
+
+The layer rounds two activations to MXFP8 before the tensor cores read them
+(e4m3 codes, one E8M0 scale per 32 elements): the latent x of every routed
+pair, written by the activation scatter into the expert GEMM's padded token
+rows, and the gated product h = silu(g) * u, rounded in the gate/up GEMM's
+epilogue.  Both are read back from the forward's workspace (its layout comes
+from lmoe_forward_workspace_views) and compared, every code and every scale
+byte of every routed pair, with the oracle's quantisation of the same
+values: the bf16 x of the pair's token, and the fp32 h the epilogue rounded
+(captured with lmoe_set_h_capture).  The three batch sizes run the three
+token-tile shapes of the expert GEMMs (16, 32 and 96 tokens per tile), whose
+epilogues store h differently.
+"""
+import numpy as np
+import pytest
+import torch
+
+import lmoe_inputs as gen
+import oracle
+from _util import device_bank, to_dev_bf16
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+_bank = {}
+
+
+def _get_bank(wl):
+    key = (wl.E, wl.d, wl.I, wl.seed)
+    if key not in _bank:
+        _bank.clear()
+        _bank[key] = device_bank(wl, DEV)
+    return _bank[key]
+
+
+def atom_scales(atoms: torch.Tensor, R: torch.Tensor, nblocks: int) -> np.ndarray:
+    """Scale bytes [len(R), nblocks] of padded rows R from 512-byte atoms of
+    128 rows x 4 blocks (row 128a + 32j + i, block b at byte
+    (a * KC + b / 4) * 512 + 16 i + 4 j + b % 4, KC = ceil(nblocks / 4))."""
+    KC = -(-nblocks // 4)
+    b = torch.arange(nblocks, device=R.device, dtype=torch.int64)[None, :]
+    r = R.to(torch.int64)[:, None]
+    off = ((r >> 7) * KC + (b >> 2)) * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4 + (b & 3)
+    return atoms[off].cpu().numpy()
+
+
+@pytest.mark.parametrize("T,tile", [(64, 16), (512, 32), (2048, 96)])
+def test_forward_mxfp8_operands_bit_exact(cuda_lib, T, tile):
+    lmoe = cuda_lib
+    wl = gen.custom(f"mxfp8_exact_{T}", T=T, d=3584, I=512)
+    d, I, k, E = wl.d, wl.I, wl.k, wl.E
+    bank = _get_bank(wl)
+    layer = lmoe.Layer(torch.from_numpy(gen.router_f32(wl)).to(DEV), bank, k=k)
+    v = lmoe.forward_workspace_views(T, d, E, k, I)
+    assert v.tile_tokens == tile
+    x = gen.x_bf16(wl)
+    idx = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    hcap = torch.full((v.rows * I,), float("nan"), dtype=torch.float32, device=DEV)
+    lmoe.set_h_capture(hcap)
+    try:
+        layer.forward(to_dev_bf16(x, DEV), topk_idx=idx)
+        torch.cuda.synchronize()
+    finally:
+        lmoe.set_h_capture(None)
+    assert layer.device_status() == 0
+    ws = layer._ws
+    P = T * k
+    R = ws[v.dst_row:v.dst_row + 4 * P].view(torch.int32).to(torch.int64)
+    Rh = R.cpu().numpy()
+    assert Rh.min() >= 0 and Rh.max() < v.rows and np.unique(Rh).size == P
+    # x: every routed pair's padded row holds MXFP8(x[t]) of its token t = p / k
+    xq = ws[v.xq:v.xq + v.rows * d].view(v.rows, d)[R].cpu().numpy()
+    xs = atom_scales(ws[v.xs:v.hq], R, d // 32)
+    rq, rs = oracle.quant_mxfp8(x)
+    tok = np.arange(P) // k
+    bad = np.nonzero((xq != rq[tok]).any(1) | (xs != rs[tok]).any(1))[0]
+    assert bad.size == 0, f"{bad.size} of {P} pairs' x rows differ from the oracle (first pair {bad[:1]})"
+    # h: every pair's codes and scales equal the oracle's rounding of the fp32 h the GEMM produced
+    h = hcap.view(v.rows, I)[R].cpu().numpy().astype(np.float64)
+    assert np.isfinite(h).all(), "the epilogue did not capture h for every routed pair"
+    hq = ws[v.hq:v.hq + v.rows * I].view(v.rows, I)[R].cpu().numpy()
+    hs = atom_scales(ws[v.hs:], R, I // 32)
+    hrq, hrs = oracle.quant_mxfp8_f64(h)
+    bad_q = np.nonzero((hq != hrq).any(1))[0]
+    bad_s = np.nonzero((hs != hrs).any(1))[0]
+    assert bad_q.size == 0 and bad_s.size == 0, (f"h of {bad_q.size} pairs (codes) / {bad_s.size} pairs (scales) of "
+                                                 f"{P} differ from the oracle's MXFP8 of the same fp32 values")
+    print(f"T={T}: {P} pairs, x {P * d} codes + {P * d // 32} scales, h {P * I} codes + {P * I // 32} scales "
+          f"bit-exact")

@@ -117,3 +117,18 @@ def test_planted_mistakes_fail(case, mistake):
     assert row_rel_err(bad, _to_bf16(y64)).max() > TOL
     with pytest.raises(AssertionError):
         assert_layer_rows(bad, y64, x, idx, w, ob, wl.d, wl.I, TOL)
+
+
+def test_threaded_oracle_helpers_equal_single_calls():
+    """The GPU tests spread oracle calls over threads; the results are the
+    single-threaded oracle's, bit for bit."""
+    from _util import oracle_rows_parallel, quantize_experts_parallel
+    wl = gen.custom("threads", T=24, d=512, I=64)
+    x = gen.x_bf16(wl)
+    idx, w = oracle.topk_softmax(oracle.router_logits(x, gen.router_f32(wl)), wl.k)
+    ob1 = oracle.quantize_experts(wl, experts=np.unique(idx))
+    ob2 = quantize_experts_parallel(wl, np.unique(idx))
+    assert all(np.array_equal(a, b) for a, b in zip(ob1.arrays, ob2.arrays))
+    tok = np.arange(1, 24, 2)
+    _, y1 = oracle.moe_tokens(x, idx, w, ob1, wl.d, wl.E, wl.I, tokens=tok, want_f64=True)
+    np.testing.assert_array_equal(oracle_rows_parallel(x, idx, w, ob2, wl.d, wl.E, wl.I, tok), y1)

@@ -11,6 +11,8 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
+
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
 
@@ -23,15 +25,42 @@ def _routing(T, E, k, seed):
 
 @pytest.mark.parametrize("T,E,k", [(64, 896, 16), (3000, 896, 16), (32768, 896, 16), (700, 2048, 8)])
 def test_permute_noalloc_matches_permute_twice(cuda_lib, T, E, k):
+    """Both entry points against each other and against the oracle's counting
+    sort (the 32768-token case is the block workload's 524,288 pairs)."""
     lmoe = cuda_lib
     for call in range(2):  # two calls in a row, different inputs
-        idx = torch.from_numpy(_routing(T, E, k, seed=T + call)).to(DEV)
+        idx_h = _routing(T, E, k, seed=T + call)
+        idx = torch.from_numpy(idx_h).to(DEV)
         ref = lmoe.permute(idx, E)[:4]
         got = lmoe.permute_noalloc(idx, E)
         torch.cuda.synchronize()
         for a, b in zip(ref, got[:4]):
             assert torch.equal(a, b)
         assert int(got[4].item()) == lmoe.OK
+        for a, b in zip(oracle.permute(idx_h, E), got[:4]):
+            np.testing.assert_array_equal(b.cpu().numpy(), a)
+
+
+def test_permute_noalloc_into_preallocated_outputs_twice(cuda_lib):
+    """With every output preallocated by the caller the call allocates
+    nothing; two calls in a row into the same tensors, the second on
+    different routing, each equal to the oracle."""
+    lmoe = cuda_lib
+    T, E, k = 1024, 896, 16
+    out = (torch.empty(E, dtype=torch.int32, device=DEV), torch.empty(E + 1, dtype=torch.int32, device=DEV),
+           torch.empty(T * k, dtype=torch.int32, device=DEV), torch.empty(T * k, dtype=torch.int32, device=DEV),
+           torch.empty(1, dtype=torch.int32, device=DEV))
+    for call in range(2):
+        idx_h = _routing(T, E, k, seed=11 + call)
+        got = lmoe.permute_noalloc(torch.from_numpy(idx_h).to(DEV), E, out=out)
+        torch.cuda.synchronize()
+        assert all(a is b for a, b in zip(got, out))
+        assert int(out[4].item()) == lmoe.OK
+        for a, b in zip(oracle.permute(idx_h, E), out[:4]):
+            np.testing.assert_array_equal(b.cpu().numpy(), a)
+    bad = (out[0][:-1],) + out[1:]
+    with pytest.raises(ValueError):
+        lmoe.permute_noalloc(torch.from_numpy(_routing(T, E, k, seed=3)).to(DEV), E, out=bad)
 
 
 def test_permute_noalloc_rejects_oversize_and_flags_bad_ids(cuda_lib):

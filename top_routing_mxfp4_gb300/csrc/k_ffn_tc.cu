@@ -142,6 +142,7 @@ struct GemmArgs {
     const float *w_sorted;  // gate weight of each permuted row q (topk_w[perm[q]])
     uint8_t *hq;    // gate/up out: [rows][Ih] e4m3
     uint8_t *hs;    // gate/up out: scale atoms [rows/128][KCh][512]
+    float *hcap;    // gate/up, diagnostics only (normally null): every fp32 h before its MXFP8 rounding, [rows][Ih]
     float *yp;      // down out: [P][Mtot]
     float *yacc;    // down out when set (fused combine): [T][Mtot] fp32 sums, zeroed by the caller
     const int32_t *perm;  // [P] pair of each permuted row (token = perm / k)
@@ -459,6 +460,7 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
                     for (int j = 0; j < 16; ++j) {
                         const float gv = __uint_as_float(v0[j]), uv = __uint_as_float(v1[j]);
                         const float h = __fdividef(gv, 1.f + __expf(-gv)) * uv;
+                        if (p.hcap && c0 + j < w.n_valid) p.hcap[(Rbase + c0 + j) * p.Ih + row0 + lane] = h;
                         uint32_t amax;
                         asm("redux.sync.max.u32 %0, %1, 0xffffffff;" : "=r"(amax) : "r"(__float_as_uint(h) & 0x7FFFFFFFu));
                         sbv[j] = mx_scale_byte(__uint_as_float(amax), 8);
@@ -969,6 +971,7 @@ cudaError_t launch_expert_gemms(const FfnArgs &a, const FfnLayout &L, char *scra
     g.items = reinterpret_cast<const int2 *>(scratch + L.items_gu);
     g.hq = hq;
     g.hs = hs;
+    g.hcap = a.hcap;
     g.Mtot = a.I;
     g.MTA = int(ceil_div(a.I, 128));
     g.KC = a.d / 128;
@@ -988,6 +991,7 @@ cudaError_t launch_expert_gemms(const FfnArgs &a, const FfnLayout &L, char *scra
     g.sfb = hs;
     g.tiles = reinterpret_cast<const int32_t *>(scratch + L.tiles_dn);
     g.items = reinterpret_cast<const int2 *>(scratch + L.items_dn);
+    g.hcap = nullptr;
     g.yp = a.yp;
     g.yacc = a.yacc;
     g.perm = a.perm;

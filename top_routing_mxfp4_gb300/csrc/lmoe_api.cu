@@ -13,6 +13,9 @@ constexpr int32_t kStatusBytes = 256;
 
 cudaEvent_t g_stage_events[LMOE_NUM_STAGE_EVENTS] = {};
 bool g_stage_events_on = false;
+// diagnostics hook (lmoe_set_h_capture): fp32 h of the gate/up epilogue
+float *g_hcap = nullptr;
+size_t g_hcap_bytes = 0;
 
 cudaError_t mark(int i, cudaStream_t st)
 {
@@ -229,6 +232,7 @@ lmoe_status lmoe_expert_ffn(const uint8_t *xq, const uint8_t *xs, const lmoe_exp
     char *ws = static_cast<char *>(workspace);
     char *fs = ws + kStatusBytes;
     const FfnLayout L = ffn_layout(P, dims->d, dims->E, dims->I);
+    if (g_hcap && g_hcap_bytes < size_t(L.rows) * dims->I * sizeof(float)) return LMOE_ERR_INVALID_ARG;
     cudaStream_t st = cudaStream_t(stream);
     cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(int32_t), st);
     if (e == cudaSuccess) e = launch_ffn_schedule(offsets, dims->E, dims->d, dims->I, L, fs, st);
@@ -236,6 +240,7 @@ lmoe_status lmoe_expert_ffn(const uint8_t *xq, const uint8_t *xs, const lmoe_exp
                                                    st);
     if (e != cudaSuccess) return cuda_status(e);
     FfnArgs f{W, offsets, perm, topk_w, int(P), dims->d, dims->E, dims->k, dims->I, yp, nullptr, reinterpret_cast<int32_t *>(ws)};
+    f.hcap = g_hcap;
     return cuda_status(launch_expert_gemms(f, L, fs, st));
 }
 
@@ -279,6 +284,7 @@ lmoe_status lmoe_forward(const uint16_t *x_bf16, const uint16_t *Wr3, const floa
     int32_t *inv = reinterpret_cast<int32_t *>(ws + L.inv);
     char *fs = ws + L.fscratch;
     const FfnLayout FL = ffn_layout(P, d, E, dims->I);
+    if (g_hcap && g_hcap_bytes < size_t(FL.rows) * dims->I * sizeof(float)) return LMOE_ERR_INVALID_ARG;
     float *yp = reinterpret_cast<float *>(ws + L.yp);
     int32_t *status = reinterpret_cast<int32_t *>(ws + L.status);
     // Large batches fuse the combine into the down GEMM: its epilogue adds
@@ -299,6 +305,7 @@ lmoe_status lmoe_forward(const uint16_t *x_bf16, const uint16_t *Wr3, const floa
     if (e == cudaSuccess) e = mark(3, st);
     if (e == cudaSuccess) {
         FfnArgs f{W, offsets, perm, w, int(P), d, E, k, dims->I, yp, yacc, status};
+        f.hcap = g_hcap;
         e = launch_expert_gemms(f, FL, fs, st, g_stage_events_on ? g_stage_events[4] : nullptr);
     }
     if (e == cudaSuccess) e = mark(5, st);
@@ -372,6 +379,30 @@ lmoe_status lmoe_set_stage_events(void *const *events, int32_t n)
         if (!events[i]) return LMOE_ERR_INVALID_ARG;
     for (int i = 0; i < n; ++i) g_stage_events[i] = cudaEvent_t(events[i]);
     g_stage_events_on = true;
+    return LMOE_OK;
+}
+
+lmoe_status lmoe_forward_workspace_views(const lmoe_dims *dims, lmoe_ffn_views *views)
+{
+    if (!dims_ok(dims) || !views) return LMOE_ERR_INVALID_ARG;
+    const FwdLayout L = fwd_layout(dims);
+    const FfnLayout F = ffn_layout(int64_t(dims->T) * dims->k, dims->d, dims->E, dims->I);
+    views->xq = int64_t(L.fscratch + F.xq);
+    views->xs = int64_t(L.fscratch + F.xs);
+    views->hq = int64_t(L.fscratch + F.hq);
+    views->hs = int64_t(L.fscratch + F.hs);
+    views->dst_row = int64_t(L.fscratch + F.dst_row);
+    views->rows = F.rows;
+    views->tile_tokens = F.NT;
+    views->slot_rows = F.SLOT;
+    return LMOE_OK;
+}
+
+lmoe_status lmoe_set_h_capture(float *h_f32, size_t bytes)
+{
+    if (h_f32 && (bytes == 0 || !aligned(h_f32, 16))) return LMOE_ERR_INVALID_ARG;
+    g_hcap = h_f32;
+    g_hcap_bytes = h_f32 ? bytes : 0;
     return LMOE_OK;
 }
 

@@ -231,6 +231,7 @@ struct FfnArgs {
     float *yp;    // [P][d] in permuted order
     float *yacc;  // when set (FfnLayout::fused only): [T][d] fp32 sums over the k pairs instead of yp
     int32_t *status;
+    float *hcap = nullptr;  // diagnostics: fp32 h before its MXFP8 rounding, [FfnLayout::rows][I]
 };
 // slot starts and per-GEMM work-item prefixes from the segment offsets
 cudaError_t launch_ffn_schedule(const int32_t *offsets, int E, int d, int I, const FfnLayout &L, char *scratch,

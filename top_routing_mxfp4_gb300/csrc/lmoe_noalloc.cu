@@ -11,11 +11,14 @@
 // The array below is file-scope device memory, so every GPU that loads the
 // library holds it until the process exits.  Its host-side name is not a
 // device address: the device address is looked up once per device with
-// cudaGetSymbolAddress (the first call on a device does that look-up; make
-// that first call before any stream capture).  All calls share the array and
+// cudaGetSymbolAddress (the first call on a device does that look-up, and
+// the first call after a device reset repeats it; make that call before any
+// stream capture).  All calls share the array and
 // it keeps the last call's contents, so calls that overlap on the GPU (two
 // streams, or two threads) race with each other and must be serialised by the
 // caller.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "lmoe_internal.cuh"
@@ -33,17 +36,39 @@ static __device__ __align__(256) uint8_t g_permute_scratch[kScratchBytes];
 constexpr int kMaxDevices = 64;
 std::mutex g_mutex;
 void *g_scratch_ptr[kMaxDevices] = {};
+CUcontext g_scratch_ctx[kMaxDevices] = {};  // the context the address belongs to
 
-// Device address of the array on the current device (looked up once per device).
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+CtxGetCurrentFn ctx_get_current()
+{
+    static CtxGetCurrentFn fn = nullptr;
+    if (!fn) {
+        cudaDriverEntryPointQueryResult q;
+        void *f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<CtxGetCurrentFn>(f);
+    }
+    return fn;
+}
+
+// Device address of the array on the current device: looked up once per
+// device and context (a device reset makes a new context, in which the
+// module may be loaded at another address; the look-up is then repeated).
 lmoe_status scratch_on_current_device(uint8_t **out)
 {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return LMOE_ERR_CUDA;
+    CUcontext ctx = nullptr;  // null until the runtime has made the device's context current
+    CtxGetCurrentFn get = ctx_get_current();
+    if (!get || get(&ctx) != CUDA_SUCCESS) return LMOE_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_mutex);
-    if (!g_scratch_ptr[dev]) {
+    if (!g_scratch_ptr[dev] || !ctx || g_scratch_ctx[dev] != ctx) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_permute_scratch) != cudaSuccess || !p) return LMOE_ERR_CUDA;
+        if (get(&ctx) != CUDA_SUCCESS) return LMOE_ERR_CUDA;  // current now
         g_scratch_ptr[dev] = p;
+        g_scratch_ctx[dev] = ctx;
     }
     *out = static_cast<uint8_t *>(g_scratch_ptr[dev]);
     return LMOE_OK;

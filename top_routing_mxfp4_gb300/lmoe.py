@@ -86,6 +86,35 @@ _set_events = _sig("lmoe_set_stage_events", ctypes.c_int, ctypes.POINTER(_vp), _
 _kernel_count = _sig("lmoe_forward_kernel_count", _i32, _DP)
 
 
+class FfnViews(ctypes.Structure):
+    _fields_ = [("xq", _i64), ("xs", _i64), ("hq", _i64), ("hs", _i64), ("dst_row", _i64), ("rows", _i64),
+                ("tile_tokens", _i32), ("slot_rows", _i32)]
+
+
+_ws_views = _sig("lmoe_forward_workspace_views", ctypes.c_int, _DP, ctypes.POINTER(FfnViews))
+_set_hcap = _sig("lmoe_set_h_capture", ctypes.c_int, _vp, _sz)
+
+
+def forward_workspace_views(T: int, d: int, E: int, k: int, I: int) -> FfnViews:
+    """Byte offsets of the expert GEMMs' MXFP8 operands inside lmoe_forward's
+    workspace (diagnostics)."""
+    v = FfnViews()
+    D = dims(T, d, E, k, I)
+    _check(_ws_views(ctypes.byref(D), ctypes.byref(v)), "lmoe_forward_workspace_views")
+    return v
+
+
+def set_h_capture(buf):
+    """Diagnostics: a float32 CUDA tensor that later forward calls fill with
+    the fp32 h values their gate/up GEMM rounds to MXFP8; None clears it."""
+    if buf is None:
+        _check(_set_hcap(None, 0), "lmoe_set_h_capture")
+        return
+    if buf.dtype != torch.float32 or not buf.is_cuda or not buf.is_contiguous():
+        raise ValueError("h capture buffer: contiguous CUDA float32 tensor expected")
+    _check(_set_hcap(_ptr(buf), buf.numel() * 4), "lmoe_set_h_capture")
+
+
 def forward_kernel_count(T: int, d: int, E: int, k: int, I: int) -> int:
     D = dims(T, d, E, k, I)
     return int(_kernel_count(ctypes.byref(D)))
@@ -303,6 +332,11 @@ def permute_noalloc(idx, E: int, out=None, stream=None):
         out = (_empty(E, torch.int32, dev), _empty(E + 1, torch.int32, dev), _empty(T * k, torch.int32, dev),
                _empty(T * k, torch.int32, dev), _empty(1, torch.int32, dev))
     counts, offsets, perm, inv, status = out
+    for t, shape, name in ((counts, (E,), "counts"), (offsets, (E + 1,), "offsets"), (perm, (T * k,), "perm"),
+                           (inv, (T * k,), "inv"), (status, (1,), "device_status")):
+        _need(t, torch.int32, shape, name)
+        if t.device != dev:
+            raise ValueError(f"{name}: on {t.device}, topk_idx on {dev}")
     _check(_permute_noalloc(_ptr(idx), ctypes.byref(D), _ptr(counts), _ptr(offsets), _ptr(perm), _ptr(inv),
                             _ptr(status), _stream(stream)), "lmoe_permute_noalloc")
     return counts, offsets, perm, inv, status
