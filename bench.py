@@ -26,6 +26,8 @@ import subprocess
 import sys
 import time
 
+import numpy as np
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
@@ -45,7 +47,42 @@ def parse():
     ap.add_argument("--workload", default="decode")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-tokens", type=int, default=16)
+    # launcher check without a GPU: the ranks start, meet over gloo and
+    # report; nothing is measured and no bench line is printed
+    ap.add_argument("--launch-selftest", action="store_true", help=argparse.SUPPRESS)
     return ap.parse_args()
+
+
+def spawn_ranks(n: int, argv) -> int:
+    """Run this script as n local ranks (one per GPU) under
+    torch.distributed.run when it was started as a single process with
+    --gpus n > 1; returns the launcher's exit code.  Rank 0 prints the line."""
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__), *argv]
+    return subprocess.call(cmd)
+
+
+def launch_selftest(ws: int, rank: int) -> None:
+    """Ranks meet over gloo, agree on the slowest rank's value with the same
+    barrier / max-over-ranks code the bench uses, and rank 0 reports how many
+    ranks took part."""
+    import torch
+    import torch.distributed as tdist
+    tdist.init_process_group("gloo")
+    try:
+        barrier(ws)
+        slowest = max_over_ranks(float(rank + 1), ws, torch.device("cpu"))
+        seen = torch.tensor([1.0])
+        tdist.all_reduce(seen)
+        if rank == 0:
+            print(json.dumps({"launch_selftest": True, "n_gpus": ws, "ranks_seen": int(seen.item()),
+                              "slowest_rank_value": slowest}), flush=True)
+    finally:
+        tdist.destroy_process_group()
 
 
 def dist_env():
@@ -405,30 +442,57 @@ def run_ours(args, ws, rank, local):
 # ---------------------------------------------------------------------------------
 
 def run_reference(args, ws, rank):
+    """The oracle as it stands on the host cores (one thread), rank 0 only.
+    A step is one token of the workload through the whole layer (routing
+    over all experts, top-k, permute, SwiGLU experts, combine); the tokens
+    cycle over the batch's first REF_TOKENS, whose experts are quantised once
+    before timing (load-time work).  Steps stop early once REF_BUDGET_S of
+    timed CPU work is spent; the line reports the steps actually timed."""
     if rank != 0:
         return
     import lmoe_inputs as gen
     import oracle
-    lmoe_inputs_built = gen.build()
+    gen.build()
     oracle.build()
-    del lmoe_inputs_built
     wl = gen.WORKLOADS[args.workload]
-    ntok = 8
-    for _ in range(args.warmup):
-        pass  # the oracle has no warm-up state; sample preparation happens in cpu_baseline
+    REF_TOKENS, REF_BUDGET_S = 8, 150.0
+    ntok = min(REF_TOKENS, wl.T)
+    x = gen.x_bf16(wl, 0, ntok)
+    Wr = gen.router_f32(wl)
+    bias = gen.router_bias(wl)
+    lg = oracle.router_logits(x, Wr, bias)
+    idx, _ = oracle.topk_softmax(lg, wl.k)
+    bank = oracle.quantize_experts(wl, experts=np.unique(idx))
+
+    def step(i):
+        xt = x[i % ntok:i % ntok + 1]
+        l = oracle.router_logits(xt, Wr, bias)
+        ix, w = oracle.topk_softmax(l, wl.k)
+        oracle.permute(ix, wl.E)
+        oracle.moe_tokens(xt, ix, w, bank, wl.d, wl.E, wl.I)
+
+    warm = min(args.warmup, 3)
+    for i in range(warm):
+        step(i)
     times = []
-    info = None
-    for _ in range(max(1, args.steps if args.steps <= 3 else 3)):
-        info = cpu_baseline(wl, ntok)
-        times.append(ntok / info["value"])
-    dt = statistics.median(times)
-    value = ntok / dt
+    for i in range(args.steps):
+        t0 = time.perf_counter()
+        step(i)
+        times.append(time.perf_counter() - t0)
+        if sum(times) > REF_BUDGET_S:
+            break
+    dt = sum(times) / len(times)
+    value = 1.0 / dt
+    sample = (f"{len(times)} steps of one token each (tokens 0..{ntok - 1} of the {wl.T}-token {wl.name} workload, "
+              f"cycled) through the whole layer: routing over all {wl.E} experts, top-{wl.k}, permute, SwiGLU "
+              f"experts, combine; {sum(times):.1f} s of CPU time")
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": len(times),
-            "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+            "steps_requested": args.steps, "warmup": warm, "warmup_requested": args.warmup,
+            "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic (seeded counter-based generator)",
             "config": {"workload": wl.name, "T": wl.T, "d": wl.d, "E": wl.E, "k": wl.k, "I": wl.I},
             "impl": "reference",
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": info["sample"]},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -436,6 +500,11 @@ def run_reference(args, ws, rank):
 def main():
     args = parse()
     ws, rank, local = dist_env()
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        sys.exit(spawn_ranks(args.gpus, sys.argv[1:]))
+    if args.launch_selftest:
+        launch_selftest(ws, rank)
+        return
     if args.impl == "reference":
         run_reference(args, ws, rank)
         return

@@ -67,3 +67,22 @@ def test_reference_arm_runs_on_rank_zero_only(capsys):
         workload, steps, warmup = "tiny", 1, 0
     bench.run_reference(A(), 2, 1)                  # rank 1 of 2: no work, no output
     assert capsys.readouterr().out == ""
+
+
+def test_bench_gpus_2_starts_two_ranks():
+    """`python bench.py --gpus 2` started as one process re-launches itself
+    as two local ranks (torch.distributed.run); here in the launcher
+    self-test mode, where the ranks meet over gloo without a GPU and rank 0
+    alone prints one line reporting both ranks."""
+    import json
+    import subprocess
+    env = dict(os.environ)
+    for v in ("WORLD_SIZE", "RANK", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT"):
+        env.pop(v, None)
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "2", "--launch-selftest"],
+                       capture_output=True, text=True, timeout=300, env=env, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    rec = json.loads(lines[0])
+    assert rec["n_gpus"] == 2 and rec["ranks_seen"] == 2 and rec["slowest_rank_value"] == 2.0
