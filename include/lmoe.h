@@ -113,6 +113,30 @@ size_t lmoe_mxfp4_bytes(int64_t nmat, int32_t rows, int32_t K, int32_t layout, s
 lmoe_status lmoe_quant_mxfp4(const float *w, int64_t nmat, int32_t rows, int32_t K, uint8_t *q, uint8_t *s,
                              int32_t layout, void *stream);
 
+/* Load-time conversion of an MXFP4 checkpoint ([EP] section 三: the checkpoint
+ * is converted to the hardware's form layer by layer as it loads): nmat
+ * stacked matrices of rows x K (K % 32 == 0) in LMOE_LAYOUT_CANONICAL (codes
+ * q[nmat][rows][K/2], 16-byte aligned; scales s[nmat][rows][K/32]) rewritten
+ * in LMOE_LAYOUT_TC into q_tc / s_tc (sizes from lmoe_mxfp4_bytes; q_tc
+ * 32-byte, s_tc 16-byte aligned).  A byte rearrangement, not a
+ * re-quantisation: every code and scale byte keeps its value, padding codes
+ * and padding scale bytes are written as 0.  The canonical arrays can be a
+ * staging buffer that the caller refills group by group of matrices (e.g.
+ * one layer or one chunk of experts at a time), so the checkpoint never
+ * takes more device memory in canonical form than one group.  Source and
+ * destination must not overlap. */
+lmoe_status lmoe_repack_mxfp4(const uint8_t *q, const uint8_t *s, int64_t nmat, int32_t rows, int32_t K, uint8_t *q_tc,
+                              uint8_t *s_tc, void *stream);
+
+/* Distribution of the E8M0 block scales ([MX] section "精度与速度的平衡":
+ * the per-expert-block scale factors are logged to watch the quantisation):
+ * hist[m][v] (uint32, [nmat][256], overwritten) = how many of matrix m's
+ * rows x K/32 blocks have scale byte v (the block's values were divided by
+ * 2^(v - 127)), read from scales s in the given layout (padding of the
+ * tensor-core layout is not counted). */
+lmoe_status lmoe_mxfp4_scale_histogram(const uint8_t *s, int64_t nmat, int32_t rows, int32_t K, int32_t layout,
+                                       uint32_t *hist, void *stream);
+
 /* ---- stages -------------------------------------------------------------- */
 
 /* MXFP8 quantisation of bf16 rows x[rows][K] (K % 32 == 0): per block of

@@ -123,22 +123,36 @@ def check_layer_rows(y_gpu_bf16, y_ref_f64, x_rows, idx_rows, w_rows, ob, d: int
     bf16 ulp of each output) is not the layer's error, and where h sits at an
     MXFP8 boundary both decisions are correct fp32 results: a row over the
     bar passes only if every element is within tol * rms plus its half ulp
-    plus the decision envelope of h.  Returns (per-row error, rows that
-    passed only through those allowances): the error is measured against the
-    exact value, max|y - y_ref| / rms, and a row uses an allowance when that
-    is above the bar."""
+    plus the decision envelope of h.
+
+    Returns (per-row error beyond the output's rounding, ulp rows, envelope
+    rows): ulp rows fail the plain bar against the oracle's own bf16 output
+    only through elements that differ from it by one bf16 ulp (the exact
+    value sits near a rounding midpoint, so either neighbour is a correct
+    rounding); envelope rows are over the bar even after the output's half
+    ulp and pass only through the h decision envelope."""
+    import oracle
     g, r = bf16_to_f64(y_gpu_bf16), np.asarray(y_ref_f64, np.float64)
     rms = np.maximum(np.sqrt((r ** 2).mean(1)), 1e-30)
-    raw = np.abs(g - r).max(1) / rms
     beyond = np.maximum(np.abs(g - r) - half_ulp_bf16(g), 0.0)
     err = beyond.max(1) / rms
-    for n in np.nonzero(err > tol)[0]:
+    env_rows = np.nonzero(err > tol)[0]
+    for n in env_rows:
         env = h_decision_envelope(x_rows[n], idx_rows[n], w_rows[n], ob, d, I)
         excess = beyond[n] - tol * rms[n] - env
         assert excess.max() <= 0, (f"row {n}: error {err[n]:.3e} of rms, beyond the bar by "
                                    f"{excess.max() / rms[n]:.3e} of rms after the output's half ulp and the "
                                    f"h decision envelope (envelope max {env.max() / rms[n]:.3e} of rms)")
-    return raw, int((raw > tol).sum())
+    ob16 = oracle.round_bf16(r)
+    plain = np.abs(g - bf16_to_f64(ob16)) / rms[:, None]
+    ulp_rows = [n for n in np.nonzero(plain.max(1) > tol)[0] if n not in set(env_rows)]
+    for n in ulp_rows:
+        over = np.nonzero(plain[n] > tol)[0]
+        a = np.asarray(y_gpu_bf16[n][over], np.int64) & 0x7FFF
+        b = ob16[n][over].astype(np.int64) & 0x7FFF
+        same_sign = (np.asarray(y_gpu_bf16[n][over]) >> 15) == (ob16[n][over] >> 15)
+        assert np.all(same_sign & (np.abs(a - b) == 1)), f"row {n}: an output over the bar is not a one-ulp flip"
+    return err, len(ulp_rows), int(env_rows.size)
 
 
 def assert_layer_rows(y_gpu_bf16, y_ref_f64, x_rows, idx_rows, w_rows, ob, d: int, I: int, tol: float):
@@ -151,10 +165,19 @@ def assert_layer_rows(y_gpu_bf16, y_ref_f64, x_rows, idx_rows, w_rows, ob, d: in
     return np.maximum(np.abs(g - r) - half_ulp_bf16(g), 0.0).max(1) / rms
 
 
-def allowance_budget(rows: int) -> int:
-    """Rows a GPU test may pass only through the rounding allowances: 1 % of
+def envelope_budget(rows: int) -> int:
+    """Rows a GPU test may pass only through the h decision envelope: 1 % of
     the rows checked (at least one)."""
     return max(1, rows // 100)
+
+
+def ulp_flip_budget(rows: int) -> int:
+    """Rows a GPU test may fail the plain bar through one-ulp output rounding
+    flips alone: 10 % of the rows (at least one).  An fp32 evaluation of the
+    d = 3584 layer flips about 0.1 % of its outputs against the oracle's
+    bf16, and a flip of an output above about 2x the row RMS is over the
+    1e-2 bar by itself, so a few per cent of rows are expected."""
+    return max(1, rows // 10)
 
 
 def _threads() -> int:

@@ -11,8 +11,8 @@ import torch
 
 import lmoe_inputs as gen
 import oracle
-from _util import (allowance_budget, check_layer_rows, device_bank, from_dev_bf16, oracle_rows_parallel,
-                   quantize_experts_parallel, to_dev_bf16)
+from _util import (check_layer_rows, device_bank, envelope_budget, from_dev_bf16, oracle_rows_parallel,
+                   quantize_experts_parallel, to_dev_bf16, ulp_flip_budget)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -55,10 +55,11 @@ def _check(wl, x, y, idx, w, logits, tokens):
     tok = np.asarray(sorted(set(int(t) for t in tokens)), np.int32)
     ob = quantize_experts_parallel(wl, np.unique(ridx[tok]))
     y64 = oracle_rows_parallel(x, ridx, rw, ob, wl.d, wl.E, wl.I, tok)
-    err, n_allow = check_layer_rows(y[tok], y64, x[tok], ridx[tok], rw[tok], ob, wl.d, wl.I, TOL)
-    print(f"{wl.name}: {tok.size} rows checked, worst {err.max():.3e} of rms, "
-          f"{n_allow} passed only through the rounding allowances")
-    assert n_allow <= allowance_budget(tok.size), f"{n_allow} of {tok.size} rows needed the allowances"
+    err, n_ulp, n_env = check_layer_rows(y[tok], y64, x[tok], ridx[tok], rw[tok], ob, wl.d, wl.I, TOL)
+    print(f"{wl.name}: {tok.size} rows checked, worst {err.max():.3e} of rms beyond the output rounding; "
+          f"{n_ulp} rows over the plain bar by one-ulp output flips only, {n_env} passed through the h envelope")
+    assert n_env <= envelope_budget(tok.size), f"{n_env} of {tok.size} rows needed the h decision envelope"
+    assert n_ulp <= ulp_flip_budget(tok.size), f"{n_ulp} of {tok.size} rows had one-ulp flips over the bar"
     return err
 
 

@@ -132,3 +132,14 @@ def test_threaded_oracle_helpers_equal_single_calls():
     tok = np.arange(1, 24, 2)
     _, y1 = oracle.moe_tokens(x, idx, w, ob1, wl.d, wl.E, wl.I, tokens=tok, want_f64=True)
     np.testing.assert_array_equal(oracle_rows_parallel(x, idx, w, ob2, wl.d, wl.E, wl.I, tok), y1)
+
+
+def test_fp32_evaluation_counts(case):
+    """The counts the GPU tests hold to their budgets: on an independent
+    fp32 evaluation no row needs the h envelope and the one-ulp flip rows
+    stay within 10 %."""
+    from _util import check_layer_rows, envelope_budget, ulp_flip_budget
+    wl, x, idx, w, ob, y64 = case
+    y32 = _fp32_layer(x, idx, w, ob, wl.d, wl.I)
+    err, n_ulp, n_env = check_layer_rows(y32, y64, x, idx, w, ob, wl.d, wl.I, TOL)
+    assert n_env <= envelope_budget(wl.T) and n_ulp <= ulp_flip_budget(wl.T)

@@ -132,6 +132,26 @@ lmoe_status lmoe_quant_mxfp4(const float *w, int64_t nmat, int32_t rows, int32_t
     return cuda_status(launch_quant_mxfp4(w, nmat, rows, K, q, s, layout, cudaStream_t(stream)));
 }
 
+lmoe_status lmoe_repack_mxfp4(const uint8_t *q, const uint8_t *s, int64_t nmat, int32_t rows, int32_t K, uint8_t *q_tc,
+                              uint8_t *s_tc, void *stream)
+{
+    if (nmat < 0 || rows <= 0 || K <= 0 || K % 32 != 0) return LMOE_ERR_INVALID_ARG;
+    if (nmat == 0) return LMOE_OK;
+    if (!q || !s || !q_tc || !s_tc || !aligned(q, 16) || !aligned(q_tc, 32) || !aligned(s_tc, 16))
+        return LMOE_ERR_INVALID_ARG;
+    return cuda_status(launch_repack_mxfp4(q, s, nmat, rows, K, q_tc, s_tc, cudaStream_t(stream)));
+}
+
+lmoe_status lmoe_mxfp4_scale_histogram(const uint8_t *s, int64_t nmat, int32_t rows, int32_t K, int32_t layout,
+                                       uint32_t *hist, void *stream)
+{
+    if (nmat < 0 || nmat > INT32_MAX || rows <= 0 || K <= 0 || K % 32 != 0) return LMOE_ERR_INVALID_ARG;
+    if (layout != LMOE_LAYOUT_CANONICAL && layout != LMOE_LAYOUT_TC) return LMOE_ERR_INVALID_ARG;
+    if (nmat == 0) return LMOE_OK;
+    if (!s || !hist || !aligned(hist, 4)) return LMOE_ERR_INVALID_ARG;
+    return cuda_status(launch_scale_histogram(s, nmat, rows, K, layout, hist, cudaStream_t(stream)));
+}
+
 lmoe_status lmoe_quant_mxfp8(const uint16_t *x_bf16, int64_t rows, int32_t K, uint8_t *q, uint8_t *s, void *stream)
 {
     if (rows < 0 || K <= 0 || K % 32 != 0) return LMOE_ERR_INVALID_ARG;

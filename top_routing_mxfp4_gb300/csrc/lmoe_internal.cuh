@@ -128,6 +128,12 @@ __host__ __device__ constexpr int64_t round_up(int64_t a, int64_t b) { return ce
 cudaError_t launch_quant_mxfp4(const float *w, int64_t nmat, int rows, int K, uint8_t *q, uint8_t *s, int layout,
                                cudaStream_t st);
 cudaError_t launch_quant_mxfp8(const uint16_t *x, int64_t rows, int K, uint8_t *q, uint8_t *s, cudaStream_t st);
+// canonical MXFP4 bytes -> the tensor-core layout (a byte rearrangement)
+cudaError_t launch_repack_mxfp4(const uint8_t *q, const uint8_t *s, int64_t nmat, int rows, int K, uint8_t *q_tc,
+                                uint8_t *s_tc, cudaStream_t st);
+// per-matrix counts of each E8M0 scale byte, hist[nmat][256]
+cudaError_t launch_scale_histogram(const uint8_t *s, int64_t nmat, int rows, int K, int layout, uint32_t *hist,
+                                   cudaStream_t st);
 // Router logits on the tensor cores (fp32 weights split into three bf16 parts).
 size_t router_scratch_bytes(int T, int d, int E);
 int router_kernel_count(int T, int d, int E);  // kernels of launch_route, top-k included

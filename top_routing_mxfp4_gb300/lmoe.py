@@ -62,6 +62,8 @@ _status_string = _sig("lmoe_status_string", ctypes.c_char_p, ctypes.c_int)
 _mxfp4_bytes = _sig("lmoe_mxfp4_bytes", _sz, _i64, _i32, _i32, _i32, ctypes.POINTER(_sz))
 _quant_mxfp4 = _sig("lmoe_quant_mxfp4", ctypes.c_int, _vp, _i64, _i32, _i32, _vp, _vp, _i32, _vp)
 _quant_mxfp8 = _sig("lmoe_quant_mxfp8", ctypes.c_int, _vp, _i64, _i32, _vp, _vp, _vp)
+_repack_mxfp4 = _sig("lmoe_repack_mxfp4", ctypes.c_int, _vp, _vp, _i64, _i32, _i32, _vp, _vp, _vp)
+_scale_hist = _sig("lmoe_mxfp4_scale_histogram", ctypes.c_int, _vp, _i64, _i32, _i32, _i32, _vp, _vp)
 _route = _sig("lmoe_route", ctypes.c_int, _vp, _vp, _vp, _DP, _vp, _vp, _vp, _vp, _sz, _vp)
 _router_bytes = _sig("lmoe_router_prepared_bytes", _sz, _i32, _i32)
 _prepare_router = _sig("lmoe_prepare_router", ctypes.c_int, _vp, _i32, _i32, _vp, _vp)
@@ -204,6 +206,32 @@ def quant_mxfp4(w: torch.Tensor, layout: int = LAYOUT_TC, q=None, s=None, stream
     return q, s
 
 
+def repack_mxfp4(q: torch.Tensor, s: torch.Tensor, nmat: int, rows: int, K: int, q_tc=None, s_tc=None, stream=None):
+    """Canonical MXFP4 bytes (uint8 codes [nmat*rows*K/2], scales
+    [nmat*rows*K/32], flat or shaped) -> the tensor-core layout, as flat uint8
+    tensors (byte rearrangement; lmoe_repack_mxfp4)."""
+    qb, sb = mxfp4_bytes(nmat, rows, K, LAYOUT_TC)
+    _need(q, torch.uint8, q.shape, "q")
+    _need(s, torch.uint8, s.shape, "s")
+    if q.numel() != nmat * rows * K // 2 or s.numel() != nmat * rows * K // 32:
+        raise ValueError("canonical MXFP4 arrays of the wrong size")
+    q_tc = _empty(qb, torch.uint8, q.device) if q_tc is None else q_tc
+    s_tc = _empty(sb, torch.uint8, q.device) if s_tc is None else s_tc
+    if q_tc.numel() < qb or s_tc.numel() < sb:
+        raise ValueError("tensor-core layout destination too small")
+    _check(_repack_mxfp4(_ptr(q), _ptr(s), nmat, rows, K, _ptr(q_tc), _ptr(s_tc), _stream(stream)),
+           "lmoe_repack_mxfp4")
+    return q_tc, s_tc
+
+
+def scale_histogram(s: torch.Tensor, nmat: int, rows: int, K: int, layout: int = LAYOUT_TC, stream=None):
+    """Per-matrix counts of each E8M0 scale byte: int32-viewed uint32 [nmat, 256]."""
+    _need(s, torch.uint8, s.shape, "s")
+    hist = _empty((nmat, 256), torch.int32, s.device)
+    _check(_scale_hist(_ptr(s), nmat, rows, K, layout, _ptr(hist), _stream(stream)), "lmoe_mxfp4_scale_histogram")
+    return hist
+
+
 def quant_mxfp8(x: torch.Tensor, stream=None):
     """bf16 [rows, K] -> (e4m3 codes uint8 [rows, K], scales uint8 [rows, K/32])."""
     rows, K = x.shape
@@ -245,6 +273,24 @@ class ExpertBank:
         q = getattr(self, which + "_q")[e0 * qb1:(e0 + n) * qb1]
         s = getattr(self, which + "_s")[e0 * sb1:(e0 + n) * sb1]
         quant_mxfp4(w.reshape(n, rows, K), LAYOUT_TC, q, s, stream)
+
+    def load_mxfp4(self, which: str, e0: int, q: torch.Tensor, s: torch.Tensor, stream=None):
+        """Copy a checkpoint's canonical MXFP4 matrices of experts [e0, e0 + n)
+        into the bank (lmoe_repack_mxfp4).  q, s: uint8 codes [n, rows, K/2]
+        and scales [n, rows, K/32] on the device, e.g. a staging buffer the
+        caller refills chunk by chunk."""
+        rows, K = (self.I, self.d) if which in ("gate", "up") else (self.d, self.I)
+        n = q.shape[0]
+        qb1, sb1 = mxfp4_bytes(1, rows, K, LAYOUT_TC)
+        qd = getattr(self, which + "_q")[e0 * qb1:(e0 + n) * qb1]
+        sd = getattr(self, which + "_s")[e0 * sb1:(e0 + n) * sb1]
+        repack_mxfp4(q, s, n, rows, K, qd, sd, stream)
+
+    def scale_histograms(self, stream=None):
+        """E8M0 scale-byte counts per expert matrix: {gate, up, down}: [E, 256]."""
+        return {w: scale_histogram(getattr(self, w + "_s"), self.E, *((self.I, self.d) if w != "down" else
+                                                                       (self.d, self.I)), LAYOUT_TC, stream)
+                for w in ("gate", "up", "down")}
 
     def struct(self) -> ExpertWeights:
         if self._struct is None:
