@@ -47,6 +47,8 @@ def parse():
     ap.add_argument("--workload", default="decode")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-tokens", type=int, default=16)
+    # batches of up to this many pairs run the small-batch kernels (default: the library's)
+    ap.add_argument("--small-batch-pairs", type=int, default=None)
     # launcher check without a GPU: the ranks start, meet over gloo and
     # report; nothing is measured and no bench line is printed
     ap.add_argument("--launch-selftest", action="store_true", help=argparse.SUPPRESS)
@@ -257,6 +259,9 @@ def run_ours(args, ws, rank, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     wl = gen.WORKLOADS[args.workload]
+    if args.small_batch_pairs is not None:
+        lmoe.set_small_batch_pairs(args.small_batch_pairs)
+    small = lmoe.forward_workspace_views(wl.T, wl.d, wl.E, wl.k, wl.I).path == 1
     layer, x, xd = setup_layer(wl, dev)
     T = wl.T
     st = torch.cuda.current_stream()
@@ -417,6 +422,7 @@ def run_ours(args, ws, rank, local):
         "dtype": "mxfp4 x mxfp8 -> f32 acc", "data": "synthetic (seeded counter-based generator)",
         "config": {"workload": wl.name, "T": T, "d": wl.d, "E": wl.E, "k": wl.k, "I": wl.I, "hidden": wl.hidden,
                    "per_gpu_batch_tokens": T, "parallelism": f"replicas x{ws}",
+                   "path": "small-batch kernels" if small else "tensor-core kernels",
                    "l2": (f"L2 flushed before every step ({scrub.numel() * 4 / 1e6:.0f} MB written, not timed); "
                           if flush else "inputs larger than L2: ")
                          + f"{touched} touched experts = {touched * per_expert_w / 1e9:.2f} GB of weights read "

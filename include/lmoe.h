@@ -223,8 +223,22 @@ lmoe_status lmoe_combine(const float *yp, const int32_t *inv, const lmoe_dims *d
 
 /* ---- whole layer ----------------------------------------------------------- */
 
-/* Scratch bytes lmoe_forward needs for these dims. */
+/* Scratch bytes lmoe_forward needs for these dims (and the current
+ * small-batch setting below). */
 size_t lmoe_workspace_size(const lmoe_dims *dims);
+
+/* Small batches ([L1] section 二, second layer: batch-1 decode): a batch of
+ * at most `max_pairs` pairs T*k (and at most 8 tokens, 256 pairs) runs
+ * lmoe_forward as three weight-streaming kernels on the CUDA cores (routing
+ * with top-k and the pair lists; gate/up with SwiGLU and MXFP8 of h; down
+ * with the gate weights and the combine) instead of the tensor-core path.
+ * Same contract and roundings; the k terms of a token are summed in a fixed
+ * order (deterministic), but not strictly slot by slot.  0 sends every batch
+ * to the tensor-core path.  Process-wide setting, not thread-safe; the
+ * workspace size of a batch depends on it.  lmoe_small_batch_pairs() reads it. */
+#define LMOE_SMALL_BATCH_PAIRS_DEFAULT 128
+lmoe_status lmoe_set_small_batch_pairs(int32_t max_pairs);
+int32_t lmoe_small_batch_pairs(void);
 
 /* route -> permute -> MXFP8 activations -> expert FFN -> combine, all on
  * `stream`.  Wr3: prepared router weights (lmoe_prepare_router).  y bf16
@@ -298,6 +312,8 @@ typedef struct {
     int64_t xq, xs, hq, hs, dst_row;
     int64_t rows;
     int32_t tile_tokens, slot_rows;
+    int32_t path; /* 0: as above; 1: small-batch path (lmoe_set_small_batch_pairs): xq/xs hold one row per
+                     token t, hq/hs one row per pair p = t*k + j, dst_row = -1, rows = T*k */
 } lmoe_ffn_views;
 lmoe_status lmoe_forward_workspace_views(const lmoe_dims *dims, lmoe_ffn_views *views);
 
@@ -309,6 +325,20 @@ lmoe_status lmoe_forward_workspace_views(const lmoe_dims *dims, lmoe_ffn_views *
  * buffer is smaller than rows * I * 4 bytes.  NULL clears the hook.  The
  * setting is process-wide and not thread-safe. */
 lmoe_status lmoe_set_h_capture(float *h_f32, size_t bytes);
+
+/* Failure-path test of the expert GEMMs' bounded waits.  Every wait on an
+ * mbarrier in the expert GEMMs gives up after a limit of SM clocks (about
+ * 2 s by default), records LMOE_ERR_TIMEOUT in the status word, and the
+ * kernel winds down (an MMA issuer first waits, again bounded, for its MMAs
+ * in flight) and returns.  With stall_first_fill set, the first pipeline
+ * stage of every CTA of the following lmoe_forward / lmoe_expert_ffn calls
+ * is never filled, so those waits run out after wait_limit_cycles; the host
+ * then reads LMOE_ERR_TIMEOUT with lmoe_last_device_status.  (0, 0) restores
+ * the normal behaviour; wait_limit_cycles alone (stall 0) only changes the
+ * limit.  After LMOE_ERR_TIMEOUT the outputs of that call are undefined and
+ * copies it had started may still land in its workspace; the caller should
+ * synchronise and treat the call as failed.  Process-wide, not thread-safe. */
+lmoe_status lmoe_set_wait_test(int32_t stall_first_fill, int64_t wait_limit_cycles);
 
 const char *lmoe_status_string(lmoe_status s);
 

@@ -173,11 +173,12 @@ def envelope_budget(rows: int) -> int:
 
 def ulp_flip_budget(rows: int) -> int:
     """Rows a GPU test may fail the plain bar through one-ulp output rounding
-    flips alone: 10 % of the rows (at least one).  An fp32 evaluation of the
-    d = 3584 layer flips about 0.1 % of its outputs against the oracle's
+    flips alone: 10 % of the rows, and at least three.  An fp32 evaluation of
+    the d = 3584 layer flips about 0.1 % of its outputs against the oracle's
     bf16, and a flip of an output above about 2x the row RMS is over the
-    1e-2 bar by itself, so a few per cent of rows are expected."""
-    return max(1, rows // 10)
+    1e-2 bar by itself, so about 3 % of rows are expected (three or more of
+    16 rows happen about once in a hundred runs at that rate)."""
+    return max(3, rows // 10)
 
 
 def _threads() -> int:

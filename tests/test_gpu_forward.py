@@ -18,6 +18,16 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
 TOL = 1e-2
 
+
+@pytest.fixture(autouse=True)
+def tensor_core_path(cuda_lib):
+    """These tests cover the tensor-core path at every batch size (the
+    small-batch path has its own tests); restored after each test."""
+    old = cuda_lib.small_batch_pairs()
+    cuda_lib.set_small_batch_pairs(0)
+    yield
+    cuda_lib.set_small_batch_pairs(old)
+
 _banks = {}
 
 

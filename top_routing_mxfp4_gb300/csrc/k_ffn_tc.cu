@@ -150,6 +150,8 @@ struct GemmArgs {
     int E, Mtot, MTA, KC, KCh, Ih;  // MTA: 128-row tiles of A
     int stages;  // shared-memory pipeline depth (<= Cfg::MAX_STAGES)
     int32_t *status;
+    long long wait_limit;  // SM clocks a bounded wait may take before it gives up
+    int stall_first_fill;  // failure-path test only: producer 0 withholds each CTA's first stage
 };
 
 template <int MODE, int NT>
@@ -241,7 +243,8 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
     uint64_t *empty = full + S;
     uint64_t *acc_full = empty + S;
     uint64_t *acc_empty = acc_full + C::ACC_STAGES;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_empty + C::ACC_STAGES);
+    uint64_t *drain = acc_empty + C::ACC_STAGES;  // per MMA issuer: its MMAs done (after a timeout)
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 2);
     int32_t *s_pad = reinterpret_cast<int32_t *>(tmem_slot + 4);
     int32_t *s_off = s_pad + (p.E + 1);
 
@@ -267,6 +270,8 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
             mbar_init(&acc_full[a], C::MATS);
             mbar_init(&acc_empty[a], 32 * C::EPI_WARPS);
         }
+        mbar_init(&drain[0], 1);
+        mbar_init(&drain[1], 1);
         mbar_init_fence();
     }
     if (warp == 0 && lane == 0) {
@@ -312,14 +317,16 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
                 const CUtensorMap *tmA = pr == 0 ? &tmA0 : &tmA1;
                 const uint8_t *sfa = pr == 0 ? p.sfa0 : p.sfa1;
                 for (int kc = 0; kc < p.KC; ++kc) {
-                    if (!mbar_wait(&empty[stage], phase ^ 1)) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1, p.wait_limit)) {
                         set_status(p.status, LMOE_ERR_TIMEOUT);
                         ok = false;
                         break;
                     }
                     if (pr == 0) LMOE_TRACE_EV(0, 0x10 | MODE, it, kc);  // producer: stage free
                     uint8_t *sb = stages + stage * C::STAGE_BYTES;
-                    if (pr == 0) {
+                    if (pr == 0 && p.stall_first_fill && it == int(blockIdx.x) && kc == 0) {
+                        // failure-path test: this stage never fills, so every wait on it runs out
+                    } else if (pr == 0) {
                         mbar_arrive_expect_tx(&full[stage], C::TX_BYTES0);
                         tma_load_2d(sb, tmA, kc * 128, arow, &full[stage]);
                         tma_load_2d(sb + C::MATS * C::A_TILE, &tmB, kc * 128, R, &full[stage]);
@@ -358,15 +365,16 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
                 ent = ent_next;
                 ent_next = entry(it + 2 * G);
                 const uint32_t N = uint32_t((w.n_valid + 15) & ~15);
-                if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1)) {
+                if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1, p.wait_limit)) {
                     set_status(p.status, LMOE_ERR_TIMEOUT);
+                    ok = false;
                     break;
                 }
                 tc_fence_after();
                 if (iss == 0) LMOE_TRACE_EV(1, 0x20 | MODE, it, 0);  // mma: accumulator free
                 const uint32_t d = tmem + uint32_t(acc * C::ACC_COLS_ITEM + iss * NT);
                 for (int kc = 0; kc < p.KC; ++kc) {
-                    if (!mbar_wait(&full[stage], phase)) {
+                    if (!mbar_wait(&full[stage], phase, p.wait_limit)) {
                         set_status(p.status, LMOE_ERR_TIMEOUT);
                         ok = false;
                         break;
@@ -398,6 +406,12 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
                     acc = 0;
                     acc_phase ^= 1;
                 }
+            }
+            if (!ok) {
+                // after a timeout: let this issuer's MMAs already in flight finish
+                // (bounded) before the tensor memory is freed
+                tc_commit(&drain[iss]);
+                mbar_wait(&drain[iss], 0, p.wait_limit);
             }
             if (iss == 0) LMOE_TRACE_END(1);
         }
@@ -437,7 +451,7 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
         auto process = [&](int it, const Item &w, const float (&wl)[NV], const int (&tl)[NV]) -> bool {
             [[maybe_unused]] const int qbase = s_off[w.e] + w.n_tile * NT;  // first permuted row of the tile (down)
             if (threadIdx.x == 64) LMOE_TRACE_EV(2, 0x40 | MODE, it, 0);  // epilogue: waiting
-            if (!mbar_wait(&acc_full[acc], acc_phase)) {
+            if (!mbar_wait(&acc_full[acc], acc_phase, p.wait_limit)) {
                 set_status(p.status, LMOE_ERR_TIMEOUT);
                 return false;
             }
@@ -815,7 +829,7 @@ int gemm_stages(int E, size_t &smem)
     cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     cudaFuncAttributes fa{};
     cudaFuncGetAttributes(&fa, k_moe_gemm<MODE, NT>);
-    const size_t fixed = 1024 + C::EPI_BYTES + (2 * 16 + 2 * C::ACC_STAGES) * 8 + 16 + size_t(2) * (E + 1) * 4;
+    const size_t fixed = 1024 + C::EPI_BYTES + (2 * 16 + 2 * C::ACC_STAGES + 2) * 8 + 16 + size_t(2) * (E + 1) * 4;
     const long avail = long(optin) - long(fa.sharedSizeBytes) - long(fixed);
     int st = int(avail / long(C::STAGE_BYTES));
     if (st > C::MAX_STAGES) st = C::MAX_STAGES;
@@ -962,6 +976,8 @@ cudaError_t launch_expert_gemms(const FfnArgs &a, const FfnLayout &L, char *scra
     g.w_sorted = reinterpret_cast<const float *>(scratch + L.w_sorted);
     g.E = a.E;
     g.status = a.status;
+    g.wait_limit = a.wait_limit > 0 ? a.wait_limit : 4000000000LL;  // ~2 s of SM clocks
+    g.stall_first_fill = a.stall_first_fill;
     // gate/up
     g.sfa0 = a.W->gate_s;
     g.sfa1 = a.W->up_s;

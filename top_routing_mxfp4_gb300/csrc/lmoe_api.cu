@@ -16,6 +16,16 @@ bool g_stage_events_on = false;
 // diagnostics hook (lmoe_set_h_capture): fp32 h of the gate/up epilogue
 float *g_hcap = nullptr;
 size_t g_hcap_bytes = 0;
+// failure-path test hook (lmoe_set_wait_test)
+int32_t g_stall = 0;
+int64_t g_wait_limit = 0;
+// batches of at most this many pairs (T * k) take the small-batch path
+int32_t g_small_pairs = LMOE_SMALL_BATCH_PAIRS_DEFAULT;
+
+bool small_path(const lmoe_dims *d)
+{
+    return d->T > 0 && small_path_fits(d->T, d->d, d->E, d->k, d->I, g_small_pairs);
+}
 
 cudaError_t mark(int i, cudaStream_t st)
 {
@@ -57,8 +67,12 @@ bool weights_ok(const lmoe_expert_weights *W)
 //   status | logits | idx | w | counts | offsets | perm | inv | permute scratch
 //   | ffn scratch (padded MXFP8 activations, h, schedule)
 //   | yp (per-pair outputs [T*k][d]) or, with the fused combine, yacc ([T][d] fp32 sums)
+// The small-batch path (lmoe_set_small_batch_pairs) uses
+//   status (+ the routing kernel's counter) | logits | idx | w | small-path scratch.
 struct FwdLayout {
     size_t status, logits, idx, w, counts, offsets, perm, inv, rscratch, pscratch, fscratch, yp, total;
+    bool small;
+    size_t sscratch;
 };
 
 FwdLayout fwd_layout(const lmoe_dims *d)
@@ -75,6 +89,12 @@ FwdLayout fwd_layout(const lmoe_dims *d)
     L.logits = take(size_t(T * E * 4));
     L.idx = take(size_t(P * 4));
     L.w = take(size_t(P * 4));
+    L.small = small_path(d);
+    if (L.small) {
+        L.sscratch = take(small_layout(d->T, d->d, d->E, d->k, d->I).total);
+        L.total = off;
+        return L;
+    }
     L.counts = take(size_t(E * 4));
     L.offsets = take(size_t((E + 1) * 4));
     L.perm = take(size_t(P * 4));
@@ -261,6 +281,8 @@ lmoe_status lmoe_expert_ffn(const uint8_t *xq, const uint8_t *xs, const lmoe_exp
     if (e != cudaSuccess) return cuda_status(e);
     FfnArgs f{W, offsets, perm, topk_w, int(P), dims->d, dims->E, dims->k, dims->I, yp, nullptr, reinterpret_cast<int32_t *>(ws)};
     f.hcap = g_hcap;
+    f.wait_limit = g_wait_limit;
+    f.stall_first_fill = g_stall;
     return cuda_status(launch_expert_gemms(f, L, fs, st));
 }
 
@@ -302,11 +324,25 @@ lmoe_status lmoe_forward(const uint16_t *x_bf16, const uint16_t *Wr3, const floa
     int32_t *offsets = reinterpret_cast<int32_t *>(ws + L.offsets);
     int32_t *perm = reinterpret_cast<int32_t *>(ws + L.perm);
     int32_t *inv = reinterpret_cast<int32_t *>(ws + L.inv);
+    int32_t *status = reinterpret_cast<int32_t *>(ws + L.status);
+    if (L.small) {
+        // three kernels; the status word and the routing kernel's counter
+        // (the next int32) start at zero
+        if (g_hcap && g_hcap_bytes < size_t(P) * dims->I * sizeof(float)) return LMOE_ERR_INVALID_ARG;
+        cudaError_t e = mark(0, st);
+        if (e == cudaSuccess) e = cudaMemsetAsync(status, 0, 2 * sizeof(int32_t), st);
+        if (e == cudaSuccess)
+            e = launch_small_forward(x_bf16, Wr3, bias, W, T, d, E, k, dims->I, lg, idx, w, y_bf16,
+                                     small_layout(T, d, E, k, dims->I), ws + L.sscratch, status, status + 1, g_hcap, st,
+                                     g_stage_events_on ? g_stage_events : nullptr);
+        if (e == cudaSuccess) e = mark(5, st);
+        if (e == cudaSuccess) e = mark(6, st);
+        return cuda_status(e);
+    }
     char *fs = ws + L.fscratch;
     const FfnLayout FL = ffn_layout(P, d, E, dims->I);
     if (g_hcap && g_hcap_bytes < size_t(FL.rows) * dims->I * sizeof(float)) return LMOE_ERR_INVALID_ARG;
     float *yp = reinterpret_cast<float *>(ws + L.yp);
-    int32_t *status = reinterpret_cast<int32_t *>(ws + L.status);
     // Large batches fuse the combine into the down GEMM: its epilogue adds
     // each pair's weighted output into the token's fp32 row (zeroed here),
     // which one pass then rounds to bf16.
@@ -326,6 +362,8 @@ lmoe_status lmoe_forward(const uint16_t *x_bf16, const uint16_t *Wr3, const floa
     if (e == cudaSuccess) {
         FfnArgs f{W, offsets, perm, w, int(P), d, E, k, dims->I, yp, yacc, status};
         f.hcap = g_hcap;
+        f.wait_limit = g_wait_limit;
+        f.stall_first_fill = g_stall;
         e = launch_expert_gemms(f, FL, fs, st, g_stage_events_on ? g_stage_events[4] : nullptr);
     }
     if (e == cudaSuccess) e = mark(5, st);
@@ -384,6 +422,7 @@ int32_t lmoe_forward_kernel_count(const lmoe_dims *dims)
 {
     if (!dims_ok(dims) || dims->T == 0) return 0;
     const int64_t P = int64_t(dims->T) * dims->k;
+    if (small_path(dims)) return 3;  // route, gate/up, down
     // router (split, GEMM, (reduction), top-k), permute (with the GEMM schedule), scatter, two GEMMs, combine
     return router_kernel_count(dims->T, dims->d, dims->E) + permute_kernel_count(P) + 1 + 2 + 1;
 }
@@ -406,7 +445,21 @@ lmoe_status lmoe_forward_workspace_views(const lmoe_dims *dims, lmoe_ffn_views *
 {
     if (!dims_ok(dims) || !views) return LMOE_ERR_INVALID_ARG;
     const FwdLayout L = fwd_layout(dims);
+    if (L.small) {
+        const SmallLayout S = small_layout(dims->T, dims->d, dims->E, dims->k, dims->I);
+        views->xq = int64_t(L.sscratch + S.xq);
+        views->xs = int64_t(L.sscratch + S.xs);
+        views->hq = int64_t(L.sscratch + S.hq);
+        views->hs = int64_t(L.sscratch + S.hs);
+        views->dst_row = -1;
+        views->rows = int64_t(dims->T) * dims->k;
+        views->tile_tokens = 0;
+        views->slot_rows = 0;
+        views->path = 1;
+        return LMOE_OK;
+    }
     const FfnLayout F = ffn_layout(int64_t(dims->T) * dims->k, dims->d, dims->E, dims->I);
+    views->path = 0;
     views->xq = int64_t(L.fscratch + F.xq);
     views->xs = int64_t(L.fscratch + F.xs);
     views->hq = int64_t(L.fscratch + F.hq);
@@ -417,6 +470,23 @@ lmoe_status lmoe_forward_workspace_views(const lmoe_dims *dims, lmoe_ffn_views *
     views->slot_rows = F.SLOT;
     return LMOE_OK;
 }
+
+lmoe_status lmoe_set_wait_test(int32_t stall_first_fill, int64_t wait_limit_cycles)
+{
+    if (wait_limit_cycles < 0 || (stall_first_fill && wait_limit_cycles == 0)) return LMOE_ERR_INVALID_ARG;
+    g_stall = stall_first_fill ? 1 : 0;
+    g_wait_limit = wait_limit_cycles;
+    return LMOE_OK;
+}
+
+lmoe_status lmoe_set_small_batch_pairs(int32_t max_pairs)
+{
+    if (max_pairs < 0) return LMOE_ERR_INVALID_ARG;
+    g_small_pairs = max_pairs;
+    return LMOE_OK;
+}
+
+int32_t lmoe_small_batch_pairs(void) { return g_small_pairs; }
 
 lmoe_status lmoe_set_h_capture(float *h_f32, size_t bytes)
 {

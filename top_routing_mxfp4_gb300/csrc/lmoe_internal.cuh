@@ -238,6 +238,8 @@ struct FfnArgs {
     float *yacc;  // when set (FfnLayout::fused only): [T][d] fp32 sums over the k pairs instead of yp
     int32_t *status;
     float *hcap = nullptr;  // diagnostics: fp32 h before its MXFP8 rounding, [FfnLayout::rows][I]
+    long long wait_limit = 0;   // bounded-wait limit in SM clocks (0: the default, ~2 s)
+    int stall_first_fill = 0;   // failure-path test: the GEMMs' first stage never fills
 };
 // slot starts and per-GEMM work-item prefixes from the segment offsets
 cudaError_t launch_ffn_schedule(const int32_t *offsets, int E, int d, int I, const FfnLayout &L, char *scratch,
@@ -254,6 +256,25 @@ cudaError_t launch_gather_pad(const uint8_t *xq, const uint8_t *xs, int T, int d
 // gate/up GEMM (+ SwiGLU, MXFP8 of h), event `mid` (if set), down GEMM (x gate weight)
 cudaError_t launch_expert_gemms(const FfnArgs &a, const FfnLayout &L, char *scratch, cudaStream_t st,
                                 cudaEvent_t mid = nullptr);
+
+// ---- small batches (k_small.cu): three weight-streaming kernels ----------------------
+constexpr int SMALL_MAX_TOKENS = 8;
+constexpr int SMALL_MAX_PAIRS = 256;
+struct SmallLayout {
+    size_t n_touched, seg_expert, seg_start, seg_pair, xq, xs, hq, hs, total;  // byte offsets / size
+};
+SmallLayout small_layout(int T, int d, int E, int k, int I);
+// whether a batch of these dims can take the small-batch path (shared-memory
+// limits), given the largest pair count the caller allows on it
+bool small_path_fits(int T, int d, int E, int k, int I, int max_pairs);
+// route + top-k + pair lists + MXFP8 x; gate/up + SwiGLU + MXFP8 h; down +
+// combine.  `counter` (an int32 that is zero when the call starts) counts the
+// routing CTAs; stage_events (optional, LMOE_NUM_STAGE_EVENTS of them): [1..3]
+// are recorded after the routing kernel, [4] after gate/up.
+cudaError_t launch_small_forward(const uint16_t *x, const uint16_t *Wr3, const float *bias, const lmoe_expert_weights *W,
+                                 int T, int d, int E, int k, int I, float *logits, int32_t *idx, float *w,
+                                 uint16_t *y, const SmallLayout &L, char *scratch, int32_t *status, int32_t *counter,
+                                 float *hcap, cudaStream_t st, const cudaEvent_t *stage_events);
 
 cudaError_t launch_combine(const float *yp, const int32_t *inv, int T, int d, int k, uint16_t *y, cudaStream_t st);
 // y = bf16(acc), n elements (n % 4 == 0)

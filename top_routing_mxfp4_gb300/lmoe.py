@@ -90,11 +90,32 @@ _kernel_count = _sig("lmoe_forward_kernel_count", _i32, _DP)
 
 class FfnViews(ctypes.Structure):
     _fields_ = [("xq", _i64), ("xs", _i64), ("hq", _i64), ("hs", _i64), ("dst_row", _i64), ("rows", _i64),
-                ("tile_tokens", _i32), ("slot_rows", _i32)]
+                ("tile_tokens", _i32), ("slot_rows", _i32), ("path", _i32)]
 
 
 _ws_views = _sig("lmoe_forward_workspace_views", ctypes.c_int, _DP, ctypes.POINTER(FfnViews))
 _set_hcap = _sig("lmoe_set_h_capture", ctypes.c_int, _vp, _sz)
+_set_wait_test = _sig("lmoe_set_wait_test", ctypes.c_int, _i32, _i64)
+_set_small = _sig("lmoe_set_small_batch_pairs", ctypes.c_int, _i32)
+
+
+def set_wait_test(stall_first_fill: bool, wait_limit_cycles: int = 0):
+    """Failure-path test hook of the expert GEMMs' bounded waits
+    (lmoe_set_wait_test); (False, 0) restores the normal behaviour."""
+    _check(_set_wait_test(1 if stall_first_fill else 0, int(wait_limit_cycles)), "lmoe_set_wait_test")
+_get_small = _sig("lmoe_small_batch_pairs", _i32)
+SMALL_BATCH_PAIRS_DEFAULT = 128
+
+
+def set_small_batch_pairs(max_pairs: int):
+    """Batches of at most this many pairs (T * k, at most 8 tokens) run the
+    small-batch path of lmoe_forward; 0 sends every batch to the tensor-core
+    path.  Process-wide."""
+    _check(_set_small(int(max_pairs)), "lmoe_set_small_batch_pairs")
+
+
+def small_batch_pairs() -> int:
+    return int(_get_small())
 
 
 def forward_workspace_views(T: int, d: int, E: int, k: int, I: int) -> FfnViews:
