@@ -17,6 +17,8 @@ itself; the tests named live in tests/test_oracle_pins.py):
   permute                -- numpy stable argsort + invariants
   MoE tokens (sparse)    -- dense brute force over all experts; numpy
                             float64 SwiGLU on decoded weights; k = E = 1 case
+  MoE tokens, FP4 mode   -- numpy float64 SwiGLU with MXFP4 activations
+  quant MXFP4 of doubles -- numpy restatement (exact floor(log2) of doubles)
   bf16 rounding          -- torch's fp32 -> bf16 conversion on every kind of
                             fp32 input (no double rounding possible), typed
                             ties / carries / overflow / subnormals (golden),
@@ -84,6 +86,9 @@ def _load():
     lib.oracle_moe_dense.argtypes = [vp, vp, vp, ctypes.POINTER(_Experts), i32, i32, i32, i32, i32, vp, i32, vp]
     lib.oracle_linear_bf16.argtypes = [vp, vp, i64, i32, i32, vp]
     lib.oracle_round_bf16.argtypes = [vp, i64, vp]
+    lib.oracle_quant_mxfp4_f64.argtypes = [vp, i64, i32, vp, vp]
+    lib.oracle_moe_tokens_act.argtypes = [vp, vp, vp, ctypes.POINTER(_Experts), i32, i32, i32, i32, i32, vp, i32,
+                                          i32, vp, vp]
     _lib = lib
     return lib
 
@@ -154,6 +159,16 @@ def quant_mxfp8_f64(x: np.ndarray):
     return q.reshape(x.shape), s.reshape(*x.shape[:-1], K // 32)
 
 
+def quant_mxfp4_f64(x: np.ndarray):
+    """float64 [rows, K] -> MXFP4 (codes [rows, K/2], scales [rows, K/32])."""
+    x = _c(x, np.float64)
+    rows, K = x.reshape(-1, x.shape[-1]).shape
+    q = np.empty((rows, K // 2), np.uint8)
+    s = np.empty((rows, K // 32), np.uint8)
+    _load().oracle_quant_mxfp4_f64(_p(x), rows, K, _p(q), _p(s))
+    return q.reshape(*x.shape[:-1], K // 2), s.reshape(*x.shape[:-1], K // 32)
+
+
 def dequant_mxfp4(q: np.ndarray, s: np.ndarray) -> np.ndarray:
     q, s = _c(q, np.uint8), _c(s, np.uint8)
     K = q.shape[-1] * 2
@@ -215,15 +230,26 @@ class Experts:
         self.struct = _Experts(*[_p(a) for a in self.arrays])
 
 
-def moe_tokens(x_bf16, idx, w, experts: Experts, d: int, E: int, I: int, tokens=None, want_f64=False):
+ACT_MXFP8, ACT_MXFP4 = 1, 2
+
+
+def moe_tokens(x_bf16, idx, w, experts: Experts, d: int, E: int, I: int, tokens=None, want_f64=False,
+               act: int = ACT_MXFP8):
+    """The layer on the listed tokens; act = ACT_MXFP8 (x and h rounded to
+    MXFP8) or ACT_MXFP4 (the full-FP4 variant: x and h rounded to MXFP4)."""
     x, idx, w = _c(x_bf16, np.uint16), _c(idx, np.int32), _c(w, np.float32)
     T, k = idx.shape
     tok = None if tokens is None else _c(tokens, np.int32)
     ntok = T if tok is None else tok.size
     y = np.empty((ntok, d), np.uint16)
     yf = np.empty((ntok, d), np.float64) if want_f64 else None
-    _load().oracle_moe_tokens(_p(x), _p(idx), _p(w), ctypes.byref(experts.struct), T, d, E, k, I,
-                              None if tok is None else _p(tok), ntok, _p(y), None if yf is None else _p(yf))
+    if act == ACT_MXFP8:
+        _load().oracle_moe_tokens(_p(x), _p(idx), _p(w), ctypes.byref(experts.struct), T, d, E, k, I,
+                                  None if tok is None else _p(tok), ntok, _p(y), None if yf is None else _p(yf))
+    else:
+        _load().oracle_moe_tokens_act(_p(x), _p(idx), _p(w), ctypes.byref(experts.struct), T, d, E, k, I,
+                                      None if tok is None else _p(tok), ntok, act, _p(y),
+                                      None if yf is None else _p(yf))
     return (y, yf) if want_f64 else y
 
 

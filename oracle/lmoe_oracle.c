@@ -180,6 +180,26 @@ void oracle_quant_mxfp8_f64(const double *x, int64_t rows, int K, uint8_t *q, ui
         }
 }
 
+void oracle_quant_mxfp4_f64(const double *x, int64_t rows, int K, uint8_t *q, uint8_t *s)
+{
+    const int nb = K / 32;
+    for (int64_t r = 0; r < rows; ++r) {
+        memset(q + r * (K / 2), 0, (size_t)(K / 2));
+        for (int b = 0; b < nb; ++b) {
+            const double *blk = x + r * K + b * 32;
+            double amax = 0.0;
+            for (int i = 0; i < 32; ++i) amax = fmax(amax, fabs(blk[i]));
+            uint8_t sb = oracle_scale_byte(amax, 2);
+            s[r * nb + b] = sb;
+            for (int i = 0; i < 32; ++i) {
+                uint8_t c = oracle_e2m1_encode(ldexp(blk[i], 127 - (int)sb));
+                int col = b * 32 + i;
+                q[r * (K / 2) + col / 2] |= (uint8_t)(c << (4 * (col & 1)));
+            }
+        }
+    }
+}
+
 void oracle_quant_mxfp8(const uint16_t *x_bf16, int64_t rows, int K, uint8_t *q, uint8_t *s)
 {
     double *tmp = (double *)malloc(sizeof(double) * (size_t)K);
@@ -359,6 +379,78 @@ void oracle_moe_tokens(const uint16_t *x_bf16, const int32_t *idx, const float *
             if (y_f64) y_f64[(int64_t)n * d + o] = y[o];
         }
     }
+    free(xhat);
+    free(f);
+    free(y);
+}
+
+/* The activation rounding of the FP4 mode: values -> MXFP4 -> decoded. */
+static void round_mxfp4(const double *v, int K, double *out)
+{
+    uint8_t *q = (uint8_t *)malloc((size_t)(K / 2));
+    uint8_t *s = (uint8_t *)malloc((size_t)(K / 32));
+    oracle_quant_mxfp4_f64(v, 1, K, q, s);
+    oracle_dequant_mxfp4(q, s, 1, K, out);
+    free(q);
+    free(s);
+}
+
+/* One expert's FFN on a decoded activation, FP4 mode: h rounded to MXFP4. */
+static void expert_ffn_fp4(const double *xhat, const oracle_experts *W, int e, int d, int I, double *out)
+{
+    double *h = (double *)malloc(sizeof(double) * (size_t)I);
+    double *hhat = (double *)malloc(sizeof(double) * (size_t)I);
+    for (int i = 0; i < I; ++i) {
+        int64_t row = (int64_t)e * I + i;
+        double g = 0.0, u = 0.0;
+        for (int c = 0; c < d; ++c) {
+            g += mxfp4_elem(W->gate_q, W->gate_s, row, d, c) * xhat[c];
+            u += mxfp4_elem(W->up_q, W->up_s, row, d, c) * xhat[c];
+        }
+        h[i] = silu(g) * u;
+    }
+    round_mxfp4(h, I, hhat);
+    for (int o = 0; o < d; ++o) {
+        int64_t row = (int64_t)e * d + o;
+        double acc = 0.0;
+        for (int i = 0; i < I; ++i) acc += mxfp4_elem(W->down_q, W->down_s, row, I, i) * hhat[i];
+        out[o] = acc;
+    }
+    free(h);
+    free(hhat);
+}
+
+void oracle_moe_tokens_act(const uint16_t *x_bf16, const int32_t *idx, const float *w, const oracle_experts *W,
+                           int T, int d, int E, int k, int I, const int32_t *tokens, int ntok, int act,
+                           uint16_t *y_bf16, double *y_f64)
+{
+    if (act != ORACLE_ACT_MXFP4) {
+        oracle_moe_tokens(x_bf16, idx, w, W, T, d, E, k, I, tokens, ntok, y_bf16, y_f64);
+        return;
+    }
+    if (!tokens) ntok = T;
+    double *xv = (double *)malloc(sizeof(double) * (size_t)d);
+    double *xhat = (double *)malloc(sizeof(double) * (size_t)d);
+    double *f = (double *)malloc(sizeof(double) * (size_t)d);
+    double *y = (double *)malloc(sizeof(double) * (size_t)d);
+    for (int n = 0; n < ntok; ++n) {
+        int t = tokens ? tokens[n] : n;
+        for (int c = 0; c < d; ++c) xv[c] = bf16_to_double(x_bf16[(int64_t)t * d + c]);
+        round_mxfp4(xv, d, xhat);
+        for (int o = 0; o < d; ++o) y[o] = 0.0;
+        for (int j = 0; j < k; ++j) { /* slot order */
+            int e = idx[(int64_t)t * k + j];
+            double wj = (double)w[(int64_t)t * k + j];
+            expert_ffn_fp4(xhat, W, e, d, I, f);
+            for (int o = 0; o < d; ++o) y[o] += wj * f[o];
+        }
+        for (int o = 0; o < d; ++o) {
+            if (y_bf16) y_bf16[(int64_t)n * d + o] = double_to_bf16(y[o]);
+            if (y_f64) y_f64[(int64_t)n * d + o] = y[o];
+        }
+    }
+    (void)E;
+    free(xv);
     free(xhat);
     free(f);
     free(y);

@@ -53,6 +53,9 @@ uint8_t oracle_scale_byte(double amax, int emax);
 void oracle_quant_mxfp4(const float *w, int64_t rows, int K, uint8_t *q, uint8_t *s);
 void oracle_quant_mxfp8(const uint16_t *x_bf16, int64_t rows, int K, uint8_t *q, uint8_t *s);
 void oracle_quant_mxfp8_f64(const double *x, int64_t rows, int K, uint8_t *q, uint8_t *s);
+/* MXFP4 of double values (the gated product h in the FP4-activation mode):
+ * the rule of oracle_quant_mxfp4, from exact double inputs. */
+void oracle_quant_mxfp4_f64(const double *x, int64_t rows, int K, uint8_t *q, uint8_t *s);
 void oracle_dequant_mxfp4(const uint8_t *q, const uint8_t *s, int64_t rows, int K, double *out);
 void oracle_dequant_mxfp8(const uint8_t *q, const uint8_t *s, int64_t rows, int K, double *out);
 
@@ -77,6 +80,15 @@ void oracle_moe_tokens(const uint16_t *x_bf16, const int32_t *idx, const float *
                        int d, int E, int k, int I, const int32_t *tokens, int ntok, uint16_t *y_bf16, double *y_f64);
 /* One expert's FFN on one token: out[d] = Wd * MXFP8(silu(Wg x^) * (Wu x^)), x^ = MXFP8(x). */
 void oracle_expert_ffn_token(const uint16_t *x_bf16_row, const oracle_experts *W, int e, int d, int I, double *out);
+/* The same layer with a choice of activation format: act 1 rounds x and h
+ * to MXFP8 (oracle_moe_tokens), act 2 to MXFP4 (e2m1 + E8M0 per 32, the
+ * weights' rule) -- the full-FP4 variant, whose numerics differ from the
+ * MXFP8 layer by the coarser activation grid. */
+#define ORACLE_ACT_MXFP8 1
+#define ORACLE_ACT_MXFP4 2
+void oracle_moe_tokens_act(const uint16_t *x_bf16, const int32_t *idx, const float *w, const oracle_experts *W,
+                           int T, int d, int E, int k, int I, const int32_t *tokens, int ntok, int act,
+                           uint16_t *y_bf16, double *y_f64);
 /* Brute force: every expert evaluated for every listed token, unselected gates zero. */
 void oracle_moe_dense(const uint16_t *x_bf16, const int32_t *idx, const float *w, const oracle_experts *W, int T,
                       int d, int E, int k, int I, const int32_t *tokens, int ntok, double *y_f64);
