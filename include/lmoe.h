@@ -77,7 +77,14 @@ typedef enum {
     LMOE_ERR_TIMEOUT = -6       /* a kernel's bounded wait ran out            */
 } lmoe_status;
 
-typedef enum { LMOE_ACT_MXFP8 = 1 } lmoe_act_fmt;
+/* Activation format of the expert GEMMs' inputs (x and h).  MXFP8: e4m3 +
+ * E8M0 per 32.  MXFP4 (the full-FP4 variant: e2m1 + E8M0 per 32, the
+ * weights' rule): taken by lmoe_forward on the small-batch path only
+ * (lmoe_set_small_batch_pairs); elsewhere it returns LMOE_ERR_UNSUPPORTED,
+ * as the tensor-core kernels for FP4 activations are not built.  Its
+ * numerics are a different layer: about 20% relative RMS away from the
+ * MXFP8 layer on decode-shaped tokens. */
+typedef enum { LMOE_ACT_MXFP8 = 1, LMOE_ACT_MXFP4 = 2 } lmoe_act_fmt;
 typedef enum { LMOE_LAYOUT_CANONICAL = 0, LMOE_LAYOUT_TC = 1 } lmoe_layout;
 
 /* Layer shape: T tokens, latent width d, E experts, top-k, expert
@@ -233,10 +240,13 @@ size_t lmoe_workspace_size(const lmoe_dims *dims);
  * with top-k and the pair lists; gate/up with SwiGLU and MXFP8 of h; down
  * with the gate weights and the combine) instead of the tensor-core path.
  * Same contract and roundings; the k terms of a token are summed in a fixed
- * order (deterministic), but not strictly slot by slot.  0 sends every batch
+ * order (deterministic), but not strictly slot by slot.  The default takes
+ * it for batch-1 steps (16 pairs), where it matches the tensor-core path's
+ * time with three launches instead of seven; beyond that its CUDA-core
+ * arithmetic makes it slower than the tensor-core path.  0 sends every batch
  * to the tensor-core path.  Process-wide setting, not thread-safe; the
  * workspace size of a batch depends on it.  lmoe_small_batch_pairs() reads it. */
-#define LMOE_SMALL_BATCH_PAIRS_DEFAULT 128
+#define LMOE_SMALL_BATCH_PAIRS_DEFAULT 16
 lmoe_status lmoe_set_small_batch_pairs(int32_t max_pairs);
 int32_t lmoe_small_batch_pairs(void);
 
@@ -313,7 +323,9 @@ typedef struct {
     int64_t rows;
     int32_t tile_tokens, slot_rows;
     int32_t path; /* 0: as above; 1: small-batch path (lmoe_set_small_batch_pairs): xq/xs hold one row per
-                     token t, hq/hs one row per pair p = t*k + j, dst_row = -1, rows = T*k */
+                     token t, hq/hs one row per pair p = t*k + j, dst_row = -1, rows = T*k; with
+                     LMOE_ACT_MXFP4 a code row holds packed e2m1 codes (d/2 or I/2 bytes, element 2i in
+                     the low nibble of byte i) */
 } lmoe_ffn_views;
 lmoe_status lmoe_forward_workspace_views(const lmoe_dims *dims, lmoe_ffn_views *views);
 

@@ -42,10 +42,11 @@ def small_path(cuda_lib):
     cuda_lib.set_small_batch_pairs(old)
 
 
-def _forward(lmoe, wl, x, hcap=False):
+def _forward(lmoe, wl, x, hcap=False, act=None):
     bias = gen.router_bias(wl)
     layer = lmoe.Layer(torch.from_numpy(gen.router_f32(wl)).to(DEV), _bank(wl), k=wl.k,
-                       bias=None if bias is None else torch.from_numpy(bias).to(DEV))
+                       bias=None if bias is None else torch.from_numpy(bias).to(DEV),
+                       act=lmoe.ACT_MXFP8 if act is None else act)
     T = x.shape[0]
     idx = torch.empty((T, wl.k), dtype=torch.int32, device=DEV)
     w = torch.empty((T, wl.k), dtype=torch.float32, device=DEV)
@@ -162,3 +163,56 @@ def test_sixteen_token_step_all_tokens_default_path(cuda_lib):
     x = gen.x_bf16(wl)
     _, y, idx, w, lg, _ = _forward(lmoe, wl, x)
     _check_all(lmoe, wl, x, y, idx, w, lg)
+
+
+@pytest.mark.parametrize("T", [1, 2, 8])
+def test_small_path_fp4_activations_all_tokens(small_path, T):
+    """The full-FP4 variant (x and h rounded to MXFP4) against the oracle's
+    FP4 mode: routing as before, every token within the bar (after the
+    output's own bf16 rounding), and both MXFP4 roundings bit for bit."""
+    lmoe = small_path
+    wl = gen.custom(f"fp4_{T}", T=T, d=3584, I=512)
+    d, I, k = wl.d, wl.I, wl.k
+    x = gen.x_bf16(wl)
+    layer, y, idx, w, lg, cap = _forward(lmoe, wl, x, hcap=True, act=lmoe.ACT_MXFP4)
+    ridx, rw = oracle.topk_softmax(lg, k)
+    np.testing.assert_array_equal(idx, ridx)
+    ob = quantize_experts_parallel(wl, np.unique(ridx))
+    _, y64 = oracle.moe_tokens(x, ridx, rw, ob, d, wl.E, I, want_f64=True, act=oracle.ACT_MXFP4)
+    from _util import bf16_to_f64, half_ulp_bf16
+    g = bf16_to_f64(y)
+    rms = np.sqrt((y64 ** 2).mean(1))
+    err = (np.maximum(np.abs(g - y64) - half_ulp_bf16(g), 0.0).max(1)) / rms
+    print(f"fp4_{T}: worst {err.max():.3e} of rms beyond the output rounding")
+    assert err.max() <= TOL
+    v = lmoe.forward_workspace_views(T, d, wl.E, k, I)
+    ws = layer._ws
+    P = T * k
+
+    def atoms(base, rows, nb):
+        KC = -(-nb // 4)
+        r = np.arange(rows)[:, None]
+        b = np.arange(nb)[None, :]
+        off = ((r >> 7) * KC + (b >> 2)) * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4 + (b & 3)
+        return ws[base:base + int(off.max()) + 1].cpu().numpy()[off]
+
+    rq, rs = oracle.quant_mxfp4_f64(bf16_to_f64(x))
+    np.testing.assert_array_equal(ws[v.xq:v.xq + T * d // 2].cpu().numpy().reshape(T, d // 2), rq)
+    np.testing.assert_array_equal(atoms(v.xs, T, d // 32), rs)
+    h = cap.view(P, I).cpu().numpy().astype(np.float64)
+    hrq, hrs = oracle.quant_mxfp4_f64(h)
+    np.testing.assert_array_equal(ws[v.hq:v.hq + P * I // 2].cpu().numpy().reshape(P, I // 2), hrq)
+    np.testing.assert_array_equal(atoms(v.hs, P, I // 32), hrs)
+
+
+def test_fp4_activations_refused_on_the_tensor_core_path(cuda_lib):
+    lmoe = cuda_lib
+    wl = gen.custom("fp4_tc", T=8, d=512, I=64)
+    old = lmoe.small_batch_pairs()
+    lmoe.set_small_batch_pairs(0)
+    try:
+        with pytest.raises(lmoe.LmoeError) as ei:
+            _forward(lmoe, wl, gen.x_bf16(wl), act=lmoe.ACT_MXFP4)
+        assert ei.value.code == lmoe.ERR_UNSUPPORTED
+    finally:
+        lmoe.set_small_batch_pairs(old)

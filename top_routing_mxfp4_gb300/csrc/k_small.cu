@@ -53,6 +53,32 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes)
     return h2;
 }
 
+// 16 e2m1 codes (8 bytes, element 2i in the low nibble of byte i) -> 8 f16x2
+// words (exact: e2m1 values are fp16 values).
+__device__ __forceinline__ void e2m1x16_to_f16x2(uint2 codes, uint32_t *out)
+{
+    asm("{\n\t.reg .b8 c0, c1, c2, c3, c4, c5, c6, c7;\n\t"
+        "mov.b32 {c0, c1, c2, c3}, %8;\n\tmov.b32 {c4, c5, c6, c7}, %9;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, c0;\n\tcvt.rn.f16x2.e2m1x2 %1, c1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, c2;\n\tcvt.rn.f16x2.e2m1x2 %3, c3;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %4, c4;\n\tcvt.rn.f16x2.e2m1x2 %5, c5;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %6, c6;\n\tcvt.rn.f16x2.e2m1x2 %7, c7;\n\t}"
+        : "=r"(out[0]), "=r"(out[1]), "=r"(out[2]), "=r"(out[3]), "=r"(out[4]), "=r"(out[5]), "=r"(out[6]),
+          "=r"(out[7])
+        : "r"(codes.x), "r"(codes.y));
+}
+
+// Two fp32 values (already divided by the block scale) -> two e2m1 codes in
+// the low byte (lo in the low nibble): round to nearest even, saturate at 6.
+__device__ __forceinline__ uint32_t e2m1x2(float hi, float lo)
+{
+    uint32_t out;
+    asm("{\n\t.reg .b8 b;\n\tcvt.rn.satfinite.e2m1x2.f32 b, %1, %2;\n\tcvt.u32.u8 %0, b;\n\t}"
+        : "=r"(out)
+        : "f"(hi), "f"(lo));
+    return out;
+}
+
 __device__ __forceinline__ float warp_sum(float v)
 {
 #pragma unroll
@@ -86,7 +112,7 @@ struct SmallPlan {
 // token (x in shared memory as bf16).  The two halves meet in shared memory
 // and the CTA writes its experts' logits.  The last CTA to finish loads all
 // logits with every thread, then one warp per token selects the top k.
-template <int TMAX>
+template <int TMAX, bool FP4>
 __global__ void __launch_bounds__(32 * R_WARPS, 2) k_small_route(const uint16_t *__restrict__ x,
                                                               const uint16_t *__restrict__ Wr3,
                                                               const float *__restrict__ bias, int T, int d, int E,
@@ -175,14 +201,22 @@ __global__ void __launch_bounds__(32 * R_WARPS, 2) k_small_route(const uint16_t 
         uint32_t amax = 0;
 #pragma unroll
         for (int i = 0; i < 32; ++i) amax = max(amax, __float_as_uint(v[i]) & 0x7FFFFFFFu);
-        const uint32_t sb = mx_scale_byte(__uint_as_float(amax), 8);
+        const uint32_t sb = mx_scale_byte(__uint_as_float(amax), FP4 ? 2 : 8);
         const float inv = mx_inv_scale(sb);
-        uint32_t c[8];
+        if constexpr (FP4) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) c[i] = e4m3x4(v[4 * i] * inv, v[4 * i + 1] * inv, v[4 * i + 2] * inv, v[4 * i + 3] * inv);
-        uint4 *dst = reinterpret_cast<uint4 *>(sp.xq + int64_t(t) * d + b * 32);
-        dst[0] = make_uint4(c[0], c[1], c[2], c[3]);
-        dst[1] = make_uint4(c[4], c[5], c[6], c[7]);
+            for (int i = 0; i < 32; ++i) v[i] *= inv;
+            *reinterpret_cast<uint4 *>(sp.xq + int64_t(t) * (d / 2) + b * 16) =
+                make_uint4(e2m1x8(v), e2m1x8(v + 8), e2m1x8(v + 16), e2m1x8(v + 24));
+        } else {
+            uint32_t c[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                c[i] = e4m3x4(v[4 * i] * inv, v[4 * i + 1] * inv, v[4 * i + 2] * inv, v[4 * i + 3] * inv);
+            uint4 *dst = reinterpret_cast<uint4 *>(sp.xq + int64_t(t) * d + b * 32);
+            dst[0] = make_uint4(c[0], c[1], c[2], c[3]);
+            dst[1] = make_uint4(c[4], c[5], c[6], c[7]);
+        }
         sp.xs[atom_offset(t, b, KC)] = uint8_t(sb);
     }
     __syncthreads();
@@ -285,6 +319,7 @@ __device__ __forceinline__ void dot16(uint2 codes, const uint32_t *xv, float &a0
 // results meet in shared memory and warp 0 forms h for the 32 rows:
 // silu(g) * u, block amax, E8M0 scale, e4m3 codes.  Further tokens of the
 // same expert reuse the weights in shared memory.
+template <bool FP4>
 __global__ void __launch_bounds__(32 * G_WARPS) k_small_gateup(const uint8_t *__restrict__ gate_q,
                                                                const uint8_t *__restrict__ gate_s,
                                                                const uint8_t *__restrict__ up_q,
@@ -337,17 +372,26 @@ __global__ void __launch_bounds__(32 * G_WARPS) k_small_gateup(const uint8_t *__
 #pragma unroll
             for (int m = 0; m < MAX_CH; ++m) {
                 const int c = lane + 32 * m;
-                uint4 v = make_uint4(0, 0, 0, 0);
                 uint32_t sb = 0;
-                if (c < nchunk) {
-                    v = __ldcg(reinterpret_cast<const uint4 *>(sp.xq + int64_t(t) * d) + c);
-                    sb = __ldcg(sp.xs + atom_offset(t, c >> 1, KCd));
-                }
-                const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+                if constexpr (FP4) {
+                    uint2 v = make_uint2(0, 0);
+                    if (c < nchunk) {
+                        v = __ldcg(reinterpret_cast<const uint2 *>(sp.xq + int64_t(t) * (d / 2)) + c);
+                        sb = __ldcg(sp.xs + atom_offset(t, c >> 1, KCd));
+                    }
+                    e2m1x16_to_f16x2(v, xr[m]);
+                } else {
+                    uint4 v = make_uint4(0, 0, 0, 0);
+                    if (c < nchunk) {
+                        v = __ldcg(reinterpret_cast<const uint4 *>(sp.xq + int64_t(t) * d) + c);
+                        sb = __ldcg(sp.xs + atom_offset(t, c >> 1, KCd));
+                    }
+                    const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    xr[m][2 * j] = e4m3x2_to_f16x2(vw[j]);
-                    xr[m][2 * j + 1] = e4m3x2_to_f16x2(vw[j] >> 16);
+                    for (int j = 0; j < 4; ++j) {
+                        xr[m][2 * j] = e4m3x2_to_f16x2(vw[j]);
+                        xr[m][2 * j + 1] = e4m3x2_to_f16x2(vw[j] >> 16);
+                    }
                 }
                 sx[m] = e8m0_to_f32(sb);
             }
@@ -386,8 +430,15 @@ __global__ void __launch_bounds__(32 * G_WARPS) k_small_gateup(const uint8_t *__
                 if (sp.hcap) sp.hcap[int64_t(p) * I + rb * 32 + lane] = h;
                 uint32_t amax;
                 asm("redux.sync.max.u32 %0, %1, 0xffffffff;" : "=r"(amax) : "r"(__float_as_uint(h) & 0x7FFFFFFFu));
-                const uint32_t sb = mx_scale_byte(__uint_as_float(amax), 8);
-                sp.hq[int64_t(p) * I + rb * 32 + lane] = uint8_t(e4m3x2(h * mx_inv_scale(sb), 0.f) & 0xFF);
+                const uint32_t sb = mx_scale_byte(__uint_as_float(amax), FP4 ? 2 : 8);
+                if constexpr (FP4) {
+                    // e2m1 code of this lane's h; lanes 2i and 2i+1 share byte i (element 2i in the low nibble)
+                    const uint32_t code = e2m1x2(0.f, h * mx_inv_scale(sb)) & 0xF;
+                    const uint32_t hi = __shfl_down_sync(0xFFFFFFFFu, code, 1);
+                    if ((lane & 1) == 0) sp.hq[int64_t(p) * (I / 2) + rb * 16 + lane / 2] = uint8_t(code | (hi << 4));
+                } else {
+                    sp.hq[int64_t(p) * I + rb * 32 + lane] = uint8_t(e4m3x2(h * mx_inv_scale(sb), 0.f) & 0xFF);
+                }
                 if (lane == 0) sp.hs[atom_offset(p, rb, KCi)] = uint8_t(sb);
             }
         }
@@ -412,6 +463,7 @@ constexpr int D_PB = 4;    // pairs whose dot products are formed together
 // and token it accumulates sum_j w_j * (its part of W_down[e_j][row] .
 // h^_(t,j)) over the token's pairs in slot order (the dot products of D_PB
 // pairs are formed together), then one warp reduction gives y[t][row].
+template <bool FP4>
 __global__ void __launch_bounds__(32 * D_WARPS) k_small_down(const uint8_t *__restrict__ down_q,
                                                              const uint8_t *__restrict__ down_s,
                                                              const int32_t *__restrict__ idx,
@@ -469,12 +521,19 @@ __global__ void __launch_bounds__(32 * D_WARPS) k_small_down(const uint8_t *__re
     pdl_enter();
     // h^ of every pair, as fp16 code values, and its block scales
     for (int i = threadIdx.x; i < P * I / 16; i += blockDim.x) {
-        const uint4 v = __ldcg(reinterpret_cast<const uint4 *>(sp.hq) + i);
         uint4 *dst = reinterpret_cast<uint4 *>(hh + size_t(i) * 8);
-        dst[0] = make_uint4(e4m3x2_to_f16x2(v.x), e4m3x2_to_f16x2(v.x >> 16), e4m3x2_to_f16x2(v.y),
-                            e4m3x2_to_f16x2(v.y >> 16));
-        dst[1] = make_uint4(e4m3x2_to_f16x2(v.z), e4m3x2_to_f16x2(v.z >> 16), e4m3x2_to_f16x2(v.w),
-                            e4m3x2_to_f16x2(v.w >> 16));
+        if constexpr (FP4) {
+            uint32_t f[8];
+            e2m1x16_to_f16x2(__ldcg(reinterpret_cast<const uint2 *>(sp.hq) + i), f);
+            dst[0] = make_uint4(f[0], f[1], f[2], f[3]);
+            dst[1] = make_uint4(f[4], f[5], f[6], f[7]);
+        } else {
+            const uint4 v = __ldcg(reinterpret_cast<const uint4 *>(sp.hq) + i);
+            dst[0] = make_uint4(e4m3x2_to_f16x2(v.x), e4m3x2_to_f16x2(v.x >> 16), e4m3x2_to_f16x2(v.y),
+                                e4m3x2_to_f16x2(v.y >> 16));
+            dst[1] = make_uint4(e4m3x2_to_f16x2(v.z), e4m3x2_to_f16x2(v.z >> 16), e4m3x2_to_f16x2(v.w),
+                                e4m3x2_to_f16x2(v.w >> 16));
+        }
     }
     for (int i = threadIdx.x; i < P * (I / 32); i += blockDim.x) {
         const int p = i / (I / 32), b = i - p * (I / 32);
@@ -623,8 +682,61 @@ bool small_path_fits(int T, int d, int E, int k, int I, int max_pairs)
     return route_smem(T, d, E) <= kSmemLimit && gateup_smem(d) <= kSmemLimit && down_group(int(P), d, I) >= 1;
 }
 
+namespace {
+
+template <bool FP4>
+cudaError_t launch_small_t(const uint16_t *x, const uint16_t *Wr3, const float *bias, const lmoe_expert_weights *W,
+                           int T, int d, int E, int k, int I, float *logits, int32_t *idx, float *w, uint16_t *y,
+                           const SmallPlan &sp, cudaStream_t st, const cudaEvent_t *stage_events)
+{
+    const int P = T * k;
+    cudaError_t e = cudaSuccess;
+    const size_t rs = route_smem(T, d, E);
+    const int rgrid = int(ceil_div(2 * E, R_WARPS));
+    if (T <= 1) {
+        if ((e = smem_attr(k_small_route<1, FP4>, rs)) != cudaSuccess) return e;
+        e = launch_pdl(k_small_route<1, FP4>, dim3(rgrid), dim3(32 * R_WARPS), rs, st, x, Wr3, bias, T, d, E, k,
+                       logits, idx, w, sp);
+    } else if (T <= 2) {
+        if ((e = smem_attr(k_small_route<2, FP4>, rs)) != cudaSuccess) return e;
+        e = launch_pdl(k_small_route<2, FP4>, dim3(rgrid), dim3(32 * R_WARPS), rs, st, x, Wr3, bias, T, d, E, k,
+                       logits, idx, w, sp);
+    } else if (T <= 4) {
+        if ((e = smem_attr(k_small_route<4, FP4>, rs)) != cudaSuccess) return e;
+        e = launch_pdl(k_small_route<4, FP4>, dim3(rgrid), dim3(32 * R_WARPS), rs, st, x, Wr3, bias, T, d, E, k,
+                       logits, idx, w, sp);
+    } else {
+        if ((e = smem_attr(k_small_route<SMALL_MAX_TOKENS, FP4>, rs)) != cudaSuccess) return e;
+        e = launch_pdl(k_small_route<SMALL_MAX_TOKENS, FP4>, dim3(rgrid), dim3(32 * R_WARPS), rs, st, x, Wr3, bias,
+                       T, d, E, k, logits, idx, w, sp);
+    }
+    if (e != cudaSuccess) return e;
+    // stage events 1..3 (routing, permute, activation rounding) all follow the routing kernel
+    for (int i = 1; stage_events && i <= 3; ++i)
+        if ((e = cudaEventRecord(stage_events[i], st)) != cudaSuccess) return e;
+    const size_t gs = gateup_smem(d);
+    if ((e = smem_attr(k_small_gateup<FP4>, gs)) != cudaSuccess) return e;
+    const int max_units = P * (I / 32);
+    const int ggrid = max_units < 152 ? max_units : 152;
+    e = launch_pdl(k_small_gateup<FP4>, dim3(ggrid), dim3(32 * G_WARPS), gs, st, W->gate_q, W->gate_s, W->up_q,
+                   W->up_s, d, I, k, sp);
+    if (e != cudaSuccess) return e;
+    if (stage_events && (e = cudaEventRecord(stage_events[4], st)) != cudaSuccess) return e;
+    const int gp = down_group(P, d, I);
+    const size_t ds = down_smem(P, d, I, gp);
+    if ((e = smem_attr(k_small_down<FP4>, ds)) != cudaSuccess) return e;
+    const int rpc = down_rows_per_cta(d);
+    const int dgrid = int(ceil_div(d, rpc));
+    e = launch_pdl(k_small_down<FP4>, dim3(dgrid), dim3(32 * D_WARPS), ds, st, W->down_q, W->down_s, idx, w, T, d, I,
+                   k, rpc, gp, y, sp);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+}  // namespace
+
 cudaError_t launch_small_forward(const uint16_t *x, const uint16_t *Wr3, const float *bias, const lmoe_expert_weights *W,
-                                 int T, int d, int E, int k, int I, float *logits, int32_t *idx, float *w,
+                                 int T, int d, int E, int k, int I, int act, float *logits, int32_t *idx, float *w,
                                  uint16_t *y, const SmallLayout &L, char *scratch, int32_t *status, int32_t *counter,
                                  float *hcap, cudaStream_t st, const cudaEvent_t *stage_events)
 {
@@ -640,48 +752,9 @@ cudaError_t launch_small_forward(const uint16_t *x, const uint16_t *Wr3, const f
     sp.hq = reinterpret_cast<uint8_t *>(scratch + L.hq);
     sp.hs = reinterpret_cast<uint8_t *>(scratch + L.hs);
     sp.hcap = hcap;
-    const int P = T * k;
-    cudaError_t e = cudaSuccess;
-    const size_t rs = route_smem(T, d, E);
-    const int rgrid = int(ceil_div(2 * E, R_WARPS));
-    if (T <= 1) {
-        if ((e = smem_attr(k_small_route<1>, rs)) != cudaSuccess) return e;
-        e = launch_pdl(k_small_route<1>, dim3(rgrid), dim3(32 * R_WARPS), rs, st, x, Wr3, bias, T, d, E, k, logits,
-                       idx, w, sp);
-    } else if (T <= 2) {
-        if ((e = smem_attr(k_small_route<2>, rs)) != cudaSuccess) return e;
-        e = launch_pdl(k_small_route<2>, dim3(rgrid), dim3(32 * R_WARPS), rs, st, x, Wr3, bias, T, d, E, k, logits,
-                       idx, w, sp);
-    } else if (T <= 4) {
-        if ((e = smem_attr(k_small_route<4>, rs)) != cudaSuccess) return e;
-        e = launch_pdl(k_small_route<4>, dim3(rgrid), dim3(32 * R_WARPS), rs, st, x, Wr3, bias, T, d, E, k, logits,
-                       idx, w, sp);
-    } else {
-        if ((e = smem_attr(k_small_route<SMALL_MAX_TOKENS>, rs)) != cudaSuccess) return e;
-        e = launch_pdl(k_small_route<SMALL_MAX_TOKENS>, dim3(rgrid), dim3(32 * R_WARPS), rs, st, x, Wr3, bias, T, d,
-                       E, k, logits, idx, w, sp);
-    }
-    if (e != cudaSuccess) return e;
-    // stage events 1..3 (routing, permute, activation rounding) all follow the routing kernel
-    for (int i = 1; stage_events && i <= 3; ++i)
-        if ((e = cudaEventRecord(stage_events[i], st)) != cudaSuccess) return e;
-    const size_t gs = gateup_smem(d);
-    if ((e = smem_attr(k_small_gateup, gs)) != cudaSuccess) return e;
-    const int max_units = P * (I / 32);
-    const int ggrid = max_units < 152 ? max_units : 152;
-    e = launch_pdl(k_small_gateup, dim3(ggrid), dim3(32 * G_WARPS), gs, st, W->gate_q, W->gate_s, W->up_q, W->up_s, d,
-                   I, k, sp);
-    if (e != cudaSuccess) return e;
-    if (stage_events && (e = cudaEventRecord(stage_events[4], st)) != cudaSuccess) return e;
-    const int gp = down_group(P, d, I);
-    const size_t ds = down_smem(P, d, I, gp);
-    if ((e = smem_attr(k_small_down, ds)) != cudaSuccess) return e;
-    const int rpc = down_rows_per_cta(d);
-    const int dgrid = int(ceil_div(d, rpc));
-    e = launch_pdl(k_small_down, dim3(dgrid), dim3(32 * D_WARPS), ds, st, W->down_q, W->down_s, idx, w, T, d, I, k,
-                   rpc, gp, y, sp);
-    if (e != cudaSuccess) return e;
-    return cudaGetLastError();
+    return act == LMOE_ACT_MXFP4
+               ? launch_small_t<true>(x, Wr3, bias, W, T, d, E, k, I, logits, idx, w, y, sp, st, stage_events)
+               : launch_small_t<false>(x, Wr3, bias, W, T, d, E, k, I, logits, idx, w, y, sp, st, stage_events);
 }
 
 }  // namespace lmoe

@@ -305,7 +305,8 @@ lmoe_status lmoe_forward(const uint16_t *x_bf16, const uint16_t *Wr3, const floa
                          void *workspace, size_t ws_bytes, void *stream)
 {
     if (!dims_ok(dims)) return LMOE_ERR_INVALID_ARG;
-    lmoe_status a = act_ok(dims);
+    // MXFP4 activations exist on the small-batch path only
+    lmoe_status a = (dims->act == LMOE_ACT_MXFP4 && small_path(dims)) ? LMOE_OK : act_ok(dims);
     if (a != LMOE_OK) return a;
     if (dims->T == 0) return LMOE_OK;
     if (!x_bf16 || !Wr3 || !y_bf16 || !aligned(x_bf16, 16) || !aligned(Wr3, 16) || !aligned(y_bf16, 16))
@@ -332,7 +333,7 @@ lmoe_status lmoe_forward(const uint16_t *x_bf16, const uint16_t *Wr3, const floa
         cudaError_t e = mark(0, st);
         if (e == cudaSuccess) e = cudaMemsetAsync(status, 0, 2 * sizeof(int32_t), st);
         if (e == cudaSuccess)
-            e = launch_small_forward(x_bf16, Wr3, bias, W, T, d, E, k, dims->I, lg, idx, w, y_bf16,
+            e = launch_small_forward(x_bf16, Wr3, bias, W, T, d, E, k, dims->I, dims->act, lg, idx, w, y_bf16,
                                      small_layout(T, d, E, k, dims->I), ws + L.sscratch, status, status + 1, g_hcap, st,
                                      g_stage_events_on ? g_stage_events : nullptr);
         if (e == cudaSuccess) e = mark(5, st);

@@ -267,12 +267,12 @@ SmallLayout small_layout(int T, int d, int E, int k, int I);
 // whether a batch of these dims can take the small-batch path (shared-memory
 // limits), given the largest pair count the caller allows on it
 bool small_path_fits(int T, int d, int E, int k, int I, int max_pairs);
-// route + top-k + pair lists + MXFP8 x; gate/up + SwiGLU + MXFP8 h; down +
-// combine.  `counter` (an int32 that is zero when the call starts) counts the
+// route + top-k + pair lists + MXFP8 (or, act == LMOE_ACT_MXFP4, MXFP4) x;
+// gate/up + SwiGLU + the same rounding of h; down + combine.  `counter` (an int32 that is zero when the call starts) counts the
 // routing CTAs; stage_events (optional, LMOE_NUM_STAGE_EVENTS of them): [1..3]
 // are recorded after the routing kernel, [4] after gate/up.
 cudaError_t launch_small_forward(const uint16_t *x, const uint16_t *Wr3, const float *bias, const lmoe_expert_weights *W,
-                                 int T, int d, int E, int k, int I, float *logits, int32_t *idx, float *w,
+                                 int T, int d, int E, int k, int I, int act, float *logits, int32_t *idx, float *w,
                                  uint16_t *y, const SmallLayout &L, char *scratch, int32_t *status, int32_t *counter,
                                  float *hcap, cudaStream_t st, const cudaEvent_t *stage_events);
 

@@ -31,6 +31,7 @@ ERR_CUDA = -4
 ERR_DEVICE_CHECK = -5
 ERR_TIMEOUT = -6
 ACT_MXFP8 = 1
+ACT_MXFP4 = 2
 LAYOUT_CANONICAL = 0
 LAYOUT_TC = 1
 
@@ -104,7 +105,7 @@ def set_wait_test(stall_first_fill: bool, wait_limit_cycles: int = 0):
     (lmoe_set_wait_test); (False, 0) restores the normal behaviour."""
     _check(_set_wait_test(1 if stall_first_fill else 0, int(wait_limit_cycles)), "lmoe_set_wait_test")
 _get_small = _sig("lmoe_small_batch_pairs", _i32)
-SMALL_BATCH_PAIRS_DEFAULT = 128
+SMALL_BATCH_PAIRS_DEFAULT = 16
 
 
 def set_small_batch_pairs(max_pairs: int):
@@ -446,8 +447,8 @@ class Layer:
     """A LatentMoE layer: router weights (fp32, prepared once into the form the
     router GEMM reads), optional logit bias, expert bank."""
 
-    def __init__(self, Wr: torch.Tensor, bank: ExpertBank, k: int = 16, bias=None):
-        self.Wr, self.bank, self.k, self.bias = Wr, bank, k, bias
+    def __init__(self, Wr: torch.Tensor, bank: ExpertBank, k: int = 16, bias=None, act: int = ACT_MXFP8):
+        self.Wr, self.bank, self.k, self.bias, self.act = Wr, bank, k, bias, act
         self.Wr3 = prepare_router(Wr)
         self._ws = None
 
@@ -460,7 +461,7 @@ class Layer:
     def forward(self, x, y=None, topk_idx=None, topk_w=None, logits=None, stream=None):
         T, d = x.shape
         _need(x, torch.bfloat16, (T, d), "x")
-        D = dims(T, d, self.bank.E, self.k, self.bank.I)
+        D = dims(T, d, self.bank.E, self.k, self.bank.I, self.act)
         y = _empty((T, d), torch.bfloat16, x.device) if y is None else y
         ws = self.workspace(T)
         W = self.bank.struct()
