@@ -855,6 +855,10 @@ cudaError_t launch_gemm(const CUtensorMap &a0, const CUtensorMap &a1, const CUte
 
 }  // namespace
 
+// Output-column bands of the fused-combine down GEMM: only 1/kDownBands of
+// the per-token fp32 rows take reductions at a time.
+constexpr int kDownBands = 2;
+
 // 128-row weight tiles per down-GEMM item (Cfg<DOWN, NT>::MATS).
 static int down_tiles_per_item(int NT) { return NT <= 96 ? 2 : 1; }
 
@@ -916,7 +920,7 @@ FfnSched ffn_sched(const FfnLayout &L, int d, int I, char *scratch)
     sc.items_gu = reinterpret_cast<int2 *>(scratch + L.items_gu);
     sc.items_dn = reinterpret_cast<int2 *>(scratch + L.items_dn);
     sc.tile_info = reinterpret_cast<int2 *>(scratch + L.tile_info);
-    sc.band = L.NT >= 64 ? 1 : 0;  // Cfg<DOWN, NT>::STAGED
+    sc.band = L.NT >= 64 ? kDownBands : 0;  // Cfg<DOWN, NT>::STAGED: the fused combine
     sc.dst_row = reinterpret_cast<int32_t *>(scratch + L.dst_row);
     return sc;
 }

@@ -161,7 +161,7 @@ cudaError_t launch_route(const uint16_t *x, const uint16_t *Wr3, const float *bi
 // T*k).  pad_off == nullptr disables them.
 struct FfnSched {
     int NT = 0, SLOT = 0, MT_gu = 0, MT_dn = 0;
-    int band = 0;  // the down GEMM runs its items in two output-column bands
+    int band = 0;  // the down GEMM runs its items in this many output-column bands (0 or 1: one)
     int32_t *pad_off = nullptr, *tiles_gu = nullptr, *tiles_dn = nullptr, *dst_row = nullptr;
     int2 *items_gu = nullptr, *items_dn = nullptr;
     int2 *tile_info = nullptr;  // per token tile: {expert, token tile within the expert}
@@ -183,11 +183,12 @@ __device__ __forceinline__ void fill_tile_info(const int32_t *scan, int E, const
         for (int R = scan[e]; R < scan[e + 1]; ++R) sc.tile_info[R] = make_int2(e, R - scan[e]);
 }
 // Entries [g0, n_gu + n_dn) with stride `step` (gate/up entries first).
+// Down entries in bands: band b holds weight tiles [b*MT/NB, (b+1)*MT/NB) of
+// every token tile, bands one after another.
 __device__ __forceinline__ void fill_item_entries(const FfnSched &sc, int n_gu, int n_dn, int64_t g0, int64_t step)
 {
     const int TT = n_gu / sc.MT_gu;
-    const int MT0 = sc.band ? (sc.MT_dn + 1) / 2 : sc.MT_dn, MT1 = sc.MT_dn - MT0;
-    const int n_dn0 = TT * MT0;
+    const int NBd = sc.band > 1 ? sc.band : 1;
     for (int64_t g = g0; g < int64_t(n_gu) + n_dn; g += step) {
         int R, m;
         int2 *dst;
@@ -197,13 +198,13 @@ __device__ __forceinline__ void fill_item_entries(const FfnSched &sc, int n_gu, 
             dst = sc.items_gu + g;
         } else {
             const int it = int(g - n_gu);
-            if (it < n_dn0) {
-                R = it / MT0;
-                m = it - R * MT0;
-            } else {
-                R = (it - n_dn0) / MT1;
-                m = MT0 + (it - n_dn0 - R * MT1);
-            }
+            // band b starts at item TT * m_lo(b), m_lo(b) = b * MT / NBd
+            int b = 0;
+            while (b + 1 < NBd && it >= TT * ((b + 1) * sc.MT_dn / NBd)) ++b;
+            const int m_lo = b * sc.MT_dn / NBd, m_len = (b + 1) * sc.MT_dn / NBd - m_lo;
+            const int r = it - TT * m_lo;
+            R = r / m_len;
+            m = m_lo + (r - R * m_len);
             dst = sc.items_dn + it;
         }
         const int2 ti = sc.tile_info[R];
