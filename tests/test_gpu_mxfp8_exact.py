@@ -45,7 +45,17 @@ def atom_scales(atoms: torch.Tensor, R: torch.Tensor, nblocks: int) -> np.ndarra
     return atoms[off].cpu().numpy()
 
 
-@pytest.mark.parametrize("T,tile", [(64, 16), (512, 32), (2048, 96)])
+@pytest.fixture(autouse=True)
+def tensor_core_path(cuda_lib):
+    """These checks cover the tensor-core path (the small-batch path has its
+    own bit-exact checks); restored after each test."""
+    old = cuda_lib.small_batch_pairs()
+    cuda_lib.set_small_batch_pairs(0)
+    yield
+    cuda_lib.set_small_batch_pairs(old)
+
+
+@pytest.mark.parametrize("T,tile", [(1, 16), (2, 16), (64, 16), (512, 32), (2048, 96)])
 def test_forward_mxfp8_operands_bit_exact(cuda_lib, T, tile):
     lmoe = cuda_lib
     wl = gen.custom(f"mxfp8_exact_{T}", T=T, d=3584, I=512)
