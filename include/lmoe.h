@@ -307,17 +307,22 @@ lmoe_status lmoe_set_stage_events(void *const *events, int32_t n);
 
 /* Where lmoe_forward keeps the expert GEMMs' MXFP8 operands inside its
  * workspace, as byte offsets from the workspace start, for these dims:
- *   xq  [rows][d]  e4m3 codes of x, one padded row per routed pair,
- *   xs  scale atoms of x: 512 bytes per 128 rows x 4 blocks of 32 along d,
- *       row R (R = 128*a + 32*j + i) block b at byte ((a*(d/128) + b/4)*512
- *       + 16*i + 4*j + b%4) (the expert weights' scale layout),
+ *   xq  [rows][d]  e4m3 codes of x, one row per routed pair, in token tiles
+ *       of tile_tokens rows packed one after another (an expert's pairs fill
+ *       whole tiles from a tile boundary),
+ *   xs  scale atoms of x: tile n's rows rr = 0 .. tile_tokens-1 are rows
+ *       32*j + i of its 512-byte atoms, one atom per 128 columns: row R
+ *       (tile n = R / tile_tokens, rr = R % tile_tokens, i = rr % 32,
+ *       j = rr / 32), block b at byte ((n*(d/128) + b/4)*512 + 16*i + 4*j +
+ *       b%4),
  *   hq  [rows][I]  e4m3 codes of the gated product h of each pair,
  *   hs  scale atoms of h (the same layout with roundup(I,128)/128 atoms per
- *       128 rows),
- *   dst_row  int32 [T*k]: the padded row of pair p = t*k + j;
- * rows = padded rows reserved, tile_tokens = tokens per expert-GEMM tile,
- * slot_rows = rows per tile slot.  Valid after an lmoe_forward call with the
- * same dims has completed; rows no pair maps to hold no defined data. */
+ *       tile),
+ *   dst_row  int32 [T*k]: the row of pair p = t*k + j;
+ * rows = rows reserved, tile_tokens = tokens per expert-GEMM tile,
+ * slot_rows = rows a tile occupies (tile_tokens: packed).  Valid after an
+ * lmoe_forward call with the same dims has completed; rows no pair maps to
+ * hold no defined data. */
 typedef struct {
     int64_t xq, xs, hq, hs, dst_row;
     int64_t rows;

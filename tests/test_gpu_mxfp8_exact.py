@@ -2,7 +2,7 @@
 
 The layer rounds two activations to MXFP8 before the tensor cores read them
 (e4m3 codes, one E8M0 scale per 32 elements): the latent x of every routed
-pair, written by the activation scatter into the expert GEMM's padded token
+pair, written by the activation scatter into the expert GEMM's tiled token
 rows, and the gated product h = silu(g) * u, rounded in the gate/up GEMM's
 epilogue.  Both are read back from the forward's workspace (its layout comes
 from lmoe_forward_workspace_views) and compared, every code and every scale
@@ -34,14 +34,16 @@ def _get_bank(wl):
     return _bank[key]
 
 
-def atom_scales(atoms: torch.Tensor, R: torch.Tensor, nblocks: int) -> np.ndarray:
-    """Scale bytes [len(R), nblocks] of padded rows R from 512-byte atoms of
-    128 rows x 4 blocks (row 128a + 32j + i, block b at byte
-    (a * KC + b / 4) * 512 + 16 i + 4 j + b % 4, KC = ceil(nblocks / 4))."""
+def atom_scales(atoms: torch.Tensor, R: torch.Tensor, nblocks: int, tile: int) -> np.ndarray:
+    """Scale bytes [len(R), nblocks] of token rows R from the tiled layout:
+    row rr = R % tile of tile R // tile, block b at byte
+    (tile_index * KC + b / 4) * 512 + 16 (rr % 32) + 4 (rr / 32) + b % 4,
+    KC = ceil(nblocks / 4)."""
     KC = -(-nblocks // 4)
     b = torch.arange(nblocks, device=R.device, dtype=torch.int64)[None, :]
     r = R.to(torch.int64)[:, None]
-    off = ((r >> 7) * KC + (b >> 2)) * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4 + (b & 3)
+    ti, rr = r // tile, r % tile
+    off = (ti * KC + (b >> 2)) * 512 + (rr & 31) * 16 + (rr >> 5) * 4 + (b & 3)
     return atoms[off].cpu().numpy()
 
 
@@ -79,9 +81,9 @@ def test_forward_mxfp8_operands_bit_exact(cuda_lib, T, tile):
     R = ws[v.dst_row:v.dst_row + 4 * P].view(torch.int32).to(torch.int64)
     Rh = R.cpu().numpy()
     assert Rh.min() >= 0 and Rh.max() < v.rows and np.unique(Rh).size == P
-    # x: every routed pair's padded row holds MXFP8(x[t]) of its token t = p / k
+    # x: every routed pair's token row holds MXFP8(x[t]) of its token t = p / k
     xq = ws[v.xq:v.xq + v.rows * d].view(v.rows, d)[R].cpu().numpy()
-    xs = atom_scales(ws[v.xs:v.hq], R, d // 32)
+    xs = atom_scales(ws[v.xs:v.hq], R, d // 32, v.tile_tokens)
     rq, rs = oracle.quant_mxfp8(x)
     tok = np.arange(P) // k
     bad = np.nonzero((xq != rq[tok]).any(1) | (xs != rs[tok]).any(1))[0]
@@ -90,7 +92,7 @@ def test_forward_mxfp8_operands_bit_exact(cuda_lib, T, tile):
     h = hcap.view(v.rows, I)[R].cpu().numpy().astype(np.float64)
     assert np.isfinite(h).all(), "the epilogue did not capture h for every routed pair"
     hq = ws[v.hq:v.hq + v.rows * I].view(v.rows, I)[R].cpu().numpy()
-    hs = atom_scales(ws[v.hs:], R, I // 32)
+    hs = atom_scales(ws[v.hs:], R, I // 32, v.tile_tokens)
     hrq, hrs = oracle.quant_mxfp8_f64(h)
     bad_q = np.nonzero((hq != hrq).any(1))[0]
     bad_s = np.nonzero((hs != hrs).any(1))[0]

@@ -16,19 +16,19 @@
 //   gate/up GEMM, item (expert e, 128 rows of I, token tile):
 //     G = Wg[e] x^T, U = Wu[e] x^T (two TMEM accumulators), epilogue
 //     h = silu(G) * U, MXFP8-quantised along I (a warp's 32 lanes are one
-//     32-row block of I) -> hq / hs in the padded token layout;
+//     32-row block of I) -> hq / hs in the tiled token layout;
 //   down GEMM, item (expert e, 128 or 256 rows of d, token tile):
 //     Y = Wd[e] h^T, epilogue yp[q][row] = topk_w[perm[q]] * Y (fp32), or,
 //     with the combine fused (large token tiles), yacc[perm[q] / k][row] +=
 //     topk_w[perm[q]] * Y by fp32 vector atomics in L2 (the k terms of a
 //     token are then summed in fp32 in an unspecified order).
 //
-// Token layout: the activations of expert e occupy `ntiles(e)` slots of SLOT
-// = roundup(NT, 128) rows starting at pad_off[e] (a multiple of 128); token r
-// of the expert sits at row pad_off[e] + (r / NT) * SLOT + r % NT.  So every
-// token tile starts on a 128-row boundary, and its scale factors are whole
-// 512-byte atoms (128 rows x 4 K-blocks) that one bulk copy moves and one
-// tcgen05.cp puts in TMEM.
+// Token layout: token tiles of NT rows are packed one after another; the
+// activations of expert e occupy `ntiles(e)` tiles starting at row pad_off[e]
+// (a multiple of NT), token r of the expert at row pad_off[e] + r.  Each
+// tile's scale factors are a 512-byte atom per 128 columns (the tile's rows
+// 0..NT-1 of a 128-row atom), which one bulk copy moves and one tcgen05.cp
+// puts in TMEM; only the codes of valid rows and whole atoms take memory.
 //
 // Persistent, warp-specialised CTA (256 or 384 threads, one per SM):
 //   warp 0     TMA producer 0 (first A tile via the packed-FP4 tensor map that
@@ -137,7 +137,7 @@ struct GemmArgs {
     const uint8_t *sfb;          // activation scale atoms [rows/128][KC][512]
     const int32_t *offsets;      // [E+1] segment starts in permuted order
     const int32_t *tiles;        // [E+1] first work item of each expert (tiles[E]: the item count)
-    const int32_t *pad_off;      // [E+1] first padded token row of each expert
+    const int32_t *pad_off;      // [E+1] first token row of each expert (tiled layout)
     const int2 *items;           // work-item table in execution order (fill_item_entries)
     const float *w_sorted;  // gate weight of each permuted row q (topk_w[perm[q]])
     uint8_t *hq;    // gate/up out: [rows][Ih] e4m3
@@ -161,7 +161,7 @@ struct Cfg {
     // weight bytes per stage, half the h traffic) up to 96-token tiles, one
     // tile beyond (so the accumulators still fit twice in TMEM).
     static constexpr int MATS = (MODE == GATEUP || NT <= 96) ? 2 : 1;
-    static constexpr int SLOT = (NT + 127) / 128 * 128;
+    static constexpr int SLOT = NT;  // rows a token tile occupies (tiles are packed)
     static constexpr int NAT = (NT + 127) / 128;  // B scale atoms per stage
     static constexpr uint32_t A_TILE = 128 * 128;  // smem bytes of one expanded FP4 A tile
     static constexpr uint32_t B_TILE = NT * 128;
@@ -284,7 +284,7 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    auto slot_row = [&](int e) { return s_pad[e]; };  // first padded row of expert e
+    auto slot_row = [&](int e) { return s_pad[e]; };  // first token row of expert e
     // Everything above reads only inputs of earlier kernels; the previous
     // kernel's outputs are read after this wait.
     pdl_enter();
@@ -339,7 +339,7 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
                         }
 #pragma unroll
                         for (int a = 0; a < C::NAT; ++a)
-                            bulk_load(sb + C::SFB_OFF + a * 512, p.sfb + (int64_t(R / 128 + a) * p.KC + kc) * 512, 512,
+                            bulk_load(sb + C::SFB_OFF + a * 512, p.sfb + (int64_t(R / NT + a) * p.KC + kc) * 512, 512,
                                       &full[stage]);
                     }
                     if (pr == 0) LMOE_TRACE_EV(0, 0x70 | MODE, it, kc);  // producer: copies issued
@@ -501,8 +501,7 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
 #pragma unroll
                         for (int j = 0; j < 16; ++j) sbl = (lane == j) ? sbv[j] : sbl;
                         const int64_t R = Rbase + c0 + lane;
-                        p.hs[((R >> 7) * p.KCh + (blk >> 2)) * 512 + (R & 31) * 16 + ((R & 127) >> 5) * 4 + (blk & 3)] =
-                            uint8_t(sbl);
+                        p.hs[tile_atom_off(R, blk, p.KCh, NT)] = uint8_t(sbl);
                     }
                 }
             }
@@ -658,17 +657,14 @@ __global__ void __launch_bounds__(1024) k_ffn_schedule(const int32_t *__restrict
     fill_item_entries(sc, tot * sc.MT_gu, tot * sc.MT_dn, threadIdx.x, blockDim.x);
 }
 
-// ---- activations into the padded token layout ------------------------------------------
+// ---- activations into the tiled token layout ------------------------------------------
 __device__ __forceinline__ int64_t pad_row(int r, int32_t pad, int NT, int SLOT)
 {
     return int64_t(pad) + int64_t(r / NT) * SLOT + (r % NT);
 }
-__device__ __forceinline__ int64_t atom_off(int64_t R, int b, int KC)
-{
-    return ((R >> 7) * KC + (b >> 2)) * 512 + (R & 31) * 16 + ((R & 127) >> 5) * 4 + (b & 3);
-}
 
-// bf16 x[T][d] -> MXFP8 rows at every padded row the token's pairs go to
+
+// bf16 x[T][d] -> MXFP8 rows at every token row the token's pairs go to
 // (dst_row, written by the permute).  Work unit (token t, destination group,
 // block b): block b of token t quantised and stored to the group's up to
 // SCATTER_KG destination rows; a token's groups are separate units, so more
@@ -740,12 +736,12 @@ __global__ void k_quant_scatter_pad(const uint16_t *__restrict__ x, int64_t nuni
             if (b == 0 && h == 0) w_sorted[__ldg(inv + p0 + j)] = __ldg(topk_w + p0 + j);
             const int64_t R = rows[j];
             *reinterpret_cast<uint4 *>(xq + R * d + b * 32 + h * 16) = make_uint4(c[0], c[1], c[2], c[3]);
-            if ((b & 3) == 0 && h == 0) *reinterpret_cast<uint32_t *>(xs + atom_off(R, b, KC)) = sb4;
+            if ((b & 3) == 0 && h == 0) *reinterpret_cast<uint32_t *>(xs + tile_atom_off(R, b, KC, sc.NT)) = sb4;
         }
     }
 }
 
-// MXFP8 rows xq/xs [T][d] (canonical) -> padded layout, row q of perm taking token perm[q]/k.
+// MXFP8 rows xq/xs [T][d] (canonical) -> tiled layout, row q of perm taking token perm[q]/k.
 __global__ void k_gather_pad(const uint8_t *__restrict__ xq, const uint8_t *__restrict__ xs, int64_t P, int d, int k,
                              int E, const int32_t *__restrict__ offsets, const int32_t *__restrict__ perm,
                              const float *__restrict__ topk_w, const int32_t *__restrict__ pad_off, int NT, int SLOT,
@@ -770,7 +766,7 @@ __global__ void k_gather_pad(const uint8_t *__restrict__ xq, const uint8_t *__re
             reinterpret_cast<uint4 *>(q_pad + R * d)[c] = __ldg(reinterpret_cast<const uint4 *>(xq + t * d) + c);
         } else {
             const int b = c - cq;
-            s_pad[atom_off(R, b, KC)] = __ldg(xs + t * nb + b);
+            s_pad[tile_atom_off(R, b, KC, NT)] = __ldg(xs + t * nb + b);
         }
     }
 }
@@ -867,10 +863,11 @@ FfnLayout ffn_layout(int64_t P, int d, int E, int I)
     FfnLayout L{};
     L.NT = P <= 4 * int64_t(E) ? 16 : (P <= 16 * int64_t(E) ? 32 : 96);
     L.fused = L.NT >= 64;  // Cfg<DOWN, NT>::STAGED
-    L.SLOT = int(round_up(L.NT, 128));
+    L.SLOT = L.NT;  // packed tiles
     const int64_t touched = P < E ? P : E;
-    L.rows = (ceil_div(P, L.NT) + touched) * L.SLOT;
-    const int64_t atoms = L.rows / 128 + 2;
+    const int64_t tiles = ceil_div(P, L.NT) + touched;  // bounds sum_e ceil(n_e / NT)
+    L.rows = tiles * L.SLOT;
+    const int64_t atoms = tiles;  // one atom per tile and 128 columns
     const int Ip = int(round_up(I, 128));
     size_t off = 0;
     auto take = [&](size_t bytes) {

@@ -65,7 +65,7 @@ bool weights_ok(const lmoe_expert_weights *W)
 
 // Workspace layout of lmoe_forward (each region 256-byte aligned):
 //   status | logits | idx | w | counts | offsets | perm | inv | permute scratch
-//   | ffn scratch (padded MXFP8 activations, h, schedule)
+//   | ffn scratch (tiled MXFP8 activations, h, schedule)
 //   | yp (per-pair outputs [T*k][d]) or, with the fused combine, yacc ([T][d] fp32 sums)
 // The small-batch path (lmoe_set_small_batch_pairs) uses
 //   status (+ the routing kernel's counter) | logits | idx | w | small-path scratch.

@@ -122,6 +122,17 @@ __device__ __forceinline__ float e4m3_to_f32(uint32_t code)
 }
 
 __host__ __device__ constexpr int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Scale byte of (token row R, block b) in the expert GEMMs' token layout:
+// tiles of NT rows packed one after another, each tile's scale factors one
+// 512-byte atom per 128 columns (KC atoms per tile); row rr = R % NT of the
+// tile at byte 16*(rr % 32) + 4*(rr / 32) + b % 4 of atom (tile * KC + b / 4).
+__host__ __device__ __forceinline__ int64_t tile_atom_off(int64_t R, int b, int KC, int NT)
+{
+    const int64_t tile = R / NT;
+    const int rr = int(R - tile * NT);
+    return (tile * KC + (b >> 2)) * 512 + (rr & 31) * 16 + (rr >> 5) * 4 + (b & 3);
+}
 __host__ __device__ constexpr int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
 
 // ---- host-side launch wrappers (each returns cudaError_t of the launch) --------------
@@ -154,10 +165,10 @@ cudaError_t launch_route(const uint16_t *x, const uint16_t *Wr3, const float *bi
                          float *logits, int32_t *idx, float *w, void *scratch, int32_t *status, cudaStream_t st);
 
 // Optional by-products of the permute for the expert GEMMs: per expert the
-// first slot row in the padded token layout (pad_off, E+1) and the first work
+// first token row in the tiled token layout (pad_off, E+1) and the first work
 // item of each GEMM (tiles_gu / tiles_dn, E+1), the expert of each token tile
 // (tile_info; the activation scatter turns it into the GEMMs' work-item
-// tables items_gu / items_dn), and per pair p its padded token row (dst_row,
+// tables items_gu / items_dn), and per pair p its token row (dst_row,
 // T*k).  pad_off == nullptr disables them.
 struct FfnSched {
     int NT = 0, SLOT = 0, MT_gu = 0, MT_dn = 0;
@@ -216,12 +227,12 @@ cudaError_t launch_permute(const int32_t *idx, int64_t P, int E, int32_t *counts
                            int32_t *inv, void *scratch, int32_t *status, cudaStream_t st,
                            const FfnSched &sched = FfnSched());
 
-// Expert FFN (tensor cores).  Activations live in a padded token layout
-// inside the FFN scratch: expert e's tokens fill slots of SLOT rows from
-// pad_off[e]; see k_ffn_tc.cu.
+// Expert FFN (tensor cores).  Activations live in a tiled token layout
+// inside the FFN scratch: expert e's tokens fill consecutive rows from
+// pad_off[e] (a whole number of NT-row tiles per expert); see k_ffn_tc.cu.
 struct FfnLayout {
-    int NT, SLOT;      // token tile and slot rows
-    int64_t rows;      // padded token rows reserved
+    int NT, SLOT;      // token tile and the rows a tile occupies (SLOT == NT: tiles are packed)
+    int64_t rows;      // token rows reserved (whole tiles)
     size_t pad_off, tiles_gu, tiles_dn, items_gu, items_dn, tile_info, xq, xs, hq, hs, hs_bytes, w_sorted, dst_row,
         total;  // byte offsets / sizes
     bool fused;  // large token tiles: the down GEMM can accumulate into the per-token output (FfnArgs::yacc)
@@ -245,12 +256,12 @@ struct FfnArgs {
 // slot starts and per-GEMM work-item prefixes from the segment offsets
 cudaError_t launch_ffn_schedule(const int32_t *offsets, int E, int d, int I, const FfnLayout &L, char *scratch,
                                 cudaStream_t st);
-// bf16 x[T][d] -> MXFP8 rows at each routed pair's padded row (dst_row from
+// bf16 x[T][d] -> MXFP8 rows at each routed pair's token row (dst_row from
 // the permute); also the gate weights in permuted order.
 // (also writes the expert GEMMs' work-item tables from the permute's tile_info)
 cudaError_t launch_quant_scatter_pad(const uint16_t *x, int T, int d, int k, int E, int I, const int32_t *inv,
                                      const float *topk_w, const FfnLayout &L, char *scratch, cudaStream_t st);
-// MXFP8 rows in token order -> padded layout (row q of perm takes token perm[q]/k)
+// MXFP8 rows in token order -> tiled layout (row q of perm takes token perm[q]/k)
 cudaError_t launch_gather_pad(const uint8_t *xq, const uint8_t *xs, int T, int d, int k, int E, const int32_t *offsets,
                               const int32_t *perm, const float *topk_w, const FfnLayout &L, char *scratch,
                               cudaStream_t st);
