@@ -49,6 +49,9 @@ def parse():
     ap.add_argument("--cpu-sample-tokens", type=int, default=16)
     # batches of up to this many pairs run the small-batch kernels (default: the library's)
     ap.add_argument("--small-batch-pairs", type=int, default=None)
+    # the decode run also measures the prefill and batch-1 workloads on the
+    # same resident bank (sub-records of its line); this skips them
+    ap.add_argument("--no-side-workloads", action="store_true")
     # launcher check without a GPU: the ranks start, meet over gloo and
     # report; nothing is measured and no bench line is printed
     ap.add_argument("--launch-selftest", action="store_true", help=argparse.SUPPRESS)
@@ -218,7 +221,122 @@ def setup_layer(wl, dev):
     x = gen.x_bf16(wl)
     xd = torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).to(dev).view(torch.bfloat16)
     torch.cuda.synchronize()
-    return layer, x, xd
+    return layer, x, xd, bank
+
+
+def roofline_for(wl, touched: int, ms_per_step: float, t_gu_s: float, peaks: dict, traffic=None) -> dict:
+    """The gate/up GEMM's roofline and the layer's fraction for a workload:
+    HBM-bound (weight bytes) below 16 pairs per expert, tensor-bound (FP8-rate
+    block-scaled MMA) above."""
+    per_expert_w = 3 * wl.I * wl.d * MXFP4_B
+    P = wl.T * wl.k
+    if P >= 16 * wl.E:
+        # prefill-shaped: the expert GEMMs are compute-bound; the block-scaled
+        # MMA (kind::mxf8f6f4) runs at the FP8 rate = 2 x the measured bf16 peak
+        fp8_peak = 2.0 * peaks["bf16_tflops"]
+        gu_flops = 2.0 * 2 * P * wl.d * wl.I            # gate + up GEMMs
+        expert_flops = 2.0 * 3 * P * wl.d * wl.I        # gate + up + down
+        proj_flops = 2.0 * 2 * wl.T * wl.d * wl.hidden  # block: the two bf16 projections
+        ideal_s = expert_flops / (fp8_peak * 1e12) + proj_flops / (peaks["bf16_tflops"] * 1e12)
+        return {"bound": "tensor", "kernel": "gate/up expert GEMM", "achieved": gu_flops / t_gu_s / 1e12,
+                "peak": fp8_peak, "unit": "TFLOP/s", "frac": gu_flops / t_gu_s / 1e12 / fp8_peak,
+                "traffic": traffic, "traffic_unit": "bytes per launch (ncu)",
+                "algorithmic_flops": gu_flops,
+                "peak_source": f"{peaks['source']} bf16 burst x 2 (nominal fp8 / bf16 ratio)",
+                "layer_tflops": (expert_flops + proj_flops) / (ms_per_step / 1e3) / 1e12,
+                "layer_frac": ideal_s / (ms_per_step / 1e3),
+                "layer_frac_note": "expert FLOPs at the FP8-rate peak"
+                                   + (" + projection FLOPs at the bf16 peak" if wl.hidden else "")
+                                   + ", as ideal time / measured step"}
+    gateup_bytes = touched * 2 * wl.I * wl.d * MXFP4_B  # weights the gate/up GEMM must stream once
+    achieved = gateup_bytes / t_gu_s / 1e9
+    layer_weight_gbs = touched * per_expert_w / (ms_per_step / 1e3) / 1e9
+    return {"bound": "hbm", "kernel": "gate/up expert GEMM", "achieved": achieved,
+            "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+            "traffic": traffic, "traffic_unit": "bytes per launch (ncu)",
+            "algorithmic_bytes": gateup_bytes, "peak_source": peaks["source"],
+            "layer_weight_gbs": layer_weight_gbs, "layer_frac": layer_weight_gbs / peaks["hbm_gbs"]}
+
+
+def time_steps(fwd, K: int, st, scrub=None) -> float:
+    """Device time of K forward passes (ms): back to back, or, with `scrub`
+    (a buffer larger than L2), each step timed alone after writing it."""
+    import torch
+    if scrub is None:
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        for _ in range(K):
+            fwd()
+        b.record(st)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for a, b in evs:
+        scrub.zero_()
+        a.record(st)
+        fwd()
+        b.record(st)
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in evs)
+
+
+def stage_times(lmoe, fwd, K: int, st, scrub=None) -> dict:
+    """Mean stage times (ms) over K passes with CUDA events at lmoe_forward's
+    stage boundaries (these serialise the launches)."""
+    import torch
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(lmoe.NUM_STAGE_EVENTS)] for _ in range(K)]
+    for row in evs:  # torch creates the CUDA event objects on first record
+        for e in row:
+            e.record(st)
+    torch.cuda.synchronize()
+    for i in range(K):
+        if scrub is not None:
+            scrub.zero_()
+        lmoe.set_stage_events(evs[i])
+        fwd()
+    torch.cuda.synchronize()
+    lmoe.set_stage_events(None)
+    return {name: sum(e[j].elapsed_time(e[j + 1]) for e in evs) / K for j, name in enumerate(lmoe.STAGES)}
+
+
+def side_record(lmoe, name: str, bank, Wr_dev, dev, steps: int, warmup: int, peaks: dict, scrub) -> dict:
+    """Another workload on the same resident expert bank, measured in the same
+    run: its own batch and workspace, timed like the headline (each step
+    alone after an L2 overwrite when its touched weights could stay in L2)."""
+    import numpy as np
+    import torch
+
+    import lmoe_inputs as gen
+    wl = gen.WORKLOADS[name]
+    assert (wl.E, wl.d, wl.I) == (bank.E, bank.d, bank.I) and not wl.hidden
+    bias = gen.router_bias(wl)
+    layer = lmoe.Layer(Wr_dev, bank, k=wl.k, bias=None if bias is None else torch.from_numpy(bias).to(dev))
+    x = torch.from_numpy(np.ascontiguousarray(gen.x_bf16(wl)).view(np.int16)).to(dev).view(torch.bfloat16)
+    y = torch.empty((wl.T, wl.d), dtype=torch.bfloat16, device=dev)
+    idx = torch.empty((wl.T, wl.k), dtype=torch.int32, device=dev)
+    st = torch.cuda.current_stream()
+
+    def fwd():
+        layer.forward(x, y=y, topk_idx=idx)
+    for _ in range(max(3, warmup)):
+        fwd()
+    torch.cuda.synchronize()
+    assert layer.device_status() == 0
+    touched = int((torch.bincount(idx.view(-1).long(), minlength=wl.E) > 0).sum())
+    per_expert_w = 3 * wl.I * wl.d * MXFP4_B
+    l2_bytes = scrub.numel() * 4 // 2
+    flush = touched * per_expert_w < 2 * l2_bytes
+    ms = time_steps(fwd, steps, st, scrub if flush else None) / steps
+    stages = stage_times(lmoe, fwd, min(steps, 50), st, scrub if flush else None)
+    small = lmoe.forward_workspace_views(wl.T, wl.d, wl.E, wl.k, wl.I).path == 1
+    layer._ws = None
+    roof = roofline_for(wl, touched, ms, stages["gate_up"] / 1e3, peaks, None if small else profiled_traffic(wl.name))
+    if small:
+        roof["kernel"] = "gate/up small-batch kernel (CUDA cores)"
+    return {"workload": wl.name, "T": wl.T, "steps": steps, "ms_per_step": ms, "value": wl.T / (ms / 1e3),
+            "unit": UNIT, "path": "small-batch kernels" if small else "tensor-core kernels",
+            "l2": "flushed before every step" if flush else "inputs larger than L2", "touched_experts": touched,
+            "roofline": roof, "stage_ms": stages}
 
 
 def cpu_baseline(wl, ntok: int):
@@ -262,7 +380,7 @@ def run_ours(args, ws, rank, local):
     if args.small_batch_pairs is not None:
         lmoe.set_small_batch_pairs(args.small_batch_pairs)
     small = lmoe.forward_workspace_views(wl.T, wl.d, wl.E, wl.k, wl.I).path == 1
-    layer, x, xd = setup_layer(wl, dev)
+    layer, x, xd, bank = setup_layer(wl, dev)
     T = wl.T
     st = torch.cuda.current_stream()
     idx = torch.empty((T, wl.k), dtype=torch.int32, device=dev)
@@ -386,36 +504,11 @@ def run_ours(args, ws, rank, local):
     barrier(ws)
 
     peaks = load_peaks()
-    gateup_bytes = touched * 2 * wl.I * wl.d * MXFP4_B  # weights the gate/up GEMM must stream once
     t_gu = stage_ms["gate_up"] / 1e3
-    layer_weight_gbs = touched * per_expert_w / (ms_per_step / 1e3) / 1e9
     launches_per_step = lmoe.forward_kernel_count(T, wl.d, wl.E, wl.k, wl.I) + (2 if wl.hidden else 0)
-    P = T * wl.k
-    if P >= 16 * wl.E:
-        # prefill-shaped: the expert GEMMs are compute-bound; the block-scaled
-        # MMA (kind::mxf8f6f4) runs at the FP8 rate = 2 x the measured bf16 peak
-        fp8_peak = 2.0 * peaks["bf16_tflops"]
-        gu_flops = 2.0 * 2 * P * wl.d * wl.I            # gate + up GEMMs
-        expert_flops = 2.0 * 3 * P * wl.d * wl.I        # gate + up + down
-        proj_flops = 2.0 * 2 * T * wl.d * wl.hidden     # block: the two bf16 projections
-        ideal_s = expert_flops / (fp8_peak * 1e12) + proj_flops / (peaks["bf16_tflops"] * 1e12)
-        roofline = {"bound": "tensor", "kernel": "gate/up expert GEMM", "achieved": gu_flops / t_gu / 1e12,
-                    "peak": fp8_peak, "unit": "TFLOP/s", "frac": gu_flops / t_gu / 1e12 / fp8_peak,
-                    "traffic": profiled_traffic(wl.name), "traffic_unit": "bytes per launch (ncu)",
-                    "algorithmic_flops": gu_flops,
-                    "peak_source": f"{peaks['source']} bf16 burst x 2 (nominal fp8 / bf16 ratio)",
-                    "layer_tflops": (expert_flops + proj_flops) / (ms_per_step / 1e3) / 1e12,
-                    "layer_frac": ideal_s / (ms_per_step / 1e3),
-                    "layer_frac_note": "expert FLOPs at the FP8-rate peak"
-                                       + (" + projection FLOPs at the bf16 peak" if wl.hidden else "")
-                                       + ", as ideal time / measured step"}
-    else:
-        achieved = gateup_bytes / t_gu / 1e9
-        roofline = {"bound": "hbm", "kernel": "gate/up expert GEMM", "achieved": achieved,
-                    "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                    "traffic": profiled_traffic(wl.name), "traffic_unit": "bytes per launch (ncu)",
-                    "algorithmic_bytes": gateup_bytes, "peak_source": peaks["source"],
-                    "layer_weight_gbs": layer_weight_gbs, "layer_frac": layer_weight_gbs / peaks["hbm_gbs"]}
+    roofline = roofline_for(wl, touched, ms_per_step, t_gu, peaks, None if small else profiled_traffic(wl.name))
+    if small:
+        roofline["kernel"] = "gate/up small-batch kernel (CUDA cores)"
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -437,6 +530,23 @@ def run_ours(args, ws, rank, local):
                 "d2h_bytes_per_step": yh.numel() * 2},
         "gpu_launches": K * launches_per_step, "clocks": clocks,
     }
+    if ws == 1 and wl.name == "decode" and not args.no_side_workloads:
+        # The same run, on the same resident expert bank: the headline re-timed
+        # with L2 written over before every step, then the prefill (T = 8192)
+        # and batch-1 (T = 1) workloads as sub-records with their own rooflines.
+        scrub_all = scrub if scrub is not None else torch.empty(2 * l2_bytes // 4, dtype=torch.float32,
+                                                                  device=dev)
+        side_sampler = ClockSampler(uuid)
+        side_sampler.start()
+        time.sleep(0.3)
+        K3 = min(K, 100)
+        ms_fl = time_steps(lambda: fwd(xin), K3, st, scrub_all) / K3
+        line["l2_flushed"] = {"ms_per_step": ms_fl, "value": whole_job_rate(T, ws, ms_fl), "unit": UNIT, "steps": K3,
+                              "note": f"each step timed alone after writing {scrub_all.numel() * 4 / 1e6:.0f} MB "
+                                      "(more than L2), not timed"}
+        line["side_workloads"] = [side_record(lmoe, "prefill", bank, layer.Wr, dev, 10, 3, peaks, scrub_all),
+                                  side_record(lmoe, "decode1", bank, layer.Wr, dev, 100, 5, peaks, scrub_all)]
+        line["side_workloads_clocks"] = side_sampler.stop()
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, args.cpu_sample_tokens)
     if rank == 0:
