@@ -122,6 +122,21 @@ def test_topk_ties_and_signed_zero(cuda_lib):
     l[3, 100:140] = 7.0
     l[4] = -1e30
     l[5, 895] = 50.0
+    # rows 6 and 7: exactly 64 and 65 values at or above the 16th largest of
+    # the 32 lane maxima (lane j holds experts j, j+32, ...), the extra ones
+    # tied at that bound: the selection's compacted-candidate limit and the
+    # first count past it
+    for r, extra in ((6, 48), (7, 49)):
+        row = (np.float32(-10.0) - rng.random(E).astype(np.float32)).astype(np.float32)
+        row[:32] = np.float32(1.0) + np.float32(0.01) * np.arange(32, dtype=np.float32)
+        n, i = 0, 1
+        while n < extra:
+            for lane in range(17, 32):
+                if n < extra:
+                    row[lane + 32 * i] = row[16]
+                    n += 1
+            i += 1
+        l[r] = row
     for E2, k2 in ((896, 16), (32, 32), (1, 1), (2048, 16), (300, 5)):
         ll = l[:, :E2] if E2 <= E else np.tile(l, (1, 3))[:, :E2].copy()
         idx, w = lmoe.topk_from_logits(torch.from_numpy(np.ascontiguousarray(ll)).to(DEV), k2)

@@ -695,9 +695,14 @@ __global__ void k_quant_scatter_pad(const uint16_t *__restrict__ x, int64_t nuni
         const int nj = min(SCATTER_KG, k - j0);
         const int64_t p0 = t * k + j0;  // first pair of the group
         // destination rows first: their loads overlap the quantisation below
-        int32_t rows[SCATTER_KG];
+        // a pair the permute rejected (expert id out of range, inv < 0) has
+        // no token row: nothing is stored for it
+        int32_t rows[SCATTER_KG], qs[SCATTER_KG];
 #pragma unroll
-        for (int j = 0; j < SCATTER_KG; ++j) rows[j] = j < nj ? __ldg(dst_row + p0 + j) : 0;
+        for (int j = 0; j < SCATTER_KG; ++j) {
+            qs[j] = j < nj ? __ldg(inv + p0 + j) : -1;
+            rows[j] = qs[j] >= 0 ? __ldg(dst_row + p0 + j) : -1;
+        }
         const uint4 *src = reinterpret_cast<const uint4 *>(x + t * d + b * 32 + h * 16);
         uint4 raw[2];
 #pragma unroll
@@ -733,12 +738,96 @@ __global__ void k_quant_scatter_pad(const uint16_t *__restrict__ x, int64_t nuni
 #pragma unroll
         for (int j = 0; j < SCATTER_KG; ++j) {
             if (j >= nj) break;
-            if (b == 0 && h == 0) w_sorted[__ldg(inv + p0 + j)] = __ldg(topk_w + p0 + j);
+            if (rows[j] < 0) continue;
+            if (b == 0 && h == 0) w_sorted[qs[j]] = __ldg(topk_w + p0 + j);
             const int64_t R = rows[j];
             *reinterpret_cast<uint4 *>(xq + R * d + b * 32 + h * 16) = make_uint4(c[0], c[1], c[2], c[3]);
             if ((b & 3) == 0 && h == 0) *reinterpret_cast<uint32_t *>(xs + tile_atom_off(R, b, KC, sc.NT)) = sb4;
         }
     }
+}
+
+// The same for large batches, one token at a time per CTA: the CTA rounds
+// the token's row to MXFP8 once into shared memory (thread b: block b of 32
+// elements), then one thread sends the row to each of the token's k token
+// rows by bulk asynchronous copies (shared -> global, whole 3.5 KB rows);
+// the scale bytes (4 blocks per 32-bit word of the atom layout) go out as
+// plain stores.  Two row buffers: one token's copies run while the next
+// token is rounded.
+constexpr int SCATTER_ROWS_THREADS = 128;
+__global__ void __launch_bounds__(SCATTER_ROWS_THREADS) k_quant_scatter_rows(
+    const uint16_t *__restrict__ x, int T, int d, int k, const int32_t *__restrict__ dst_row,
+    const int32_t *__restrict__ inv, const float *__restrict__ topk_w, uint8_t *__restrict__ xq, uint8_t *__restrict__ xs,
+    float *__restrict__ w_sorted, FfnSched sc, int E)
+{
+    extern __shared__ __align__(128) uint8_t qrow_smem[];  // [2][d] e4m3 codes
+    __shared__ int32_t rows_s[2][32];
+    pdl_enter();
+    fill_item_entries(sc, sc.tiles_gu[E], sc.tiles_dn[E], blockIdx.x * int64_t(blockDim.x) + threadIdx.x,
+                      int64_t(gridDim.x) * blockDim.x);
+    const int nb = d / 32, KC = d / 128;
+    int it = 0;
+    for (int t = blockIdx.x; t < T; t += gridDim.x, ++it) {
+        uint8_t *buf = qrow_smem + (it & 1) * d;
+        int32_t *rows = rows_s[it & 1];
+        // the copies that read this buffer two tokens ago have read it
+        if (threadIdx.x == 0) tc::bulk_wait_read<1>();
+        if (threadIdx.x < k) {
+            const int64_t p = int64_t(t) * k + threadIdx.x;
+            const int32_t q = __ldg(inv + p);  // < 0: the permute rejected the pair
+            rows[threadIdx.x] = q >= 0 ? __ldg(dst_row + p) : -1;
+            if (q >= 0) w_sorted[q] = __ldg(topk_w + p);
+        }
+        __syncthreads();
+        for (int b0 = 0; b0 < nb; b0 += blockDim.x) {
+            const int b = b0 + threadIdx.x;
+            uint32_t sb = 0;
+            if (b < nb) {
+                const uint4 *src = reinterpret_cast<const uint4 *>(x + int64_t(t) * d + b * 32);
+                uint4 raw[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) raw[i] = __ldg(src + i);
+                const uint32_t *rw = reinterpret_cast<const uint32_t *>(raw);
+                float v[32];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    v[2 * i] = __uint_as_float(rw[i] << 16);
+                    v[2 * i + 1] = __uint_as_float(rw[i] & 0xFFFF0000u);
+                }
+                uint32_t amax = 0;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) amax = max(amax, __float_as_uint(v[i]) & 0x7FFFFFFFu);
+                sb = mx_scale_byte(__uint_as_float(amax), 8);
+                const float iv = mx_inv_scale(sb);
+                uint32_t c[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    c[i] = e4m3x4(v[4 * i] * iv, v[4 * i + 1] * iv, v[4 * i + 2] * iv, v[4 * i + 3] * iv);
+                uint4 *dst = reinterpret_cast<uint4 *>(buf + b * 32);
+                dst[0] = make_uint4(c[0], c[1], c[2], c[3]);
+                dst[1] = make_uint4(c[4], c[5], c[6], c[7]);
+            }
+            // blocks 4c .. 4c+3 sit in adjacent lanes (nb and b0 are multiples of 4)
+            uint32_t sb4 = sb;
+            sb4 |= __shfl_down_sync(0xFFFFFFFFu, sb, 1) << 8;
+            sb4 |= __shfl_down_sync(0xFFFFFFFFu, sb, 2) << 16;
+            sb4 |= __shfl_down_sync(0xFFFFFFFFu, sb, 3) << 24;
+            if (b < nb && (b & 3) == 0) {
+                for (int j = 0; j < k; ++j) {
+                    const int32_t R = rows[j];
+                    if (R >= 0) *reinterpret_cast<uint32_t *>(xs + tile_atom_off(R, b, KC, sc.NT)) = sb4;
+                }
+            }
+        }
+        tc::fence_async_shared();  // the row's generic-proxy writes, before the async copies read it
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            for (int j = 0; j < k; ++j)
+                if (rows[j] >= 0) tc::bulk_store(xq + int64_t(rows[j]) * d, buf, uint32_t(d));
+            tc::bulk_commit();
+        }
+    }
+    if (threadIdx.x == 0) tc::bulk_wait<0>();  // the copies are complete before the grid is
 }
 
 // MXFP8 rows xq/xs [T][d] (canonical) -> tiled layout, row q of perm taking token perm[q]/k.
@@ -922,11 +1011,31 @@ FfnSched ffn_sched(const FfnLayout &L, int d, int I, char *scratch)
     return sc;
 }
 
+// Batches from this many tokens take the whole-row scatter (k_quant_scatter_rows).
+constexpr int kScatterRowsMinTokens = 1024;
+
 cudaError_t launch_quant_scatter_pad(const uint16_t *x, int T, int d, int k, int E, int I, const int32_t *inv,
                                      const float *topk_w, const FfnLayout &L, char *scratch, cudaStream_t st)
 {
     const int64_t nunits = int64_t(T) * ceil_div(k, SCATTER_KG) * (d / 32);
     if (nunits == 0) return cudaSuccess;
+    if (T >= kScatterRowsMinTokens) {
+        // one token per CTA at a time, whole rows by bulk copies
+        const int grid = T < 16 * num_sms() ? T : 16 * num_sms();
+        const size_t smem = size_t(2) * d;
+        if (smem > 48 * 1024) {
+            cudaError_t e = cudaFuncSetAttribute(k_quant_scatter_rows, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 int(smem));
+            if (e != cudaSuccess) return e;
+        }
+        const cudaError_t le_ = launch_pdl(
+            k_quant_scatter_rows, dim3(grid), dim3(SCATTER_ROWS_THREADS), smem, st, x, T, d, k,
+            reinterpret_cast<const int32_t *>(scratch + L.dst_row), inv, topk_w, reinterpret_cast<uint8_t *>(scratch + L.xq),
+            reinterpret_cast<uint8_t *>(scratch + L.xs), reinterpret_cast<float *>(scratch + L.w_sorted),
+            ffn_sched(L, d, I, scratch), E);
+        if (le_ != cudaSuccess) return le_;
+        return cudaGetLastError();
+    }
     const int grid = int(ceil_div(2 * nunits, 128) < 152 * 32 ? ceil_div(2 * nunits, 128) : 152 * 32);
     {
         const cudaError_t le_ = launch_pdl(k_quant_scatter_pad, dim3(grid), dim3(128), 0, st, x, nunits, d, k, reinterpret_cast<const int32_t *>(scratch + L.dst_row), inv, topk_w, reinterpret_cast<uint8_t *>(scratch + L.xq), reinterpret_cast<uint8_t *>(scratch + L.xs), reinterpret_cast<float *>(scratch + L.w_sorted), ffn_sched(L, d, I, scratch), E);

@@ -4,9 +4,9 @@
 //
 //   1. k_perm_hist    per chunk of CHUNK pairs: histogram over experts
 //                     (shared-memory atomics only count, so order-free).
-//   2. k_perm_scan    per expert: exclusive scan over chunks, counts; then an
-//                     exclusive scan over experts -> offsets; every chunk's
-//                     start position per expert.
+//   2. k_perm_scan    per expert: exclusive scan over chunks (each chunk's
+//                     start within the expert), counts; then an exclusive scan
+//                     over experts -> offsets.
 //   3. k_perm_scatter per chunk, 8 warps on 8 consecutive sub-chunks: per-warp
 //                     histograms -> each warp's start per expert; each warp then
 //                     walks its pairs in order, ranking equal experts within a
@@ -16,7 +16,7 @@
 namespace lmoe {
 namespace {
 
-constexpr int CHUNK = 4096;
+constexpr int CHUNK = PERMUTE_CHUNK;
 constexpr int WARPS = 8;
 constexpr int SUB = CHUNK / WARPS;  // 512 pairs per warp
 constexpr int MAXE = 2048;
@@ -108,11 +108,18 @@ __global__ void __launch_bounds__(1024) k_perm_scan(int32_t *__restrict__ blockh
     __shared__ int32_t cnt[MAXE];
     __shared__ int32_t warp_tot[32];
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        // 16 chunks' counts loaded before any is overwritten, so the loads
+        // overlap instead of one round trip per chunk
         int32_t run = 0;
-        for (int b = 0; b < nblk; ++b) {
-            const int32_t c = blockhist[int64_t(b) * E + e];
-            blockhist[int64_t(b) * E + e] = run;
-            run += c;
+        for (int b0 = 0; b0 < nblk; b0 += 16) {
+            int32_t c[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) c[j] = b0 + j < nblk ? blockhist[int64_t(b0 + j) * E + e] : 0;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                if (b0 + j < nblk) blockhist[int64_t(b0 + j) * E + e] = run;
+                run += c[j];
+            }
         }
         cnt[e] = run;
         counts[e] = run;
@@ -144,13 +151,8 @@ __global__ void __launch_bounds__(1024) k_perm_scan(int32_t *__restrict__ blockh
     if (i0 < E) offsets[i0] = excl;
     if (i0 + 1 < E) offsets[i0 + 1] = excl + a;
     if (i0 + 1 == E || i0 + 2 == E) offsets[E] = excl + a + (i0 + 1 < E ? b : 0);
-    __syncthreads();
-    // chunk starts: offsets[e] + exclusive count over earlier chunks
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        const int32_t base = offsets[e];
-        for (int bb = 0; bb < nblk; ++bb) blockhist[int64_t(bb) * E + e] += base;
-    }
     if (sc.pad_off) {
+        __syncthreads();
         __shared__ int32_t tmp[MAXE], scn[MAXE + 1];
         ffn_schedule_from_counts<1024>(cnt, E, sc, tmp, scn, warp_tot);
     }
@@ -178,9 +180,10 @@ __global__ void __launch_bounds__(256) k_perm_scatter(const int32_t *__restrict_
         if (my[i] >= 0) atomicAdd(&wh[wid * E + my[i]], 1);
     }
     __syncthreads();
-    // per expert: exclusive scan over the warps, plus the chunk start
+    // per expert: exclusive scan over the warps, plus the chunk's start
+    // (the expert's offset + the chunk's start within the expert)
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        int32_t run = blockstart[int64_t(blockIdx.x) * E + e];
+        int32_t run = blockstart[int64_t(blockIdx.x) * E + e] + __ldg(offsets + e);
 #pragma unroll
         for (int w = 0; w < WARPS; ++w) {
             const int32_t c = wh[w * E + e];

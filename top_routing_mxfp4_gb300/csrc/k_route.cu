@@ -16,10 +16,11 @@ template <int NV>
 __global__ void __launch_bounds__(256) k_topk_softmax(const float *__restrict__ logits, int T, int E, int k,
                                                       int32_t *__restrict__ idx, float *__restrict__ w)
 {
+    __shared__ float2 cand[8][64];  // per warp: the selection's candidates
     pdl_enter();
     const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (t >= T) return;
-    select_topk<NV>(logits + int64_t(t) * E, E, k, idx + int64_t(t) * k, w + int64_t(t) * k);
+    select_topk<NV>(logits + int64_t(t) * E, E, k, idx + int64_t(t) * k, w + int64_t(t) * k, cand[threadIdx.x >> 5]);
 }
 
 // Split-K partial logits summed in slice order (then + bias), written to
@@ -44,7 +45,7 @@ __global__ void __launch_bounds__(NTHREADS) k_reduce_topk(const float *__restric
         logits[base + e] = v;
     }
     __syncthreads();
-    if (threadIdx.x < 32) select_topk<NV>(row, E, k, idx + int64_t(t) * k, w + int64_t(t) * k);
+    if (threadIdx.x < 32) select_topk<NV, false>(row, E, k, idx + int64_t(t) * k, w + int64_t(t) * k, nullptr);
 }
 
 }  // namespace

@@ -124,6 +124,7 @@ __global__ void __launch_bounds__(32 * R_WARPS, 2) k_small_route(const uint16_t 
     uint16_t *x_s = reinterpret_cast<uint16_t *>(r_smem);  // [T][d] bf16
     __shared__ float hsum[R_WARPS][TMAX];
     __shared__ int s_last;
+    __shared__ float2 s_cand[TMAX][64];  // per selecting warp: the selection's candidates
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     pdl_enter();
     const int nch = d / 16;  // 16-byte chunks of a half row
@@ -241,9 +242,10 @@ __global__ void __launch_bounds__(32 * R_WARPS, 2) k_small_route(const uint16_t 
     __syncthreads();
     if (warp < T) {
         const int t = warp;
-        if (E <= 256) select_topk<8>(lg_s + t * E, E, k, idx + int64_t(t) * k, wts + int64_t(t) * k);
-        else if (E <= 896) select_topk<28>(lg_s + t * E, E, k, idx + int64_t(t) * k, wts + int64_t(t) * k);
-        else select_topk<64>(lg_s + t * E, E, k, idx + int64_t(t) * k, wts + int64_t(t) * k);
+        float2 *cand = s_cand[t];
+        if (E <= 256) select_topk<8>(lg_s + t * E, E, k, idx + int64_t(t) * k, wts + int64_t(t) * k, cand);
+        else if (E <= 896) select_topk<28>(lg_s + t * E, E, k, idx + int64_t(t) * k, wts + int64_t(t) * k, cand);
+        else select_topk<64>(lg_s + t * E, E, k, idx + int64_t(t) * k, wts + int64_t(t) * k, cand);
     }
     __syncthreads();
     // pairs sorted by (expert, pair id): position = number of pairs before it

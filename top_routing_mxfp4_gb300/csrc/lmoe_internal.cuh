@@ -222,6 +222,9 @@ __device__ __forceinline__ void fill_item_entries(const FfnSched &sc, int n_gu, 
         *dst = make_int2(ti.x | (m << 16), ti.y);
     }
 }
+// pairs per block of the multi-block permute (its scratch: one histogram of
+// E counts per block)
+constexpr int PERMUTE_CHUNK = 2048;
 size_t permute_scratch_bytes(int64_t P, int E);
 cudaError_t launch_permute(const int32_t *idx, int64_t P, int E, int32_t *counts, int32_t *offsets, int32_t *perm,
                            int32_t *inv, void *scratch, int32_t *status, cudaStream_t st,

@@ -29,7 +29,8 @@ namespace {
 // LMOE_PERMUTE_NOALLOC_MAX_PAIRS pairs and 2048 experts
 constexpr size_t kStatusBytes = 256;
 constexpr size_t kScratchBytes =
-    kStatusBytes + size_t((LMOE_PERMUTE_NOALLOC_MAX_PAIRS + 4095) / 4096) * 2048 * sizeof(int32_t);
+    kStatusBytes + size_t((LMOE_PERMUTE_NOALLOC_MAX_PAIRS + lmoe::PERMUTE_CHUNK - 1) / lmoe::PERMUTE_CHUNK) * 2048 *
+                       sizeof(int32_t);
 
 static __device__ __align__(256) uint8_t g_permute_scratch[kScratchBytes];
 

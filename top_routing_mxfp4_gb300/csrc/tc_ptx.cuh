@@ -106,6 +106,13 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, int x, int 
                  "r"(smem_u32(src))
                  : "memory");
 }
+// Shared -> global bulk copy of a contiguous range (both addresses 16-byte
+// aligned, size % 16 == 0), in this thread's current bulk async group.
+__device__ __forceinline__ void bulk_store(void *dst, const void *src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(smem_u32(src)), "r"(bytes)
+                 : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until at most N of this thread's bulk groups still read shared memory.
 template <int N>
