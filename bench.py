@@ -107,8 +107,9 @@ def gemm_source_hash() -> str:
 
 
 def profiled_traffic(workload: str):
-    """DRAM bytes per gate/up launch from the committed ncu summary of this
-    workload, or None when the GEMM source has changed since the capture."""
+    """DRAM bytes per step of the expert GEMMs (the fused kernel, or gate/up +
+    down) from the committed ncu summary of this workload, or None when the
+    GEMM source has changed since the capture."""
     path = os.path.join(ROOT, "profiles", f"k_moe_gemm_{workload}.md")
     if not os.path.exists(path):
         return None
@@ -119,10 +120,12 @@ def profiled_traffic(workload: str):
             meta[k.strip()] = v.strip()
     if meta.get("gemm_source_sha256_16") != gemm_source_hash():
         return None
+    total = None
     for kv in meta.get("traffic_bytes_per_launch", "").split():
-        if kv.startswith("gate_up="):
-            return int(kv.split("=")[1])
-    return None
+        key, _, val = kv.partition("=")
+        if key in ("ffn", "gate_up", "down"):
+            total = (total or 0) + int(val)
+    return total
 
 
 def barrier(ws: int) -> None:
@@ -224,12 +227,16 @@ def setup_layer(wl, dev):
     return layer, x, xd, bank
 
 
-def roofline_for(wl, touched: int, ms_per_step: float, t_gu_s: float, peaks: dict, traffic=None) -> dict:
-    """The gate/up GEMM's roofline and the layer's fraction for a workload:
-    HBM-bound (weight bytes) below 16 pairs per expert, tensor-bound (FP8-rate
-    block-scaled MMA) above."""
+def roofline_for(wl, touched: int, ms_per_step: float, stages: dict, peaks: dict, traffic=None) -> dict:
+    """The roofline of the expert GEMMs (gate/up + down: one fused kernel for
+    decode-sized token tiles, two kernels otherwise; their time from the
+    stage events) and the layer's fraction for a workload: HBM-bound (the
+    touched experts' weight bytes) below 16 pairs per expert, tensor-bound
+    (FP8-rate block-scaled MMA) above."""
     per_expert_w = 3 * wl.I * wl.d * MXFP4_B
     P = wl.T * wl.k
+    t_ffn = (stages["gate_up"] + stages["down"]) / 1e3
+    kernel = "expert GEMMs (gate/up + down)"
     if P >= 16 * wl.E:
         # prefill-shaped: the expert GEMMs are compute-bound; the block-scaled
         # MMA (kind::mxf8f6f4) runs at the FP8 rate = 2 x the measured bf16 peak
@@ -238,23 +245,25 @@ def roofline_for(wl, touched: int, ms_per_step: float, t_gu_s: float, peaks: dic
         expert_flops = 2.0 * 3 * P * wl.d * wl.I        # gate + up + down
         proj_flops = 2.0 * 2 * wl.T * wl.d * wl.hidden  # block: the two bf16 projections
         ideal_s = expert_flops / (fp8_peak * 1e12) + proj_flops / (peaks["bf16_tflops"] * 1e12)
-        return {"bound": "tensor", "kernel": "gate/up expert GEMM", "achieved": gu_flops / t_gu_s / 1e12,
-                "peak": fp8_peak, "unit": "TFLOP/s", "frac": gu_flops / t_gu_s / 1e12 / fp8_peak,
-                "traffic": traffic, "traffic_unit": "bytes per launch (ncu)",
-                "algorithmic_flops": gu_flops,
+        t_gu = stages["gate_up"] / 1e3
+        return {"bound": "tensor", "kernel": kernel, "achieved": expert_flops / t_ffn / 1e12,
+                "peak": fp8_peak, "unit": "TFLOP/s", "frac": expert_flops / t_ffn / 1e12 / fp8_peak,
+                "traffic": traffic, "traffic_unit": "DRAM bytes per step of the expert GEMMs (ncu)",
+                "algorithmic_flops": expert_flops,
+                "gate_up_frac": gu_flops / t_gu / 1e12 / fp8_peak,
                 "peak_source": f"{peaks['source']} bf16 burst x 2 (nominal fp8 / bf16 ratio)",
                 "layer_tflops": (expert_flops + proj_flops) / (ms_per_step / 1e3) / 1e12,
                 "layer_frac": ideal_s / (ms_per_step / 1e3),
                 "layer_frac_note": "expert FLOPs at the FP8-rate peak"
                                    + (" + projection FLOPs at the bf16 peak" if wl.hidden else "")
                                    + ", as ideal time / measured step"}
-    gateup_bytes = touched * 2 * wl.I * wl.d * MXFP4_B  # weights the gate/up GEMM must stream once
-    achieved = gateup_bytes / t_gu_s / 1e9
-    layer_weight_gbs = touched * per_expert_w / (ms_per_step / 1e3) / 1e9
-    return {"bound": "hbm", "kernel": "gate/up expert GEMM", "achieved": achieved,
+    weight_bytes = touched * per_expert_w  # weights the expert GEMMs must stream once
+    achieved = weight_bytes / t_ffn / 1e9
+    layer_weight_gbs = weight_bytes / (ms_per_step / 1e3) / 1e9
+    return {"bound": "hbm", "kernel": kernel, "achieved": achieved,
             "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-            "traffic": traffic, "traffic_unit": "bytes per launch (ncu)",
-            "algorithmic_bytes": gateup_bytes, "peak_source": peaks["source"],
+            "traffic": traffic, "traffic_unit": "DRAM bytes per step of the expert GEMMs (ncu)",
+            "algorithmic_bytes": weight_bytes, "peak_source": peaks["source"],
             "layer_weight_gbs": layer_weight_gbs, "layer_frac": layer_weight_gbs / peaks["hbm_gbs"]}
 
 
@@ -330,9 +339,9 @@ def side_record(lmoe, name: str, bank, Wr_dev, dev, steps: int, warmup: int, pea
     stages = stage_times(lmoe, fwd, min(steps, 50), st, scrub if flush else None)
     small = lmoe.forward_workspace_views(wl.T, wl.d, wl.E, wl.k, wl.I).path == 1
     layer._ws = None
-    roof = roofline_for(wl, touched, ms, stages["gate_up"] / 1e3, peaks, None if small else profiled_traffic(wl.name))
+    roof = roofline_for(wl, touched, ms, stages, peaks, None if small else profiled_traffic(wl.name))
     if small:
-        roof["kernel"] = "gate/up small-batch kernel (CUDA cores)"
+        roof["kernel"] = "small-batch gate/up + down kernels (CUDA cores)"
     return {"workload": wl.name, "T": wl.T, "steps": steps, "ms_per_step": ms, "value": wl.T / (ms / 1e3),
             "unit": UNIT, "path": "small-batch kernels" if small else "tensor-core kernels",
             "l2": "flushed before every step" if flush else "inputs larger than L2", "touched_experts": touched,
@@ -504,11 +513,10 @@ def run_ours(args, ws, rank, local):
     barrier(ws)
 
     peaks = load_peaks()
-    t_gu = stage_ms["gate_up"] / 1e3
     launches_per_step = lmoe.forward_kernel_count(T, wl.d, wl.E, wl.k, wl.I) + (2 if wl.hidden else 0)
-    roofline = roofline_for(wl, touched, ms_per_step, t_gu, peaks, None if small else profiled_traffic(wl.name))
+    roofline = roofline_for(wl, touched, ms_per_step, stage_ms, peaks, None if small else profiled_traffic(wl.name))
     if small:
-        roofline["kernel"] = "gate/up small-batch kernel (CUDA cores)"
+        roofline["kernel"] = "small-batch gate/up + down kernels (CUDA cores)"
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,

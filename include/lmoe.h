@@ -298,8 +298,10 @@ int32_t lmoe_forward_kernel_count(const lmoe_dims *dims);
  * CUDA events (cudaEvent_t handles, created by the caller) on its stream at
  * the stage boundaries: [0] start, [1] after routing, [2] after permute,
  * [3] after the MXFP8 activation scatter, [4] after the gate/up GEMM,
- * [5] after the down GEMM, [6] after combine.  n = 0 clears the hook.  The
- * setting is process-wide and not thread-safe; it only adds event records. */
+ * [5] after the down GEMM, [6] after combine.  Where the two expert GEMMs run
+ * as one kernel (token tiles of up to 32 rows), [4] and [5] both follow that
+ * kernel.  n = 0 clears the hook.  The setting is process-wide and not
+ * thread-safe; it only adds event records. */
 #define LMOE_NUM_STAGE_EVENTS 7
 lmoe_status lmoe_set_stage_events(void *const *events, int32_t n);
 
@@ -347,7 +349,8 @@ lmoe_status lmoe_set_h_capture(float *h_f32, size_t bytes);
  * mbarrier in the expert GEMMs gives up after a limit of SM clocks (about
  * 2 s by default), records LMOE_ERR_TIMEOUT in the status word, and the
  * kernel winds down (an MMA issuer first waits, again bounded, for its MMAs
- * in flight) and returns.  With stall_first_fill set, the first pipeline
+ * in flight) and returns; so does the wait of a down item, in the kernel
+ * that runs both GEMMs, for its token tile's h.  With stall_first_fill set, the first pipeline
  * stage of every CTA of the following lmoe_forward / lmoe_expert_ffn calls
  * is never filled, so those waits run out after wait_limit_cycles; the host
  * then reads LMOE_ERR_TIMEOUT with lmoe_last_device_status.  (0, 0) restores

@@ -75,8 +75,8 @@ __device__ uint32_t g_lmoe_trace_n;
         }                                                                                                   \
     } while (0)
 __shared__ uint32_t s_trace[2 * 3 * TRACE_PER_ROLE];
-// Every CTA's start and end (%globaltimer, ns) per GEMM mode: [mode][cta][2].
-__device__ unsigned long long g_lmoe_cta_ns[2][1024][2];
+// Every CTA's start and end (%globaltimer, ns) per GEMM mode (gate/up, down, fused): [mode][cta][2].
+__device__ unsigned long long g_lmoe_cta_ns[3][1024][2];
 __device__ __forceinline__ unsigned long long lmoe_globaltimer()
 {
     unsigned long long t;
@@ -130,7 +130,11 @@ __device__ __forceinline__ void red_add_v4(float *dst, float4 v, uint64_t policy
                  : "memory");
 }
 
-enum { GATEUP = 0, DOWN = 1 };
+// FUSED: one persistent kernel runs the gate/up items and then the down
+// items; a down item's h loads wait until every gate/up item of its token
+// tile has stored h (a per-tile counter), so CTAs done with gate/up start on
+// down items instead of idling through the gate/up tail and a kernel boundary.
+enum { GATEUP = 0, DOWN = 1, FUSED = 2 };
 
 struct GemmArgs {
     const uint8_t *sfa0, *sfa1;  // weight scale atoms [E][RTa][KC][512]
@@ -152,6 +156,7 @@ struct GemmArgs {
     int32_t *status;
     long long wait_limit;  // SM clocks a bounded wait may take before it gives up
     int stall_first_fill;  // failure-path test only: producer 0 withholds each CTA's first stage
+    int32_t *tile_done;    // fused kernel: per token tile, epilogue warps done storing h (zeroed by the schedule)
 };
 
 template <int MODE, int NT>
@@ -202,7 +207,8 @@ struct Cfg {
     static constexpr int THREADS = 32 * (4 + EPI_WARPS);
     static constexpr int CW = NT < 32 ? NT : 32;  // accumulator columns per TMEM load (down)
     static constexpr int STG_STRIDE = 36;
-    static constexpr uint32_t EPI_WARP_BYTES = !STAGED ? 0 : (MODE == DOWN ? CW * STG_STRIDE * 4 : 16 * 32);
+    static constexpr uint32_t EPI_WARP_BYTES = !STAGED ? 0 : (MODE != GATEUP ? CW * STG_STRIDE * 4 : 16 * 32);
+    static_assert(MODE != FUSED || MATS == 2, "the fused kernel needs the same stage layout for both GEMMs");
     static constexpr uint32_t EPI_BYTES = EPI_WARPS * EPI_WARP_BYTES;
 };
 
@@ -231,8 +237,11 @@ __device__ __forceinline__ Item item_at(int2 v, const int32_t *s_off, int nt)
 template <int MODE, int NT>
 __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
     k_moe_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
-               const __grid_constant__ CUtensorMap tmB, const GemmArgs p)
+               const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmD,
+               const __grid_constant__ CUtensorMap tmH, const GemmArgs p, const GemmArgs q)
 {
+    // p: the kernel's GEMM (the gate/up GEMM in the fused kernel), q: the
+    // fused kernel's down GEMM (tmD: its weights, tmH: h); unused otherwise
     using C = Cfg<MODE, NT>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -256,11 +265,21 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
         s_pad[i] = __ldcg(p.pad_off + i);
         s_off[i] = __ldcg(p.offsets + i);
     }
-    const int total = __ldcg(p.tiles + p.E);
+    // fused: gate/up items [0, n_gu), then down items [n_gu, total)
+    const int n_gu = MODE == FUSED ? __ldcg(p.tiles + p.E) : 0;
+    const int total = MODE == FUSED ? n_gu + __ldcg(q.tiles + q.E) : __ldcg(p.tiles + p.E);
     const int G = int(gridDim.x);
     // this CTA's item-table entries at index i (clamped: entries past the end
     // are loaded but never used); the table may come from the previous kernel
-    auto entry = [&](int i) { return __ldcg(p.items + (i < total ? i : total - 1)); };
+    auto entry = [&](int i) {
+        const int j = i < total ? i : total - 1;
+        if (MODE == FUSED && j >= n_gu) return __ldcg(q.items + (j - n_gu));
+        return __ldcg(p.items + j);
+    };
+    auto mode_of = [&](int i) { return MODE == FUSED ? (i < n_gu ? int(GATEUP) : int(DOWN)) : int(MODE); };
+    // h of a token tile is complete once every epilogue warp of each of its
+    // gate/up items has counted itself in
+    [[maybe_unused]] const int h_ready = p.MTA * C::EPI_WARPS;
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 2);  // one expect_tx arrival per producer
@@ -278,6 +297,10 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
         prefetch_tensormap(&tmA0);
         if (C::MATS == 2) prefetch_tensormap(&tmA1);
         prefetch_tensormap(&tmB);
+        if (MODE == FUSED) {
+            prefetch_tensormap(&tmD);
+            prefetch_tensormap(&tmH);
+        }
     }
     if (warp == 1) tmem_alloc(tmem_slot, 512);
     tc_fence_before();
@@ -307,16 +330,20 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
                 const Item w = item_at(ent, s_off, NT);
                 ent = ent_next;
                 ent_next = entry(it + 2 * G);
+                const int mode = mode_of(it);
+                const GemmArgs &a = (MODE == FUSED && mode == DOWN) ? q : p;
                 const int R = slot_row(w.e) + w.n_tile * C::SLOT;
                 // gate/up: tile m of both matrices; down: tiles 2m and 2m+1 (an odd
                 // last tile loads tile 2m twice and the epilogue drops the copy)
-                const int mt0 = MODE == GATEUP ? w.m_tile : C::MATS * w.m_tile;
-                const int mt1 = MODE == GATEUP ? w.m_tile : (mt0 + 1 < p.MTA ? mt0 + 1 : mt0);
-                const int arow = w.e * p.Mtot + (pr == 0 ? mt0 : mt1) * 128;
-                const int64_t sfa_base = (int64_t(w.e) * p.MTA + (pr == 0 ? mt0 : mt1)) * p.KC;
-                const CUtensorMap *tmA = pr == 0 ? &tmA0 : &tmA1;
-                const uint8_t *sfa = pr == 0 ? p.sfa0 : p.sfa1;
-                for (int kc = 0; kc < p.KC; ++kc) {
+                const int mt0 = mode == GATEUP ? w.m_tile : C::MATS * w.m_tile;
+                const int mt1 = mode == GATEUP ? w.m_tile : (mt0 + 1 < a.MTA ? mt0 + 1 : mt0);
+                const int arow = w.e * a.Mtot + (pr == 0 ? mt0 : mt1) * 128;
+                const int64_t sfa_base = (int64_t(w.e) * a.MTA + (pr == 0 ? mt0 : mt1)) * a.KC;
+                const CUtensorMap *tmA = (MODE == FUSED && mode == DOWN) ? &tmD : (pr == 0 ? &tmA0 : &tmA1);
+                const CUtensorMap *tmBx = (MODE == FUSED && mode == DOWN) ? &tmH : &tmB;
+                const uint8_t *sfa = pr == 0 ? a.sfa0 : a.sfa1;
+                bool h_waited = !(MODE == FUSED && mode == DOWN);
+                for (int kc = 0; kc < a.KC; ++kc) {
                     if (!mbar_wait(&empty[stage], phase ^ 1, p.wait_limit)) {
                         set_status(p.status, LMOE_ERR_TIMEOUT);
                         ok = false;
@@ -329,17 +356,35 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
                     } else if (pr == 0) {
                         mbar_arrive_expect_tx(&full[stage], C::TX_BYTES0);
                         tma_load_2d(sb, tmA, kc * 128, arow, &full[stage]);
-                        tma_load_2d(sb + C::MATS * C::A_TILE, &tmB, kc * 128, R, &full[stage]);
                         bulk_load(sb + C::SFA_OFF, sfa + (sfa_base + kc) * 512, 512, &full[stage]);
+                        if (!h_waited) {
+                            // fused down item: the weights are on their way; h of
+                            // this token tile must be complete before it is read
+                            h_waited = wait_count(a.tile_done + R / NT, h_ready, p.wait_limit);
+                            if (!h_waited) {
+                                set_status(p.status, LMOE_ERR_TIMEOUT);
+                                ok = false;
+                                break;
+                            }
+                        }
+                        tma_load_2d(sb + C::MATS * C::A_TILE, tmBx, kc * 128, R, &full[stage]);
                     } else {
                         mbar_arrive_expect_tx(&full[stage], C::TX_BYTES1);
                         if (C::MATS == 2) {
                             tma_load_2d(sb + C::A_TILE, tmA, kc * 128, arow, &full[stage]);
                             bulk_load(sb + C::SFA_OFF + 512, sfa + (sfa_base + kc) * 512, 512, &full[stage]);
                         }
+                        if (!h_waited) {
+                            h_waited = wait_count(a.tile_done + R / NT, h_ready, p.wait_limit);
+                            if (!h_waited) {
+                                set_status(p.status, LMOE_ERR_TIMEOUT);
+                                ok = false;
+                                break;
+                            }
+                        }
 #pragma unroll
-                        for (int a = 0; a < C::NAT; ++a)
-                            bulk_load(sb + C::SFB_OFF + a * 512, p.sfb + (int64_t(R / NT + a) * p.KC + kc) * 512, 512,
+                        for (int a2 = 0; a2 < C::NAT; ++a2)
+                            bulk_load(sb + C::SFB_OFF + a2 * 512, a.sfb + (int64_t(R / NT + a2) * a.KC + kc) * 512, 512,
                                       &full[stage]);
                     }
                     if (pr == 0) LMOE_TRACE_EV(0, 0x70 | MODE, it, kc);  // producer: copies issued
@@ -364,6 +409,7 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
                 const Item w = item_at(ent, s_off, NT);
                 ent = ent_next;
                 ent_next = entry(it + 2 * G);
+                const int KCi = (MODE == FUSED && mode_of(it) == DOWN) ? q.KC : p.KC;
                 const uint32_t N = uint32_t((w.n_valid + 15) & ~15);
                 if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1, p.wait_limit)) {
                     set_status(p.status, LMOE_ERR_TIMEOUT);
@@ -373,7 +419,7 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
                 tc_fence_after();
                 if (iss == 0) LMOE_TRACE_EV(1, 0x20 | MODE, it, 0);  // mma: accumulator free
                 const uint32_t d = tmem + uint32_t(acc * C::ACC_COLS_ITEM + iss * NT);
-                for (int kc = 0; kc < p.KC; ++kc) {
+                for (int kc = 0; kc < KCi; ++kc) {
                     if (!mbar_wait(&full[stage], phase, p.wait_limit)) {
                         set_status(p.status, LMOE_ERR_TIMEOUT);
                         ok = false;
@@ -417,7 +463,7 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
         }
     } else {
         // ---------------- epilogue (warps 2 .. 1 + EPI_WARPS) ----------------
-        const int q = warp & 3;             // TMEM lane quarter of this warp
+        const int lq = warp & 3;            // TMEM lane quarter of this warp
         const int half = (warp - 2) >> 2;   // which of the quarter's NW warps
         // the fused combine's per-token fp32 rows take every pair's reduction:
         // keep them in L2 in preference to the streamed weights
@@ -432,9 +478,11 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
         // outstanding load before its item comes up; the item's table entry
         // was loaded two items before that.
         constexpr int NV = (NT + 31) / 32;
-        auto fetch = [&](int2 ent, Item &nx, float (&wn)[NV], int (&tn)[NV]) {
+        // the down GEMM's arguments (the fused kernel's second GEMM)
+        const GemmArgs &dn = MODE == FUSED ? q : p;
+        auto fetch = [&](int i, int2 ent, Item &nx, float (&wn)[NV], int (&tn)[NV]) {
             nx = item_at(ent, s_off, NT);
-            if (MODE == DOWN) {
+            if (mode_of(i) == DOWN) {
                 // Unconditional loads at clamped rows (entries past the tile are
                 // never used) of raw pair ids: a select or a division here would
                 // wait for the load.
@@ -442,13 +490,14 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
                 const int qlast = s_off[p.E] - 1;
 #pragma unroll
                 for (int i = 0; i < NV; ++i) {
-                    const int q = min(qb + 32 * i + lane, qlast);
-                    wn[i] = __ldg(p.w_sorted + q);
-                    tn[i] = __ldg(p.perm + q);
+                    const int qq = min(qb + 32 * i + lane, qlast);
+                    wn[i] = __ldg(dn.w_sorted + qq);
+                    tn[i] = __ldg(dn.perm + qq);
                 }
             }
         };
         auto process = [&](int it, const Item &w, const float (&wl)[NV], const int (&tl)[NV]) -> bool {
+            const int mode = mode_of(it);
             [[maybe_unused]] const int qbase = s_off[w.e] + w.n_tile * NT;  // first permuted row of the tile (down)
             if (threadIdx.x == 64) LMOE_TRACE_EV(2, 0x40 | MODE, it, 0);  // epilogue: waiting
             if (!mbar_wait(&acc_full[acc], acc_phase, p.wait_limit)) {
@@ -457,9 +506,9 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
             }
             tc_fence_after();
             if (threadIdx.x == 64) LMOE_TRACE_EV(2, 0x50 | MODE, it, 0);  // epilogue: accumulator ready
-            const uint32_t tbase = tmem + (uint32_t(32 * q) << 16) + uint32_t(acc * C::ACC_COLS_ITEM);
-            if (MODE == GATEUP && w.m_tile * 128 + 32 * q < p.Mtot) {
-                const int row0 = w.m_tile * 128 + 32 * q;  // first row of I held by this warp
+            const uint32_t tbase = tmem + (uint32_t(32 * lq) << 16) + uint32_t(acc * C::ACC_COLS_ITEM);
+            if (mode == GATEUP && w.m_tile * 128 + 32 * lq < p.Mtot) {
+                const int row0 = w.m_tile * 128 + 32 * lq;  // first row of I held by this warp
                 const int blk = row0 / 32;                 // MX block of I held by this warp
                 const int64_t Rbase = int64_t(slot_row(w.e)) + int64_t(w.n_tile) * C::SLOT;
                 for (int c0 = 16 * half; c0 < w.n_valid; c0 += 16 * C::NW) {
@@ -505,7 +554,15 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
                     }
                 }
             }
-            if (MODE == DOWN) {
+            if (MODE == FUSED && mode == GATEUP) {
+                // this warp's part of h for the token tile is stored: count it
+                // in (release), for the down items that read the tile's h
+                __threadfence();
+                asm volatile("fence.proxy.async.global;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) atomicAdd(p.tile_done + (slot_row(w.e) / NT + w.n_tile), 1);
+            }
+            if (mode == DOWN) {
                 // accumulator h holds output rows (MATS m + h) * 128 + 32q + lane;
                 // work units (h, column chunk) alternate between the quarter's NW warps
                 constexpr int CW = C::CW;
@@ -514,7 +571,7 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
                 for (int u = half; u < C::MATS * nch; u += C::NW) {
                     const int h = u / nch, c0 = (u - h * nch) * CW;
                     const int mt = C::MATS * w.m_tile + h;
-                    if (mt >= p.MTA) continue;  // odd last tile: second accumulator is a copy
+                    if (mt >= dn.MTA) continue;  // odd last tile: second accumulator is a copy
                     uint32_t v[CW];
                     tmem_ld_cols<CW>(tbase + h * NT + c0, v);
                     tmem_ld_wait();
@@ -526,7 +583,7 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
                         wsel = (c0 / 32 == i) ? wl[i] : wsel;
                         tsel = (c0 / 32 == i) ? tl[i] : tsel;
                     }
-                    tsel /= p.k;  // pair -> token
+                    tsel /= dn.k;  // pair -> token
                     if constexpr (C::STAGED) {
                         // transpose through shared memory: sf[c][row], row stride STG_STRIDE
                         __syncwarp();
@@ -535,7 +592,7 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
                         __syncwarp();
                         // lane l: token column c = 4 pp + l / 8, 4 rows starting at 4 (l % 8)
                         const int f4 = 4 * (lane & 7);
-                        const int col = mt * 128 + 32 * q + f4;
+                        const int col = mt * 128 + 32 * lq + f4;
 #pragma unroll
                         for (int pp = 0; pp < CW / 4; ++pp) {
                             const int c = 4 * pp + (lane >> 3);
@@ -547,19 +604,19 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
                                 a.y *= wc;
                                 a.z *= wc;
                                 a.w *= wc;
-                                if (p.yacc)
-                                    red_add_v4(p.yacc + int64_t(tc) * p.Mtot + col, a, keep_policy);
+                                if (dn.yacc)
+                                    red_add_v4(dn.yacc + int64_t(tc) * dn.Mtot + col, a, keep_policy);
                                 else
-                                    *reinterpret_cast<float4 *>(p.yp + int64_t(qbase + c0 + c) * p.Mtot + col) = a;
+                                    *reinterpret_cast<float4 *>(dn.yp + int64_t(qbase + c0 + c) * dn.Mtot + col) = a;
                             }
                         }
                     } else {
                         // lane = output row; each column's 32 rows are one 128-byte store
-                        float *yrow = p.yp + int64_t(qbase + c0) * p.Mtot + mt * 128 + 32 * q + lane;
+                        float *yrow = dn.yp + int64_t(qbase + c0) * dn.Mtot + mt * 128 + 32 * lq + lane;
 #pragma unroll
                         for (int j = 0; j < CW; ++j) {
                             const float wc = __shfl_sync(0xFFFFFFFFu, wsel, (c0 & 31) + j);
-                            if (c0 + j < w.n_valid) yrow[int64_t(j) * p.Mtot] = wc * __uint_as_float(v[j]);
+                            if (c0 + j < w.n_valid) yrow[int64_t(j) * dn.Mtot] = wc * __uint_as_float(v[j]);
                         }
                     }
                 }
@@ -576,19 +633,19 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
         Item nA{}, nB{};
         float wA[NV], wB[NV];
         int tA[NV], tB[NV];
-        if (int(blockIdx.x) < total) fetch(ent0, nA, wA, tA);
-        if (int(blockIdx.x) + G < total) fetch(ent1, nB, wB, tB);
+        if (int(blockIdx.x) < total) fetch(blockIdx.x, ent0, nA, wA, tA);
+        if (int(blockIdx.x) + G < total) fetch(blockIdx.x + G, ent1, nB, wB, tB);
         int2 eA = entry(blockIdx.x + 2 * G), eB = entry(blockIdx.x + 3 * G);  // next entries of the two sets
         for (int it = blockIdx.x; it < total; it += 2 * G) {
             if (!process(it, nA, wA, tA)) break;
             if (it + 2 * G < total) {
-                fetch(eA, nA, wA, tA);
+                fetch(it + 2 * G, eA, nA, wA, tA);
                 eA = entry(it + 4 * G);
             }
             if (it + G >= total) break;
             if (!process(it + G, nB, wB, tB)) break;
             if (it + 3 * G < total) {
-                fetch(eB, nB, wB, tB);
+                fetch(it + 3 * G, eB, nB, wB, tB);
                 eB = entry(it + 5 * G);
             }
         }
@@ -922,17 +979,25 @@ int gemm_stages(int E, size_t &smem)
     return st;
 }
 
+// One GEMM (MODE GATEUP / DOWN: maps a0, a1, b and `args`), or both in the
+// fused kernel (a0, a1, b and `args` the gate/up GEMM; d, h and `args2` the
+// down GEMM).
 template <int MODE, int NT>
 cudaError_t launch_gemm(const CUtensorMap &a0, const CUtensorMap &a1, const CUtensorMap &b, GemmArgs args,
-                        cudaStream_t st)
+                        cudaStream_t st, const CUtensorMap *d = nullptr, const CUtensorMap *h = nullptr,
+                        const GemmArgs *args2 = nullptr)
 {
     size_t smem = 0;
     args.stages = gemm_stages<MODE, NT>(args.E, smem);
     if (args.stages < 2) return cudaErrorInvalidConfiguration;
+    if (MODE == FUSED && (!d || !h || !args2)) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(k_moe_gemm<MODE, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
+    GemmArgs q = args2 ? *args2 : args;
+    q.stages = args.stages;
     {
-        const cudaError_t le_ = launch_pdl(k_moe_gemm<MODE, NT>, dim3(num_sms()), dim3(Cfg<MODE, NT>::THREADS), smem, st, a0, a1, b, args);
+        const cudaError_t le_ = launch_pdl(k_moe_gemm<MODE, NT>, dim3(num_sms()), dim3(Cfg<MODE, NT>::THREADS), smem, st,
+                                           a0, a1, b, d ? *d : a0, h ? *h : b, args, q);
         if (le_ != cudaSuccess) return le_;
     }
     return cudaGetLastError();
@@ -978,6 +1043,7 @@ FfnLayout ffn_layout(int64_t P, int d, int E, int I)
     L.hs_bytes = size_t(atoms) * (Ip / 128) * 512;
     L.w_sorted = take(size_t(P) * 4);
     L.dst_row = take(size_t(P) * 4);
+    L.tile_done = take(size_t(max_tiles) * 4);
     L.total = off;
     return L;
 }
@@ -1008,6 +1074,7 @@ FfnSched ffn_sched(const FfnLayout &L, int d, int I, char *scratch)
     sc.tile_info = reinterpret_cast<int2 *>(scratch + L.tile_info);
     sc.band = L.NT >= 64 ? kDownBands : 0;  // Cfg<DOWN, NT>::STAGED: the fused combine
     sc.dst_row = reinterpret_cast<int32_t *>(scratch + L.dst_row);
+    sc.tile_done = reinterpret_cast<int32_t *>(scratch + L.tile_done);
     return sc;
 }
 
@@ -1103,31 +1170,37 @@ cudaError_t launch_expert_gemms(const FfnArgs &a, const FfnLayout &L, char *scra
     g.KC = a.d / 128;
     g.KCh = Ip / 128;
     g.Ih = a.I;
-    cudaError_t e = L.NT == 16   ? launch_gemm<GATEUP, 16>(mg, mu, mx, g, st)
-                    : L.NT == 32 ? launch_gemm<GATEUP, 32>(mg, mu, mx, g, st)
-                                 : launch_gemm<GATEUP, 96>(mg, mu, mx, g, st);
+    g.tile_done = reinterpret_cast<int32_t *>(scratch + L.tile_done);
+    // down
+    GemmArgs gd = g;
+    gd.sfa0 = a.W->down_s;
+    gd.sfa1 = a.W->down_s;  // the second tile of a down item is the next tile of the same matrix
+    gd.sfb = hs;
+    gd.tiles = reinterpret_cast<const int32_t *>(scratch + L.tiles_dn);
+    gd.items = reinterpret_cast<const int2 *>(scratch + L.items_dn);
+    gd.hcap = nullptr;
+    gd.yp = a.yp;
+    gd.yacc = a.yacc;
+    gd.perm = a.perm;
+    gd.k = a.k;
+    gd.Mtot = a.d;
+    gd.MTA = a.d / 128;
+    gd.KC = Ip / 128;
+    if (L.NT <= 32) {
+        // decode-sized token tiles: both GEMMs in one persistent kernel (the
+        // stage-boundary event, if asked for, follows it)
+        cudaError_t e = L.NT == 16 ? launch_gemm<FUSED, 16>(mg, mu, mx, g, st, &md, &mh, &gd)
+                                   : launch_gemm<FUSED, 32>(mg, mu, mx, g, st, &md, &mh, &gd);
+        if (e == cudaSuccess && mid) e = cudaEventRecord(mid, st);
+        return e;
+    }
+    cudaError_t e = launch_gemm<GATEUP, 96>(mg, mu, mx, g, st);
     if (e != cudaSuccess) return e;
     if (mid) {
         e = cudaEventRecord(mid, st);
         if (e != cudaSuccess) return e;
     }
-    // down
-    g.sfa0 = a.W->down_s;
-    g.sfa1 = a.W->down_s;  // the second tile of a down item is the next tile of the same matrix
-    g.sfb = hs;
-    g.tiles = reinterpret_cast<const int32_t *>(scratch + L.tiles_dn);
-    g.items = reinterpret_cast<const int2 *>(scratch + L.items_dn);
-    g.hcap = nullptr;
-    g.yp = a.yp;
-    g.yacc = a.yacc;
-    g.perm = a.perm;
-    g.k = a.k;
-    g.Mtot = a.d;
-    g.MTA = a.d / 128;
-    g.KC = Ip / 128;
-    return L.NT == 16   ? launch_gemm<DOWN, 16>(md, md, mh, g, st)
-           : L.NT == 32 ? launch_gemm<DOWN, 32>(md, md, mh, g, st)
-                        : launch_gemm<DOWN, 96>(md, md, mh, g, st);
+    return launch_gemm<DOWN, 96>(md, md, mh, gd, st);
 }
 
 }  // namespace lmoe

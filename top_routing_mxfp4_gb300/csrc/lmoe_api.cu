@@ -424,8 +424,10 @@ int32_t lmoe_forward_kernel_count(const lmoe_dims *dims)
     if (!dims_ok(dims) || dims->T == 0) return 0;
     const int64_t P = int64_t(dims->T) * dims->k;
     if (small_path(dims)) return 3;  // route, gate/up, down
-    // router (split, GEMM, (reduction), top-k), permute (with the GEMM schedule), scatter, two GEMMs, combine
-    return router_kernel_count(dims->T, dims->d, dims->E) + permute_kernel_count(P) + 1 + 2 + 1;
+    // router (split, GEMM, (reduction), top-k), permute (with the GEMM schedule), scatter, the two
+    // expert GEMMs (one fused kernel for small token tiles), combine
+    const int gemms = ffn_layout(P, dims->d, dims->E, dims->I).NT <= 32 ? 1 : 2;
+    return router_kernel_count(dims->T, dims->d, dims->E) + permute_kernel_count(P) + 1 + gemms + 1;
 }
 
 lmoe_status lmoe_set_stage_events(void *const *events, int32_t n)

@@ -176,6 +176,7 @@ struct FfnSched {
     int32_t *pad_off = nullptr, *tiles_gu = nullptr, *tiles_dn = nullptr, *dst_row = nullptr;
     int2 *items_gu = nullptr, *items_dn = nullptr;
     int2 *tile_info = nullptr;  // per token tile: {expert, token tile within the expert}
+    int32_t *tile_done = nullptr;  // per token tile: the fused GEMM kernel's h-complete counter (zeroed here)
 };
 
 // Work-item tables of the two expert GEMMs, in execution order: entry i is
@@ -191,7 +192,10 @@ struct FfnSched {
 __device__ __forceinline__ void fill_tile_info(const int32_t *scan, int E, const FfnSched &sc, int nthreads)
 {
     for (int e = threadIdx.x; e < E; e += nthreads)
-        for (int R = scan[e]; R < scan[e + 1]; ++R) sc.tile_info[R] = make_int2(e, R - scan[e]);
+        for (int R = scan[e]; R < scan[e + 1]; ++R) {
+            sc.tile_info[R] = make_int2(e, R - scan[e]);
+            if (sc.tile_done) sc.tile_done[R] = 0;
+        }
 }
 // Entries [g0, n_gu + n_dn) with stride `step` (gate/up entries first).
 // Down entries in bands: band b holds weight tiles [b*MT/NB, (b+1)*MT/NB) of
@@ -237,7 +241,7 @@ struct FfnLayout {
     int NT, SLOT;      // token tile and the rows a tile occupies (SLOT == NT: tiles are packed)
     int64_t rows;      // token rows reserved (whole tiles)
     size_t pad_off, tiles_gu, tiles_dn, items_gu, items_dn, tile_info, xq, xs, hq, hs, hs_bytes, w_sorted, dst_row,
-        total;  // byte offsets / sizes
+        tile_done, total;  // byte offsets / sizes
     bool fused;  // large token tiles: the down GEMM can accumulate into the per-token output (FfnArgs::yacc)
 };
 FfnLayout ffn_layout(int64_t P, int d, int E, int I);

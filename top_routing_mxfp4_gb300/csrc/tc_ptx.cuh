@@ -113,6 +113,23 @@ __device__ __forceinline__ void bulk_store(void *dst, const void *src, uint32_t 
     asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(smem_u32(src)), "r"(bytes)
                  : "memory");
 }
+// Spin (bounded by `limit` SM clocks) until the counter at `ctr` (global
+// memory, written by other CTAs) reaches `target`: acquire loads, then a proxy
+// fence so that this thread's later asynchronous (TMA) reads of global memory
+// see what the counting threads stored before counting.  False on timeout.
+__device__ __forceinline__ bool wait_count(const int32_t *ctr, int32_t target, long long limit)
+{
+    const long long t0 = clock64();
+    for (;;) {
+        int32_t v;
+        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+        if (v >= target) break;
+        if (clock64() - t0 > limit) return false;
+        __nanosleep(32);
+    }
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    return true;
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until at most N of this thread's bulk groups still read shared memory.
 template <int N>
