@@ -277,6 +277,25 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
         return __ldcg(p.items + j);
     };
     auto mode_of = [&](int i) { return MODE == FUSED ? (i < n_gu ? int(GATEUP) : int(DOWN)) : int(MODE); };
+    // This CTA's items in order: ordinal i -> item index.  One GEMM: every
+    // G-th item.  Fused: the gate/up items every G-th, then the down items in
+    // rounds over the CTAs (consecutive items, adjacent weight rows, run at
+    // the same time on neighbouring CTAs), where the first X rounds leave out
+    // the r CTAs that drew an extra gate/up item (r = n_gu mod G; X down
+    // items take about the pipeline stages of one gate/up item), so that
+    // those CTAs do not finish last.
+    const int c = int(blockIdx.x);
+    const int gu_c = MODE == FUSED ? (n_gu > c ? (n_gu - c + G - 1) / G : 0) : 0;
+    const int n_dn = total - n_gu;
+    const int r_gu = n_gu % G;
+    const int X = (MODE == FUSED && r_gu > 0) ? (p.KC + q.KC / 2) / q.KC : 0;
+    int dn_c = 0;  // this CTA's down items
+    if (MODE == FUSED) {
+        if (c >= r_gu)
+            for (int k = 0; k < X && k * (G - r_gu) + (c - r_gu) < n_dn; ++k) ++dn_c;
+        const int base = X * (G - r_gu) + c;
+        if (n_dn > base) dn_c += (n_dn - base + G - 1) / G;
+    }
     // h of a token tile is complete once every epilogue warp of each of its
     // gate/up items has counted itself in
     [[maybe_unused]] const int h_ready = p.MTA * C::EPI_WARPS;
@@ -308,13 +327,20 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     auto slot_row = [&](int e) { return s_pad[e]; };  // first token row of expert e
+    const int n_mine = MODE == FUSED ? gu_c + dn_c : (total > c ? (total - c + G - 1) / G : 0);
+    auto seq = [&](int i) {
+        if (MODE != FUSED || i < gu_c) return c + i * G;
+        const int j = i - gu_c;
+        if (c >= r_gu && j < X) return n_gu + j * (G - r_gu) + (c - r_gu);
+        return n_gu + X * (G - r_gu) + (j - (c >= r_gu ? X : 0)) * G + c;
+    };
     // Everything above reads only inputs of earlier kernels; the previous
     // kernel's outputs are read after this wait.
     pdl_enter();
     int2 ent0 = make_int2(0, 0), ent1 = make_int2(0, 0);  // the first two entries
-    if (int(blockIdx.x) < total) {
-        ent0 = entry(blockIdx.x);
-        ent1 = entry(blockIdx.x + G);
+    if (n_mine > 0) {
+        ent0 = entry(seq(0));
+        ent1 = entry(seq(1));
     }
 
     if (warp == 0 || warp == 3 + C::EPI_WARPS) {
@@ -326,10 +352,11 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
             uint32_t phase = 0;
             bool ok = true;
             int2 ent = ent0, ent_next = ent1;
-            for (int it = blockIdx.x; it < total && ok; it += G) {
+            for (int i = 0; i < n_mine && ok; ++i) {
+                const int it = seq(i);
                 const Item w = item_at(ent, s_off, NT);
                 ent = ent_next;
-                ent_next = entry(it + 2 * G);
+                ent_next = entry(seq(i + 2));
                 const int mode = mode_of(it);
                 const GemmArgs &a = (MODE == FUSED && mode == DOWN) ? q : p;
                 const int R = slot_row(w.e) + w.n_tile * C::SLOT;
@@ -405,10 +432,11 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
             int2 ent = ent0, ent_next = ent1;
-            for (int it = blockIdx.x; it < total && ok; it += G) {
+            for (int i = 0; i < n_mine && ok; ++i) {
+                const int it = seq(i);
                 const Item w = item_at(ent, s_off, NT);
                 ent = ent_next;
-                ent_next = entry(it + 2 * G);
+                ent_next = entry(seq(i + 2));
                 const int KCi = (MODE == FUSED && mode_of(it) == DOWN) ? q.KC : p.KC;
                 const uint32_t N = uint32_t((w.n_valid + 15) & ~15);
                 if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1, p.wait_limit)) {
@@ -633,20 +661,20 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
         Item nA{}, nB{};
         float wA[NV], wB[NV];
         int tA[NV], tB[NV];
-        if (int(blockIdx.x) < total) fetch(blockIdx.x, ent0, nA, wA, tA);
-        if (int(blockIdx.x) + G < total) fetch(blockIdx.x + G, ent1, nB, wB, tB);
-        int2 eA = entry(blockIdx.x + 2 * G), eB = entry(blockIdx.x + 3 * G);  // next entries of the two sets
-        for (int it = blockIdx.x; it < total; it += 2 * G) {
-            if (!process(it, nA, wA, tA)) break;
-            if (it + 2 * G < total) {
-                fetch(it + 2 * G, eA, nA, wA, tA);
-                eA = entry(it + 4 * G);
+        if (0 < n_mine) fetch(seq(0), ent0, nA, wA, tA);
+        if (1 < n_mine) fetch(seq(1), ent1, nB, wB, tB);
+        int2 eA = entry(seq(2)), eB = entry(seq(3));  // next entries of the two sets
+        for (int i = 0; i < n_mine; i += 2) {
+            if (!process(seq(i), nA, wA, tA)) break;
+            if (i + 2 < n_mine) {
+                fetch(seq(i + 2), eA, nA, wA, tA);
+                eA = entry(seq(i + 4));
             }
-            if (it + G >= total) break;
-            if (!process(it + G, nB, wB, tB)) break;
-            if (it + 3 * G < total) {
-                fetch(it + 3 * G, eB, nB, wB, tB);
-                eB = entry(it + 5 * G);
+            if (i + 1 >= n_mine) break;
+            if (!process(seq(i + 1), nB, wB, tB)) break;
+            if (i + 3 < n_mine) {
+                fetch(seq(i + 3), eB, nB, wB, tB);
+                eB = entry(seq(i + 5));
             }
         }
         if (threadIdx.x == 64) LMOE_TRACE_END(2);
@@ -1186,11 +1214,12 @@ cudaError_t launch_expert_gemms(const FfnArgs &a, const FfnLayout &L, char *scra
     gd.Mtot = a.d;
     gd.MTA = a.d / 128;
     gd.KC = Ip / 128;
-    if (L.NT <= 32) {
-        // decode-sized token tiles: both GEMMs in one persistent kernel (the
-        // stage-boundary event, if asked for, follows it)
-        cudaError_t e = L.NT == 16 ? launch_gemm<FUSED, 16>(mg, mu, mx, g, st, &md, &mh, &gd)
-                                   : launch_gemm<FUSED, 32>(mg, mu, mx, g, st, &md, &mh, &gd);
+    if (ffn_fused(L)) {
+        // both GEMMs in one persistent kernel (the stage-boundary event, if
+        // asked for, follows it)
+        cudaError_t e = L.NT == 16   ? launch_gemm<FUSED, 16>(mg, mu, mx, g, st, &md, &mh, &gd)
+                        : L.NT == 32 ? launch_gemm<FUSED, 32>(mg, mu, mx, g, st, &md, &mh, &gd)
+                                     : launch_gemm<FUSED, 96>(mg, mu, mx, g, st, &md, &mh, &gd);
         if (e == cudaSuccess && mid) e = cudaEventRecord(mid, st);
         return e;
     }

@@ -426,7 +426,7 @@ int32_t lmoe_forward_kernel_count(const lmoe_dims *dims)
     if (small_path(dims)) return 3;  // route, gate/up, down
     // router (split, GEMM, (reduction), top-k), permute (with the GEMM schedule), scatter, the two
     // expert GEMMs (one fused kernel for small token tiles), combine
-    const int gemms = ffn_layout(P, dims->d, dims->E, dims->I).NT <= 32 ? 1 : 2;
+    const int gemms = ffn_fused(ffn_layout(P, dims->d, dims->E, dims->I)) ? 1 : 2;
     return router_kernel_count(dims->T, dims->d, dims->E) + permute_kernel_count(P) + 1 + gemms + 1;
 }
 

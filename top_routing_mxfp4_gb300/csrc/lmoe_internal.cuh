@@ -245,6 +245,10 @@ struct FfnLayout {
     bool fused;  // large token tiles: the down GEMM can accumulate into the per-token output (FfnArgs::yacc)
 };
 FfnLayout ffn_layout(int64_t P, int d, int E, int I);
+// Whether the two expert GEMMs of this layout run as one fused kernel: for
+// decode-sized token tiles (at 96-token tiles the fused kernel measured
+// slower than two kernels).
+inline bool ffn_fused(const FfnLayout &L) { return L.NT <= 32; }
 // The permute by-products the forward asks for, pointing into the FFN scratch.
 FfnSched ffn_sched(const FfnLayout &L, int d, int I, char *scratch);
 
