@@ -9,26 +9,29 @@ namespace lmoe {
 namespace {
 
 __global__ void __launch_bounds__(128) k_combine(const float *__restrict__ yp, const int32_t *__restrict__ inv, int T,
-                                                 int d, int k, uint16_t *__restrict__ y)
+                                                 int d, int k, uint16_t *__restrict__ y, int inv_early)
 {
-    pdl_enter();
     __shared__ int32_t rows[32];
     const int t = blockIdx.x;
-    if (threadIdx.x < k) rows[threadIdx.x] = __ldg(inv + int64_t(t) * k + threadIdx.x);
+    // inv_early: inv was complete before the kernel this one follows started
+    // (inside the layer call), so it is read before waiting for that kernel
+    if (inv_early && threadIdx.x < k) rows[threadIdx.x] = __ldg(inv + int64_t(t) * k + threadIdx.x);
+    pdl_enter();
+    if (!inv_early && threadIdx.x < k) rows[threadIdx.x] = __ldg(inv + int64_t(t) * k + threadIdx.x);
     __syncthreads();
     const int nv = d / 4;
     for (int c = threadIdx.x + blockIdx.y * blockDim.x; c < nv; c += blockDim.x * gridDim.y) {
-        // the k rows' loads go out in batches of 8 before they are summed (in
-        // slot order), so each batch costs one memory latency, not eight
+        // the k rows' loads go out in batches of 16 before they are summed (in
+        // slot order), so each batch costs one memory latency, not sixteen
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int j0 = 0; j0 < k; j0 += 8) {
-            float4 v[8];
+        for (int j0 = 0; j0 < k; j0 += 16) {
+            float4 v[16];
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-                v[j] = j0 + j < k ? __ldg(reinterpret_cast<const float4 *>(yp + int64_t(rows[j0 + j]) * d) + c)
+            for (int j = 0; j < 16; ++j)
+                v[j] = j0 + j < k ? __ldcg(reinterpret_cast<const float4 *>(yp + int64_t(rows[j0 + j]) * d) + c)
                                   : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
+            for (int j = 0; j < 16; ++j) {
                 if (j0 + j < k) {
                     acc.x += v[j].x;
                     acc.y += v[j].y;
@@ -72,11 +75,12 @@ cudaError_t launch_acc_to_bf16(const float *acc, int64_t n, uint16_t *y, cudaStr
                       reinterpret_cast<const float4 *>(acc), n4, reinterpret_cast<uint2 *>(y));
 }
 
-cudaError_t launch_combine(const float *yp, const int32_t *inv, int T, int d, int k, uint16_t *y, cudaStream_t st)
+cudaError_t launch_combine(const float *yp, const int32_t *inv, int T, int d, int k, uint16_t *y, cudaStream_t st,
+                           bool inv_early)
 {
     if (T == 0) return cudaSuccess;
     const int ysplit = T >= 1024 ? 1 : (T >= 128 ? 2 : 7);  // enough CTAs for small T
-    return launch_pdl(k_combine, dim3(T, ysplit), dim3(128), 0, st, yp, inv, T, d, k, y);
+    return launch_pdl(k_combine, dim3(T, ysplit), dim3(128), 0, st, yp, inv, T, d, k, y, inv_early ? 1 : 0);
 }
 
 }  // namespace lmoe

@@ -291,7 +291,7 @@ lmoe_status lmoe_combine(const float *yp, const int32_t *inv, const lmoe_dims *d
     if (!dims_ok(dims)) return LMOE_ERR_INVALID_ARG;
     if (dims->T == 0) return LMOE_OK;
     if (!yp || !inv || !y_bf16 || !aligned(yp, 16) || !aligned(y_bf16, 16)) return LMOE_ERR_INVALID_ARG;
-    return cuda_status(launch_combine(yp, inv, dims->T, dims->d, dims->k, y_bf16, cudaStream_t(stream)));
+    return cuda_status(launch_combine(yp, inv, dims->T, dims->d, dims->k, y_bf16, cudaStream_t(stream), false));
 }
 
 size_t lmoe_workspace_size(const lmoe_dims *dims)
@@ -369,7 +369,7 @@ lmoe_status lmoe_forward(const uint16_t *x_bf16, const uint16_t *Wr3, const floa
     }
     if (e == cudaSuccess) e = mark(5, st);
     if (e == cudaSuccess)
-        e = yacc ? launch_acc_to_bf16(yacc, int64_t(T) * d, y_bf16, st) : launch_combine(yp, inv, T, d, k, y_bf16, st);
+        e = yacc ? launch_acc_to_bf16(yacc, int64_t(T) * d, y_bf16, st) : launch_combine(yp, inv, T, d, k, y_bf16, st, true);
     if (e == cudaSuccess) e = mark(6, st);
     return cuda_status(e);
 }

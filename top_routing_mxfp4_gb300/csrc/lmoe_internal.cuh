@@ -299,7 +299,10 @@ cudaError_t launch_small_forward(const uint16_t *x, const uint16_t *Wr3, const f
                                  uint16_t *y, const SmallLayout &L, char *scratch, int32_t *status, int32_t *counter,
                                  float *hcap, cudaStream_t st, const cudaEvent_t *stage_events);
 
-cudaError_t launch_combine(const float *yp, const int32_t *inv, int T, int d, int k, uint16_t *y, cudaStream_t st);
+// inv_early: inv is complete before the kernel preceding the combine starts
+// (true inside lmoe_forward; false for the standalone entry point).
+cudaError_t launch_combine(const float *yp, const int32_t *inv, int T, int d, int k, uint16_t *y, cudaStream_t st,
+                           bool inv_early);
 // y = bf16(acc), n elements (n % 4 == 0)
 cudaError_t launch_acc_to_bf16(const float *acc, int64_t n, uint16_t *y, cudaStream_t st);
 
