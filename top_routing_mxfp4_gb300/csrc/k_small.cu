@@ -283,57 +283,83 @@ __global__ void __launch_bounds__(32 * R_WARPS, 2) k_small_route(const uint16_t 
 
 // ---- kernel 2: gate/up, SwiGLU, MXFP8 of h --------------------------------------------------
 
-constexpr int G_WARPS = 16;   // 64 rows (32 gate + 32 up) per unit
-constexpr int G_RPW = 4;      // rows per warp
+constexpr int G_WARPS = 16;   // 4 row tiles of 16 (32 gate + 32 up rows) x 4 quarters of K per unit
+constexpr int G_PAIRS = SMALL_MAX_TOKENS;  // pairs of one expert a unit serves at most (one per token)
 
-// a += the 16 products of e2m1 codes (8 bytes, element 2i in the low nibble
-// of byte i) with x^ (8 f16x2 words, element 2i in the low half): each code
-// is widened to fp16 and multiplied in fp16, which is exact (at most 6
-// significant bits, within the fp16 range), then the products are added in
-// fp32, even and odd elements into separate sums.
-__device__ __forceinline__ void dot16(uint2 codes, const uint32_t *xv, float &a0, float &a1)
+// Four e2m1 code pairs (a 32-bit word, element 2i in the low nibble of byte
+// i) -> four f16x2 words (exact: e2m1 values are fp16 values), element 2i in
+// the low half of word i.
+__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t codes, uint32_t &w0, uint32_t &w1, uint32_t &w2, uint32_t &w3)
 {
-    uint32_t w[8];
-    asm("{\n\t.reg .b8 c0, c1, c2, c3, c4, c5, c6, c7;\n\t"
-        "mov.b32 {c0, c1, c2, c3}, %8;\n\tmov.b32 {c4, c5, c6, c7}, %9;\n\t"
+    asm("{\n\t.reg .b8 c0, c1, c2, c3;\n\t"
+        "mov.b32 {c0, c1, c2, c3}, %4;\n\t"
         "cvt.rn.f16x2.e2m1x2 %0, c0;\n\tcvt.rn.f16x2.e2m1x2 %1, c1;\n\t"
-        "cvt.rn.f16x2.e2m1x2 %2, c2;\n\tcvt.rn.f16x2.e2m1x2 %3, c3;\n\t"
-        "cvt.rn.f16x2.e2m1x2 %4, c4;\n\tcvt.rn.f16x2.e2m1x2 %5, c5;\n\t"
-        "cvt.rn.f16x2.e2m1x2 %6, c6;\n\tcvt.rn.f16x2.e2m1x2 %7, c7;\n\t}"
-        : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
-        : "r"(codes.x), "r"(codes.y));
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const __half2 prod = __hmul2(*reinterpret_cast<const __half2 *>(&w[i]), *reinterpret_cast<const __half2 *>(&xv[i]));
-        const float2 f = __half22float2(prod);
-        a0 += f.x;
-        a1 += f.y;
-    }
+        "cvt.rn.f16x2.e2m1x2 %2, c2;\n\tcvt.rn.f16x2.e2m1x2 %3, c3;\n\t}"
+        : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
+        : "r"(codes));
 }
 
-// Unit = (touched expert u, block rb of 32 rows of I).  Its 32 gate and 32
-// up weight rows (two contiguous ranges of the bank) are brought into
-// shared memory by two bulk asynchronous copies; meanwhile the threads load
-// the rows' scale words, and each lane loads x^ of the unit's first token
-// for its own chunks into registers (fp16 code values, exact, and the block
-// scales).  Lane l of a warp takes the 16-element chunks l, l + 32, ... of
-// each of the warp's 4 rows, one independent sum per chunk; the 64 row
-// results meet in shared memory and warp 0 forms h for the 32 rows:
-// silu(g) * u, block amax, E8M0 scale, e4m3 codes.  Further tokens of the
-// same expert reuse the weights in shared memory.
+// D += A B for one 16 x 16 (row-major fp16) by 16 x 8 (column-major fp16)
+// block, fp32 accumulation: the warp-level tensor-core instruction, used
+// here for its cheap exact fp16 products at one to eight tokens.
+__device__ __forceinline__ void mma_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint32_t b0, uint32_t b1)
+{
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+                 "{%0, %1, %2, %3};"
+                 : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Shared-memory layout of one gate/up unit (byte offsets; row strides padded
+// so that the warps' loads hit distinct banks).
+struct GateupSmem {
+    int wrow, xrow;                      // weight row stride (bytes), x row stride (halves)
+    size_t w, sf, sx, xh, part, total;
+    __host__ __device__ GateupSmem(int d, int npair)
+    {
+        wrow = d / 2 + 16;
+        xrow = d + 32;
+        w = 0;                                         // [64][wrow] e2m1 codes
+        sf = w + size_t(64) * wrow;                    // [d/32][64] weight block scales (fp32)
+        sx = sf + size_t(d / 32) * 64 * 4;             // [d/32][G_PAIRS] x block scales (fp32)
+        xh = sx + size_t(d / 32) * G_PAIRS * 4;        // [npair][xrow] x^ as fp16
+        part = xh + size_t(npair) * xrow * 2;          // [4][64][G_PAIRS] K-quarter partial sums
+        total = part + size_t(4) * 64 * G_PAIRS * 4;
+    }
+};
+
+// Unit = (touched expert u, block rb of 32 rows of I): its 32 gate and 32 up
+// weight rows come into shared memory by one bulk asynchronous copy per row
+// (rows padded); meanwhile the threads turn the rows' block scales and x^ of
+// the expert's pairs (at most one per token, so at most G_PAIRS) into fp32
+// scales and fp16 code values (both exact).  Warp w takes the 16-row tile
+// w % 4 over the quarter w / 4 of K: per 32-element scale block, two
+// m16n8k16 tensor-core products (e2m1 codes widened to fp16, x^ in fp16; the
+// products are exact) give the block's sums for the unit's pairs (the MMA's N
+// columns), which are scaled by the two E8M0 block scales and added in fp32.
+// K is consumed in a permuted order inside each block, the same for both
+// operands: lane (g, t) takes elements 8t .. 8t+7 of the block (one 32-bit
+// word of codes per row), the first four in the first product and the last
+// four in the second.  The four quarters' sums meet in shared memory (added in
+// quarter order) and warp j forms h of pair slot j: silu(g) * u, its MXFP8
+// block over the 32 rows, stored as the pair's row of h.
 template <bool FP4>
 __global__ void __launch_bounds__(32 * G_WARPS) k_small_gateup(const uint8_t *__restrict__ gate_q,
                                                                const uint8_t *__restrict__ gate_s,
                                                                const uint8_t *__restrict__ up_q,
                                                                const uint8_t *__restrict__ up_s, int d, int I, int k,
-                                                               SmallPlan sp)
+                                                               int npair_max, SmallPlan sp)
 {
     extern __shared__ __align__(128) uint8_t g_smem[];
-    const int KCd = d / 128, RTI = (I + 127) / 128, KCi = (I + 127) / 128;
-    uint8_t *wq = g_smem;                                                // [64][d/2] codes
-    uint32_t *sw = reinterpret_cast<uint32_t *>(g_smem + 64 * (d / 2));  // [64][KCd] scale words
-    __shared__ float gu[64];
+    const GateupSmem L(d, npair_max);
+    uint8_t *wq = g_smem + L.w;
+    float *sf = reinterpret_cast<float *>(g_smem + L.sf);
+    float *sx = reinterpret_cast<float *>(g_smem + L.sx);
+    uint16_t *xh = reinterpret_cast<uint16_t *>(g_smem + L.xh);
+    float *part = reinterpret_cast<float *>(g_smem + L.part);
     __shared__ __align__(8) uint64_t bar;
+    const int KCd = d / 128, RTI = (I + 127) / 128, KCi = (I + 127) / 128, nbk = d / 32;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         tc::mbar_init(&bar, 1);
@@ -343,108 +369,136 @@ __global__ void __launch_bounds__(32 * G_WARPS) k_small_gateup(const uint8_t *__
     pdl_enter();
     const int nt = __ldcg(sp.n_touched);
     const int nrb = I / 32;
-    const uint32_t half_bytes = uint32_t(32 * (d / 2));
-    const int nchunk = d / 16;
+    const uint32_t row_bytes = uint32_t(d / 2);
     uint32_t parity = 0;
     for (int unit = blockIdx.x; unit < nt * nrb; unit += gridDim.x) {
         const int u = unit / nrb, rb = unit - u * nrb;
         const int e = __ldcg(sp.seg_expert + u);
         const int q0 = __ldcg(sp.seg_start + u), q1 = __ldcg(sp.seg_start + u + 1);
+        const int np = min(q1 - q0, npair_max);
         __syncthreads();  // the previous unit is done with every buffer
-        if (threadIdx.x == 0) {
-            tc::fence_async_shared();
-            tc::mbar_arrive_expect_tx(&bar, 2 * half_bytes);
+        if (warp == 0) {
+            if (lane == 0) {
+                tc::fence_async_shared();
+                tc::mbar_arrive_expect_tx(&bar, 64 * row_bytes);
+            }
+            __syncwarp();
             const int64_t r0 = int64_t(e) * I + rb * 32;
-            tc::bulk_load(wq, gate_q + r0 * (d / 2), half_bytes, &bar);
-            tc::bulk_load(wq + half_bytes, up_q + r0 * (d / 2), half_bytes, &bar);
+            tc::bulk_load(wq + lane * L.wrow, gate_q + (r0 + lane) * row_bytes, row_bytes, &bar);
+            tc::bulk_load(wq + (32 + lane) * L.wrow, up_q + (r0 + lane) * row_bytes, row_bytes, &bar);
         }
+        // weight block scales: one 32-bit word = four blocks of one row
         for (int i = threadIdx.x; i < 64 * KCd; i += blockDim.x) {
             const int r = i / KCd, kc = i - r * KCd;
             const int row = rb * 32 + (r & 31);
             const uint8_t *ms = r < 32 ? gate_s : up_s;
-            sw[i] = __ldg(reinterpret_cast<const uint32_t *>(ms + ((int64_t(e) * RTI + (row >> 7)) * KCd + kc) * 512 +
-                                                            (row & 31) * 16 + ((row & 127) >> 5) * 4));
+            const uint32_t wd = __ldg(reinterpret_cast<const uint32_t *>(
+                ms + ((int64_t(e) * RTI + (row >> 7)) * KCd + kc) * 512 + (row & 31) * 16 + ((row & 127) >> 5) * 4));
+#pragma unroll
+            for (int j = 0; j < 4; ++j) sf[(4 * kc + j) * 64 + r] = e8m0_to_f32((wd >> (8 * j)) & 0xFF);
         }
-        bool landed = false;
-        for (int q = q0; q < q1; ++q) {
-            const int p = __ldcg(sp.seg_pair + q), t = p / k;
-            // this lane's chunks of x^_t
-            uint32_t xr[MAX_CH][8];
-            float sx[MAX_CH];
+        // x^ of the unit's pairs: 16-element chunks as fp16, and block scales
+        for (int i = threadIdx.x; i < np * (d / 16); i += blockDim.x) {
+            const int j = i / (d / 16), c = i - j * (d / 16);
+            const int t = __ldcg(sp.seg_pair + q0 + j) / k;
+            uint32_t h[8];
+            if constexpr (FP4) {
+                e2m1x16_to_f16x2(__ldcg(reinterpret_cast<const uint2 *>(sp.xq + int64_t(t) * (d / 2)) + c), h);
+            } else {
+                const uint4 v = __ldcg(reinterpret_cast<const uint4 *>(sp.xq + int64_t(t) * d) + c);
+                const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-            for (int m = 0; m < MAX_CH; ++m) {
-                const int c = lane + 32 * m;
-                uint32_t sb = 0;
-                if constexpr (FP4) {
-                    uint2 v = make_uint2(0, 0);
-                    if (c < nchunk) {
-                        v = __ldcg(reinterpret_cast<const uint2 *>(sp.xq + int64_t(t) * (d / 2)) + c);
-                        sb = __ldcg(sp.xs + atom_offset(t, c >> 1, KCd));
-                    }
-                    e2m1x16_to_f16x2(v, xr[m]);
-                } else {
-                    uint4 v = make_uint4(0, 0, 0, 0);
-                    if (c < nchunk) {
-                        v = __ldcg(reinterpret_cast<const uint4 *>(sp.xq + int64_t(t) * d) + c);
-                        sb = __ldcg(sp.xs + atom_offset(t, c >> 1, KCd));
-                    }
-                    const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        xr[m][2 * j] = e4m3x2_to_f16x2(vw[j]);
-                        xr[m][2 * j + 1] = e4m3x2_to_f16x2(vw[j] >> 16);
-                    }
+                for (int q = 0; q < 4; ++q) {
+                    h[2 * q] = e4m3x2_to_f16x2(vw[q]);
+                    h[2 * q + 1] = e4m3x2_to_f16x2(vw[q] >> 16);
                 }
-                sx[m] = e8m0_to_f32(sb);
             }
-            if (!landed) {
-                if (!tc::mbar_wait(&bar, parity)) {
-                    set_status(sp.status, LMOE_ERR_TIMEOUT);
-                    return;
-                }
-                landed = true;
-            }
-            __syncthreads();  // scale words visible; gu free
-#pragma unroll
-            for (int rr = 0; rr < G_RPW; ++rr) {
-                const int r = warp * G_RPW + rr;  // 0..31 gate rows, 32..63 up rows
-                const uint2 *wrow = reinterpret_cast<const uint2 *>(wq + r * (d / 2));
-                float acc = 0.f;
-#pragma unroll
-                for (int m = 0; m < MAX_CH; ++m) {
-                    const int c = lane + 32 * m;
-                    if (c < nchunk) {
-                        const uint2 cw = wrow[c];
-                        const int b = c >> 1;  // scale block of the chunk
-                        const float s_w = e8m0_to_f32((sw[r * KCd + (b >> 2)] >> (8 * (b & 3))) & 0xFF);
-                        float a0 = 0.f, a1 = 0.f;
-                        dot16(cw, xr[m], a0, a1);
-                        acc = fmaf((a0 + a1) * s_w, sx[m], acc);
-                    }
-                }
-                const float v = warp_sum(acc);
-                if (lane == 0) gu[r] = v;
-            }
-            __syncthreads();
-            if (warp == 0) {
-                const float gv = gu[lane], uv = gu[32 + lane];
-                const float h = __fdividef(gv, 1.f + __expf(-gv)) * uv;
-                if (sp.hcap) sp.hcap[int64_t(p) * I + rb * 32 + lane] = h;
-                uint32_t amax;
-                asm("redux.sync.max.u32 %0, %1, 0xffffffff;" : "=r"(amax) : "r"(__float_as_uint(h) & 0x7FFFFFFFu));
-                const uint32_t sb = mx_scale_byte(__uint_as_float(amax), FP4 ? 2 : 8);
-                if constexpr (FP4) {
-                    // e2m1 code of this lane's h; lanes 2i and 2i+1 share byte i (element 2i in the low nibble)
-                    const uint32_t code = e2m1x2(0.f, h * mx_inv_scale(sb)) & 0xF;
-                    const uint32_t hi = __shfl_down_sync(0xFFFFFFFFu, code, 1);
-                    if ((lane & 1) == 0) sp.hq[int64_t(p) * (I / 2) + rb * 16 + lane / 2] = uint8_t(code | (hi << 4));
-                } else {
-                    sp.hq[int64_t(p) * I + rb * 32 + lane] = uint8_t(e4m3x2(h * mx_inv_scale(sb), 0.f) & 0xFF);
-                }
-                if (lane == 0) sp.hs[atom_offset(p, rb, KCi)] = uint8_t(sb);
-            }
+            uint4 *dst = reinterpret_cast<uint4 *>(xh + j * L.xrow + 16 * c);
+            dst[0] = make_uint4(h[0], h[1], h[2], h[3]);
+            dst[1] = make_uint4(h[4], h[5], h[6], h[7]);
+            if ((c & 1) == 0) sx[(c >> 1) * G_PAIRS + j] = e8m0_to_f32(__ldcg(sp.xs + atom_offset(t, c >> 1, KCd)));
+        }
+        __syncthreads();
+        if (!tc::mbar_wait(&bar, parity)) {
+            set_status(sp.status, LMOE_ERR_TIMEOUT);
+            return;
         }
         parity ^= 1;
+        // block products on the tensor cores
+        const int mt = warp & 3, kq = warp >> 2;
+        const int g = lane >> 2, t4 = lane & 3;
+        const uint8_t *rowg = wq + (16 * mt + g) * L.wrow + 4 * t4;
+        const uint8_t *rowg8 = rowg + 8 * L.wrow;
+        const bool col_ok = g < np;  // this lane's B column (pair slot g)
+        const uint16_t *xcol = xh + (col_ok ? g : 0) * L.xrow + 8 * t4;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        const int b0 = kq * (nbk / 4), b1 = b0 + nbk / 4;
+        for (int b = b0; b < b1; ++b) {
+            const uint32_t wg = *reinterpret_cast<const uint32_t *>(rowg + 16 * b);
+            const uint32_t wg8 = *reinterpret_cast<const uint32_t *>(rowg8 + 16 * b);
+            uint4 xv = make_uint4(0, 0, 0, 0);
+            if (col_ok) xv = *reinterpret_cast<const uint4 *>(xcol + 32 * b);
+            uint32_t ag0, ag1, ag2, ag3, ah0, ah1, ah2, ah3;
+            e2m1x8_to_f16x2(wg, ag0, ag1, ag2, ag3);
+            e2m1x8_to_f16x2(wg8, ah0, ah1, ah2, ah3);
+            float c[4] = {0.f, 0.f, 0.f, 0.f};
+            mma_16816(c, ag0, ah0, ag1, ah1, xv.x, xv.y);
+            mma_16816(c, ag2, ah2, ag3, ah3, xv.z, xv.w);
+            const float s0 = sf[b * 64 + 16 * mt + g], s8 = sf[b * 64 + 16 * mt + g + 8];
+            const float2 xs2 = *reinterpret_cast<const float2 *>(sx + b * G_PAIRS + 2 * t4);
+            acc[0] = fmaf(c[0] * s0, xs2.x, acc[0]);
+            acc[1] = fmaf(c[1] * s0, xs2.y, acc[1]);
+            acc[2] = fmaf(c[2] * s8, xs2.x, acc[2]);
+            acc[3] = fmaf(c[3] * s8, xs2.y, acc[3]);
+        }
+        float *pw = part + (kq * 64 + 16 * mt + g) * G_PAIRS + 2 * t4;
+        pw[0] = acc[0];
+        pw[1] = acc[1];
+        pw[8 * G_PAIRS] = acc[2];
+        pw[8 * G_PAIRS + 1] = acc[3];
+        __syncthreads();
+        if (warp < np) {
+            const int j = warp;
+            const int p = __ldcg(sp.seg_pair + q0 + j);
+            float gv = 0.f, uv = 0.f;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                gv += part[(q * 64 + lane) * G_PAIRS + j];
+                uv += part[(q * 64 + 32 + lane) * G_PAIRS + j];
+            }
+            const float h = __fdividef(gv, 1.f + __expf(-gv)) * uv;
+            if (sp.hcap) sp.hcap[int64_t(p) * I + rb * 32 + lane] = h;
+            uint32_t amax;
+            asm("redux.sync.max.u32 %0, %1, 0xffffffff;" : "=r"(amax) : "r"(__float_as_uint(h) & 0x7FFFFFFFu));
+            const uint32_t sb = mx_scale_byte(__uint_as_float(amax), FP4 ? 2 : 8);
+            if constexpr (FP4) {
+                // e2m1 code of this lane's h; lanes 2i and 2i+1 share byte i (element 2i in the low nibble)
+                const uint32_t code = e2m1x2(0.f, h * mx_inv_scale(sb)) & 0xF;
+                const uint32_t hi = __shfl_down_sync(0xFFFFFFFFu, code, 1);
+                if ((lane & 1) == 0) sp.hq[int64_t(p) * (I / 2) + rb * 16 + lane / 2] = uint8_t(code | (hi << 4));
+            } else {
+                sp.hq[int64_t(p) * I + rb * 32 + lane] = uint8_t(e4m3x2(h * mx_inv_scale(sb), 0.f) & 0xFF);
+            }
+            if (lane == 0) sp.hs[atom_offset(p, rb, KCi)] = uint8_t(sb);
+        }
+    }
+}
+
+// a += the 16 products of e2m1 codes (8 bytes, element 2i in the low nibble
+// of byte i) with fp16 values (8 f16x2 words, element 2i in the low half):
+// each code is widened to fp16 and multiplied in fp16, which is exact (at
+// most 6 significant bits, within the fp16 range), then the products are
+// added in fp32, even and odd elements into separate sums.
+__device__ __forceinline__ void dot16(uint2 codes, const uint32_t *xv, float &a0, float &a1)
+{
+    uint32_t w[8];
+    e2m1x16_to_f16x2(codes, w);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const __half2 prod = __hmul2(*reinterpret_cast<const __half2 *>(&w[i]), *reinterpret_cast<const __half2 *>(&xv[i]));
+        const float2 f = __half22float2(prod);
+        a0 += f.x;
+        a1 += f.y;
     }
 }
 
@@ -648,7 +702,7 @@ size_t route_smem(int T, int d, int E)
     const size_t xs = size_t(T) * d * 2;
     return xs > sel ? xs : sel;
 }
-size_t gateup_smem(int d) { return size_t(64) * (d / 2) + size_t(64) * (d / 128) * 4; }
+size_t gateup_smem(int T, int d) { return GateupSmem(d, T < G_PAIRS ? T : G_PAIRS).total; }
 int down_rows_per_cta(int d) { return int(round_up(ceil_div(d, 152), 8)); }
 size_t down_fixed_smem(int P, int I) { return size_t(P) * I * 2 + size_t(P) * (I / 32) * 4 + size_t(P) * 8; }
 size_t down_pair_bytes(int d, int I)
@@ -681,7 +735,7 @@ bool small_path_fits(int T, int d, int E, int k, int I, int max_pairs)
     if (T < 1 || P > max_pairs || P > SMALL_MAX_PAIRS || T > SMALL_MAX_TOKENS) return false;
     if (E > 2048 || d % 128 != 0 || d > 32 * 16 * MAX_CH || I % 32 != 0 || I > 1024) return false;
     if (down_rows_per_cta(d) > D_WARPS * D_RPW) return false;
-    return route_smem(T, d, E) <= kSmemLimit && gateup_smem(d) <= kSmemLimit && down_group(int(P), d, I) >= 1;
+    return route_smem(T, d, E) <= kSmemLimit && gateup_smem(T, d) <= kSmemLimit && down_group(int(P), d, I) >= 1;
 }
 
 namespace {
@@ -716,12 +770,13 @@ cudaError_t launch_small_t(const uint16_t *x, const uint16_t *Wr3, const float *
     // stage events 1..3 (routing, permute, activation rounding) all follow the routing kernel
     for (int i = 1; stage_events && i <= 3; ++i)
         if ((e = cudaEventRecord(stage_events[i], st)) != cudaSuccess) return e;
-    const size_t gs = gateup_smem(d);
+    const int npair_max = T < G_PAIRS ? T : G_PAIRS;
+    const size_t gs = gateup_smem(T, d);
     if ((e = smem_attr(k_small_gateup<FP4>, gs)) != cudaSuccess) return e;
     const int max_units = P * (I / 32);
     const int ggrid = max_units < 152 ? max_units : 152;
     e = launch_pdl(k_small_gateup<FP4>, dim3(ggrid), dim3(32 * G_WARPS), gs, st, W->gate_q, W->gate_s, W->up_q,
-                   W->up_s, d, I, k, sp);
+                   W->up_s, d, I, k, npair_max, sp);
     if (e != cudaSuccess) return e;
     if (stage_events && (e = cudaEventRecord(stage_events[4], st)) != cudaSuccess) return e;
     const int gp = down_group(P, d, I);

@@ -134,24 +134,12 @@ __device__ __forceinline__ void softmax_store(const RoundOut &out, int k, int32_
     }
 }
 
-template <int NV, bool CANDIDATES = true>
-__device__ __forceinline__ void select_topk(const float *row, int E, int k, int32_t *idx_t, float *w_t, float2 *cand)
+// (The candidate path of select_topk, below.)
+template <int NV>
+__device__ __forceinline__ void select_topk_candidates(const float *row, int E, int k, int32_t *idx_t, float *w_t,
+                                                       float2 *cand)
 {
     const int lane = threadIdx.x & 31;
-    if constexpr (NV > 32 || !CANDIDATES) {
-        // wide rows (E > 1024), or a caller short of registers: the rounds
-        // over all values
-        float v[NV];
-#pragma unroll
-        for (int i = 0; i < NV; ++i) {
-            const int e = lane + 32 * i;
-            v[i] = e < E ? row[e] : -INFINITY;
-        }
-        RoundOut out;
-        topk_rounds_all<NV>(v, k, out);
-        softmax_store(out, k, idx_t, w_t);
-        return;
-    }
     int total;
     {
         float v[NV];
@@ -211,6 +199,28 @@ __device__ __forceinline__ void select_topk(const float *row, int E, int k, int3
         topk_rounds_all<NV>(v, k, out);
     }
     softmax_store(out, k, idx_t, w_t);
+}
+
+// select_topk: see above.
+template <int NV, bool CANDIDATES = true>
+__device__ __forceinline__ void select_topk(const float *row, int E, int k, int32_t *idx_t, float *w_t, float2 *cand)
+{
+    const int lane = threadIdx.x & 31;
+    if constexpr (NV > 32 || !CANDIDATES) {
+        // wide rows (E > 1024), or a caller short of registers: the rounds
+        // over all values
+        float v[NV];
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+            const int e = lane + 32 * i;
+            v[i] = e < E ? row[e] : -INFINITY;
+        }
+        RoundOut out;
+        topk_rounds_all<NV>(v, k, out);
+        softmax_store(out, k, idx_t, w_t);
+    } else {
+        select_topk_candidates<NV>(row, E, k, idx_t, w_t, cand);
+    }
 }
 
 }  // namespace lmoe
