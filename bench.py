@@ -267,9 +267,31 @@ def roofline_for(wl, touched: int, ms_per_step: float, stages: dict, peaks: dict
             "layer_weight_gbs": layer_weight_gbs, "layer_frac": layer_weight_gbs / peaks["hbm_gbs"]}
 
 
+class L2Flush:
+    """Overwrites L2 between timed steps: a buffer twice the L2 size is
+    written, then a second one as large is read, so that L2 holds clean lines
+    when the step starts (the dirty lines of the write are written back here,
+    not during the timed step)."""
+
+    def __init__(self, l2_bytes: int, dev):
+        import torch
+        self.w = torch.empty(2 * l2_bytes // 4, dtype=torch.float32, device=dev)
+        self.r = torch.zeros(2 * l2_bytes // 4, dtype=torch.float32, device=dev)
+        self.out = torch.empty((), dtype=torch.float32, device=dev)
+        self.bytes = self.w.numel() * 4
+
+    def run(self):
+        import torch
+        self.w.zero_()
+        torch.sum(self.r, out=self.out)
+
+    def describe(self) -> str:
+        return f"{self.bytes / 1e6:.0f} MB written, then {self.bytes / 1e6:.0f} MB of another buffer read"
+
+
 def time_steps(fwd, K: int, st, scrub=None) -> float:
     """Device time of K forward passes (ms): back to back, or, with `scrub`
-    (a buffer larger than L2), each step timed alone after writing it."""
+    (an L2Flush), each step timed alone after the flush."""
     import torch
     if scrub is None:
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -281,7 +303,7 @@ def time_steps(fwd, K: int, st, scrub=None) -> float:
         return a.elapsed_time(b)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     for a, b in evs:
-        scrub.zero_()
+        scrub.run()
         a.record(st)
         fwd()
         b.record(st)
@@ -300,7 +322,7 @@ def stage_times(lmoe, fwd, K: int, st, scrub=None) -> dict:
     torch.cuda.synchronize()
     for i in range(K):
         if scrub is not None:
-            scrub.zero_()
+            scrub.run()
         lmoe.set_stage_events(evs[i])
         fwd()
     torch.cuda.synchronize()
@@ -333,7 +355,7 @@ def side_record(lmoe, name: str, bank, Wr_dev, dev, steps: int, warmup: int, pea
     assert layer.device_status() == 0
     touched = int((torch.bincount(idx.view(-1).long(), minlength=wl.E) > 0).sum())
     per_expert_w = 3 * wl.I * wl.d * MXFP4_B
-    l2_bytes = scrub.numel() * 4 // 2
+    l2_bytes = scrub.bytes // 2
     flush = touched * per_expert_w < 2 * l2_bytes
     ms = time_steps(fwd, steps, st, scrub if flush else None) / steps
     stages = stage_times(lmoe, fwd, min(steps, 50), st, scrub if flush else None)
@@ -423,7 +445,7 @@ def run_ours(args, ws, rank, local):
     # each step is timed alone with events after the flush.
     l2_bytes = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or 129 * 2 ** 20)
     flush = touched * per_expert_w < 2 * l2_bytes
-    scrub = torch.empty(2 * l2_bytes // 4, dtype=torch.float32, device=dev) if flush else None
+    scrub = L2Flush(l2_bytes, dev) if flush else None
 
     try:
         uuid = str(torch.cuda.get_device_properties(dev).uuid)
@@ -443,7 +465,7 @@ def run_ours(args, ws, rank, local):
     if flush:
         step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
         for a, b in step_ev:
-            scrub.zero_()
+            scrub.run()
             a.record(st)
             fwd(xin)
             b.record(st)
@@ -468,7 +490,7 @@ def run_ours(args, ws, rank, local):
     torch.cuda.synchronize()
     for i in range(K2):
         if flush:
-            scrub.zero_()
+            scrub.run()
         lmoe.set_stage_events(evs[i])
         fwd(xin)
     torch.cuda.synchronize()
@@ -492,7 +514,7 @@ def run_ours(args, ws, rank, local):
     if flush:
         e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
         for a, b in e2e_ev:
-            scrub.zero_()
+            scrub.run()
             a.record(st)
             xdev.copy_(xh, non_blocking=True)
             fwd(xdev)
@@ -524,7 +546,7 @@ def run_ours(args, ws, rank, local):
         "config": {"workload": wl.name, "T": T, "d": wl.d, "E": wl.E, "k": wl.k, "I": wl.I, "hidden": wl.hidden,
                    "per_gpu_batch_tokens": T, "parallelism": f"replicas x{ws}",
                    "path": "small-batch kernels" if small else "tensor-core kernels",
-                   "l2": (f"L2 flushed before every step ({scrub.numel() * 4 / 1e6:.0f} MB written, not timed); "
+                   "l2": (f"L2 flushed before every step ({scrub.describe()}, not timed); "
                           if flush else "inputs larger than L2: ")
                          + f"{touched} touched experts = {touched * per_expert_w / 1e9:.2f} GB of weights read "
                            f"per step (L2 {l2_bytes / 2 ** 20:.0f} MB)"},
@@ -542,16 +564,15 @@ def run_ours(args, ws, rank, local):
         # The same run, on the same resident expert bank: the headline re-timed
         # with L2 written over before every step, then the prefill (T = 8192)
         # and batch-1 (T = 1) workloads as sub-records with their own rooflines.
-        scrub_all = scrub if scrub is not None else torch.empty(2 * l2_bytes // 4, dtype=torch.float32,
-                                                                  device=dev)
+        scrub_all = scrub if scrub is not None else L2Flush(l2_bytes, dev)
         side_sampler = ClockSampler(uuid)
         side_sampler.start()
         time.sleep(0.3)
         K3 = min(K, 100)
         ms_fl = time_steps(lambda: fwd(xin), K3, st, scrub_all) / K3
         line["l2_flushed"] = {"ms_per_step": ms_fl, "value": whole_job_rate(T, ws, ms_fl), "unit": UNIT, "steps": K3,
-                              "note": f"each step timed alone after writing {scrub_all.numel() * 4 / 1e6:.0f} MB "
-                                      "(more than L2), not timed"}
+                              "note": f"each step timed alone after an L2 flush ({scrub_all.describe()}), "
+                                      "not timed"}
         line["side_workloads"] = [side_record(lmoe, "prefill", bank, layer.Wr, dev, 10, 3, peaks, scrub_all),
                                   side_record(lmoe, "decode1", bank, layer.Wr, dev, 100, 5, peaks, scrub_all)]
         line["side_workloads_clocks"] = side_sampler.stop()

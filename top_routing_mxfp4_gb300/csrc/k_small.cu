@@ -324,32 +324,36 @@ struct GateupSmem {
         sf = w + size_t(64) * wrow;                    // [d/32][64] weight block scales (fp32)
         sx = sf + size_t(d / 32) * 64 * 4;             // [d/32][G_PAIRS] x block scales (fp32)
         xh = sx + size_t(d / 32) * G_PAIRS * 4;        // [npair][xrow] x^ as fp16
-        part = xh + size_t(npair) * xrow * 2;          // [4][64][G_PAIRS] K-quarter partial sums
-        total = part + size_t(4) * 64 * G_PAIRS * 4;
+        part = xh + size_t(npair) * xrow * 2;          // [2][4][64][G_PAIRS] K-quarter partial sums (x^ rows: tokens)
+        total = part + size_t(2) * 4 * 64 * G_PAIRS * 4;  // two units' sums
     }
 };
 
 // Unit = (touched expert u, block rb of 32 rows of I): its 32 gate and 32 up
-// weight rows come into shared memory by one bulk asynchronous copy per row
-// (rows padded); meanwhile the threads turn the rows' block scales and x^ of
-// the expert's pairs (at most one per token, so at most G_PAIRS) into fp32
-// scales and fp16 code values (both exact).  Warp w takes the 16-row tile
-// w % 4 over the quarter w / 4 of K: per 32-element scale block, two
-// m16n8k16 tensor-core products (e2m1 codes widened to fp16, x^ in fp16; the
-// products are exact) give the block's sums for the unit's pairs (the MMA's N
+// weight rows, in four quarters of K.  Warp group q (warps 4q .. 4q+3) owns
+// quarter q throughout: it copies that quarter of the unit's 64 rows into
+// shared memory (one bulk asynchronous copy per row, rows padded), turns the
+// quarter's block scales and x^ of the expert's pairs (at most one per token,
+// so at most G_PAIRS) into fp32 scales and fp16 code values (both exact),
+// waits for its copies, and forms the quarter's block products: warp 4q + m
+// takes the 16-row tile m; per 32-element scale block, two m16n8k16
+// tensor-core products (e2m1 codes widened to fp16, x^ in fp16, exact
+// products) give the block's sums for the unit's pairs (the MMA's N
 // columns), which are scaled by the two E8M0 block scales and added in fp32.
 // K is consumed in a permuted order inside each block, the same for both
 // operands: lane (g, t) takes elements 8t .. 8t+7 of the block (one 32-bit
 // word of codes per row), the first four in the first product and the last
-// four in the second.  The four quarters' sums meet in shared memory (added in
-// quarter order) and warp j forms h of pair slot j: silu(g) * u, its MXFP8
-// block over the 32 rows, stored as the pair's row of h.
+// four in the second.  As soon as a group is done with its quarter it issues
+// the copies of the next unit's quarter, so the next unit's weights stream
+// in while this unit is finished.  The four quarters' sums meet in shared
+// memory (added in quarter order) and warp j forms h of pair slot j:
+// silu(g) * u, its MXFP8 block over the 32 rows, stored as the pair's row.
 template <bool FP4>
 __global__ void __launch_bounds__(32 * G_WARPS) k_small_gateup(const uint8_t *__restrict__ gate_q,
                                                                const uint8_t *__restrict__ gate_s,
                                                                const uint8_t *__restrict__ up_q,
-                                                               const uint8_t *__restrict__ up_s, int d, int I, int k,
-                                                               int npair_max, SmallPlan sp)
+                                                               const uint8_t *__restrict__ up_s, int T, int d, int I,
+                                                               int k, int npair_max, SmallPlan sp)
 {
     extern __shared__ __align__(128) uint8_t g_smem[];
     const GateupSmem L(d, npair_max);
@@ -358,81 +362,163 @@ __global__ void __launch_bounds__(32 * G_WARPS) k_small_gateup(const uint8_t *__
     float *sx = reinterpret_cast<float *>(g_smem + L.sx);
     uint16_t *xh = reinterpret_cast<uint16_t *>(g_smem + L.xh);
     float *part = reinterpret_cast<float *>(g_smem + L.part);
-    __shared__ __align__(8) uint64_t bar;
-    const int KCd = d / 128, RTI = (I + 127) / 128, KCi = (I + 127) / 128, nbk = d / 32;
+    __shared__ __align__(8) uint64_t bar[4];
+    const int KCd = d / 128, RTI = (I + 127) / 128, KCi = (I + 127) / 128;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (threadIdx.x == 0) {
-        tc::mbar_init(&bar, 1);
-        tc::mbar_init_fence();
-    }
+    const int q = warp >> 2, mt = warp & 3, gt = threadIdx.x & 127;  // quarter, row tile, thread in group
+    if (threadIdx.x < 4) tc::mbar_init(&bar[threadIdx.x], 1);
+    if (threadIdx.x == 0) tc::mbar_init_fence();
     __syncthreads();
-    pdl_enter();
-    const int nt = __ldcg(sp.n_touched);
+    // this quarter's 128-element chunks of K: [kc0, kc1) (a quarter may be
+    // empty when d < 512), 64 code bytes per row each
+    const int kc0 = q * KCd / 4, kc1 = (q + 1) * KCd / 4, nkq = kc1 - kc0;
+    const uint32_t qbytes = uint32_t(nkq) * 64, qoff = uint32_t(kc0) * 64;
     const int nrb = I / 32;
-    const uint32_t row_bytes = uint32_t(d / 2);
-    uint32_t parity = 0;
-    for (int unit = blockIdx.x; unit < nt * nrb; unit += gridDim.x) {
-        const int u = unit / nrb, rb = unit - u * nrb;
-        const int e = __ldcg(sp.seg_expert + u);
-        const int q0 = __ldcg(sp.seg_start + u), q1 = __ldcg(sp.seg_start + u + 1);
-        const int np = min(q1 - q0, npair_max);
-        __syncthreads();  // the previous unit is done with every buffer
-        if (warp == 0) {
-            if (lane == 0) {
-                tc::fence_async_shared();
-                tc::mbar_arrive_expect_tx(&bar, 64 * row_bytes);
-            }
-            __syncwarp();
-            const int64_t r0 = int64_t(e) * I + rb * 32;
-            tc::bulk_load(wq + lane * L.wrow, gate_q + (r0 + lane) * row_bytes, row_bytes, &bar);
-            tc::bulk_load(wq + (32 + lane) * L.wrow, up_q + (r0 + lane) * row_bytes, row_bytes, &bar);
-        }
-        // weight block scales: one 32-bit word = four blocks of one row
-        for (int i = threadIdx.x; i < 64 * KCd; i += blockDim.x) {
-            const int r = i / KCd, kc = i - r * KCd;
-            const int row = rb * 32 + (r & 31);
-            const uint8_t *ms = r < 32 ? gate_s : up_s;
-            const uint32_t wd = __ldg(reinterpret_cast<const uint32_t *>(
-                ms + ((int64_t(e) * RTI + (row >> 7)) * KCd + kc) * 512 + (row & 31) * 16 + ((row & 127) >> 5) * 4));
+    pdl_enter();
+    // First round of loads: n_touched, this CTA's first unit (expert, pair
+    // range; blockIdx.x < P * I / 32 keeps the reads in bounds) and quarter q
+    // of x^ of every token with its block scales (the same for every unit).
+    const int nt = __ldcg(sp.n_touched);
+    int e_n = __ldcg(sp.seg_expert + blockIdx.x / nrb);
+    int q0_n = __ldcg(sp.seg_start + blockIdx.x / nrb), q1_n = __ldcg(sp.seg_start + blockIdx.x / nrb + 1);
+    const int cq = 8 * nkq;  // 16-element chunks of the quarter
+    {
+        uint4 xv[4];
+        uint32_t xb[4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) sf[(4 * kc + j) * 64 + r] = e8m0_to_f32((wd >> (8 * j)) & 0xFF);
-        }
-        // x^ of the unit's pairs: 16-element chunks as fp16, and block scales
-        for (int i = threadIdx.x; i < np * (d / 16); i += blockDim.x) {
-            const int j = i / (d / 16), c = i - j * (d / 16);
-            const int t = __ldcg(sp.seg_pair + q0 + j) / k;
-            uint32_t h[8];
-            if constexpr (FP4) {
-                e2m1x16_to_f16x2(__ldcg(reinterpret_cast<const uint2 *>(sp.xq + int64_t(t) * (d / 2)) + c), h);
-            } else {
-                const uint4 v = __ldcg(reinterpret_cast<const uint4 *>(sp.xq + int64_t(t) * d) + c);
-                const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    h[2 * q] = e4m3x2_to_f16x2(vw[q]);
-                    h[2 * q + 1] = e4m3x2_to_f16x2(vw[q] >> 16);
+        for (int m = 0; m < 4; ++m) {  // T * cq <= 512 (T <= 8, d <= 4096)
+            const int i = gt + 128 * m;
+            xv[m] = make_uint4(0, 0, 0, 0);
+            xb[m] = 0;
+            if (i < T * cq) {
+                const int t = i / cq, c = 8 * kc0 + (i - t * cq);
+                if constexpr (FP4) {
+                    const uint2 v = __ldcg(reinterpret_cast<const uint2 *>(sp.xq + int64_t(t) * (d / 2)) + c);
+                    xv[m] = make_uint4(v.x, v.y, 0, 0);
+                } else {
+                    xv[m] = __ldcg(reinterpret_cast<const uint4 *>(sp.xq + int64_t(t) * d) + c);
                 }
+                if ((c & 1) == 0) xb[m] = __ldcg(sp.xs + atom_offset(t, c >> 1, KCd));
             }
-            uint4 *dst = reinterpret_cast<uint4 *>(xh + j * L.xrow + 16 * c);
-            dst[0] = make_uint4(h[0], h[1], h[2], h[3]);
-            dst[1] = make_uint4(h[4], h[5], h[6], h[7]);
-            if ((c & 1) == 0) sx[(c >> 1) * G_PAIRS + j] = e8m0_to_f32(__ldcg(sp.xs + atom_offset(t, c >> 1, KCd)));
         }
-        __syncthreads();
-        if (!tc::mbar_wait(&bar, parity)) {
-            set_status(sp.status, LMOE_ERR_TIMEOUT);
-            return;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const int i = gt + 128 * m;
+            if (i < T * cq) {
+                const int t = i / cq, c = 8 * kc0 + (i - t * cq);
+                uint32_t h[8];
+                if constexpr (FP4) {
+                    e2m1x16_to_f16x2(make_uint2(xv[m].x, xv[m].y), h);
+                } else {
+                    const uint32_t vw[4] = {xv[m].x, xv[m].y, xv[m].z, xv[m].w};
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        h[2 * v] = e4m3x2_to_f16x2(vw[v]);
+                        h[2 * v + 1] = e4m3x2_to_f16x2(vw[v] >> 16);
+                    }
+                }
+                uint4 *dst = reinterpret_cast<uint4 *>(xh + t * L.xrow + 16 * c);
+                dst[0] = make_uint4(h[0], h[1], h[2], h[3]);
+                dst[1] = make_uint4(h[4], h[5], h[6], h[7]);
+                if ((c & 1) == 0) sx[(c >> 1) * G_PAIRS + t] = e8m0_to_f32(xb[m]);
+            }
         }
-        parity ^= 1;
-        // block products on the tensor cores
-        const int mt = warp & 3, kq = warp >> 2;
+    }
+    const int nunits = nt * nrb;
+    // this group's copies of quarter q of `unit`'s 64 rows (expert e)
+    auto issue = [&](int unit, int e) {
+        if (warp != 4 * q) return;
+        const int rb = unit % nrb;
+        if (lane == 0) {
+            tc::fence_async_shared();
+            tc::mbar_arrive_expect_tx(&bar[q], 64 * qbytes);
+        }
+        __syncwarp();
+        if (qbytes == 0) return;
+        const int64_t r0 = int64_t(e) * I + rb * 32 + lane;
+        tc::bulk_load(wq + lane * L.wrow + qoff, gate_q + r0 * (d / 2) + qoff, qbytes, &bar[q]);
+        tc::bulk_load(wq + (32 + lane) * L.wrow + qoff, up_q + r0 * (d / 2) + qoff, qbytes, &bar[q]);
+    };
+    // a unit's quarter-q block-scale words (<= 512 per quarter: 4 a thread) and
+    // the pair ids of its pair slots (loads only: used one unit later)
+    auto fetch = [&](int unit, int e, int q0, int q1, uint32_t (&wd)[4], int (&pid)[G_PAIRS]) {
+        const int rb = unit % nrb;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const int i = gt + 128 * m;
+            wd[m] = 0;
+            if (i < 64 * nkq) {
+                const int r = i / nkq, kc = kc0 + (i - r * nkq);
+                const int row = rb * 32 + (r & 31);
+                const uint8_t *ms = r < 32 ? gate_s : up_s;
+                wd[m] = __ldg(reinterpret_cast<const uint32_t *>(
+                    ms + ((int64_t(e) * RTI + (row >> 7)) * KCd + kc) * 512 + (row & 31) * 16 + ((row & 127) >> 5) * 4));
+            }
+        }
+        const int np = min(q1 - q0, npair_max);
+#pragma unroll
+        for (int j = 0; j < G_PAIRS; ++j) pid[j] = j < np ? __ldcg(sp.seg_pair + q0 + j) : -1;
+    };
+    // the tokens of the pair slots, 4 bits each (0xF: no pair)
+    auto slot_tokens = [&](const int (&pid)[G_PAIRS]) {
+        uint32_t sl = 0xFFFFFFFFu;
+#pragma unroll
+        for (int j = 0; j < G_PAIRS; ++j)
+            if (pid[j] >= 0) sl = (sl & ~(0xFu << (4 * j))) | (uint32_t(pid[j] / k) << (4 * j));
+        return sl;
+    };
+    auto group_sync = [&]() { asm volatile("bar.sync %0, 128;" ::"r"(1 + q) : "memory"); };
+    uint32_t wd[4] = {0, 0, 0, 0};
+    int pid[G_PAIRS];
+#pragma unroll
+    for (int j = 0; j < G_PAIRS; ++j) pid[j] = -1;
+    int e = e_n, q0 = q0_n, q1 = q1_n;
+    if (int(blockIdx.x) < nunits) {
+        issue(blockIdx.x, e);
+        fetch(blockIdx.x, e, q0, q1, wd, pid);
+    }
+    uint32_t parity = 0;
+    int it = 0;
+    for (int unit = blockIdx.x; unit < nunits; unit += gridDim.x, ++it) {
+        const int rb = unit % nrb;
+        const int np = min(q1 - q0, npair_max);
+        const uint32_t slots = slot_tokens(pid);
+        // the next unit's descriptor (used after this unit's products)
+        const int unit_n = unit + int(gridDim.x);
+        if (unit_n < nunits) {
+            e_n = __ldcg(sp.seg_expert + unit_n / nrb);
+            q0_n = __ldcg(sp.seg_start + unit_n / nrb);
+            q1_n = __ldcg(sp.seg_start + unit_n / nrb + 1);
+        }
+        // quarter q's weight block scales as fp32
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const int i = gt + 128 * m;
+            if (i < 64 * nkq) {
+                const int r = i / nkq, kc = kc0 + (i - r * nkq);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) sf[(4 * kc + j) * 64 + r] = e8m0_to_f32((wd[m] >> (8 * j)) & 0xFF);
+            }
+        }
+        group_sync();  // the quarter's scales are in place (and, the first time, x^)
+        // a wait that runs out records the timeout; every thread then leaves
+        // at the CTA barrier below (the products of this unit are discarded)
+        const bool landed = tc::mbar_wait(&bar[q], parity);
+        if (!landed && gt == 0) set_status(sp.status, LMOE_ERR_TIMEOUT);
+        // block products on the tensor cores: lane (g, t4) reads pair slot g's
+        // token (the B column) and accumulates pair slots 2 t4, 2 t4 + 1 (C)
         const int g = lane >> 2, t4 = lane & 3;
         const uint8_t *rowg = wq + (16 * mt + g) * L.wrow + 4 * t4;
         const uint8_t *rowg8 = rowg + 8 * L.wrow;
-        const bool col_ok = g < np;  // this lane's B column (pair slot g)
-        const uint16_t *xcol = xh + (col_ok ? g : 0) * L.xrow + 8 * t4;
+        const int tb = int((slots >> (4 * g)) & 0xF);          // token of B column g (15: none)
+        const int tc0 = int((slots >> (8 * t4)) & 0xF);        // token of C column 2 t4
+        const int tc1 = int((slots >> (8 * t4 + 4)) & 0xF);    // token of C column 2 t4 + 1
+        const bool col_ok = g < np;
+        const uint16_t *xcol = xh + (col_ok ? tb : 0) * L.xrow + 8 * t4;
+        const float *sx0 = sx + (2 * t4 < np ? tc0 : 0), *sx1 = sx + (2 * t4 + 1 < np ? tc1 : 0);
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        const int b0 = kq * (nbk / 4), b1 = b0 + nbk / 4;
+        const int b0 = 4 * kc0, b1 = 4 * kc1;
+#pragma unroll 4
         for (int b = b0; b < b1; ++b) {
             const uint32_t wg = *reinterpret_cast<const uint32_t *>(rowg + 16 * b);
             const uint32_t wg8 = *reinterpret_cast<const uint32_t *>(rowg8 + 16 * b);
@@ -441,30 +527,48 @@ __global__ void __launch_bounds__(32 * G_WARPS) k_small_gateup(const uint8_t *__
             uint32_t ag0, ag1, ag2, ag3, ah0, ah1, ah2, ah3;
             e2m1x8_to_f16x2(wg, ag0, ag1, ag2, ag3);
             e2m1x8_to_f16x2(wg8, ah0, ah1, ah2, ah3);
-            float c[4] = {0.f, 0.f, 0.f, 0.f};
-            mma_16816(c, ag0, ah0, ag1, ah1, xv.x, xv.y);
-            mma_16816(c, ag2, ah2, ag3, ah3, xv.z, xv.w);
+            // the block's two halves as independent products, then added
+            float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+            mma_16816(c0, ag0, ah0, ag1, ah1, xv.x, xv.y);
+            mma_16816(c1, ag2, ah2, ag3, ah3, xv.z, xv.w);
             const float s0 = sf[b * 64 + 16 * mt + g], s8 = sf[b * 64 + 16 * mt + g + 8];
-            const float2 xs2 = *reinterpret_cast<const float2 *>(sx + b * G_PAIRS + 2 * t4);
-            acc[0] = fmaf(c[0] * s0, xs2.x, acc[0]);
-            acc[1] = fmaf(c[1] * s0, xs2.y, acc[1]);
-            acc[2] = fmaf(c[2] * s8, xs2.x, acc[2]);
-            acc[3] = fmaf(c[3] * s8, xs2.y, acc[3]);
+            const float x0 = sx0[b * G_PAIRS], x1 = sx1[b * G_PAIRS];
+            acc[0] = fmaf((c0[0] + c1[0]) * s0, x0, acc[0]);
+            acc[1] = fmaf((c0[1] + c1[1]) * s0, x1, acc[1]);
+            acc[2] = fmaf((c0[2] + c1[2]) * s8, x0, acc[2]);
+            acc[3] = fmaf((c0[3] + c1[3]) * s8, x1, acc[3]);
         }
-        float *pw = part + (kq * 64 + 16 * mt + g) * G_PAIRS + 2 * t4;
+        float *pw = part + (((it & 1) * 4 + q) * 64 + 16 * mt + g) * G_PAIRS + 2 * t4;
         pw[0] = acc[0];
         pw[1] = acc[1];
         pw[8 * G_PAIRS] = acc[2];
         pw[8 * G_PAIRS + 1] = acc[3];
-        __syncthreads();
+        parity ^= 1;
+        // the next unit's scale words and pair tokens (its descriptor has arrived)
+        uint32_t wd_n[4] = {0, 0, 0, 0};
+        int pid_n[G_PAIRS];
+#pragma unroll
+        for (int j = 0; j < G_PAIRS; ++j) pid_n[j] = -1;
+        const bool next = landed && unit_n < nunits;
+        if (next) fetch(unit_n, e_n, q0_n, q1_n, wd_n, pid_n);
+        group_sync();  // the group is done with its quarter of the weights and scales
+        if (next) issue(unit_n, e_n);
+        if (__syncthreads_or(!landed)) {  // every quarter's sums are in place, or some wait ran out
+            // copies already issued for the next unit land before the CTA ends (bounded)
+            if (next) tc::mbar_wait(&bar[q], parity);
+            return;
+        }
         if (warp < np) {
             const int j = warp;
-            const int p = __ldcg(sp.seg_pair + q0 + j);
+            int p = 0;
+#pragma unroll
+            for (int jj = 0; jj < G_PAIRS; ++jj) p = jj == j ? pid[jj] : p;
+            const float *pu = part + (it & 1) * 4 * 64 * G_PAIRS;
             float gv = 0.f, uv = 0.f;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                gv += part[(q * 64 + lane) * G_PAIRS + j];
-                uv += part[(q * 64 + 32 + lane) * G_PAIRS + j];
+            for (int qq = 0; qq < 4; ++qq) {
+                gv += pu[(qq * 64 + lane) * G_PAIRS + j];
+                uv += pu[(qq * 64 + 32 + lane) * G_PAIRS + j];
             }
             const float h = __fdividef(gv, 1.f + __expf(-gv)) * uv;
             if (sp.hcap) sp.hcap[int64_t(p) * I + rb * 32 + lane] = h;
@@ -481,6 +585,13 @@ __global__ void __launch_bounds__(32 * G_WARPS) k_small_gateup(const uint8_t *__
             }
             if (lane == 0) sp.hs[atom_offset(p, rb, KCi)] = uint8_t(sb);
         }
+        e = e_n;
+        q0 = q0_n;
+        q1 = q1_n;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) wd[m] = wd_n[m];
+#pragma unroll
+        for (int j = 0; j < G_PAIRS; ++j) pid[j] = pid_n[j];
     }
 }
 
@@ -776,7 +887,7 @@ cudaError_t launch_small_t(const uint16_t *x, const uint16_t *Wr3, const float *
     const int max_units = P * (I / 32);
     const int ggrid = max_units < 152 ? max_units : 152;
     e = launch_pdl(k_small_gateup<FP4>, dim3(ggrid), dim3(32 * G_WARPS), gs, st, W->gate_q, W->gate_s, W->up_q,
-                   W->up_s, d, I, k, npair_max, sp);
+                   W->up_s, T, d, I, k, npair_max, sp);
     if (e != cudaSuccess) return e;
     if (stage_events && (e = cudaEventRecord(stage_events[4], st)) != cudaSuccess) return e;
     const int gp = down_group(P, d, I);
