@@ -283,7 +283,7 @@ class L2Flush:
     def run(self):
         import torch
         self.w.zero_()
-        torch.sum(self.r, out=self.out)
+        torch.sum(self.r, dim=0, out=self.out)
 
     def describe(self) -> str:
         return f"{self.bytes / 1e6:.0f} MB written, then {self.bytes / 1e6:.0f} MB of another buffer read"

@@ -363,7 +363,7 @@ cudaError_t launch_route(const uint16_t *x, const uint16_t *Wr3, const float *bi
     if (KS == 1) {
         e = dispatch<3, OUT_F32>(NB, ma, mb, a, st);
         if (e != cudaSuccess) return e;
-        return launch_topk_softmax(logits, T, E, k, idx, w, st);
+        return launch_topk_softmax(logits, T, E, k, idx, w, st, status);
     }
     a.out = partial;
     a.bias = nullptr;

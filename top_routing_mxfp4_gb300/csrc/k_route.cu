@@ -6,6 +6,7 @@
 #include <math.h>
 
 #include "lmoe_internal.cuh"
+#include "tc_ptx.cuh"
 #include "topk_select.cuh"
 
 namespace lmoe {
@@ -21,6 +22,57 @@ __global__ void __launch_bounds__(256) k_topk_softmax(const float *__restrict__ 
     const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (t >= T) return;
     select_topk<NV>(logits + int64_t(t) * E, E, k, idx + int64_t(t) * k, w + int64_t(t) * k, cand[threadIdx.x >> 5]);
+}
+
+// Large batches: a persistent grid, 8 warps a CTA, each warp one token of a
+// group of 8 consecutive tokens.  The group's logit rows (contiguous, E % 4
+// == 0) arrive by one bulk asynchronous copy into one of two shared-memory
+// buffers while the warps select the previous group's tokens from the other,
+// so the selection never waits on a global load.
+constexpr int TOPK_GROUP = 8;
+template <int NV>
+__global__ void __launch_bounds__(256) k_topk_softmax_staged(const float *__restrict__ logits, int T, int E, int k,
+                                                             int32_t *__restrict__ idx, float *__restrict__ w,
+                                                             int32_t *status)
+{
+    extern __shared__ __align__(128) float rows_s[];  // [2][TOPK_GROUP][E]
+    __shared__ float2 cand[TOPK_GROUP][64];            // per warp: the selection's candidates
+    __shared__ __align__(8) uint64_t bar[2];
+    const int warp = threadIdx.x >> 5;
+    if (threadIdx.x == 0) {
+        tc::mbar_init(&bar[0], 1);
+        tc::mbar_init(&bar[1], 1);
+        tc::mbar_init_fence();
+    }
+    __syncthreads();
+    pdl_enter();
+    const int ngroups = (T + TOPK_GROUP - 1) / TOPK_GROUP;
+    auto issue = [&](int gidx, int buf) {  // thread 0: the group's rows into buffer buf
+        const int t0 = gidx * TOPK_GROUP, nt = min(TOPK_GROUP, T - t0);
+        const uint32_t bytes = uint32_t(nt) * uint32_t(E) * 4;
+        tc::fence_async_shared();
+        tc::mbar_arrive_expect_tx(&bar[buf], bytes);
+        tc::bulk_load(rows_s + size_t(buf) * TOPK_GROUP * E, logits + int64_t(t0) * E, bytes, &bar[buf]);
+    };
+    int gidx = blockIdx.x, it = 0;
+    if (threadIdx.x == 0 && gidx < ngroups) issue(gidx, 0);
+    for (; gidx < ngroups; gidx += gridDim.x, ++it) {
+        const int buf = it & 1;
+        const int gn = gidx + int(gridDim.x);
+        if (threadIdx.x == 0 && gn < ngroups) issue(gn, buf ^ 1);  // the other buffer is free (barrier below)
+        if (!tc::mbar_wait(&bar[buf], uint32_t((it >> 1) & 1))) {
+            if (threadIdx.x == 0) set_status(status, LMOE_ERR_TIMEOUT);
+            break;
+        }
+        const int t = gidx * TOPK_GROUP + warp;
+        if (t < T)
+            select_topk<NV>(rows_s + (size_t(buf) * TOPK_GROUP + warp) * E, E, k, idx + int64_t(t) * k,
+                            w + int64_t(t) * k, cand[warp]);
+        __syncthreads();  // every warp is done with buffer buf before it is refilled
+    }
+    // a copy issued for a group this CTA did not reach (after a timeout) lands before the CTA ends
+    if (threadIdx.x == 0 && gidx < ngroups && gidx + int(gridDim.x) < ngroups)
+        tc::mbar_wait(&bar[(it & 1) ^ 1], uint32_t(((it + 1) >> 1) & 1));
 }
 
 // Split-K partial logits summed in slice order (then + bias), written to
@@ -66,9 +118,28 @@ cudaError_t launch_reduce_topk(const float *part, int KS, int T, int E, const fl
     return launch_pdl(k_reduce_topk<64, 256>, dim3(T), block, smem, st, part, KS, T, E, bias, logits, k, idx, w);
 }
 
-cudaError_t launch_topk_softmax(const float *logits, int T, int E, int k, int32_t *idx, float *w, cudaStream_t st)
+cudaError_t launch_topk_softmax(const float *logits, int T, int E, int k, int32_t *idx, float *w, cudaStream_t st,
+                                int32_t *status)
 {
     if (T == 0) return cudaSuccess;
+    if (status && E % 4 == 0 && E <= 896 && T >= 1024) {
+        // large batches: staged rows, a persistent grid of two CTAs per SM
+        // (what the selection's registers allow)
+        const size_t smem = size_t(2) * TOPK_GROUP * E * 4;
+        const int ngroups = int(ceil_div(T, TOPK_GROUP));
+        const int grid = ngroups < 2 * 152 ? ngroups : 2 * 152;
+        cudaError_t e = E <= 256 ? cudaFuncSetAttribute(k_topk_softmax_staged<8>,
+                                                         cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem))
+                                 : cudaFuncSetAttribute(k_topk_softmax_staged<28>,
+                                                        cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+        if (e != cudaSuccess) return e;
+        e = E <= 256 ? launch_pdl(k_topk_softmax_staged<8>, dim3(grid), dim3(256), smem, st, logits, T, E, k, idx, w,
+                                  status)
+                     : launch_pdl(k_topk_softmax_staged<28>, dim3(grid), dim3(256), smem, st, logits, T, E, k, idx, w,
+                                  status);
+        if (e != cudaSuccess) return e;
+        return cudaGetLastError();
+    }
     const int grid = int(ceil_div(T, 8));
     if (E <= 256) { const cudaError_t le_ = launch_pdl(k_topk_softmax<8>, dim3(grid), dim3(256), 0, st, logits, T, E, k, idx, w); if (le_ != cudaSuccess) return le_; }
     else if (E <= 896) { const cudaError_t le_ = launch_pdl(k_topk_softmax<28>, dim3(grid), dim3(256), 0, st, logits, T, E, k, idx, w); if (le_ != cudaSuccess) return le_; }

@@ -154,7 +154,10 @@ size_t linear_scratch_bytes(int T, int K, int N);
 cudaError_t launch_linear_bf16(const uint16_t *x, const uint16_t *W, int T, int K, int N, uint16_t *out, void *scratch,
                                int32_t *status, cudaStream_t st);
 // Top-k + softmax of fp32 logits [T][E].
-cudaError_t launch_topk_softmax(const float *logits, int T, int E, int k, int32_t *idx, float *w, cudaStream_t st);
+// status: the workspace's status word (the staged large-batch kernel's
+// bounded waits report there); null selects the unstaged kernel.
+cudaError_t launch_topk_softmax(const float *logits, int T, int E, int k, int32_t *idx, float *w, cudaStream_t st,
+                                int32_t *status = nullptr);
 // split-K partial logits [KS][T][E] -> logits (+ bias) and their top-k + softmax, one launch
 cudaError_t launch_reduce_topk(const float *part, int KS, int T, int E, const float *bias, float *logits, int k,
                                int32_t *idx, float *w, cudaStream_t st);
