@@ -236,17 +236,17 @@ size_t lmoe_workspace_size(const lmoe_dims *dims);
 
 /* Small batches ([L1] section 二, second layer: batch-1 decode): a batch of
  * at most `max_pairs` pairs T*k (and at most 8 tokens, 256 pairs) runs
- * lmoe_forward as three weight-streaming kernels on the CUDA cores (routing
- * with top-k and the pair lists; gate/up with SwiGLU and MXFP8 of h; down
- * with the gate weights and the combine) instead of the tensor-core path.
- * Same contract and roundings; the k terms of a token are summed in a fixed
- * order (deterministic), but not strictly slot by slot.  The default takes
- * it for batch-1 steps (16 pairs), where it matches the tensor-core path's
- * time with three launches instead of seven; beyond that its CUDA-core
- * arithmetic makes it slower than the tensor-core path.  0 sends every batch
- * to the tensor-core path.  Process-wide setting, not thread-safe; the
- * workspace size of a batch depends on it.  lmoe_small_batch_pairs() reads it. */
-#define LMOE_SMALL_BATCH_PAIRS_DEFAULT 16
+ * lmoe_forward as three weight-streaming kernels (routing with top-k and the
+ * pair lists; gate/up with SwiGLU and MXFP8 of h, on warp-level tensor-core
+ * products; down with the gate weights and the combine) instead of the
+ * tensor-core path.  Same contract and roundings; the k terms of a token are
+ * summed in a fixed order (deterministic), but not strictly slot by slot.  It
+ * is also the path of the MXFP4-activation variant (LMOE_ACT_MXFP4).  The
+ * default is 0: every batch takes the tensor-core path, which with its fused
+ * expert kernel measures faster at batch 1 too (54.2 against 58.9 us per
+ * step, L2 flushed).  Process-wide setting, not thread-safe; the workspace
+ * size of a batch depends on it.  lmoe_small_batch_pairs() reads it. */
+#define LMOE_SMALL_BATCH_PAIRS_DEFAULT 0
 lmoe_status lmoe_set_small_batch_pairs(int32_t max_pairs);
 int32_t lmoe_small_batch_pairs(void);
 

@@ -105,7 +105,7 @@ def set_wait_test(stall_first_fill: bool, wait_limit_cycles: int = 0):
     (lmoe_set_wait_test); (False, 0) restores the normal behaviour."""
     _check(_set_wait_test(1 if stall_first_fill else 0, int(wait_limit_cycles)), "lmoe_set_wait_test")
 _get_small = _sig("lmoe_small_batch_pairs", _i32)
-SMALL_BATCH_PAIRS_DEFAULT = 16
+SMALL_BATCH_PAIRS_DEFAULT = 0
 
 
 def set_small_batch_pairs(max_pairs: int):
