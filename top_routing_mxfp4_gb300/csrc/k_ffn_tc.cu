@@ -148,7 +148,7 @@ struct GemmArgs {
     uint8_t *hs;    // gate/up out: scale atoms [rows/128][KCh][512]
     float *hcap;    // gate/up, diagnostics only (normally null): every fp32 h before its MXFP8 rounding, [rows][Ih]
     float *yp;      // down out: [P][Mtot]
-    float *yacc;    // down out when set (fused combine): [T][Mtot] fp32 sums, zeroed by the caller
+    float *yacc;    // down out when set (fused combine): [T][Mtot] fp32 sums, zeroed before the kernel (by the gate/up kernel)
     const int32_t *perm;  // [P] pair of each permuted row (token = perm / k)
     int k;
     int E, Mtot, MTA, KC, KCh, Ih;  // MTA: 128-row tiles of A
@@ -157,6 +157,10 @@ struct GemmArgs {
     long long wait_limit;  // SM clocks a bounded wait may take before it gives up
     int stall_first_fill;  // failure-path test only: producer 0 withholds each CTA's first stage
     int32_t *tile_done;    // fused kernel: per token tile, epilogue warps done storing h (zeroed by the schedule)
+    // gate/up kernel: a buffer its epilogue warps zero between items (the down
+    // GEMM's fused-combine sums), n4 16-byte units; null: none
+    float4 *zero;
+    int64_t zero_n4;
 };
 
 template <int MODE, int NT>
@@ -658,6 +662,21 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
             }
             return true;
         };
+        // the buffer to zero: this CTA's slice [z, z1), a few units per
+        // epilogue thread after each item, the rest after the last one
+        int64_t z = 0, z1 = 0;
+        if (MODE == GATEUP && p.zero) {
+            const int64_t per = (p.zero_n4 + G - 1) / G;
+            z = min(p.zero_n4, int64_t(blockIdx.x) * per);
+            z1 = min(p.zero_n4, z + per);
+        }
+        const int et = threadIdx.x - 64, ne = 32 * C::EPI_WARPS;  // epilogue thread index and count
+        const int64_t zstep = n_mine > 0 ? ((z1 - z) / n_mine + ne - 1) / ne * ne : 0;
+        auto zero_some = [&](int64_t count) {
+            const int64_t end = min(z1, z + count);
+            for (int64_t u = z + et; u < end; u += ne) p.zero[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            z = end;
+        };
         Item nA{}, nB{};
         float wA[NV], wB[NV];
         int tA[NV], tB[NV];
@@ -670,13 +689,16 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
                 fetch(seq(i + 2), eA, nA, wA, tA);
                 eA = entry(seq(i + 4));
             }
+            zero_some(zstep);
             if (i + 1 >= n_mine) break;
             if (!process(seq(i + 1), nB, wB, tB)) break;
             if (i + 3 < n_mine) {
                 fetch(seq(i + 3), eB, nB, wB, tB);
                 eB = entry(seq(i + 5));
             }
+            zero_some(zstep);
         }
+        zero_some(z1 - z);
         if (threadIdx.x == 64) LMOE_TRACE_END(2);
     }
     tc_fence_before();
@@ -1199,8 +1221,13 @@ cudaError_t launch_expert_gemms(const FfnArgs &a, const FfnLayout &L, char *scra
     g.KCh = Ip / 128;
     g.Ih = a.I;
     g.tile_done = reinterpret_cast<int32_t *>(scratch + L.tile_done);
+    // the fused combine's sums start at zero: the gate/up epilogue clears them
+    g.zero = a.yacc ? reinterpret_cast<float4 *>(a.yacc) : nullptr;
+    g.zero_n4 = a.yacc ? int64_t(a.P / a.k) * a.d / 4 : 0;
     // down
     GemmArgs gd = g;
+    gd.zero = nullptr;
+    gd.zero_n4 = 0;
     gd.sfa0 = a.W->down_s;
     gd.sfa1 = a.W->down_s;  // the second tile of a down item is the next tile of the same matrix
     gd.sfb = hs;

@@ -358,7 +358,6 @@ lmoe_status lmoe_forward(const uint16_t *x_bf16, const uint16_t *Wr3, const floa
                            ffn_sched(FL, d, dims->I, fs));
     if (e == cudaSuccess) e = mark(2, st);
     if (e == cudaSuccess) e = launch_quant_scatter_pad(x_bf16, T, d, k, E, dims->I, inv, w, FL, fs, st);
-    if (e == cudaSuccess && yacc) e = cudaMemsetAsync(yacc, 0, size_t(T) * d * sizeof(float), st);
     if (e == cudaSuccess) e = mark(3, st);
     if (e == cudaSuccess) {
         FfnArgs f{W, offsets, perm, w, int(P), d, E, k, dims->I, yp, yacc, status};

@@ -261,7 +261,7 @@ struct FfnArgs {
     const float *topk_w;
     int P, d, E, k, I;
     float *yp;    // [P][d] in permuted order
-    float *yacc;  // when set (FfnLayout::fused only): [T][d] fp32 sums over the k pairs instead of yp
+    float *yacc;  // when set (FfnLayout::fused only): [T][d] fp32 sums over the k pairs instead of yp (the gate/up kernel zeroes it)
     int32_t *status;
     float *hcap = nullptr;  // diagnostics: fp32 h before its MXFP8 rounding, [FfnLayout::rows][I]
     long long wait_limit = 0;   // bounded-wait limit in SM clocks (0: the default, ~2 s)
