@@ -289,6 +289,23 @@ class L2Flush:
         return f"{self.bytes / 1e6:.0f} MB written, then {self.bytes / 1e6:.0f} MB of another buffer read"
 
 
+def scale_histogram_record(bank) -> dict:
+    """The bank's E8M0 weight-scale histograms (lmoe_mxfp4_scale_histogram:
+    256 bins per expert matrix, counted on the GPU), summed over the experts
+    for each of gate, up and down, with each matrix's scale range."""
+    rec = {}
+    for w, h in bank.scale_histograms().items():
+        h = h.cpu().long()                       # [E, 256]
+        tot = h.sum(0)
+        nz = [int(b) for b in (tot > 0).nonzero().flatten()]
+        per_lo = [int((row > 0).nonzero().min()) for row in h]
+        per_hi = [int((row > 0).nonzero().max()) for row in h]
+        rec[w] = {"bins": {str(b): int(tot[b]) for b in nz},
+                  "scale_exponent_range": [nz[0] - 127, nz[-1] - 127] if nz else None,
+                  "per_matrix_exponent_span_max": max(hi - lo for lo, hi in zip(per_lo, per_hi)) if nz else 0}
+    return rec
+
+
 def time_steps(fwd, K: int, st, scrub=None) -> float:
     """Device time of K forward passes (ms): back to back, or, with `scrub`
     (an L2Flush), each step timed alone after the flush."""
@@ -559,6 +576,7 @@ def run_ours(args, ws, rank, local):
         "e2e": {"value": whole_job_rate(T, ws, e2e_ms / K), "unit": UNIT, "h2d_bytes_per_step": xh.numel() * 2,
                 "d2h_bytes_per_step": yh.numel() * 2},
         "gpu_launches": K * launches_per_step, "clocks": clocks,
+        "weight_scale_histogram": scale_histogram_record(bank),
     }
     if ws == 1 and wl.name == "decode" and not args.no_side_workloads:
         # The same run, on the same resident expert bank: the headline re-timed

@@ -309,37 +309,39 @@ lmoe_status lmoe_set_stage_events(void *const *events, int32_t n);
 
 /* Where lmoe_forward keeps the expert GEMMs' MXFP8 operands inside its
  * workspace, as byte offsets from the workspace start, for these dims:
- *   xq  [rows][d]  e4m3 codes of x, one row per routed pair, in token tiles
- *       of tile_tokens rows packed one after another (an expert's pairs fill
- *       whole tiles from a tile boundary),
- *   xs  scale atoms of x: tile n's rows rr = 0 .. tile_tokens-1 are rows
- *       32*j + i of its 512-byte atoms, one atom per 128 columns: row R
- *       (tile n = R / tile_tokens, rr = R % tile_tokens, i = rr % 32,
- *       j = rr / 32), block b at byte ((n*(d/128) + b/4)*512 + 16*i + 4*j +
- *       b%4),
- *   hq  [rows][I]  e4m3 codes of the gated product h of each pair,
+ *   xq  [rows][d]  e4m3 codes of x, one row per routed pair at its position
+ *       in expert-sorted (permuted) order, code_row[p]; expert e's pairs
+ *       form token tiles of tile_tokens rows from its first pair on,
+ *   xs  scale atoms of x, one 512-byte atom per token tile and 128 columns:
+ *       a pair's atom row R = dst_row[p] (its tile n = R / tile_tokens, row
+ *       rr = R % tile_tokens in the tile, i = rr % 32, j = rr / 32), block b
+ *       at byte ((n*(d/128) + b/4)*512 + 16*i + 4*j + b%4),
+ *   hq  [rows][I]  e4m3 codes of the gated product h of each pair (row
+ *       code_row[p]),
  *   hs  scale atoms of h (the same layout with roundup(I,128)/128 atoms per
  *       tile),
- *   dst_row  int32 [T*k]: the row of pair p = t*k + j;
- * rows = rows reserved, tile_tokens = tokens per expert-GEMM tile,
- * slot_rows = rows a tile occupies (tile_tokens: packed).  Valid after an
- * lmoe_forward call with the same dims has completed; rows no pair maps to
- * hold no defined data. */
+ *   dst_row   int32 [T*k]: the atom row of pair p = t*k + j,
+ *   code_row  int32 [T*k]: the code row of pair p (the permute's inverse map);
+ * rows = code rows reserved (T*k plus one tile), tile_tokens = tokens per
+ * expert-GEMM tile, slot_rows = atom rows a tile occupies (tile_tokens).
+ * Valid after an lmoe_forward call with the same dims has completed; rows no
+ * pair maps to hold no defined data. */
 typedef struct {
     int64_t xq, xs, hq, hs, dst_row;
     int64_t rows;
     int32_t tile_tokens, slot_rows;
     int32_t path; /* 0: as above; 1: small-batch path (lmoe_set_small_batch_pairs): xq/xs hold one row per
-                     token t, hq/hs one row per pair p = t*k + j, dst_row = -1, rows = T*k; with
+                     token t, hq/hs one row per pair p = t*k + j, dst_row = code_row = -1, rows = T*k; with
                      LMOE_ACT_MXFP4 a code row holds packed e2m1 codes (d/2 or I/2 bytes, element 2i in
                      the low nibble of byte i) */
+    int64_t code_row;
 } lmoe_ffn_views;
 lmoe_status lmoe_forward_workspace_views(const lmoe_dims *dims, lmoe_ffn_views *views);
 
 /* When h_f32 is set (device buffer of `bytes` bytes, 16-byte aligned), every
  * later lmoe_forward / lmoe_expert_ffn call also writes the fp32 value of
  * each h its gate/up GEMM rounds to MXFP8 at h_f32[R][i] (R the pair's
- * padded row as in lmoe_ffn_views, I floats per row), so a test can check
+ * code row as in lmoe_ffn_views, I floats per row), so a test can check
  * the rounding bit for bit.  Calls return LMOE_ERR_INVALID_ARG while the
  * buffer is smaller than rows * I * 4 bytes.  NULL clears the hook.  The
  * setting is process-wide and not thread-safe. */

@@ -78,20 +78,22 @@ def test_forward_mxfp8_operands_bit_exact(cuda_lib, T, tile):
     assert layer.device_status() == 0
     ws = layer._ws
     P = T * k
-    R = ws[v.dst_row:v.dst_row + 4 * P].view(torch.int32).to(torch.int64)
-    Rh = R.cpu().numpy()
-    assert Rh.min() >= 0 and Rh.max() < v.rows and np.unique(Rh).size == P
-    # x: every routed pair's token row holds MXFP8(x[t]) of its token t = p / k
-    xq = ws[v.xq:v.xq + v.rows * d].view(v.rows, d)[R].cpu().numpy()
+    R = ws[v.dst_row:v.dst_row + 4 * P].view(torch.int32).to(torch.int64)  # atom rows (scale factors)
+    Q = ws[v.code_row:v.code_row + 4 * P].view(torch.int32).to(torch.int64)  # code rows (permuted order)
+    Rh, Qh = R.cpu().numpy(), Q.cpu().numpy()
+    assert Rh.min() >= 0 and np.unique(Rh).size == P
+    assert np.array_equal(np.sort(Qh), np.arange(P)) and v.rows == P + v.tile_tokens
+    # x: every routed pair's code row holds MXFP8(x[t]) of its token t = p / k
+    xq = ws[v.xq:v.xq + v.rows * d].view(v.rows, d)[Q].cpu().numpy()
     xs = atom_scales(ws[v.xs:v.hq], R, d // 32, v.tile_tokens)
     rq, rs = oracle.quant_mxfp8(x)
     tok = np.arange(P) // k
     bad = np.nonzero((xq != rq[tok]).any(1) | (xs != rs[tok]).any(1))[0]
     assert bad.size == 0, f"{bad.size} of {P} pairs' x rows differ from the oracle (first pair {bad[:1]})"
     # h: every pair's codes and scales equal the oracle's rounding of the fp32 h the GEMM produced
-    h = hcap.view(v.rows, I)[R].cpu().numpy().astype(np.float64)
+    h = hcap.view(v.rows, I)[Q].cpu().numpy().astype(np.float64)
     assert np.isfinite(h).all(), "the epilogue did not capture h for every routed pair"
-    hq = ws[v.hq:v.hq + v.rows * I].view(v.rows, I)[R].cpu().numpy()
+    hq = ws[v.hq:v.hq + v.rows * I].view(v.rows, I)[Q].cpu().numpy()
     hs = atom_scales(ws[v.hs:], R, I // 32, v.tile_tokens)
     hrq, hrs = oracle.quant_mxfp8_f64(h)
     bad_q = np.nonzero((hq != hrq).any(1))[0]

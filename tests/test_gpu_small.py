@@ -155,6 +155,23 @@ def test_small_and_tensor_core_paths_agree(small_path):
     assert (np.abs(a - b).max(1) / np.sqrt((b ** 2).mean(1))).max() < TOL
 
 
+@pytest.mark.parametrize("T", [1, 2, 8])
+def test_default_path_decode_shape_all_tokens(cuda_lib, T):
+    """The library's default choice of path at one, two and eight tokens (the
+    tensor-core path with its fused expert kernel, since the small-batch
+    path is opt-in), every token against the oracle."""
+    lmoe = cuda_lib
+    assert lmoe.small_batch_pairs() == lmoe.SMALL_BATCH_PAIRS_DEFAULT == 0
+    wl = gen.custom(f"dflt{T}", T=T, d=3584, I=512)
+    assert lmoe.forward_workspace_views(T, wl.d, wl.E, wl.k, wl.I).path == 0
+    x = gen.x_bf16(wl)
+    _, y, idx, w, lg, _ = _forward(lmoe, wl, x)
+    _check_all(lmoe, wl, x, y, idx, w, lg)
+    # deterministic run to run (the combine sums each token's pairs in slot order)
+    _, y2, _, _, _, _ = _forward(lmoe, wl, x)
+    np.testing.assert_array_equal(y2, y)
+
+
 def test_sixteen_token_step_all_tokens_default_path(cuda_lib):
     """A 16-token decode step (256 pairs) with the library's default choice of
     path, every token against the oracle."""

@@ -23,12 +23,16 @@
 //     topk_w[perm[q]] * Y by fp32 vector atomics in L2 (the k terms of a
 //     token are then summed in fp32 in an unspecified order).
 //
-// Token layout: token tiles of NT rows are packed one after another; the
-// activations of expert e occupy `ntiles(e)` tiles starting at row pad_off[e]
-// (a multiple of NT), token r of the expert at row pad_off[e] + r.  Each
-// tile's scale factors are a 512-byte atom per 128 columns (the tile's rows
-// 0..NT-1 of a 128-row atom), which one bulk copy moves and one tcgen05.cp
-// puts in TMEM; only the codes of valid rows and whole atoms take memory.
+// Token layout: the codes of the activations (x^ for gate/up, h^ for down)
+// are one row per routed pair in permuted order: expert e's pairs occupy rows
+// offsets[e] .. offsets[e+1]-1, and its token tile n is the NT rows from
+// offsets[e] + n*NT (a partial last tile reads the next expert's rows, or the
+// NT rows reserved past the end, as padding whose product columns are
+// dropped).  Each tile's scale factors are a 512-byte atom per 128 columns
+// (the tile's rows 0..NT-1 of a 128-row atom), which one bulk copy moves and
+// one tcgen05.cp puts in TMEM; tiles are numbered per expert from
+// pad_off[e] / NT, and a pair's "atom row" (tile * NT + row in tile) is its
+// dst_row.
 //
 // Persistent, warp-specialised CTA (256 or 384 threads, one per SM):
 //   warp 0     TMA producer 0 (first A tile via the packed-FP4 tensor map that
@@ -363,7 +367,8 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
                 ent_next = entry(seq(i + 2));
                 const int mode = mode_of(it);
                 const GemmArgs &a = (MODE == FUSED && mode == DOWN) ? q : p;
-                const int R = slot_row(w.e) + w.n_tile * C::SLOT;
+                const int R = slot_row(w.e) + w.n_tile * C::SLOT;  // the tile's atom row (scale factors)
+                const int Rc = s_off[w.e] + w.n_tile * NT;         // its first code row (permuted order)
                 // gate/up: tile m of both matrices; down: tiles 2m and 2m+1 (an odd
                 // last tile loads tile 2m twice and the epilogue drops the copy)
                 const int mt0 = mode == GATEUP ? w.m_tile : C::MATS * w.m_tile;
@@ -398,7 +403,7 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
                                 break;
                             }
                         }
-                        tma_load_2d(sb + C::MATS * C::A_TILE, tmBx, kc * 128, R, &full[stage]);
+                        tma_load_2d(sb + C::MATS * C::A_TILE, tmBx, kc * 128, Rc, &full[stage]);
                     } else {
                         mbar_arrive_expect_tx(&full[stage], C::TX_BYTES1);
                         if (C::MATS == 2) {
@@ -542,7 +547,8 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
             if (mode == GATEUP && w.m_tile * 128 + 32 * lq < p.Mtot) {
                 const int row0 = w.m_tile * 128 + 32 * lq;  // first row of I held by this warp
                 const int blk = row0 / 32;                 // MX block of I held by this warp
-                const int64_t Rbase = int64_t(slot_row(w.e)) + int64_t(w.n_tile) * C::SLOT;
+                const int64_t Rbase = int64_t(slot_row(w.e)) + int64_t(w.n_tile) * C::SLOT;  // atom rows
+                const int64_t Cbase = int64_t(s_off[w.e]) + int64_t(w.n_tile) * NT;           // code rows
                 for (int c0 = 16 * half; c0 < w.n_valid; c0 += 16 * C::NW) {
                     uint32_t v0[16], v1[16];
                     tmem_ld16(tbase + c0, v0);
@@ -555,7 +561,7 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
                     for (int j = 0; j < 16; ++j) {
                         const float gv = __uint_as_float(v0[j]), uv = __uint_as_float(v1[j]);
                         const float h = __fdividef(gv, 1.f + __expf(-gv)) * uv;
-                        if (p.hcap && c0 + j < w.n_valid) p.hcap[(Rbase + c0 + j) * p.Ih + row0 + lane] = h;
+                        if (p.hcap && c0 + j < w.n_valid) p.hcap[(Cbase + c0 + j) * p.Ih + row0 + lane] = h;
                         uint32_t amax;
                         asm("redux.sync.max.u32 %0, %1, 0xffffffff;" : "=r"(amax) : "r"(__float_as_uint(h) & 0x7FFFFFFFu));
                         sbv[j] = mx_scale_byte(__uint_as_float(amax), 8);
@@ -569,10 +575,10 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
                         // lane l stores 16 codes of token column l/2 (rows 16*(l&1) ..)
                         const int c = lane >> 1;
                         if (c0 + c < w.n_valid)
-                            *reinterpret_cast<uint4 *>(p.hq + (Rbase + c0 + c) * p.Ih + row0 + 16 * (lane & 1)) =
+                            *reinterpret_cast<uint4 *>(p.hq + (Cbase + c0 + c) * p.Ih + row0 + 16 * (lane & 1)) =
                                 *reinterpret_cast<const uint4 *>(stg + 16 * lane);
                     } else {
-                        uint8_t *hrow = p.hq + (Rbase + c0) * p.Ih + row0 + lane;
+                        uint8_t *hrow = p.hq + (Cbase + c0) * p.Ih + row0 + lane;
 #pragma unroll
                         for (int j = 0; j < 16; ++j)
                             if (c0 + j < w.n_valid) hrow[int64_t(j) * p.Ih] = uint8_t(code[j]);
@@ -848,7 +854,7 @@ __global__ void k_quant_scatter_pad(const uint16_t *__restrict__ x, int64_t nuni
             if (rows[j] < 0) continue;
             if (b == 0 && h == 0) w_sorted[qs[j]] = __ldg(topk_w + p0 + j);
             const int64_t R = rows[j];
-            *reinterpret_cast<uint4 *>(xq + R * d + b * 32 + h * 16) = make_uint4(c[0], c[1], c[2], c[3]);
+            *reinterpret_cast<uint4 *>(xq + int64_t(qs[j]) * d + b * 32 + h * 16) = make_uint4(c[0], c[1], c[2], c[3]);
             if ((b & 3) == 0 && h == 0) *reinterpret_cast<uint32_t *>(xs + tile_atom_off(R, b, KC, sc.NT)) = sb4;
         }
     }
@@ -868,7 +874,7 @@ __global__ void __launch_bounds__(SCATTER_ROWS_THREADS) k_quant_scatter_rows(
     float *__restrict__ w_sorted, FfnSched sc, int E)
 {
     extern __shared__ __align__(128) uint8_t qrow_smem[];  // [2][d] e4m3 codes
-    __shared__ int32_t rows_s[2][32];
+    __shared__ int32_t rows_s[2][32], qrow_s[2][32];  // per slot: atom row, code row (permuted order)
     pdl_enter();
     fill_item_entries(sc, sc.tiles_gu[E], sc.tiles_dn[E], blockIdx.x * int64_t(blockDim.x) + threadIdx.x,
                       int64_t(gridDim.x) * blockDim.x);
@@ -876,13 +882,14 @@ __global__ void __launch_bounds__(SCATTER_ROWS_THREADS) k_quant_scatter_rows(
     int it = 0;
     for (int t = blockIdx.x; t < T; t += gridDim.x, ++it) {
         uint8_t *buf = qrow_smem + (it & 1) * d;
-        int32_t *rows = rows_s[it & 1];
+        int32_t *rows = rows_s[it & 1], *qrows = qrow_s[it & 1];
         // the copies that read this buffer two tokens ago have read it
         if (threadIdx.x == 0) tc::bulk_wait_read<1>();
         if (threadIdx.x < k) {
             const int64_t p = int64_t(t) * k + threadIdx.x;
             const int32_t q = __ldg(inv + p);  // < 0: the permute rejected the pair
             rows[threadIdx.x] = q >= 0 ? __ldg(dst_row + p) : -1;
+            qrows[threadIdx.x] = q;
             if (q >= 0) w_sorted[q] = __ldg(topk_w + p);
         }
         __syncthreads();
@@ -930,7 +937,7 @@ __global__ void __launch_bounds__(SCATTER_ROWS_THREADS) k_quant_scatter_rows(
         __syncthreads();
         if (threadIdx.x == 0) {
             for (int j = 0; j < k; ++j)
-                if (rows[j] >= 0) tc::bulk_store(xq + int64_t(rows[j]) * d, buf, uint32_t(d));
+                if (rows[j] >= 0) tc::bulk_store(xq + int64_t(qrows[j]) * d, buf, uint32_t(d));
             tc::bulk_commit();
         }
     }
@@ -959,7 +966,7 @@ __global__ void k_gather_pad(const uint8_t *__restrict__ xq, const uint8_t *__re
         const int64_t pr = __ldg(perm + qrow), t = pr / k;
         if (c == 0) w_sorted[qrow] = __ldg(topk_w + pr);
         if (c < cq) {
-            reinterpret_cast<uint4 *>(q_pad + R * d)[c] = __ldg(reinterpret_cast<const uint4 *>(xq + t * d) + c);
+            reinterpret_cast<uint4 *>(q_pad + qrow * d)[c] = __ldg(reinterpret_cast<const uint4 *>(xq + t * d) + c);
         } else {
             const int b = c - cq;
             s_pad[tile_atom_off(R, b, KC, NT)] = __ldg(xs + t * nb + b);
@@ -1070,8 +1077,11 @@ FfnLayout ffn_layout(int64_t P, int d, int E, int I)
     L.SLOT = L.NT;  // packed tiles
     const int64_t touched = P < E ? P : E;
     const int64_t tiles = ceil_div(P, L.NT) + touched;  // bounds sum_e ceil(n_e / NT)
-    L.rows = tiles * L.SLOT;
-    const int64_t atoms = tiles;  // one atom per tile and 128 columns
+    // code rows: one per pair in permuted order, plus one tile's worth that
+    // the last expert's last tile may read past the end (those columns of its
+    // products are dropped); scale factors: one atom per tile and 128 columns
+    L.rows = P + L.NT;
+    const int64_t atoms = tiles;
     const int Ip = int(round_up(I, 128));
     size_t off = 0;
     auto take = [&](size_t bytes) {
@@ -1082,7 +1092,7 @@ FfnLayout ffn_layout(int64_t P, int d, int E, int I)
     L.pad_off = take(size_t(E + 1) * 4);
     L.tiles_gu = take(size_t(E + 1) * 4);
     L.tiles_dn = take(size_t(E + 1) * 4);
-    const int64_t max_tiles = L.rows / L.SLOT;
+    const int64_t max_tiles = tiles;
     L.items_gu = take(size_t(max_tiles * ceil_div(I, 128)) * sizeof(int2));
     L.items_dn = take(size_t(max_tiles * ceil_div(d / 128, down_tiles_per_item(L.NT))) * sizeof(int2));
     L.tile_info = take(size_t(max_tiles) * sizeof(int2));

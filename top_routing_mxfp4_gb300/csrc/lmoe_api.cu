@@ -65,7 +65,7 @@ bool weights_ok(const lmoe_expert_weights *W)
 
 // Workspace layout of lmoe_forward (each region 256-byte aligned):
 //   status | logits | idx | w | counts | offsets | perm | inv | permute scratch
-//   | ffn scratch (tiled MXFP8 activations, h, schedule)
+//   | ffn scratch (MXFP8 activations and h in permuted order, their scale atoms per token tile, schedule)
 //   | yp (per-pair outputs [T*k][d]) or, with the fused combine, yacc ([T][d] fp32 sums)
 // The small-batch path (lmoe_set_small_batch_pairs) uses
 //   status (+ the routing kernel's counter) | logits | idx | w | small-path scratch.
@@ -454,6 +454,7 @@ lmoe_status lmoe_forward_workspace_views(const lmoe_dims *dims, lmoe_ffn_views *
         views->hq = int64_t(L.sscratch + S.hq);
         views->hs = int64_t(L.sscratch + S.hs);
         views->dst_row = -1;
+        views->code_row = -1;
         views->rows = int64_t(dims->T) * dims->k;
         views->tile_tokens = 0;
         views->slot_rows = 0;
@@ -467,6 +468,7 @@ lmoe_status lmoe_forward_workspace_views(const lmoe_dims *dims, lmoe_ffn_views *
     views->hq = int64_t(L.fscratch + F.hq);
     views->hs = int64_t(L.fscratch + F.hs);
     views->dst_row = int64_t(L.fscratch + F.dst_row);
+    views->code_row = int64_t(L.inv);
     views->rows = F.rows;
     views->tile_tokens = F.NT;
     views->slot_rows = F.SLOT;

@@ -168,11 +168,12 @@ cudaError_t launch_route(const uint16_t *x, const uint16_t *Wr3, const float *bi
                          float *logits, int32_t *idx, float *w, void *scratch, int32_t *status, cudaStream_t st);
 
 // Optional by-products of the permute for the expert GEMMs: per expert the
-// first token row in the tiled token layout (pad_off, E+1) and the first work
-// item of each GEMM (tiles_gu / tiles_dn, E+1), the expert of each token tile
-// (tile_info; the activation scatter turns it into the GEMMs' work-item
-// tables items_gu / items_dn), and per pair p its token row (dst_row,
-// T*k).  pad_off == nullptr disables them.
+// first atom row of its token tiles (pad_off = first tile * NT, E+1) and the
+// first work item of each GEMM (tiles_gu / tiles_dn, E+1), the expert of each
+// token tile (tile_info; the activation scatter turns it into the GEMMs'
+// work-item tables items_gu / items_dn), and per pair p its atom row (dst_row,
+// T*k: tile * NT + row in tile, which locates its scale factors; its codes sit
+// at its permuted position).  pad_off == nullptr disables them.
 struct FfnSched {
     int NT = 0, SLOT = 0, MT_gu = 0, MT_dn = 0;
     int band = 0;  // the down GEMM runs its items in this many output-column bands (0 or 1: one)
@@ -237,12 +238,13 @@ cudaError_t launch_permute(const int32_t *idx, int64_t P, int E, int32_t *counts
                            int32_t *inv, void *scratch, int32_t *status, cudaStream_t st,
                            const FfnSched &sched = FfnSched());
 
-// Expert FFN (tensor cores).  Activations live in a tiled token layout
-// inside the FFN scratch: expert e's tokens fill consecutive rows from
-// pad_off[e] (a whole number of NT-row tiles per expert); see k_ffn_tc.cu.
+// Expert FFN (tensor cores).  Activation codes live one row per pair in
+// permuted order inside the FFN scratch, their scale factors in one atom per
+// NT-row token tile (tiles numbered per expert from pad_off[e] / NT); see
+// k_ffn_tc.cu.
 struct FfnLayout {
     int NT, SLOT;      // token tile and the rows a tile occupies (SLOT == NT: tiles are packed)
-    int64_t rows;      // token rows reserved (whole tiles)
+    int64_t rows;      // code rows reserved: one per pair (permuted order) + one tile past the end
     size_t pad_off, tiles_gu, tiles_dn, items_gu, items_dn, tile_info, xq, xs, hq, hs, hs_bytes, w_sorted, dst_row,
         tile_done, total;  // byte offsets / sizes
     bool fused;  // large token tiles: the down GEMM can accumulate into the per-token output (FfnArgs::yacc)
@@ -270,8 +272,9 @@ struct FfnArgs {
 // slot starts and per-GEMM work-item prefixes from the segment offsets
 cudaError_t launch_ffn_schedule(const int32_t *offsets, int E, int d, int I, const FfnLayout &L, char *scratch,
                                 cudaStream_t st);
-// bf16 x[T][d] -> MXFP8 rows at each routed pair's token row (dst_row from
-// the permute); also the gate weights in permuted order.
+// bf16 x[T][d] -> MXFP8 codes at each routed pair's permuted row (inv) and
+// scales at its atom row (dst_row, from the permute); also the gate weights
+// in permuted order.
 // (also writes the expert GEMMs' work-item tables from the permute's tile_info)
 cudaError_t launch_quant_scatter_pad(const uint16_t *x, int T, int d, int k, int E, int I, const int32_t *inv,
                                      const float *topk_w, const FfnLayout &L, char *scratch, cudaStream_t st);
