@@ -146,6 +146,63 @@ def test_topk_ties_and_signed_zero(cuda_lib):
         np.testing.assert_allclose(w.cpu().numpy(), rw, rtol=1e-6, atol=1e-9)
 
 
+def _warp_bound_row(rng, E, extra):
+    """A logits row whose 16th largest 32-expert group maximum is 1.0 (groups
+    0..15 peak at 1.0 + 0.01 g, the rest lie below -10), with `extra` more
+    values tied at 1.0 in the groups' other slots: 16 + extra values at or
+    above the bound."""
+    row = (np.float32(-10.0) - rng.random(E).astype(np.float32)).astype(np.float32)
+    for g in range(16):
+        row[32 * g] = np.float32(1.0) + np.float32(0.01) * np.float32(g)
+    n = 0
+    for g in range(1, 16):
+        for j in range(1, 32):
+            if n < extra:
+                row[32 * g + j] = np.float32(1.0)
+                n += 1
+    assert n == extra
+    return row
+
+
+def test_split_k_route_topk_ties(cuda_lib):
+    """The split-K router's reduction + top-k kernel (small batches) on
+    crafted logits: token t's row of x is one-hot at column t, so its logits
+    are exactly column t of the router weights.  Rows: all equal (every
+    expert a candidate), signed zeros, many ties, exactly 64 and 65 values at
+    the bound the block's candidate narrowing uses (16th largest maximum of the
+    32-expert groups), group maxima tied at that bound, and a plain row."""
+    lmoe = cuda_lib
+    rng = np.random.default_rng(23)
+    T, d, E, k = 8, 512, 896, 16
+    cols = [np.zeros(E, np.float32)]
+    r = rng.standard_normal(E).astype(np.float32)
+    r[::2] = -0.0
+    cols.append(r)
+    cols.append((np.round(rng.standard_normal(E) * 2) / 2).astype(np.float32))
+    cols.append(_warp_bound_row(rng, E, 48))
+    cols.append(_warp_bound_row(rng, E, 49))
+    r = (np.float32(-10.0) - rng.random(E).astype(np.float32)).astype(np.float32)
+    r[32 * np.arange(20)] = np.float32(2.0)  # 20 group maxima tied, the bound among them
+    cols.append(r)
+    r = rng.standard_normal(E).astype(np.float32)
+    r[100:140] = 7.0
+    cols.append(r)
+    cols.append(rng.standard_normal(E).astype(np.float32))
+    Wr = (rng.standard_normal((E, d)) * 0.05).astype(np.float32)
+    for t, c in enumerate(cols):
+        Wr[:, t] = c
+    x = np.zeros((T, d), np.uint16)
+    x[np.arange(T), np.arange(T)] = 0x3F80  # bf16 1.0
+    logits, idx, w = lmoe.route(to_dev_bf16(x, DEV), torch.from_numpy(Wr).to(DEV), k)
+    torch.cuda.synchronize()
+    lg = logits.cpu().numpy()
+    # the logits are the crafted columns (signed zeros may come back as +0)
+    np.testing.assert_array_equal(lg, Wr[:, :T].T + np.float32(0.0))
+    ridx, rw = oracle.topk_softmax(lg, k)
+    np.testing.assert_array_equal(idx.cpu().numpy(), ridx)
+    np.testing.assert_allclose(w.cpu().numpy(), rw, rtol=1e-6, atol=1e-9)
+
+
 @pytest.mark.parametrize("T,E,k,skew", [(8, 896, 16, 0), (64, 896, 16, 0), (300, 896, 16, 1), (8192, 896, 16, 1),
                                         (1000, 2048, 8, 0), (1, 4, 4, 0), (0, 896, 16, 0), (5000, 7, 3, 0)])
 def test_permute_bit_exact(cuda_lib, T, E, k, skew):

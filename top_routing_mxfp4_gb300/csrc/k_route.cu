@@ -76,9 +76,17 @@ __global__ void __launch_bounds__(256) k_topk_softmax_staged(const float *__rest
 }
 
 // Split-K partial logits summed in slice order (then + bias), written to
-// `logits` and kept in shared memory, where warp 0 selects the top-k: one CTA
-// per token (one thread per expert), one launch instead of a reduction pass
-// and a selection pass.
+// `logits` and kept in shared memory, then the top-k: one CTA per token (one
+// thread per expert), one launch instead of a reduction pass and a selection
+// pass.  When every expert has its own thread and k is at most the number of
+// warps, the block narrows the choice first, as select_topk does within a
+// warp: the k-th largest of the warps' maxima is a lower bound of the k-th
+// largest logit (k warps hold a value at least that large), so the k best are
+// among the values not below it; each thread holding such a value appends it
+// to a shared candidate list (in any order: the selection orders by value,
+// then expert id), and with at most 64 candidates warp 0 runs the rounds over
+// two values per lane.  Otherwise warp 0 runs the rounds over all values.
+// Either way the selection is the same.
 template <int NV, int NTHREADS>
 __global__ void __launch_bounds__(NTHREADS) k_reduce_topk(const float *__restrict__ part, int KS, int T, int E,
                                                      const float *__restrict__ bias, float *__restrict__ logits, int k,
@@ -86,7 +94,12 @@ __global__ void __launch_bounds__(NTHREADS) k_reduce_topk(const float *__restric
 {
     pdl_enter();
     extern __shared__ float row[];  // [E]
+    __shared__ uint32_t wmax[32];   // per warp: the order key of its largest value
+    __shared__ float2 cand[64];     // candidates: (value, expert id)
+    __shared__ int ncand;
+    __shared__ uint32_t s_bound;
     const int t = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t TM = int64_t(T) * E, base = int64_t(t) * E;
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
         float acc = 0.f;
@@ -96,7 +109,49 @@ __global__ void __launch_bounds__(NTHREADS) k_reduce_topk(const float *__restric
         row[e] = v;
         logits[base + e] = v;
     }
-    __syncthreads();
+    const int nw = (E + 31) / 32;
+    if (E <= int(blockDim.x) && k <= nw) {
+        // thread e holds expert e (absent experts: key 0, below every value's key)
+        const int e = threadIdx.x;
+        const float v = e < E ? row[e] : -INFINITY;
+        const uint32_t key = e < E ? order_key(v) : 0u;
+        uint32_t m;
+        asm volatile("redux.sync.max.u32 %0, %1, 0xffffffff;" : "=r"(m) : "r"(key));
+        if (lane == 0) wmax[warp] = m;
+        if (threadIdx.x == 0) ncand = 0;
+        __syncthreads();
+        if (warp == 0) {
+            // the k-th largest warp maximum (ranks by key desc, warp asc: distinct)
+            const uint32_t mk = lane < nw ? wmax[lane] : 0u;
+            int rank = 0;
+#pragma unroll
+            for (int o = 0; o < 32; ++o) {
+                const uint32_t ok = __shfl_sync(0xFFFFFFFFu, mk, o);
+                rank += (ok > mk || (ok == mk && o < lane)) ? 1 : 0;
+            }
+            const unsigned who = __ballot_sync(0xFFFFFFFFu, lane < nw && rank == k - 1);
+            if (lane == 0) s_bound = wmax[__ffs(int(who)) - 1];  // exactly one warp has rank k - 1
+        }
+        __syncthreads();
+        if (e < E && key >= s_bound) {
+            const int pos = atomicAdd(&ncand, 1);
+            if (pos < 64) cand[pos] = make_float2(v, __int_as_float(e));
+        }
+        __syncthreads();
+        const int nc = ncand;
+        if (nc <= 64) {
+            if (warp == 0) {
+                const float2 c0 = lane < nc ? cand[lane] : make_float2(-INFINITY, __int_as_float(0x7FFFFFFF));
+                const float2 c1 = lane + 32 < nc ? cand[lane + 32] : make_float2(-INFINITY, __int_as_float(0x7FFFFFFF));
+                RoundOut out;
+                topk_rounds_two(c0.x, __float_as_int(c0.y), c1.x, __float_as_int(c1.y), k, out);
+                softmax_store(out, k, idx + int64_t(t) * k, w + int64_t(t) * k);
+            }
+            return;
+        }
+    } else {
+        __syncthreads();
+    }
     if (threadIdx.x < 32) select_topk<NV, false>(row, E, k, idx + int64_t(t) * k, w + int64_t(t) * k, nullptr);
 }
 
