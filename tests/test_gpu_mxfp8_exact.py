@@ -102,3 +102,43 @@ def test_forward_mxfp8_operands_bit_exact(cuda_lib, T, tile):
                                                  f"{P} differ from the oracle's MXFP8 of the same fp32 values")
     print(f"T={T}: {P} pairs, x {P * d} codes + {P * d // 32} scales, h {P * I} codes + {P * I // 32} scales "
           f"bit-exact")
+
+
+@pytest.mark.parametrize("T,skew", [(1, False), (64, False), (64, True)])
+def test_forward_permute_matches_oracle(cuda_lib, T, skew):
+    """The forward's permute of a small batch (done inside the routing kernel
+    from per-expert token masks): every pair's code row is the oracle's
+    stable counting-sort position, and its scale-atom row follows from the
+    oracle's counts, offsets and the token tile.  Skewed routing puts more
+    than one token tile's worth of pairs on some experts."""
+    lmoe = cuda_lib
+    kw = dict(zipf_s=1.2, zipf_beta=0.5) if skew else {}  # skewed: up to 50 pairs on one expert
+    wl = gen.custom(f"perm_small_{T}_{int(skew)}", T=T, d=3584, I=512, **kw)
+    d, I, k, E = wl.d, wl.I, wl.k, wl.E
+    bank = _get_bank(wl)
+    bias = gen.router_bias(wl)
+    layer = lmoe.Layer(torch.from_numpy(gen.router_f32(wl)).to(DEV), bank, k=k,
+                       bias=None if bias is None else torch.from_numpy(bias).to(DEV))
+    v = lmoe.forward_workspace_views(T, d, E, k, I)
+    x = gen.x_bf16(wl)
+    idx = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    y1 = layer.forward(to_dev_bf16(x, DEV), topk_idx=idx).clone()
+    torch.cuda.synchronize()
+    assert layer.device_status() == 0
+    ih = idx.cpu().numpy()
+    counts, offsets, perm, inv = oracle.permute(ih, E)
+    P, NT = T * k, v.tile_tokens
+    ws = layer._ws
+    Q = ws[v.code_row:v.code_row + 4 * P].view(torch.int32).cpu().numpy()
+    R = ws[v.dst_row:v.dst_row + 4 * P].view(torch.int32).cpu().numpy()
+    np.testing.assert_array_equal(Q, inv)
+    tiles = (counts.astype(np.int64) + NT - 1) // NT
+    pad = np.concatenate([[0], np.cumsum(tiles)[:-1]]) * NT  # first atom row of each expert's tiles
+    e = ih.reshape(-1)
+    np.testing.assert_array_equal(R, pad[e] + (inv - offsets[e]))
+    if skew:
+        assert counts.max() > NT, "the skewed case should put several token tiles on one expert"
+    # a second call (the masks and the counter are cleared per call) gives the same layer output
+    y2 = layer.forward(to_dev_bf16(x, DEV), topk_idx=idx)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2)

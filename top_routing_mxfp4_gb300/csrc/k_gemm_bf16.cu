@@ -347,7 +347,8 @@ cudaError_t launch_split_router(const float *Wr, int E, int d, uint16_t *Wr3, cu
 }
 
 cudaError_t launch_route(const uint16_t *x, const uint16_t *Wr3, const float *bias, int T, int d, int E, int k,
-                         float *logits, int32_t *idx, float *w, void *scratch, int32_t *status, cudaStream_t st)
+                         float *logits, int32_t *idx, float *w, void *scratch, int32_t *status, cudaStream_t st,
+                         const PermByMask &pm)
 {
     if (T == 0) return cudaSuccess;
     const __nv_bfloat16 *w3 = reinterpret_cast<const __nv_bfloat16 *>(Wr3);
@@ -361,6 +362,7 @@ cudaError_t launch_route(const uint16_t *x, const uint16_t *Wr3, const float *bi
         return cudaErrorInvalidValue;
     DenseArgs a{E, T, d, int(ceil_div(E, 128)), int(ceil_div(T, NB)), KS, d / 64 / KS, bias, logits, status};
     if (KS == 1) {
+        if (pm.mask) return cudaErrorInvalidValue;  // the permute rides on the split-K top-k kernel only
         e = dispatch<3, OUT_F32>(NB, ma, mb, a, st);
         if (e != cudaSuccess) return e;
         return launch_topk_softmax(logits, T, E, k, idx, w, st, status);
@@ -369,7 +371,14 @@ cudaError_t launch_route(const uint16_t *x, const uint16_t *Wr3, const float *bi
     a.bias = nullptr;
     e = dispatch<3, OUT_PARTIAL>(NB, ma, mb, a, st);
     if (e != cudaSuccess) return e;
-    return launch_reduce_topk(partial, KS, T, E, bias, logits, k, idx, w, st);
+    return launch_reduce_topk(partial, KS, T, E, bias, logits, k, idx, w, st, pm);
+}
+
+bool route_can_permute(int T, int d, int E, int k)
+{
+    int NB, KS;
+    plan(T, E, d, NB, KS);
+    return KS > 1 && T >= 1 && T <= 64 && E <= 896 && k <= 32;
 }
 
 size_t linear_scratch_bytes(int T, int K, int N)

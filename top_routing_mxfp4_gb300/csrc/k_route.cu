@@ -7,6 +7,7 @@
 
 #include "lmoe_internal.cuh"
 #include "tc_ptx.cuh"
+#include "schedule.cuh"
 #include "topk_select.cuh"
 
 namespace lmoe {
@@ -87,10 +88,38 @@ __global__ void __launch_bounds__(256) k_topk_softmax_staged(const float *__rest
 // then expert id), and with at most 64 candidates warp 0 runs the rounds over
 // two values per lane.  Otherwise warp 0 runs the rounds over all values.
 // Either way the selection is the same.
+// The permute of a small batch from the token masks (PermByMask), by the
+// last CTA of k_reduce_topk: NTHREADS threads, E <= 1024, T <= 64.
+template <int NTHREADS>
+__device__ void permute_from_masks(const PermByMask &pm, int T, int E, int k, const int32_t *idx)
+{
+    __shared__ unsigned long long msk[1024];
+    __shared__ int32_t cnt[1024], tmp[1024], scan[1025], off_s[1025], wt[32];
+    for (int e = threadIdx.x; e < E; e += NTHREADS) {
+        const unsigned long long m = __ldcg(pm.mask + e);
+        msk[e] = m;
+        cnt[e] = __popcll(m);
+        pm.counts[e] = cnt[e];
+    }
+    __syncthreads();
+    block_scan<NTHREADS>(cnt, E, off_s, wt);
+    for (int e = threadIdx.x; e <= E; e += NTHREADS) pm.offsets[e] = off_s[e];
+    ffn_schedule_from_counts<NTHREADS>(cnt, E, pm.sc, tmp, scan, wt);
+    // pair p = t*k + j of expert e: position offsets[e] + (tokens below t
+    // that chose e), its atom row in the expert's token tiles
+    for (int p = threadIdx.x; p < T * k; p += NTHREADS) {
+        const int t = p / k, e = __ldcg(idx + p);
+        const int32_t pos = off_s[e] + __popcll(msk[e] & ((1ull << t) - 1ull));
+        pm.inv[p] = pos;
+        pm.perm[pos] = p;
+        pm.sc.dst_row[p] = padded_row(pos, off_s[e], scan[e] * pm.sc.SLOT, pm.sc.NT, pm.sc.SLOT);
+    }
+}
+
 template <int NV, int NTHREADS>
 __global__ void __launch_bounds__(NTHREADS) k_reduce_topk(const float *__restrict__ part, int KS, int T, int E,
                                                      const float *__restrict__ bias, float *__restrict__ logits, int k,
-                                                     int32_t *__restrict__ idx, float *__restrict__ w)
+                                                     int32_t *__restrict__ idx, float *__restrict__ w, PermByMask pm)
 {
     pdl_enter();
     extern __shared__ float row[];  // [E]
@@ -110,6 +139,7 @@ __global__ void __launch_bounds__(NTHREADS) k_reduce_topk(const float *__restric
         logits[base + e] = v;
     }
     const int nw = (E + 31) / 32;
+    bool selected = false;  // by the block's candidate narrowing
     if (E <= int(blockDim.x) && k <= nw) {
         // thread e holds expert e (absent experts: key 0, below every value's key)
         const int e = threadIdx.x;
@@ -147,30 +177,46 @@ __global__ void __launch_bounds__(NTHREADS) k_reduce_topk(const float *__restric
                 topk_rounds_two(c0.x, __float_as_int(c0.y), c1.x, __float_as_int(c1.y), k, out);
                 softmax_store(out, k, idx + int64_t(t) * k, w + int64_t(t) * k);
             }
-            return;
+            selected = true;
         }
     } else {
         __syncthreads();
     }
-    if (threadIdx.x < 32) select_topk<NV, false>(row, E, k, idx + int64_t(t) * k, w + int64_t(t) * k, nullptr);
+    if (!selected && threadIdx.x < 32) select_topk<NV, false>(row, E, k, idx + int64_t(t) * k, w + int64_t(t) * k, nullptr);
+    if (!pm.mask) return;
+    // this token's bit in its experts' masks; the last CTA to count itself in
+    // does the permute
+    if (threadIdx.x < 32) {
+        __syncwarp();
+        if (threadIdx.x < k) atomicOr(pm.mask + idx[int64_t(t) * k + threadIdx.x], 1ull << t);
+    }
+    __shared__ int s_last;
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = atomicAdd(pm.counter, 1) == int(gridDim.x) - 1;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    permute_from_masks<NTHREADS>(pm, T, E, k, idx);
 }
 
 }  // namespace
 
 cudaError_t launch_reduce_topk(const float *part, int KS, int T, int E, const float *bias, float *logits, int k,
-                               int32_t *idx, float *w, cudaStream_t st)
+                               int32_t *idx, float *w, cudaStream_t st, const PermByMask &pm)
 {
     if (T == 0) return cudaSuccess;
     const size_t smem = size_t(E) * sizeof(float);  // E <= 2048: within the default 48 KB
     // one thread per expert (KS loads each) up to 896 experts; beyond, 256
     // threads, so that the selecting warp may keep its 64 values per lane in
     // registers (a 1024-thread block allows 64 registers a thread)
-    const dim3 block(unsigned(E <= 896 ? round_up(E, 32) : 256));
+    const dim3 block(unsigned(E <= 896 ? (pm.mask ? 1024 : round_up(E, 32)) : 256));
+    if (pm.mask && (E > 896 || T > 64)) return cudaErrorInvalidValue;  // the block's permute: 1024 threads, 64 tokens
     if (E <= 256)
-        return launch_pdl(k_reduce_topk<8, 1024>, dim3(T), block, smem, st, part, KS, T, E, bias, logits, k, idx, w);
+        return launch_pdl(k_reduce_topk<8, 1024>, dim3(T), block, smem, st, part, KS, T, E, bias, logits, k, idx, w, pm);
     if (E <= 896)
-        return launch_pdl(k_reduce_topk<28, 1024>, dim3(T), block, smem, st, part, KS, T, E, bias, logits, k, idx, w);
-    return launch_pdl(k_reduce_topk<64, 256>, dim3(T), block, smem, st, part, KS, T, E, bias, logits, k, idx, w);
+        return launch_pdl(k_reduce_topk<28, 1024>, dim3(T), block, smem, st, part, KS, T, E, bias, logits, k, idx, w, pm);
+    return launch_pdl(k_reduce_topk<64, 256>, dim3(T), block, smem, st, part, KS, T, E, bias, logits, k, idx, w, pm);
 }
 
 cudaError_t launch_topk_softmax(const float *logits, int T, int E, int k, int32_t *idx, float *w, cudaStream_t st,

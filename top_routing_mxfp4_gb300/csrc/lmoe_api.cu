@@ -22,6 +22,14 @@ int64_t g_wait_limit = 0;
 // batches of at most this many pairs (T * k) take the small-batch path
 int32_t g_small_pairs = LMOE_SMALL_BATCH_PAIRS_DEFAULT;
 
+// Batches of at most 64 tokens on the tensor-core path: the routing kernel
+// also does the permute (PermByMask: token masks per expert, the status
+// region's third int32 its CTA counter), so no permute kernel runs.
+bool permute_in_route(int T, int d, int E, int k, const FfnLayout &FL)
+{
+    return route_can_permute(T, d, E, k) && ffn_fused(FL) && FL.SLOT == FL.NT;
+}
+
 bool small_path(const lmoe_dims *d)
 {
     return d->T > 0 && small_path_fits(d->T, d->d, d->E, d->k, d->I, g_small_pairs);
@@ -64,13 +72,13 @@ bool weights_ok(const lmoe_expert_weights *W)
 }
 
 // Workspace layout of lmoe_forward (each region 256-byte aligned):
-//   status | logits | idx | w | counts | offsets | perm | inv | permute scratch
+//   status | token masks | logits | idx | w | counts | offsets | perm | inv | permute scratch
 //   | ffn scratch (MXFP8 activations and h in permuted order, their scale atoms per token tile, schedule)
 //   | yp (per-pair outputs [T*k][d]) or, with the fused combine, yacc ([T][d] fp32 sums)
 // The small-batch path (lmoe_set_small_batch_pairs) uses
 //   status (+ the routing kernel's counter) | logits | idx | w | small-path scratch.
 struct FwdLayout {
-    size_t status, logits, idx, w, counts, offsets, perm, inv, rscratch, pscratch, fscratch, yp, total;
+    size_t status, tmask, logits, idx, w, counts, offsets, perm, inv, rscratch, pscratch, fscratch, yp, total;
     bool small;
     size_t sscratch;
 };
@@ -86,6 +94,7 @@ FwdLayout fwd_layout(const lmoe_dims *d)
         return o;
     };
     L.status = take(kStatusBytes);
+    L.tmask = take(size_t(E * 8));  // small batches: the routing kernel's token masks (see permute_in_route)
     L.logits = take(size_t(T * E * 4));
     L.idx = take(size_t(P * 4));
     L.w = take(size_t(P * 4));
@@ -349,11 +358,23 @@ lmoe_status lmoe_forward(const uint16_t *x_bf16, const uint16_t *Wr3, const floa
     // which one pass then rounds to bf16.
     float *yacc = FL.fused ? yp : nullptr;
 
+    const bool pr = permute_in_route(T, d, E, k, FL);
+    PermByMask pm;
+    if (pr) {
+        pm.mask = reinterpret_cast<unsigned long long *>(ws + L.tmask);
+        pm.counter = status + 2;
+        pm.counts = counts;
+        pm.offsets = offsets;
+        pm.perm = perm;
+        pm.inv = inv;
+        pm.sc = ffn_sched(FL, d, dims->I, fs);
+    }
     cudaError_t e = mark(0, st);
-    if (e == cudaSuccess) e = cudaMemsetAsync(status, 0, sizeof(int32_t), st);
-    if (e == cudaSuccess) e = launch_route(x_bf16, Wr3, bias, T, d, E, k, lg, idx, w, ws + L.rscratch, status, st);
+    // the status word (and, with the permute in the routing kernel, its counter and the token masks) start at zero
+    if (e == cudaSuccess) e = cudaMemsetAsync(status, 0, pr ? L.tmask - L.status + size_t(E) * 8 : sizeof(int32_t), st);
+    if (e == cudaSuccess) e = launch_route(x_bf16, Wr3, bias, T, d, E, k, lg, idx, w, ws + L.rscratch, status, st, pm);
     if (e == cudaSuccess) e = mark(1, st);
-    if (e == cudaSuccess)
+    if (e == cudaSuccess && !pr)
         e = launch_permute(idx, P, E, counts, offsets, perm, inv, ws + L.pscratch, status, st,
                            ffn_sched(FL, d, dims->I, fs));
     if (e == cudaSuccess) e = mark(2, st);
@@ -425,8 +446,10 @@ int32_t lmoe_forward_kernel_count(const lmoe_dims *dims)
     if (small_path(dims)) return 3;  // route, gate/up, down
     // router (split, GEMM, (reduction), top-k), permute (with the GEMM schedule), scatter, the two
     // expert GEMMs (one fused kernel for small token tiles), combine
-    const int gemms = ffn_fused(ffn_layout(P, dims->d, dims->E, dims->I)) ? 1 : 2;
-    return router_kernel_count(dims->T, dims->d, dims->E) + permute_kernel_count(P) + 1 + gemms + 1;
+    const FfnLayout FL = ffn_layout(P, dims->d, dims->E, dims->I);
+    const int gemms = ffn_fused(FL) ? 1 : 2;
+    const int perms = permute_in_route(dims->T, dims->d, dims->E, dims->k, FL) ? 0 : permute_kernel_count(P);
+    return router_kernel_count(dims->T, dims->d, dims->E) + perms + 1 + gemms + 1;
 }
 
 lmoe_status lmoe_set_stage_events(void *const *events, int32_t n)

@@ -158,14 +158,6 @@ cudaError_t launch_linear_bf16(const uint16_t *x, const uint16_t *W, int T, int 
 // bounded waits report there); null selects the unstaged kernel.
 cudaError_t launch_topk_softmax(const float *logits, int T, int E, int k, int32_t *idx, float *w, cudaStream_t st,
                                 int32_t *status = nullptr);
-// split-K partial logits [KS][T][E] -> logits (+ bias) and their top-k + softmax, one launch
-cudaError_t launch_reduce_topk(const float *part, int KS, int T, int E, const float *bias, float *logits, int k,
-                               int32_t *idx, float *w, cudaStream_t st);
-// Router logits + top-k + softmax (split, GEMM, split-K reduction, selection).
-// fp32 router weights [E][d] -> three bf16 planes [3][E][d] whose sum is exact
-cudaError_t launch_split_router(const float *Wr, int E, int d, uint16_t *Wr3, cudaStream_t st);
-cudaError_t launch_route(const uint16_t *x, const uint16_t *Wr3, const float *bias, int T, int d, int E, int k,
-                         float *logits, int32_t *idx, float *w, void *scratch, int32_t *status, cudaStream_t st);
 
 // Optional by-products of the permute for the expert GEMMs: per expert the
 // first atom row of its token tiles (pad_off = first tile * NT, E+1) and the
@@ -230,6 +222,30 @@ __device__ __forceinline__ void fill_item_entries(const FfnSched &sc, int n_gu, 
         *dst = make_int2(ti.x | (m << 16), ti.y);
     }
 }
+// Small batches (T <= 64): the permute done by the routing kernel.  Each
+// token's CTA sets bit t of mask[e] for its selected experts; the last CTA to
+// finish derives counts, offsets, the FFN schedule and, per pair p = t*k + j
+// with expert e, its sorted position offsets[e] + popcount(mask[e] & (2^t - 1))
+// (the stable counting sort's order: within an expert, pairs by token) into
+// inv[p], perm[pos] and the pair's atom row.  mask and counter are zero when
+// the call starts.  mask == null: not used.
+struct PermByMask {
+    unsigned long long *mask = nullptr;  // [E]
+    int32_t *counter = nullptr;          // CTAs done
+    int32_t *counts = nullptr, *offsets = nullptr, *perm = nullptr, *inv = nullptr;
+    FfnSched sc;
+};
+// split-K partial logits [KS][T][E] -> logits (+ bias) and their top-k + softmax, one launch
+cudaError_t launch_reduce_topk(const float *part, int KS, int T, int E, const float *bias, float *logits, int k,
+                               int32_t *idx, float *w, cudaStream_t st, const PermByMask &pm = PermByMask());
+// Router logits + top-k + softmax (split, GEMM, split-K reduction, selection).
+// fp32 router weights [E][d] -> three bf16 planes [3][E][d] whose sum is exact
+cudaError_t launch_split_router(const float *Wr, int E, int d, uint16_t *Wr3, cudaStream_t st);
+cudaError_t launch_route(const uint16_t *x, const uint16_t *Wr3, const float *bias, int T, int d, int E, int k,
+                         float *logits, int32_t *idx, float *w, void *scratch, int32_t *status, cudaStream_t st,
+                         const PermByMask &pm = PermByMask());
+// whether launch_route can also do the permute (PermByMask) for these dims
+bool route_can_permute(int T, int d, int E, int k);
 // pairs per block of the multi-block permute (its scratch: one histogram of
 // E counts per block)
 constexpr int PERMUTE_CHUNK = 2048;
