@@ -243,7 +243,7 @@ size_t lmoe_workspace_size(const lmoe_dims *dims);
  * summed in a fixed order (deterministic), but not strictly slot by slot.  It
  * is also the path of the MXFP4-activation variant (LMOE_ACT_MXFP4).  The
  * default is 0: every batch takes the tensor-core path, which with its fused
- * expert kernel measures faster at batch 1 too (54.2 against 58.9 us per
+ * expert kernel measures faster at batch 1 too (51.8 against 58.9 us per
  * step, L2 flushed).  Process-wide setting, not thread-safe; the workspace
  * size of a batch depends on it.  lmoe_small_batch_pairs() reads it. */
 #define LMOE_SMALL_BATCH_PAIRS_DEFAULT 0
@@ -251,8 +251,9 @@ lmoe_status lmoe_set_small_batch_pairs(int32_t max_pairs);
 int32_t lmoe_small_batch_pairs(void);
 
 /* route -> permute -> MXFP8 activations -> expert FFN -> combine, all on
- * `stream`.  Wr3: prepared router weights (lmoe_prepare_router).  y bf16
- * [T][d].  Optional outputs (NULL to skip): topk_idx [T][k], topk_w [T][k],
+ * `stream` (up to 64 tokens the routing kernel does the permute as well).
+ * Wr3: prepared router weights (lmoe_prepare_router).  y bf16 [T][d].
+ * Optional outputs (NULL to skip): topk_idx [T][k], topk_w [T][k],
  * logits [T][E]. */
 lmoe_status lmoe_forward(const uint16_t *x_bf16, const uint16_t *Wr3, const float *bias, const lmoe_expert_weights *W,
                          const lmoe_dims *dims, uint16_t *y_bf16, int32_t *topk_idx, float *topk_w, float *logits,
