@@ -89,30 +89,54 @@ __global__ void __launch_bounds__(256) k_topk_softmax_staged(const float *__rest
 // two values per lane.  Otherwise warp 0 runs the rounds over all values.
 // Either way the selection is the same.
 // The permute of a small batch from the token masks (PermByMask), by the
-// last CTA of k_reduce_topk: NTHREADS threads, E <= 1024, T <= 64.
+// last CTA of k_reduce_topk: NTHREADS threads, E <= 1024, T <= 64.  The
+// pairs' expert ids are requested first; counts and token tiles per expert
+// go through one scan as (count | tiles << 16) (both totals stay below 2^16:
+// at most 64 * 32 pairs and as many tiles).
 template <int NTHREADS>
 __device__ void permute_from_masks(const PermByMask &pm, int T, int E, int k, const int32_t *idx)
 {
+    constexpr int PPT = (64 * 32 + NTHREADS - 1) / NTHREADS;  // pairs per thread: T * k <= 64 * 32
     __shared__ unsigned long long msk[1024];
-    __shared__ int32_t cnt[1024], tmp[1024], scan[1025], off_s[1025], wt[32];
+    __shared__ int32_t pk[1024], scan[1025], tile0[1025], wt[32];
+    const int P = T * k;
+    int ep[PPT];
+#pragma unroll
+    for (int i = 0; i < PPT; ++i) {
+        const int p = threadIdx.x + i * NTHREADS;
+        ep[i] = p < P ? __ldcg(idx + p) : 0;
+    }
     for (int e = threadIdx.x; e < E; e += NTHREADS) {
         const unsigned long long m = __ldcg(pm.mask + e);
+        const int32_t c = __popcll(m);
         msk[e] = m;
-        cnt[e] = __popcll(m);
-        pm.counts[e] = cnt[e];
+        pk[e] = c | (((c + pm.sc.NT - 1) / pm.sc.NT) << 16);
+        pm.counts[e] = c;
     }
     __syncthreads();
-    block_scan<NTHREADS>(cnt, E, off_s, wt);
-    for (int e = threadIdx.x; e <= E; e += NTHREADS) pm.offsets[e] = off_s[e];
-    ffn_schedule_from_counts<NTHREADS>(cnt, E, pm.sc, tmp, scan, wt);
+    block_scan<NTHREADS>(pk, E, scan, wt);
+    for (int e = threadIdx.x; e <= E; e += NTHREADS) {
+        const int32_t off = scan[e] & 0xFFFF, tp = scan[e] >> 16;
+        scan[e] = off;
+        tile0[e] = tp;
+        pm.offsets[e] = off;
+        pm.sc.pad_off[e] = tp * pm.sc.SLOT;
+        pm.sc.tiles_gu[e] = tp * pm.sc.MT_gu;
+        pm.sc.tiles_dn[e] = tp * pm.sc.MT_dn;
+    }
+    __syncthreads();
+    fill_tile_info(tile0, E, pm.sc, NTHREADS);
     // pair p = t*k + j of expert e: position offsets[e] + (tokens below t
     // that chose e), its atom row in the expert's token tiles
-    for (int p = threadIdx.x; p < T * k; p += NTHREADS) {
-        const int t = p / k, e = __ldcg(idx + p);
-        const int32_t pos = off_s[e] + __popcll(msk[e] & ((1ull << t) - 1ull));
+#pragma unroll
+    for (int i = 0; i < PPT; ++i) {
+        const int p = threadIdx.x + i * NTHREADS;
+        if (p >= P) break;
+        const int t = p / k, e = ep[i];
+        const int32_t pos = scan[e] + __popcll(msk[e] & ((1ull << t) - 1ull));
         pm.inv[p] = pos;
         pm.perm[pos] = p;
-        pm.sc.dst_row[p] = padded_row(pos, off_s[e], scan[e] * pm.sc.SLOT, pm.sc.NT, pm.sc.SLOT);
+        pm.sc.dst_row[p] = padded_row(pos, scan[e], tile0[e] * pm.sc.SLOT, pm.sc.NT, pm.sc.SLOT);
     }
 }
 
