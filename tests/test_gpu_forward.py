@@ -115,6 +115,17 @@ def test_forward_ragged_shapes(cuda_lib):
     _check(wl, x, y, idx, w, lg, list(range(0, 45, 4)))
 
 
+@pytest.mark.parametrize("T,E,k", [(64, 256, 32), (64, 896, 1), (17, 130, 9)])
+def test_forward_small_batch_routing_edges(cuda_lib, T, E, k):
+    """Batches the routing kernel permutes itself (up to 64 tokens): every
+    token's bit of the 64-bit masks in use (T = 64), the largest k (more
+    selections than warps: the selection's fall-back rounds), k = 1, and an
+    expert count that is not a multiple of 32."""
+    wl = gen.custom(f"route_edge_{T}_{E}_{k}", T=T, d=512, I=64, E=E, k=k)
+    x, y, idx, w, lg = _run_forward(cuda_lib, wl)
+    _check(wl, x, y, idx, w, lg, sorted(set([0, 1, T // 2, T - 1])))
+
+
 def _token_tile(wl):
     """Token tile the library picks for a batch (by the mean pairs per expert)."""
     return 16 if wl.P <= 4 * wl.E else 32 if wl.P <= 16 * wl.E else 96
