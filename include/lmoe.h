@@ -323,6 +323,15 @@ lmoe_status lmoe_set_stage_events(void *const *events, int32_t n);
  *       tile),
  *   dst_row   int32 [T*k]: the atom row of pair p = t*k + j,
  *   code_row  int32 [T*k]: the code row of pair p (the permute's inverse map);
+ *   ksplit    int32 [128][4] or -1: at 16-token tiles, when the batch can
+ *       have at most half as many gate/up work items as the GPU has SMs
+ *       (items <= (T*k + m*15)/16 token tiles x roundup(I,128)/128 weight
+ *       tiles, m = min(T*k, E); at most 128 items; d >= 256), each item runs
+ *       as two K halves on two SMs and the later half forms h from the sum
+ *       of both; entry [i][q] counts the halves of item i (items in
+ *       token-tile order, weight tile fastest) that its epilogue warp q
+ *       (rows 32q .. 32q+31 of the item's 128) stored: 2 for a split item
+ *       whose warp holds rows of I, 0 otherwise (-1: no such layout);
  * rows = code rows reserved (T*k plus one tile), tile_tokens = tokens per
  * expert-GEMM tile, slot_rows = atom rows a tile occupies (tile_tokens).
  * Valid after an lmoe_forward call with the same dims has completed; rows no
@@ -336,6 +345,7 @@ typedef struct {
                      LMOE_ACT_MXFP4 a code row holds packed e2m1 codes (d/2 or I/2 bytes, element 2i in
                      the low nibble of byte i) */
     int64_t code_row;
+    int64_t ksplit;
 } lmoe_ffn_views;
 lmoe_status lmoe_forward_workspace_views(const lmoe_dims *dims, lmoe_ffn_views *views);
 

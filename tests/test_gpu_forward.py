@@ -126,6 +126,45 @@ def test_forward_small_batch_routing_edges(cuda_lib, T, E, k):
     _check(wl, x, y, idx, w, lg, sorted(set([0, 1, T // 2, T - 1])))
 
 
+@pytest.mark.parametrize("d,I,k", [(3584, 512, 19), (3584, 512, 20), (1408, 160, 16), (256, 512, 16),
+                                   (128, 512, 16)])
+def test_forward_split_k_gateup(cuda_lib, d, I, k):
+    """Batch 1 with at most half as many gate/up work items as SMs: each item
+    runs as two K halves on two SMs and the later half forms h from the sum
+    of both halves' fp32 accumulators.  Cases: 19 experts x 4 weight tiles =
+    76 items (the most that split on 152 SMs) and 80 (the first that do
+    not), 11 K chunks (halves of 5 and 6) with I = 160 (three of the second
+    weight tile's four epilogue warps hold no rows of I), one K chunk per
+    half (d = 256), and one K chunk in all (d = 128: no split).  The
+    arrival counters show which items split; the output is checked against
+    the oracle and repeated bit for bit."""
+    lmoe = cuda_lib
+    wl = gen.custom(f"ksplit_{d}_{I}_{k}", T=1, d=d, I=I, E=64, k=k)
+    layer = lmoe.Layer(torch.from_numpy(gen.router_f32(wl)).to(DEV), _bank(wl), k=k)
+    v = lmoe.forward_workspace_views(1, d, wl.E, k, I)
+    assert v.path == 0 and v.tile_tokens == 16 and v.ksplit >= 0
+    x = gen.x_bf16(wl)
+    idx = torch.empty((1, k), dtype=torch.int32, device=DEV)
+    w = torch.empty((1, k), dtype=torch.float32, device=DEV)
+    logits = torch.empty((1, wl.E), dtype=torch.float32, device=DEV)
+    ys = []
+    for _ in range(2):
+        y = layer.forward(to_dev_bf16(x, DEV), topk_idx=idx, topk_w=w, logits=logits)
+        torch.cuda.synchronize()
+        assert layer.device_status() == 0
+        ys.append(from_dev_bf16(y))
+    assert np.array_equal(ys[0], ys[1])
+    MT = -(-I // 128)
+    n_items = k * MT  # one token tile per selected expert
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    split = 2 * n_items <= sms and n_items <= 128 and d // 128 >= 2
+    cnt = layer._ws[v.ksplit:v.ksplit + 128 * 16].view(torch.int32).view(128, 4)[:n_items].cpu().numpy()
+    m = np.arange(n_items)[:, None] % MT
+    has_rows = 128 * m + 32 * np.arange(4)[None, :] < I
+    np.testing.assert_array_equal(cnt, np.where(has_rows & split, 2, 0))
+    _check(wl, x, ys[0], idx.cpu().numpy(), w.cpu().numpy(), logits.cpu().numpy(), [0])
+
+
 def _token_tile(wl):
     """Token tile the library picks for a batch (by the mean pairs per expert)."""
     return 16 if wl.P <= 4 * wl.E else 32 if wl.P <= 16 * wl.E else 96

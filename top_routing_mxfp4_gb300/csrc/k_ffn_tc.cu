@@ -140,6 +140,10 @@ __device__ __forceinline__ void red_add_v4(float *dst, float4 v, uint64_t policy
 // down items instead of idling through the gate/up tail and a kernel boundary.
 enum { GATEUP = 0, DOWN = 1, FUSED = 2 };
 
+// fp32 accumulators of one split-K gate/up half: 4 epilogue warps x 2
+// matrices x 16 token columns x 32 rows
+constexpr size_t kKsplitHalfBytes = size_t(4) * 2 * 16 * 32 * 4;
+
 struct GemmArgs {
     const uint8_t *sfa0, *sfa1;  // weight scale atoms [E][RTa][KC][512]
     const uint8_t *sfb;          // activation scale atoms [rows/128][KC][512]
@@ -161,6 +165,11 @@ struct GemmArgs {
     long long wait_limit;  // SM clocks a bounded wait may take before it gives up
     int stall_first_fill;  // failure-path test only: producer 0 withholds each CTA's first stage
     int32_t *tile_done;    // fused kernel: per token tile, epilogue warps done storing h (zeroed by the schedule)
+    // fused kernel at 16-token tiles, gate/up items split in two K halves:
+    // each half's fp32 accumulators (kKsplitHalfBytes per item and half) and
+    // per item and epilogue warp the halves done (zeroed by the schedule); null: no split
+    float *kpart;
+    int32_t *kcnt;
     // gate/up kernel: a buffer its epilogue warps zero between items (the down
     // GEMM's fused-combine sums), n4 16-byte units; null: none
     float4 *zero;
@@ -217,6 +226,9 @@ struct Cfg {
     static constexpr int STG_STRIDE = 36;
     static constexpr uint32_t EPI_WARP_BYTES = !STAGED ? 0 : (MODE != GATEUP ? CW * STG_STRIDE * 4 : 16 * 32);
     static_assert(MODE != FUSED || MATS == 2, "the fused kernel needs the same stage layout for both GEMMs");
+    // gate/up items in two K halves (small batches): one 16-column chunk per epilogue warp
+    static constexpr bool KSPLIT = MODE == FUSED && NT == 16;
+    static_assert(!KSPLIT || (NW == 1 && !STAGED), "split-K epilogue layout");
     static constexpr uint32_t EPI_BYTES = EPI_WARPS * EPI_WARP_BYTES;
 };
 
@@ -242,7 +254,7 @@ __device__ __forceinline__ Item item_at(int2 v, const int32_t *s_off, int nt)
     return r;
 }
 
-template <int MODE, int NT>
+template <int MODE, int NT, bool SPLIT = false>
 __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
     k_moe_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmD,
@@ -273,16 +285,34 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
         s_pad[i] = __ldcg(p.pad_off + i);
         s_off[i] = __ldcg(p.offsets + i);
     }
-    // fused: gate/up items [0, n_gu), then down items [n_gu, total)
-    const int n_gu = MODE == FUSED ? __ldcg(p.tiles + p.E) : 0;
-    const int total = MODE == FUSED ? n_gu + __ldcg(q.tiles + q.E) : __ldcg(p.tiles + p.E);
     const int G = int(gridDim.x);
+    // Small batches, whose gate/up items fit in half the CTAs: each gate/up
+    // item runs as two K halves on two CTAs (items [0, n_gu_tab) the first
+    // halves, [n_gu_tab, 2 n_gu_tab) the second).  One SM streams an item's
+    // weights only as fast as its ring's bytes in flight allow, so two SMs
+    // per item halve that phase; each half stores its fp32 accumulators and
+    // the later of the two forms h from their sum.
+    const int n_gu_tab = MODE == FUSED ? __ldcg(p.tiles + p.E) : 0;
+    constexpr bool KSPLIT = SPLIT && C::KSPLIT;  // a separate instance: the other batches' code is unchanged
+    const int KS = (KSPLIT && p.kpart && p.kcnt && n_gu_tab > 0 && 2 * n_gu_tab <= G &&
+                    n_gu_tab <= KSPLIT_MAX_ITEMS && p.KC >= 2)
+                       ? 2
+                       : 1;
+    // fused: gate/up items [0, n_gu), then down items [n_gu, total)
+    const int n_gu = KS * n_gu_tab;
+    const int total = MODE == FUSED ? n_gu + __ldcg(q.tiles + q.E) : __ldcg(p.tiles + p.E);
     // this CTA's item-table entries at index i (clamped: entries past the end
     // are loaded but never used); the table may come from the previous kernel
     auto entry = [&](int i) {
         const int j = i < total ? i : total - 1;
         if (MODE == FUSED && j >= n_gu) return __ldcg(q.items + (j - n_gu));
-        return __ldcg(p.items + j);
+        return __ldcg(p.items + (KS == 2 && j >= n_gu_tab ? j - n_gu_tab : j));
+    };
+    // the K chunks [k0, k1) item it accumulates (of KCf)
+    auto krange = [&](int it, int KCf, int &k0, int &k1) {
+        const bool second = KS == 2 && it < n_gu && it >= n_gu_tab;
+        k0 = KS == 2 && it < n_gu ? (second ? KCf / 2 : 0) : 0;
+        k1 = KS == 2 && it < n_gu && !second ? KCf / 2 : KCf;
     };
     auto mode_of = [&](int i) { return MODE == FUSED ? (i < n_gu ? int(GATEUP) : int(DOWN)) : int(MODE); };
     // This CTA's items in order: ordinal i -> item index.  One GEMM: every
@@ -296,7 +326,7 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
     const int gu_c = MODE == FUSED ? (n_gu > c ? (n_gu - c + G - 1) / G : 0) : 0;
     const int n_dn = total - n_gu;
     const int r_gu = n_gu % G;
-    const int X = (MODE == FUSED && r_gu > 0) ? (p.KC + q.KC / 2) / q.KC : 0;
+    const int X = (MODE == FUSED && r_gu > 0 && KS == 1) ? (p.KC + q.KC / 2) / q.KC : 0;
     int dn_c = 0;  // this CTA's down items
     if (MODE == FUSED) {
         if (c >= r_gu)
@@ -379,7 +409,9 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
                 const CUtensorMap *tmBx = (MODE == FUSED && mode == DOWN) ? &tmH : &tmB;
                 const uint8_t *sfa = pr == 0 ? a.sfa0 : a.sfa1;
                 bool h_waited = !(MODE == FUSED && mode == DOWN);
-                for (int kc = 0; kc < a.KC; ++kc) {
+                int k0, k1;
+                krange(it, a.KC, k0, k1);
+                for (int kc = k0; kc < k1; ++kc) {
                     if (!mbar_wait(&empty[stage], phase ^ 1, p.wait_limit)) {
                         set_status(p.status, LMOE_ERR_TIMEOUT);
                         ok = false;
@@ -387,7 +419,7 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
                     }
                     if (pr == 0) LMOE_TRACE_EV(0, 0x10 | MODE, it, kc);  // producer: stage free
                     uint8_t *sb = stages + stage * C::STAGE_BYTES;
-                    if (pr == 0 && p.stall_first_fill && it == int(blockIdx.x) && kc == 0) {
+                    if (pr == 0 && p.stall_first_fill && it == int(blockIdx.x) && kc == k0) {
                         // failure-path test: this stage never fills, so every wait on it runs out
                     } else if (pr == 0) {
                         mbar_arrive_expect_tx(&full[stage], C::TX_BYTES0);
@@ -446,7 +478,8 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
                 const Item w = item_at(ent, s_off, NT);
                 ent = ent_next;
                 ent_next = entry(seq(i + 2));
-                const int KCi = (MODE == FUSED && mode_of(it) == DOWN) ? q.KC : p.KC;
+                int k0, k1;
+                krange(it, (MODE == FUSED && mode_of(it) == DOWN) ? q.KC : p.KC, k0, k1);
                 const uint32_t N = uint32_t((w.n_valid + 15) & ~15);
                 if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1, p.wait_limit)) {
                     set_status(p.status, LMOE_ERR_TIMEOUT);
@@ -456,7 +489,7 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
                 tc_fence_after();
                 if (iss == 0) LMOE_TRACE_EV(1, 0x20 | MODE, it, 0);  // mma: accumulator free
                 const uint32_t d = tmem + uint32_t(acc * C::ACC_COLS_ITEM + iss * NT);
-                for (int kc = 0; kc < KCi; ++kc) {
+                for (int kc = k0; kc < k1; ++kc) {
                     if (!mbar_wait(&full[stage], phase, p.wait_limit)) {
                         set_status(p.status, LMOE_ERR_TIMEOUT);
                         ok = false;
@@ -475,7 +508,7 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
                         mma_mxf8f6f4(d, ad + 2 * kk, bd + 2 * kk, idesc_mxf4_e4m3(N, uint32_t(kk)), sfa, sfb,
-                                     (kc > 0 || kk > 0) ? 1u : 0u);
+                                     (kc > k0 || kk > 0) ? 1u : 0u);
                     tc_commit(&empty[stage]);
                     if (iss == 0) LMOE_TRACE_EV(1, 0x80 | MODE, it, kc);  // mma: stage issued
                     if (++stage == S) {
@@ -544,6 +577,10 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
             tc_fence_after();
             if (threadIdx.x == 64) LMOE_TRACE_EV(2, 0x50 | MODE, it, 0);  // epilogue: accumulator ready
             const uint32_t tbase = tmem + (uint32_t(32 * lq) << 16) + uint32_t(acc * C::ACC_COLS_ITEM);
+            // split-K half: which half, and the gate/up item it belongs to
+            const int kh = (KS == 2 && mode == GATEUP && it >= n_gu_tab) ? 1 : 0;
+            const int kj = it - kh * n_gu_tab;
+            bool count_h = KS == 1 || kh == 1;  // this warp counts its part of h in (rows past I: the second half)
             if (mode == GATEUP && w.m_tile * 128 + 32 * lq < p.Mtot) {
                 const int row0 = w.m_tile * 128 + 32 * lq;  // first row of I held by this warp
                 const int blk = row0 / 32;                 // MX block of I held by this warp
@@ -554,6 +591,40 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
                     tmem_ld16(tbase + c0, v0);
                     tmem_ld16(tbase + NT + c0, v1);
                     tmem_ld_wait();
+                    if constexpr (KSPLIT) {
+                        if (KS == 2) {
+                            // store this half's sums, count in; the later half adds the other's
+                            constexpr int HW = 2 * 16 * 32;  // floats per warp and half
+                            float *mine = p.kpart + ((int64_t(kj) * 2 + kh) * 4 + lq) * HW;
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) {
+                                mine[j * 32 + lane] = __uint_as_float(v0[j]);
+                                mine[(16 + j) * 32 + lane] = __uint_as_float(v1[j]);
+                            }
+                            __threadfence();
+                            __syncwarp();
+                            int first = 0;
+                            if (lane == 0) first = atomicAdd(p.kcnt + kj * 4 + lq, 1) == 0;
+                            first = __shfl_sync(0xFFFFFFFFu, first, 0);
+                            count_h = !first;
+                            if (first) break;
+                            __threadfence();
+                            const float *other = p.kpart + ((int64_t(kj) * 2 + (1 - kh)) * 4 + lq) * HW;
+                            float o0[16], o1[16];
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) {
+                                o0[j] = __ldcg(other + j * 32 + lane);
+                                o1[j] = __ldcg(other + (16 + j) * 32 + lane);
+                            }
+                            // first half + second half, the same sum whichever finishes last
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) {
+                                const float a0 = __uint_as_float(v0[j]), a1 = __uint_as_float(v1[j]);
+                                v0[j] = __float_as_uint(kh ? o0[j] + a0 : a0 + o0[j]);
+                                v1[j] = __float_as_uint(kh ? o1[j] + a1 : a1 + o1[j]);
+                            }
+                        }
+                    }
                     // 16 independent columns: SiLU-gated product, block amax over
                     // the warp's 32 rows of I, E8M0 scale, e4m3 code
                     uint32_t sbv[16], code[16];
@@ -592,7 +663,7 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1)
                     }
                 }
             }
-            if (MODE == FUSED && mode == GATEUP) {
+            if (MODE == FUSED && mode == GATEUP && count_h) {
                 // this warp's part of h for the token tile is stored: count it
                 // in (release), for the down items that read the tile's h
                 __threadfence();
@@ -1019,7 +1090,7 @@ int num_sms()
 
 // Deepest pipeline that fits the per-block shared-memory limit (dynamic part
 // after the kernel's static shared memory) and the TMEM column budget.
-template <int MODE, int NT>
+template <int MODE, int NT, bool SPLIT>
 int gemm_stages(int E, size_t &smem)
 {
     using C = Cfg<MODE, NT>;
@@ -1027,7 +1098,7 @@ int gemm_stages(int E, size_t &smem)
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     cudaFuncAttributes fa{};
-    cudaFuncGetAttributes(&fa, k_moe_gemm<MODE, NT>);
+    cudaFuncGetAttributes(&fa, k_moe_gemm<MODE, NT, SPLIT>);
     const size_t fixed = 1024 + C::EPI_BYTES + (2 * 16 + 2 * C::ACC_STAGES + 2) * 8 + 16 + size_t(2) * (E + 1) * 4;
     const long avail = long(optin) - long(fa.sharedSizeBytes) - long(fixed);
     int st = int(avail / long(C::STAGE_BYTES));
@@ -1039,21 +1110,22 @@ int gemm_stages(int E, size_t &smem)
 // One GEMM (MODE GATEUP / DOWN: maps a0, a1, b and `args`), or both in the
 // fused kernel (a0, a1, b and `args` the gate/up GEMM; d, h and `args2` the
 // down GEMM).
-template <int MODE, int NT>
+template <int MODE, int NT, bool SPLIT = false>
 cudaError_t launch_gemm(const CUtensorMap &a0, const CUtensorMap &a1, const CUtensorMap &b, GemmArgs args,
                         cudaStream_t st, const CUtensorMap *d = nullptr, const CUtensorMap *h = nullptr,
                         const GemmArgs *args2 = nullptr)
 {
     size_t smem = 0;
-    args.stages = gemm_stages<MODE, NT>(args.E, smem);
+    args.stages = gemm_stages<MODE, NT, SPLIT>(args.E, smem);
     if (args.stages < 2) return cudaErrorInvalidConfiguration;
     if (MODE == FUSED && (!d || !h || !args2)) return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(k_moe_gemm<MODE, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    cudaError_t e =
+        cudaFuncSetAttribute(k_moe_gemm<MODE, NT, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
     GemmArgs q = args2 ? *args2 : args;
     q.stages = args.stages;
     {
-        const cudaError_t le_ = launch_pdl(k_moe_gemm<MODE, NT>, dim3(num_sms()), dim3(Cfg<MODE, NT>::THREADS), smem, st,
+        const cudaError_t le_ = launch_pdl(k_moe_gemm<MODE, NT, SPLIT>, dim3(num_sms()), dim3(Cfg<MODE, NT>::THREADS), smem, st,
                                            a0, a1, b, d ? *d : a0, h ? *h : b, args, q);
         if (le_ != cudaSuccess) return le_;
     }
@@ -1068,6 +1140,18 @@ constexpr int kDownBands = 2;
 
 // 128-row weight tiles per down-GEMM item (Cfg<DOWN, NT>::MATS).
 static int down_tiles_per_item(int NT) { return NT <= 96 ? 2 : 1; }
+
+// Whether a batch of P pairs over E experts can have at most half as many
+// gate/up work items (MT weight tiles per token tile) as the grid has CTAs,
+// so that the fused kernel's split-K instance may run it: the token tiles
+// sum_e ceil(n_e / NT) over the touched experts are at most
+// (P + touched (NT - 1)) / NT.  The kernel checks the actual count again.
+static bool ksplit_possible(int64_t P, int E, int NT, int MT, int KC)
+{
+    const int64_t touched = P < E ? P : E;
+    const int64_t items = (P + touched * (NT - 1)) / NT * MT;
+    return KC >= 2 && items <= KSPLIT_MAX_ITEMS && 2 * items <= num_sms();
+}
 
 FfnLayout ffn_layout(int64_t P, int d, int E, int I)
 {
@@ -1104,6 +1188,12 @@ FfnLayout ffn_layout(int64_t P, int d, int E, int I)
     L.w_sorted = take(size_t(P) * 4);
     L.dst_row = take(size_t(P) * 4);
     L.tile_done = take(size_t(max_tiles) * 4);
+    // split-K gate/up halves (the fused kernel at 16-token tiles): per item
+    // and half the fp32 accumulators of both matrices (4 warps x 2 x 16 x 32),
+    // per item one arrival counter per epilogue warp
+    const bool ks = L.NT == 16;
+    L.kpart = take(ks ? size_t(KSPLIT_MAX_ITEMS) * 2 * kKsplitHalfBytes : 0);
+    L.kcnt = take(ks ? size_t(KSPLIT_MAX_ITEMS) * 4 * sizeof(int32_t) : 0);
     L.total = off;
     return L;
 }
@@ -1135,6 +1225,7 @@ FfnSched ffn_sched(const FfnLayout &L, int d, int I, char *scratch)
     sc.band = L.NT >= 64 ? kDownBands : 0;  // Cfg<DOWN, NT>::STAGED: the fused combine
     sc.dst_row = reinterpret_cast<int32_t *>(scratch + L.dst_row);
     sc.tile_done = reinterpret_cast<int32_t *>(scratch + L.tile_done);
+    sc.kcnt = L.NT == 16 ? reinterpret_cast<int32_t *>(scratch + L.kcnt) : nullptr;
     return sc;
 }
 
@@ -1231,6 +1322,8 @@ cudaError_t launch_expert_gemms(const FfnArgs &a, const FfnLayout &L, char *scra
     g.KCh = Ip / 128;
     g.Ih = a.I;
     g.tile_done = reinterpret_cast<int32_t *>(scratch + L.tile_done);
+    g.kpart = L.NT == 16 ? reinterpret_cast<float *>(scratch + L.kpart) : nullptr;
+    g.kcnt = L.NT == 16 ? reinterpret_cast<int32_t *>(scratch + L.kcnt) : nullptr;
     // the fused combine's sums start at zero: the gate/up epilogue clears them
     g.zero = a.yacc ? reinterpret_cast<float4 *>(a.yacc) : nullptr;
     g.zero_n4 = a.yacc ? int64_t(a.P / a.k) * a.d / 4 : 0;
@@ -1254,7 +1347,9 @@ cudaError_t launch_expert_gemms(const FfnArgs &a, const FfnLayout &L, char *scra
     if (ffn_fused(L)) {
         // both GEMMs in one persistent kernel (the stage-boundary event, if
         // asked for, follows it)
-        cudaError_t e = L.NT == 16   ? launch_gemm<FUSED, 16>(mg, mu, mx, g, st, &md, &mh, &gd)
+        const bool split = L.NT == 16 && g.kpart && ksplit_possible(a.P, a.E, L.NT, g.MTA, g.KC);
+        cudaError_t e = split        ? launch_gemm<FUSED, 16, true>(mg, mu, mx, g, st, &md, &mh, &gd)
+                        : L.NT == 16 ? launch_gemm<FUSED, 16>(mg, mu, mx, g, st, &md, &mh, &gd)
                         : L.NT == 32 ? launch_gemm<FUSED, 32>(mg, mu, mx, g, st, &md, &mh, &gd)
                                      : launch_gemm<FUSED, 96>(mg, mu, mx, g, st, &md, &mh, &gd);
         if (e == cudaSuccess && mid) e = cudaEventRecord(mid, st);

@@ -478,6 +478,7 @@ lmoe_status lmoe_forward_workspace_views(const lmoe_dims *dims, lmoe_ffn_views *
         views->hs = int64_t(L.sscratch + S.hs);
         views->dst_row = -1;
         views->code_row = -1;
+        views->ksplit = -1;
         views->rows = int64_t(dims->T) * dims->k;
         views->tile_tokens = 0;
         views->slot_rows = 0;
@@ -492,6 +493,7 @@ lmoe_status lmoe_forward_workspace_views(const lmoe_dims *dims, lmoe_ffn_views *
     views->hs = int64_t(L.fscratch + F.hs);
     views->dst_row = int64_t(L.fscratch + F.dst_row);
     views->code_row = int64_t(L.inv);
+    views->ksplit = F.NT == 16 ? int64_t(L.fscratch + F.kcnt) : -1;
     views->rows = F.rows;
     views->tile_tokens = F.NT;
     views->slot_rows = F.SLOT;

@@ -173,7 +173,11 @@ struct FfnSched {
     int2 *items_gu = nullptr, *items_dn = nullptr;
     int2 *tile_info = nullptr;  // per token tile: {expert, token tile within the expert}
     int32_t *tile_done = nullptr;  // per token tile: the fused GEMM kernel's h-complete counter (zeroed here)
+    int32_t *kcnt = nullptr;  // per gate/up item (the first KSPLIT_MAX_ITEMS): 4 split-K arrival counters (zeroed here)
 };
+// Gate/up items of one fused-kernel launch that may run as two K halves
+// (the halves' fp32 accumulators have room for this many items).
+constexpr int KSPLIT_MAX_ITEMS = 128;
 
 // Work-item tables of the two expert GEMMs, in execution order: entry i is
 // item i as {expert | weight tile << 16, token tile within the expert}.
@@ -207,6 +211,7 @@ __device__ __forceinline__ void fill_item_entries(const FfnSched &sc, int n_gu, 
             R = int(g) / sc.MT_gu;
             m = int(g) - R * sc.MT_gu;
             dst = sc.items_gu + g;
+            if (sc.kcnt && g < KSPLIT_MAX_ITEMS) reinterpret_cast<int4 *>(sc.kcnt)[g] = make_int4(0, 0, 0, 0);
         } else {
             const int it = int(g - n_gu);
             // band b starts at item TT * m_lo(b), m_lo(b) = b * MT / NBd
@@ -262,7 +267,7 @@ struct FfnLayout {
     int NT, SLOT;      // token tile and the rows a tile occupies (SLOT == NT: tiles are packed)
     int64_t rows;      // code rows reserved: one per pair (permuted order) + one tile past the end
     size_t pad_off, tiles_gu, tiles_dn, items_gu, items_dn, tile_info, xq, xs, hq, hs, hs_bytes, w_sorted, dst_row,
-        tile_done, total;  // byte offsets / sizes
+        tile_done, kpart, kcnt, total;  // byte offsets / sizes (kpart, kcnt: 16-token tiles only, else empty)
     bool fused;  // large token tiles: the down GEMM can accumulate into the per-token output (FfnArgs::yacc)
 };
 FfnLayout ffn_layout(int64_t P, int d, int E, int I);

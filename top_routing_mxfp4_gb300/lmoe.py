@@ -91,7 +91,7 @@ _kernel_count = _sig("lmoe_forward_kernel_count", _i32, _DP)
 
 class FfnViews(ctypes.Structure):
     _fields_ = [("xq", _i64), ("xs", _i64), ("hq", _i64), ("hs", _i64), ("dst_row", _i64), ("rows", _i64),
-                ("tile_tokens", _i32), ("slot_rows", _i32), ("path", _i32), ("code_row", _i64)]
+                ("tile_tokens", _i32), ("slot_rows", _i32), ("path", _i32), ("code_row", _i64), ("ksplit", _i64)]
 
 
 _ws_views = _sig("lmoe_forward_workspace_views", ctypes.c_int, _DP, ctypes.POINTER(FfnViews))
