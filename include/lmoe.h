@@ -243,7 +243,7 @@ size_t lmoe_workspace_size(const lmoe_dims *dims);
  * summed in a fixed order (deterministic), but not strictly slot by slot.  It
  * is also the path of the MXFP4-activation variant (LMOE_ACT_MXFP4).  The
  * default is 0: every batch takes the tensor-core path, which with its fused
- * expert kernel measures faster at batch 1 too (50.1 against 58.9 us per
+ * expert kernel measures faster at batch 1 too (45.6 against 58.9 us per
  * step, L2 flushed).  Process-wide setting, not thread-safe; the workspace
  * size of a batch depends on it.  lmoe_small_batch_pairs() reads it. */
 #define LMOE_SMALL_BATCH_PAIRS_DEFAULT 0
