@@ -110,3 +110,37 @@ def test_mxfp4_byte_counts(lib):
     assert lmoe.mxfp4_bytes(2, 64, 64, lmoe.LAYOUT_TC) == (2 * 64 * 64, 2 * 1 * 1 * 512)
     with pytest.raises(ValueError):
         lmoe.mxfp4_bytes(1, 8, 48, lmoe.LAYOUT_TC)
+
+
+@pytest.mark.parametrize("T,tile", [(1, 16), (64, 16), (512, 32), (2048, 96)])
+def test_forward_workspace_views_layout(lib, T, tile):
+    """lmoe_forward_workspace_views is host arithmetic: at every token-tile
+    shape the views lie inside lmoe_workspace_size and do not overlap; the
+    split-K arrival counters (int32 [128][4], zeroed 16 bytes at a time by the
+    schedule) exist at 16-token tiles only and are 16-byte aligned."""
+    from top_routing_mxfp4_gb300 import lmoe
+    d, E, k, I = 3584, 896, 16, 512
+    ws_size = lib.lmoe_workspace_size
+    ws_size.restype = ctypes.c_size_t
+    ws_size.argtypes = [ctypes.POINTER(lmoe.Dims)]
+    old = lmoe.small_batch_pairs()
+    lmoe.set_small_batch_pairs(0)  # the tensor-core path's layout
+    try:
+        total = ws_size(ctypes.byref(lmoe.Dims(T, d, E, k, I, 1)))
+        v = lmoe.forward_workspace_views(T, d, E, k, I)
+    finally:
+        lmoe.set_small_batch_pairs(old)
+    assert v.path == 0 and v.tile_tokens == tile
+    P = T * k
+    regions = {"xq": (v.xq, v.rows * d), "hq": (v.hq, v.rows * I), "dst_row": (v.dst_row, 4 * P),
+               "code_row": (v.code_row, 4 * P)}
+    if tile == 16:
+        assert v.ksplit >= 0 and v.ksplit % 16 == 0
+        regions["ksplit"] = (v.ksplit, 128 * 4 * 4)
+    else:
+        assert v.ksplit == -1
+    spans = sorted(regions.items(), key=lambda kv: kv[1][0])
+    for name, (off, size) in spans:
+        assert 0 <= off and off + size <= total, name
+    for (n0, (o0, s0)), (n1, (o1, _)) in zip(spans, spans[1:]):
+        assert o0 + s0 <= o1, f"{n0} overlaps {n1}"
